@@ -1,0 +1,188 @@
+/*
+ * dflash_verify.h -- C ABI of the GB300 (sm_103a) draft-verification library.
+ *
+ * The library performs the verification step of block-drafted speculative
+ * decoding (DFlash / DFlash2) on a batch of requests: a block of gamma draft
+ * tokens per request is checked against the target model's logits at every
+ * draft position, and the step emits the accepted tokens, one corrected or
+ * bonus token, and the accept length.
+ *
+ * Sources of the operation (page title, then section):
+ *  - "DFlash2 用投机解码给 Qwen 提速" (bml.asia): the draft/verify loop
+ *    (one target forward over prefix + drafts, then accept each draft token
+ *    in order, resample from the target at the first rejection and stop);
+ *    the model-card settings (block size 8, temperature 1.0, top-p 0.95,
+ *    top-k 20); rejection sampling keeps the output distribution identical.
+ *  - "无损加速是真的吗？Qwen3.8-27B-DFlash2如何保证输出与目标模型完全一致"
+ *    (rytg.cn): section "投机解码如何白嫖速度" (a block of 8, 7 tokens
+ *    verified per step; step 3 "裁决": from the first mismatch the target
+ *    resamples from its own distribution), the lossless definition (greedy
+ *    output identical to the target, sampling preserves its distribution) and
+ *    the acceptance length (tokens produced per verification step).
+ *  - Standard speculative sampling: accept a draft token d with probability
+ *    min(1, p(d)/q(d)); at the first rejection draw from the normalised
+ *    residual max(0, p - q); when every draft is accepted draw a bonus token
+ *    from the target distribution of the last position.
+ *  - Philox4x32-10 (Salmon et al., "Parallel Random Numbers: As Easy as 1, 2,
+ *    3", SC'11) for the uniforms, keyed by (seed, request, position).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked [device] are CUDA device pointers; [host] are host
+ *    pointers. The caller owns every buffer; the library keeps no pointer
+ *    after a call returns and allocates no device memory. Inputs are not
+ *    modified.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream). Device work is enqueued on it; calls with only [device]
+ *    buffers return without waiting for the GPU.
+ *  - Logits are dense row-major arrays of bf16 (dtype DFLASH_BF16, raw
+ *    bfloat16) or fp32 (DFLASH_F32). Rows need no particular alignment.
+ *  - Return value: DFLASH_OK, or an error code when the arguments are
+ *    rejected (nothing is enqueued) or a CUDA launch fails;
+ *    dflash_last_error() describes the last error of the calling thread.
+ *  - Data problems found on the GPU never trap: they OR DFLASH_STATUS_* bits
+ *    into *status (a [device] uint32, optional, never cleared by the
+ *    library), and the outputs stay in range.
+ *  - Filtering: temperature T > 0 scales logits as x / T; top-k keeps the k
+ *    largest logits, ties to the lower token index (top_k <= 0 or >= V:
+ *    off); softmax over the survivors; top-p keeps the shortest prefix of
+ *    that order whose mass reaches top_p (top_p >= 1: off) and renormalises.
+ *    Supported: 1 <= top_k <= DFLASH_MAX_TOP_K with any top_p in (0, 1], or
+ *    top-k off with top_p >= 1 (full-vocabulary softmax). Other combinations
+ *    return DFLASH_ERR_UNSUPPORTED.
+ */
+#ifndef DFLASH_VERIFY_H
+#define DFLASH_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DFLASH_ABI_VERSION 1
+#define DFLASH_MAX_TOP_K 32
+
+/* logits storage type */
+enum { DFLASH_BF16 = 0, DFLASH_F32 = 1 };
+
+/* return codes */
+enum {
+  DFLASH_OK = 0,
+  DFLASH_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad top_p, small workspace */
+  DFLASH_ERR_UNSUPPORTED = 2, /* filter combination outside the supported set */
+  DFLASH_ERR_CUDA = 3         /* a CUDA call failed (message in dflash_last_error) */
+};
+
+/* device status bits (OR-ed into *status) */
+#define DFLASH_STATUS_BAD_TOKEN 1u       /* a draft token outside [0, V): never accepted */
+#define DFLASH_STATUS_BAD_ROW 2u         /* a row read by the step holds a NaN or has an
+                                            infinite maximum; that request's output is
+                                            unspecified but in range */
+#define DFLASH_STATUS_TIMEOUT 4u         /* a bounded on-chip wait gave up (the call's
+                                            outputs are then unspecified) */
+#define DFLASH_STATUS_BAD_TEMPERATURE 8u /* temperature negative, NaN or infinite: the
+                                            request is verified greedily */
+
+/* ABI version of the loaded library (DFLASH_ABI_VERSION). */
+int dflash_abi_version(void);
+
+/* Message of the last error returned to the calling thread ("" if none). */
+const char* dflash_last_error(void);
+
+/* Bytes of device workspace dflash_verify / dflash_verify_greedy need for a
+ * batch of this shape (greedy: pass top_k = 1, top_p = 1). 0 when the
+ * arguments are invalid or unsupported. */
+size_t dflash_workspace_bytes(int B, int gamma, int V, int dtype, int top_k, float top_p);
+
+/* Bytes of device workspace dflash_filter / dflash_sample need for R rows. */
+size_t dflash_rows_workspace_bytes(int R, int V, int dtype, int top_k, float top_p);
+
+/* Prepares a workspace for first use (zero-fills it on `stream`). Needed once
+ * per allocation, and again after any call on it returned DFLASH_ERR_CUDA or
+ * raised DFLASH_STATUS_TIMEOUT; every successful call leaves it ready for the
+ * next. Calls sharing one workspace must be ordered (same stream, or
+ * synchronised). */
+int dflash_workspace_init(void* workspace, size_t bytes, void* stream);
+
+/* Batched verification (sampling, with greedy requests mixed in).
+ *
+ * target_logits [device] [B, gamma+1, V] dtype: target logits at the gamma
+ *     draft positions and the bonus position.
+ * draft_logits  [device] [B, gamma, V] dtype: the drafter's logits at each
+ *     draft position. Rows of greedy requests are not read (may be garbage).
+ * draft_tokens  [device] int32 [B, gamma]: the drafts, which must be samples
+ *     from the drafter's filtered distribution for the step to be lossless.
+ * temperature   [device] float [B]: T > 0 samples; T == 0 verifies that
+ *     request greedily (argmax prefix match); other values: greedy plus
+ *     DFLASH_STATUS_BAD_TEMPERATURE.
+ * top_k, top_p: the filter applied to both target and draft distributions.
+ * seed: Philox key; request b at position i uses counter (i, b, 0, 0):
+ *     output word 0 -> the accept uniform, word 1 -> the residual / bonus
+ *     uniform, each (w >> 8) * 2^-24.
+ * out_tokens     [device] int32 [B, gamma+1]: accepted drafts, then the
+ *     corrected or bonus token, then -1 padding.
+ * out_accept_len [device] int32 [B]: tokens emitted, in [1, gamma+1].
+ * workspace [device], workspace_bytes >= dflash_workspace_bytes(...),
+ *     prepared by dflash_workspace_init.
+ * Accept test at position i: u < p_i(d_i) / q_i(d_i) in fp32 (q = 0 with
+ * p > 0 accepts; p = q = 0 rejects). The residual and bonus draws take the
+ * smallest token index whose cumulative weight (ascending token order)
+ * exceeds u * total. 1 <= gamma <= 64, 1 <= V < 2^31, B >= 1. */
+int dflash_verify(const void* target_logits, const void* draft_logits,
+                  const int32_t* draft_tokens, int B, int gamma, int V, int dtype,
+                  const float* temperature, int top_k, float top_p, uint64_t seed,
+                  int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                  size_t workspace_bytes, uint32_t* status, void* stream);
+
+/* Greedy verification of every request: a_i = argmax target_logits[b, i, :]
+ * (lowest index on ties); n = length of the prefix with draft_tokens[b, i] ==
+ * a_i; emits d_0..d_{n-1}, a_n and accept length n + 1. Draft logits are not
+ * needed. Arguments as for dflash_verify (workspace sized with top_k = 1,
+ * top_p = 1). */
+int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B,
+                         int gamma, int V, int dtype, int32_t* out_tokens,
+                         int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                         uint32_t* status, void* stream);
+
+/* dflash_verify with [host] inputs and outputs: copies the logits (the draft
+ * rows of sampling requests only), drafts and temperatures into the caller's
+ * [device] staging buffer, verifies, copies tokens, accept lengths and the
+ * status word back, and waits for `stream`. Pinned host memory makes the
+ * copies asynchronous. staging_bytes >= dflash_host_staging_bytes(...). */
+size_t dflash_host_staging_bytes(int B, int gamma, int V, int dtype);
+int dflash_verify_host(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, int B, int gamma, int V, int dtype,
+                       const float* temperature, int top_k, float top_p, uint64_t seed,
+                       int32_t* out_tokens, int32_t* out_accept_len, uint32_t* out_status,
+                       void* staging, size_t staging_bytes, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/* Filtered distribution of R rows: for row r, the kept tokens in (logit
+ * desc, index asc) order, out_idx[r, 0..n-1], their probabilities
+ * out_prob[r, 0..n-1] (fp32) and n = out_count[r] (slots n..top_k-1 hold -1
+ * and 0). temperature [device] [R] > 0. Requires 1 <= top_k <=
+ * DFLASH_MAX_TOP_K. logits [device] [R, V]. */
+int dflash_filter(const void* logits, int R, int V, int dtype, const float* temperature,
+                  int top_k, float top_p, int32_t* out_idx, float* out_prob,
+                  int32_t* out_count, void* workspace, size_t workspace_bytes,
+                  uint32_t* status, void* stream);
+
+/* One token per row from its filtered distribution (the drafter's side of
+ * the loop): temperature[r] == 0 takes the argmax; otherwise the inverse CDF
+ * in ascending token order with the accept uniform of Philox counter
+ * (r, 0, 1, 0). out_tokens [device] int32 [R]. */
+int dflash_sample(const void* logits, int R, int V, int dtype, const float* temperature,
+                  int top_k, float top_p, uint64_t seed, int32_t* out_tokens, void* workspace,
+                  size_t workspace_bytes, uint32_t* status, void* stream);
+
+/* The uniforms the step draws: out_accept[b * npos + i] and
+ * out_draw[b * npos + i] for counter (i, b, stream_id, 0) under `seed`
+ * ([device] float arrays of B * npos). For audits and tests. */
+int dflash_uniforms(uint64_t seed, int B, int npos, int stream_id, float* out_accept,
+                    float* out_draw, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DFLASH_VERIFY_H */
