@@ -1,0 +1,374 @@
+#!/usr/bin/env python3
+"""Benchmark of the draft-verification step on GB300.
+
+One step = one batched verification (target/draft logits in, tokens and
+accept lengths out) of the concurrency-32 mixed workload: B=32 requests,
+block 8 (gamma=7), V=248320, bf16 logits, temperatures cycling 0 (greedy) /
+0.6 / 1.0, top-k 20, top-p 0.95. The metric is verified draft positions per
+second (B * gamma per step) with the achieved HBM bandwidth in the roofline
+block. Inputs rotate over 3 independently generated sets (each about 238 MB,
+together well above the 129 MB L2), so no step finds its logits in L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+N > 1 runs under torch.distributed.run: every rank verifies its own batch (the
+step shards by request, no data exchange), timing is the max over ranks.
+``--impl reference`` times the CPU oracle (fp64, host threads) on samples of
+the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "b32_mixed_v248320"
+METRIC = "verified draft-positions/sec and achieved HBM GB/s (B=32, block 8, V=248320)"
+UNIT = "verified draft positions/s"
+N_SETS = 3
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_sweep_b32_mixed_v248320.md")
+CSRC = os.path.join(ROOT, "speculative_decoding_verification_83_gb300", "csrc")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    try:
+        text = open(PROFILE_SUMMARY).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0}, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = f"/tmp/dflash_clocks_{os.getpid()}.csv"
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.remove(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": float(max(smax)) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def algorithmic_bytes(inp) -> int:
+    """Logit bytes one step must read: every target row, and the draft rows of
+    requests that sample (greedy requests never read their draft rows)."""
+    B, gamma, V = inp.shape
+    es = 2 if inp.target.dtype == np.uint16 else 4
+    n_samp = int(np.sum(inp.temperature > 0))
+    rows = B * (gamma + 1) + n_samp * gamma
+    return rows * V * es
+
+
+def cpu_baseline(inp, d, threads=None):
+    """The oracle (as it stands) on the host cores: one full batch."""
+    import oracle
+
+    B, gamma, V = inp.shape
+    threads = threads or oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, inp.seed,
+                  threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": B * gamma / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"one {WORKLOAD} batch of {B} requests (fp64 C oracle, {threads} host "
+                      f"threads), {dt:.2f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    inp = synth.make_workload(WORKLOAD, data_seed=0, seed=0)
+    B, gamma, V = inp.shape
+    d, _, _ = oracle.sample_rows(inp.draft.reshape(B * gamma, V),
+                                 synth.draft_sampling_temperatures(inp.temperature, gamma),
+                                 inp.top_k, inp.top_p, 1000)
+    d = d.reshape(B, gamma)
+    threads = oracle.default_threads()
+    # size each step so that warmup + steps stay within about two minutes
+    t0 = time.perf_counter()
+    oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, 0,
+                  threads=threads, requests=[1])
+    per_req = max(1e-3, time.perf_counter() - t0)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_req = int(max(1, min(B, budget / per_req)))
+    order = [b % B for b in range(1, 1 + n_req)]  # starts with a sampling request
+    for _ in range(args.warmup):
+        oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, 0,
+                      threads=threads, requests=order)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, s,
+                      threads=threads, requests=order)
+    dt = time.perf_counter() - t0
+    value = args.steps * n_req * gamma / dt
+    sample = f"{n_req} of the {B} requests per step (fp64 C oracle, {threads} host threads)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "B": B, "gamma": gamma, "V": V,
+                                        "top_k": 20, "top_p": 0.95},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- our arm
+def run_gpu(args):
+    import torch
+
+    import speculative_decoding_verification_83_gb300 as dv
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device(f"cuda:{local_rank}")
+    dv.build()
+    lib = dv.load()
+
+    # ---- inputs: N_SETS independent batches, resident in HBM
+    sets_np, sets_dev = [], []
+    for s in range(N_SETS):
+        sets_np.append(synth.make_workload(WORKLOAD, data_seed=1000 * rank + s, seed=s))
+    B, gamma, V = sets_np[0].shape
+    dt_code = dv.DFLASH_BF16
+    rows_ws = dv.Workspace(dv.rows_workspace_bytes(B * gamma, V, dt_code, 20, 0.95), dev)
+    for inp in sets_np:
+        X = synth.to_torch(inp.target, dev)
+        Y = synth.to_torch(inp.draft, dev)
+        T = torch.from_numpy(inp.temperature).to(dev)
+        # drafts: the library's own sampler on the draft rows (argmax for greedy requests)
+        Trows = torch.from_numpy(synth.draft_sampling_temperatures(inp.temperature, gamma)).to(dev)
+        d = dv.sample_rows(Y.view(B * gamma, V), Trows, inp.top_k, inp.top_p, 7 + inp.seed,
+                           workspace=rows_ws).view(B, gamma).contiguous()
+        sets_dev.append((X, Y, d, T))
+    torch.cuda.synchronize()
+    top_k, top_p = sets_np[0].top_k, sets_np[0].top_p
+    ws = dv.Workspace(dv.workspace_bytes(B, gamma, V, dt_code, top_k, top_p), dev)
+    out_tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    calls = []
+    for s, (X, Y, d, T) in enumerate(sets_dev):
+        calls.append((X.data_ptr(), Y.data_ptr(), d.data_ptr(), B, gamma, V, dt_code, T.data_ptr(),
+                      top_k, top_p, s + 1, out_tok.data_ptr(), out_len.data_ptr(), ws.ptr, ws.nbytes,
+                      status.data_ptr(), sp))
+    fn = lib.dflash_verify
+
+    def step(i):
+        rc = fn(*calls[i % N_SETS])
+        if rc:
+            raise RuntimeError(lib.dflash_last_error().decode())
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"status word {int(status.item())} after warm-up")
+
+    # ---- timed region: K steps back to back, one event pair per launch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    start.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(i)
+        evs[i][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if world > 1:
+        torch.distributed.barrier()
+    region_ms = start.elapsed_time(end)
+    launch_ms = np.array([a.elapsed_time(b) for a, b in evs])
+    t_region = torch.tensor([region_ms], device=dev, dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t_region, op=torch.distributed.ReduceOp.MAX)
+    region_ms = float(t_region.item())
+    ms_per_step = region_ms / args.steps
+    value = world * args.steps * B * gamma / (region_ms / 1e3)
+
+    # ---- roofline of the kernel (one launch = one step)
+    alg = algorithmic_bytes(sets_np[0])
+    avg_launch_s = float(launch_ms.mean()) / 1e3
+    achieved = alg / avg_launch_s / 1e9
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    traffic = profiled_traffic()
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic,
+                "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "algorithmic_bytes_per_launch": alg,
+                "avg_launch_us": avg_launch_s * 1e6,
+                "p50_launch_us": float(np.median(launch_ms)) * 1e3}
+
+    # ---- end to end through the host-buffer entry point (pinned host memory)
+    inp = sets_np[0]
+
+    def pin(a):
+        return synth.to_torch(a, "cpu").pin_memory()
+
+    hX, hY = pin(inp.target), pin(inp.draft)
+    hd = sets_dev[0][2].cpu().pin_memory()
+    hT = pin(inp.temperature)
+    h_tok = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
+    h_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+    h_st = torch.zeros((1,), dtype=torch.int32).pin_memory()
+    staging = torch.empty(dv.host_staging_bytes(B, gamma, V, dt_code), dtype=torch.uint8,
+                          device=dev)
+    n_e2e = max(3, min(50, args.steps))
+    for i in range(2):
+        dv.verify_host(hX, hY, hd, hT, top_k, top_p, i, h_tok, h_len, h_st, staging, ws)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        dv.verify_host(hX, hY, hd, hT, top_k, top_p, i, h_tok, h_len, h_st, staging, ws)
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    n_samp = int(np.sum(inp.temperature > 0))
+    h2d = (B * (gamma + 1) + n_samp * gamma) * V * 2 + B * gamma * 4 + B * 4
+    d2h = B * (gamma + 1) * 4 + B * 4 + 4
+    t_e2e = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+    if world > 1:
+        torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
+    e2e = {"value": world * B * gamma / float(t_e2e.item()), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": float(t_e2e.item()) * 1e3}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return 0
+    lens = out_len.cpu().numpy()
+    cpu = cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy()) if world == 1 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": B, "gamma": gamma, "V": V, "top_k": top_k,
+                   "top_p": top_p, "temperatures": "cycling 0 (greedy) / 0.6 / 1.0",
+                   "l2": f"inputs rotate over {N_SETS} sets of "
+                         f"{(sets_np[0].target.nbytes + sets_np[0].draft.nbytes) / 1e6:.0f} MB "
+                         "(larger than L2 together)",
+                   "per_rank_batch": B},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "mean_accept_len_last_step": float(lens.mean()),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

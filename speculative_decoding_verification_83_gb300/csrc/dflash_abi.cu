@@ -1,0 +1,371 @@
+// dflash_abi.cu -- the extern "C" entry points declared in include/dflash_verify.h:
+// argument checks, workspace layout, launch configuration and the host-buffer
+// path. No device memory is allocated here; every buffer belongs to the caller.
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/dflash_verify.h"
+#include "dflash_internal.h"
+
+using namespace dflash;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof g_last_error, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  static std::mutex mu;
+  static int cached[64] = {0};
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+int esize_of(int dtype) { return dtype == DFLASH_BF16 ? 2 : (dtype == DFLASH_F32 ? 4 : 0); }
+
+// Filter mode of a call: 1 = top-k (1..32) with any top_p, 0 = unsupported,
+// -1 = invalid.
+int filter_mode(int V, int top_k, float top_p) {
+  if (!(top_p > 0.0f) || std::isnan(top_p)) return -1;
+  const bool k_on = top_k > 0 && top_k < V;
+  if (k_on && top_k <= DFLASH_MAX_TOP_K) return 1;
+  return 0;
+}
+
+int check_shape(int B, int gamma, int V, int dtype) {
+  if (B < 1 || B > kMaxB) return fail(DFLASH_ERR_INVALID_ARG, "B=%d outside [1, %d]", B, kMaxB);
+  if (gamma < 1 || gamma > kMaxGamma)
+    return fail(DFLASH_ERR_INVALID_ARG, "gamma=%d outside [1, %d]", gamma, kMaxGamma);
+  if (V < 1) return fail(DFLASH_ERR_INVALID_ARG, "V=%d must be >= 1", V);
+  if (!esize_of(dtype)) return fail(DFLASH_ERR_INVALID_ARG, "dtype=%d is neither bf16 nor fp32", dtype);
+  return DFLASH_OK;
+}
+
+int check_aligned(const void* p, int esize, const char* name) {
+  if (((uintptr_t)p) % (uintptr_t)esize)
+    return fail(DFLASH_ERR_INVALID_ARG, "%s is not aligned to its element size", name);
+  return DFLASH_OK;
+}
+
+size_t verify_workspace(int B, int gamma, int V, int dtype) {
+  const Geometry g = make_geometry(V, esize_of(dtype));
+  return make_layout(B * (2 * gamma + 1), B, g).total;
+}
+
+void bind_workspace(Params& p, void* ws, int n_slots, int n_requests) {
+  const WorkspaceLayout L = make_layout(n_slots, n_requests, p.geo);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  p.row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
+  p.req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
+  p.abort_flag = reinterpret_cast<uint32_t*>(base + L.abort_flag);
+  p.tile_keys = reinterpret_cast<uint32_t*>(base + L.tile_keys);
+  p.res_key = reinterpret_cast<uint32_t*>(base + L.res_key);
+  p.res_idx = reinterpret_cast<int32_t*>(base + L.res_idx);
+  p.res_flag = reinterpret_cast<uint32_t*>(base + L.res_flag);
+  p.n_slots = n_slots;
+}
+
+int run(Params& p, int total_slots, void* stream) {
+  const int sms = sm_count();
+  if (sms <= 0) return fail(DFLASH_ERR_CUDA, "no CUDA device");
+  const long long pieces = (long long)total_slots * p.geo.ppr;
+  long long grid = (long long)sms * kCtasPerSm;
+  if (grid > pieces) grid = pieces;
+  if (grid < 1) grid = 1;
+  const int e = launch_sweep(p, (int)grid, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "launching the verification kernel");
+  return DFLASH_OK;
+}
+
+Params base_params(int dtype, int V) {
+  Params p;
+  memset(&p, 0, sizeof p);
+  p.dtype = dtype == DFLASH_BF16 ? 0 : 1;
+  p.geo = make_geometry(V, esize_of(dtype));
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dflash_abi_version(void) { return DFLASH_ABI_VERSION; }
+
+const char* dflash_last_error(void) { return g_last_error; }
+
+size_t dflash_workspace_bytes(int B, int gamma, int V, int dtype, int top_k, float top_p) {
+  if (B < 1 || B > kMaxB || gamma < 1 || gamma > kMaxGamma || V < 1 || !esize_of(dtype)) return 0;
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode <= 0 && !(top_k == 1 && top_p >= 1.0f)) return 0;
+  return verify_workspace(B, gamma, V, dtype);
+}
+
+size_t dflash_rows_workspace_bytes(int R, int V, int dtype, int top_k, float top_p) {
+  if (R < 1 || V < 1 || !esize_of(dtype) || filter_mode(V, top_k, top_p) <= 0) return 0;
+  const int chunk = R < kMaxCounterSlots ? R : kMaxCounterSlots;
+  return make_layout(chunk, 1, make_geometry(V, esize_of(dtype))).total;
+}
+
+int dflash_workspace_init(void* workspace, size_t bytes, void* stream) {
+  if (!workspace && bytes) return fail(DFLASH_ERR_INVALID_ARG, "null workspace");
+  if (!bytes) return DFLASH_OK;
+  cudaError_t e = cudaMemsetAsync(workspace, 0, bytes, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "clearing the workspace");
+  return DFLASH_OK;
+}
+
+int dflash_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
+                  int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
+                  uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                  size_t workspace_bytes, uint32_t* status, void* stream) {
+  int rc = check_shape(B, gamma, V, dtype);
+  if (rc) return rc;
+  if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
+      !workspace)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
+  if (mode == 0)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d, top_k < V)", top_k,
+                (double)top_p, DFLASH_MAX_TOP_K);
+  const int es = esize_of(dtype);
+  if ((rc = check_aligned(target_logits, es, "target_logits")) ||
+      (rc = check_aligned(draft_logits, es, "draft_logits")))
+    return rc;
+  if (workspace_bytes < verify_workspace(B, gamma, V, dtype))
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, verify_workspace(B, gamma, V, dtype));
+  Params p = base_params(dtype, V);
+  p.target = static_cast<const unsigned char*>(target_logits);
+  p.draft = static_cast<const unsigned char*>(draft_logits);
+  p.draft_tokens = draft_tokens;
+  p.temperature = temperature;
+  p.B = B;
+  p.gamma = gamma;
+  p.top_k = top_k;
+  p.top_p = top_p >= 1.0f ? 1.0f : top_p;
+  p.seed = seed;
+  p.task = kTaskVerify;
+  p.out_tokens = out_tokens;
+  p.out_len = out_accept_len;
+  p.status = status;
+  bind_workspace(p, workspace, B * (2 * gamma + 1), B);
+  // the slot count depends on the device-side temperatures; launch for the maximum
+  return run(p, B * (2 * gamma + 1), stream);
+}
+
+int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
+                         int dtype, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                         size_t workspace_bytes, uint32_t* status, void* stream) {
+  int rc = check_shape(B, gamma, V, dtype);
+  if (rc) return rc;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_accept_len || !workspace)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if ((rc = check_aligned(target_logits, esize_of(dtype), "target_logits"))) return rc;
+  if (workspace_bytes < verify_workspace(B, gamma, V, dtype))
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, verify_workspace(B, gamma, V, dtype));
+  Params p = base_params(dtype, V);
+  p.target = static_cast<const unsigned char*>(target_logits);
+  p.draft_tokens = draft_tokens;
+  p.B = B;
+  p.gamma = gamma;
+  p.top_k = 1;
+  p.top_p = 1.0f;
+  p.task = kTaskVerifyGreedy;
+  p.out_tokens = out_tokens;
+  p.out_len = out_accept_len;
+  p.status = status;
+  bind_workspace(p, workspace, B * (2 * gamma + 1), B);
+  return run(p, B * (gamma + 1), stream);
+}
+
+size_t dflash_host_staging_bytes(int B, int gamma, int V, int dtype) {
+  const int es = esize_of(dtype);
+  if (B < 1 || gamma < 1 || V < 1 || !es) return 0;
+  const size_t row = (size_t)V * es;
+  size_t off = 0;
+  off = align_up(off + row * (size_t)B * (gamma + 1), 256);  // target
+  off = align_up(off + row * (size_t)B * gamma, 256);        // draft
+  off = align_up(off + sizeof(int32_t) * (size_t)B * gamma, 256);
+  off = align_up(off + sizeof(float) * (size_t)B, 256);
+  off = align_up(off + sizeof(int32_t) * (size_t)B * (gamma + 1), 256);
+  off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
+  off = align_up(off + sizeof(uint32_t), 256);
+  return off;
+}
+
+int dflash_verify_host(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
+                       int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
+                       uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, uint32_t* out_status,
+                       void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+  int rc = check_shape(B, gamma, V, dtype);
+  if (rc) return rc;
+  if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
+      !staging || !workspace)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if (staging_bytes < dflash_host_staging_bytes(B, gamma, V, dtype))
+    return fail(DFLASH_ERR_INVALID_ARG, "staging buffer too small");
+  const int es = esize_of(dtype);
+  const size_t row = (size_t)V * es;
+  unsigned char* s = static_cast<unsigned char*>(staging);
+  size_t off = 0;
+  unsigned char* d_target = s + off;
+  off = align_up(off + row * (size_t)B * (gamma + 1), 256);
+  unsigned char* d_draft = s + off;
+  off = align_up(off + row * (size_t)B * gamma, 256);
+  int32_t* d_tokens_in = reinterpret_cast<int32_t*>(s + off);
+  off = align_up(off + sizeof(int32_t) * (size_t)B * gamma, 256);
+  float* d_temp = reinterpret_cast<float*>(s + off);
+  off = align_up(off + sizeof(float) * (size_t)B, 256);
+  int32_t* d_out = reinterpret_cast<int32_t*>(s + off);
+  off = align_up(off + sizeof(int32_t) * (size_t)B * (gamma + 1), 256);
+  int32_t* d_len = reinterpret_cast<int32_t*>(s + off);
+  off = align_up(off + sizeof(int32_t) * (size_t)B, 256);
+  uint32_t* d_status = reinterpret_cast<uint32_t*>(s + off);
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e;
+#define DFLASH_TRY(call, what)                       \
+  do {                                               \
+    e = (call);                                      \
+    if (e != cudaSuccess) return cuda_fail(e, what); \
+  } while (0)
+  DFLASH_TRY(cudaMemcpyAsync(d_target, target_logits, row * (size_t)B * (gamma + 1), cudaMemcpyHostToDevice, st),
+             "copying target logits");
+  // draft rows: only requests that sample read them; copy runs of such requests
+  for (int b = 0; b < B;) {
+    const float t = temperature[b];
+    if (!(t > 0.0f && std::isfinite(t))) {
+      ++b;
+      continue;
+    }
+    int e_b = b + 1;
+    while (e_b < B && temperature[e_b] > 0.0f && std::isfinite(temperature[e_b])) ++e_b;
+    const size_t off_b = row * (size_t)b * gamma, bytes = row * (size_t)(e_b - b) * gamma;
+    DFLASH_TRY(cudaMemcpyAsync(d_draft + off_b, static_cast<const unsigned char*>(draft_logits) + off_b, bytes,
+                               cudaMemcpyHostToDevice, st),
+               "copying draft logits");
+    b = e_b;
+  }
+  DFLASH_TRY(cudaMemcpyAsync(d_tokens_in, draft_tokens, sizeof(int32_t) * (size_t)B * gamma,
+                             cudaMemcpyHostToDevice, st),
+             "copying draft tokens");
+  DFLASH_TRY(cudaMemcpyAsync(d_temp, temperature, sizeof(float) * (size_t)B, cudaMemcpyHostToDevice, st),
+             "copying temperatures");
+  DFLASH_TRY(cudaMemsetAsync(d_status, 0, sizeof(uint32_t), st), "clearing the status word");
+  rc = dflash_verify(d_target, d_draft, d_tokens_in, B, gamma, V, dtype, d_temp, top_k, top_p, seed, d_out, d_len,
+                     workspace, workspace_bytes, d_status, stream);
+  if (rc) return rc;
+  DFLASH_TRY(cudaMemcpyAsync(out_tokens, d_out, sizeof(int32_t) * (size_t)B * (gamma + 1),
+                             cudaMemcpyDeviceToHost, st),
+             "copying tokens back");
+  DFLASH_TRY(cudaMemcpyAsync(out_accept_len, d_len, sizeof(int32_t) * (size_t)B, cudaMemcpyDeviceToHost, st),
+             "copying accept lengths back");
+  if (out_status)
+    DFLASH_TRY(cudaMemcpyAsync(out_status, d_status, sizeof(uint32_t), cudaMemcpyDeviceToHost, st),
+               "copying the status back");
+  DFLASH_TRY(cudaStreamSynchronize(st), "waiting for the stream");
+#undef DFLASH_TRY
+  return DFLASH_OK;
+}
+
+static int rows_task(int task, const void* logits, int R, int V, int dtype, const float* temperature, int top_k,
+                     float top_p, uint64_t seed, int32_t* out_tokens, int32_t* out_idx, float* out_prob,
+                     int32_t* out_count, void* workspace, size_t workspace_bytes, uint32_t* status, void* stream) {
+  if (R < 1 || V < 1 || !esize_of(dtype))
+    return fail(DFLASH_ERR_INVALID_ARG, "bad shape R=%d V=%d dtype=%d", R, V, dtype);
+  if (!logits || !temperature || !workspace) return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
+  if (mode == 0)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d, top_k < V)", top_k,
+                (double)top_p, DFLASH_MAX_TOP_K);
+  int rc = check_aligned(logits, esize_of(dtype), "logits");
+  if (rc) return rc;
+  const size_t need = dflash_rows_workspace_bytes(R, V, dtype, top_k, top_p);
+  if (workspace_bytes < need)
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
+                need);
+  Params p = base_params(dtype, V);
+  p.temperature = temperature;
+  p.gamma = 1;
+  p.top_k = top_k;
+  p.top_p = top_p >= 1.0f ? 1.0f : top_p;
+  p.seed = seed;
+  p.task = task;
+  p.status = status;
+  const int chunk = R < kMaxCounterSlots ? R : kMaxCounterSlots;
+  bind_workspace(p, workspace, chunk, 1);
+  // rows go through launches of at most kMaxCounterSlots rows each (the size
+  // of the workspace's counter header); the sampler keys its uniforms by the
+  // absolute row index, so each launch is told where its rows start
+  for (int r0 = 0; r0 < R; r0 += chunk) {
+    const int n = R - r0 < chunk ? R - r0 : chunk;
+    const size_t row_bytes = (size_t)V * esize_of(dtype);
+    p.target = static_cast<const unsigned char*>(logits) + (size_t)r0 * row_bytes;
+    p.temperature = temperature + r0;
+    p.B = n;
+    p.row_base = r0;
+    p.out_tokens = out_tokens ? out_tokens + r0 : nullptr;
+    p.out_idx = out_idx ? out_idx + (size_t)r0 * top_k : nullptr;
+    p.out_prob = out_prob ? out_prob + (size_t)r0 * top_k : nullptr;
+    p.out_count = out_count ? out_count + r0 : nullptr;
+    rc = run(p, n, stream);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_filter(const void* logits, int R, int V, int dtype, const float* temperature, int top_k, float top_p,
+                  int32_t* out_idx, float* out_prob, int32_t* out_count, void* workspace, size_t workspace_bytes,
+                  uint32_t* status, void* stream) {
+  if (!out_idx || !out_prob || !out_count) return fail(DFLASH_ERR_INVALID_ARG, "null output pointer");
+  return rows_task(kTaskFilter, logits, R, V, dtype, temperature, top_k, top_p, 0, nullptr, out_idx, out_prob,
+                   out_count, workspace, workspace_bytes, status, stream);
+}
+
+int dflash_sample(const void* logits, int R, int V, int dtype, const float* temperature, int top_k, float top_p,
+                  uint64_t seed, int32_t* out_tokens, void* workspace, size_t workspace_bytes, uint32_t* status,
+                  void* stream) {
+  if (!out_tokens) return fail(DFLASH_ERR_INVALID_ARG, "null output pointer");
+  return rows_task(kTaskSample, logits, R, V, dtype, temperature, top_k, top_p, seed, out_tokens, nullptr, nullptr,
+                   nullptr, workspace, workspace_bytes, status, stream);
+}
+
+int dflash_uniforms(uint64_t seed, int B, int npos, int stream_id, float* out_accept, float* out_draw, void* stream) {
+  if (B < 1 || npos < 1 || (!out_accept && !out_draw))
+    return fail(DFLASH_ERR_INVALID_ARG, "bad uniforms arguments");
+  const int e = launch_uniforms(seed, B, npos, stream_id, out_accept, out_draw, stream);
+  if (e) return cuda_fail((cudaError_t)e, "launching the uniforms kernel");
+  return DFLASH_OK;
+}
+
+}  // extern "C"

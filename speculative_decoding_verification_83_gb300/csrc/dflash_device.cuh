@@ -1,0 +1,226 @@
+// dflash_device.cuh -- device helpers for the draft-verification kernels:
+// order-preserving logit keys, Philox4x32-10, bulk-copy and mbarrier PTX,
+// warp collectives.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+namespace dflash {
+
+// ---- logit order --------------------------------------------------------------
+// Logits are ordered by value, -0 equal to +0, ties to the lower token index.
+// key() maps an fp32 value to a uint32 whose unsigned order is that value
+// order (zeros collapse to +0); NaNs land above +inf (positive sign bit clear)
+// or below -inf, and a row holding one is rejected separately.
+__device__ __forceinline__ uint32_t key_of(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u << 1) == 0u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float value_of_key(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(u);
+}
+constexpr uint32_t kKeyPosInf = 0xff800000u;   // key_of(+inf)
+constexpr uint32_t kKeyNegInf = 0x007fffffu;   // key_of(-inf)
+
+// A row is unusable when its largest key is not a finite value.
+__device__ __forceinline__ bool key_is_finite(uint32_t k) { return k > kKeyNegInf && k < kKeyPosInf; }
+
+// composite sort key: larger logit first, then lower index
+__device__ __forceinline__ unsigned long long composite(uint32_t key, int32_t idx) {
+  return ((unsigned long long)key << 32) | (unsigned long long)(0xffffffffu - (uint32_t)idx);
+}
+__device__ __forceinline__ int32_t composite_idx(unsigned long long c) {
+  return (int32_t)(0xffffffffu - (uint32_t)(c & 0xffffffffull));
+}
+__device__ __forceinline__ uint32_t composite_key(unsigned long long c) { return (uint32_t)(c >> 32); }
+
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+
+// ---- Philox4x32-10 (Salmon et al., SC'11) ----------------------------------------
+// Ten rounds; each round multiplies words 0 and 2 by the two round
+// multipliers, mixes the high halves with words 1 and 3 and the key, and the
+// key advances by the two Weyl increments between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    if (r > 0) {
+      k.x += 0x9E3779B9u;
+      k.y += 0xBB67AE85u;
+    }
+    const uint32_t hi_a = __umulhi(0xD2511F53u, c.x), lo_a = 0xD2511F53u * c.x;
+    const uint32_t hi_b = __umulhi(0xCD9E8D57u, c.z), lo_b = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi_b ^ c.y ^ k.x, lo_b, hi_a ^ c.w ^ k.y, lo_a);
+  }
+  return c;
+}
+// 24-bit dyadic uniform in [0, 1), exact in fp32
+__device__ __forceinline__ float uniform24(uint32_t w) { return (float)(w >> 8) * (1.0f / 16777216.0f); }
+
+__device__ __forceinline__ uint4 step_uniform_words(unsigned long long seed, uint32_t request,
+                                                    uint32_t position, uint32_t stream) {
+  return philox4x32_10(make_uint4(position, request, stream, 0u),
+                       make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+}
+
+// ---- shared-memory barriers and bulk copies ----------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+                   smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// non-blocking probe of a phase (no suspension)
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: gives up after kWaitLimitNs or when another CTA raised the
+// abort flag; returns false then.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile uint32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// named barrier over the finisher group only
+__device__ __forceinline__ void fin_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// GPU-scope acquire-release fence (orders this thread's, and what it has
+// observed of its CTA's, memory operations against other CTAs)
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// ---- warp collectives ---------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    float n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+__device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
+  uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
+  uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
+  return ((unsigned long long)hi << 32) | lo;
+}
+
+// Bitonic sort of 64 composites held two per lane (element e = lane + 32*r),
+// descending: afterwards lane l holds ranks l (a) and l + 32 (b).
+__device__ __forceinline__ void warp_sort64_desc(unsigned long long& a, unsigned long long& b, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 64; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      if (stride == 32) {
+        // partners are the two registers of one lane; size == 64: all descending
+        unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+        a = hi;
+        b = lo;
+      } else {
+        const bool lower = (lane & stride) == 0;
+        {
+          const int e = lane;
+          const bool desc = (e & size) == 0;
+          unsigned long long o = shfl_xor_u64(a, stride);
+          unsigned long long mx = a > o ? a : o, mn = a > o ? o : a;
+          a = (lower == desc) ? mx : mn;
+        }
+        {
+          const int e = lane + 32;
+          const bool desc = (e & size) == 0;
+          unsigned long long o = shfl_xor_u64(b, stride);
+          unsigned long long mx = b > o ? b : o, mn = b > o ? o : b;
+          b = (lower == desc) ? mx : mn;
+        }
+      }
+    }
+  }
+}
+
+// Bitonic sort of 32 (key, weight) pairs across a warp, ascending by key.
+__device__ __forceinline__ void warp_sort32_asc(int32_t& key, float& w, int lane) {
+#pragma unroll
+  for (int size = 2; size <= 32; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      const bool lower = (lane & stride) == 0;
+      const bool asc = (lane & size) == 0 || size == 32;
+      int32_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
+      float ow = __shfl_xor_sync(0xffffffffu, w, stride);
+      const bool take_small = (lower == asc);
+      const bool other_smaller = ok < key;
+      if (take_small == other_smaller && ok != key) {
+        key = ok;
+        w = ow;
+      }
+    }
+  }
+}
+
+}  // namespace dflash

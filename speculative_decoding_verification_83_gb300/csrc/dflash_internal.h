@@ -1,0 +1,135 @@
+// dflash_internal.h -- shapes, workspace layout and kernel parameters shared by
+// the host side (dflash_abi.cu) and the kernels (dflash_sweep.cu).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace dflash {
+
+// ---- fixed tiling -------------------------------------------------------------
+// One "piece" is a 16 KB contiguous run of a row's 16-byte-aligned body, moved
+// into shared memory by one bulk (TMA) copy. 256 consumer threads read it as
+// 1024 16-byte vectors, thread t taking vectors t, t+256, t+512, t+768. A
+// "tile" is what 8 neighbouring consumer lanes read: 32 vectors (256 bf16 or
+// 128 fp32 logits); its largest logit is recorded for the row-level selection.
+//
+// A CTA (one per SM) has three roles: warps 0-7 consume pieces, warp 8 is the
+// producer (bulk copies), warps 9-12 are the finisher group (publishes
+// finished pieces to the other CTAs, runs row and request finals).
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kFinWarps = 4;
+constexpr int kFin = kFinWarps * 32;
+constexpr int kFinBase = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = kFinBase + kFin;
+constexpr int kPieceBytes = 16384;
+constexpr int kVecPerPiece = kPieceBytes / 16;
+constexpr int kVecPerThread = kVecPerPiece / kConsumers;
+constexpr int kTileLanes = 8;
+constexpr int kTilesPerPiece = kConsumers / kTileLanes;
+constexpr int kStages = 8;       // ring of bulk-copy stages
+constexpr int kKeyQueue = 32;    // pieces the finisher group may lag behind
+constexpr int kCtasPerSm = 1;
+
+constexpr int kMaxTopK = 32;     // one kept token per lane of a warp
+constexpr int kCandCap = 64;     // candidates sorted in registers (2 per lane)
+constexpr int kCandTileCap = 128;
+constexpr int kKeyCache = 2048;  // tile keys of one row cached in shared memory
+constexpr int kMaxGamma = 32;
+constexpr int kMaxRowsPerRequest = 2 * kMaxGamma + 1;
+constexpr int kMaxB = 2048;
+
+enum Task : int { kTaskVerify = 0, kTaskVerifyGreedy = 1, kTaskFilter = 2, kTaskSample = 3 };
+
+// Row geometry: the head (elements before the first 16-byte boundary) and
+// tail (after the last one) are read with plain loads by the row-final stage;
+// the body goes through the pieces. Rows of one tensor may have different
+// heads when V * element size is not a multiple of 16, so every count is per
+// row and ppr (pieces per row) is the maximum over rows.
+struct Geometry {
+  int V;
+  int esize;     // 2 (bf16) or 4 (fp32)
+  int ppr;       // pieces per row (>= 1)
+  int tiles;     // ppr * kTilesPerPiece
+};
+
+struct Params {
+  // inputs
+  const unsigned char* target;  // verify: [B, gamma+1, V]; rows tasks: [R, V]
+  const unsigned char* draft;   // verify: [B, gamma, V]
+  const int32_t* draft_tokens;  // [B, gamma]
+  const float* temperature;     // [B] or [R]
+  int B;                        // requests (verify) or rows (rows tasks)
+  int gamma;
+  int dtype;                    // 0 bf16, 1 fp32
+  int top_k;                    // effective k for sampling rows, 1..kMaxTopK
+  float top_p;
+  unsigned long long seed;
+  int task;
+  int row_base;                 // rows tasks: index of this launch's first row
+  Geometry geo;
+  // outputs
+  int32_t* out_tokens;
+  int32_t* out_len;
+  int32_t* out_idx;
+  float* out_prob;
+  int32_t* out_count;
+  uint32_t* status;
+  // workspace (zero-initialised once; counters reset by their last user)
+  uint32_t* row_cnt;    // [n_slots]
+  uint32_t* req_cnt;    // [B]
+  uint32_t* abort_flag; // [1]
+  uint32_t* tile_keys;  // [n_slots, geo.tiles]
+  uint32_t* res_key;    // [n_slots, kMaxTopK]
+  int32_t* res_idx;     // [n_slots, kMaxTopK]
+  uint32_t* res_flag;   // [n_slots]
+  int n_slots;
+};
+
+struct WorkspaceLayout {
+  size_t row_cnt, req_cnt, abort_flag, tile_keys, res_key, res_idx, res_flag, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline Geometry make_geometry(int V, int esize) {
+  Geometry g;
+  g.V = V;
+  g.esize = esize;
+  long long body_vec_max = (long long)V * esize / 16;
+  long long ppr = (body_vec_max + kVecPerPiece - 1) / kVecPerPiece;
+  g.ppr = (int)(ppr < 1 ? 1 : ppr);
+  g.tiles = g.ppr * kTilesPerPiece;
+  return g;
+}
+
+// The hand-off counters live in a fixed header at the start of every
+// workspace, at offsets that do not depend on the call's shape: every call
+// returns the counters it used to zero, so a workspace stays ready for the
+// next call of any shape. The per-row data follows the header.
+constexpr int kMaxCounterSlots = kMaxB * kMaxRowsPerRequest;  // also the rows-task chunk
+
+inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g) {
+  (void)n_requests;
+  WorkspaceLayout L;
+  size_t off = 0;
+  L.req_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxB, 256);
+  L.row_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
+  L.abort_flag = off; off = align_up(off + sizeof(uint32_t), 256);
+  L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
+  L.res_key = off;    off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * kMaxTopK, 256);
+  L.res_idx = off;    off = align_up(off + sizeof(int32_t) * (size_t)n_slots * kMaxTopK, 256);
+  L.res_flag = off;   off = align_up(off + sizeof(uint32_t) * (size_t)n_slots, 256);
+  L.total = off;
+  return L;
+}
+
+// launches (dflash_sweep.cu); return a cudaError_t value
+int launch_sweep(const Params& p, int grid, void* stream);
+int sweep_smem_bytes();
+int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* out_accept,
+                    float* out_draw, void* stream);
+
+}  // namespace dflash

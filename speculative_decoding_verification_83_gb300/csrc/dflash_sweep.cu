@@ -1,0 +1,942 @@
+// dflash_sweep.cu -- the draft-verification step as one persistent kernel.
+//
+// Pass structure (one launch, one CTA per SM, three warp roles):
+//  1. Stream. Every row the step needs (target rows of every request, draft
+//     rows of sampling requests) is cut into 16 KB pieces of its aligned body.
+//     The producer warp moves pieces into an 8-stage shared-memory ring with
+//     1-D bulk copies (TMA). The 8 consumer warps reduce every 256-element
+//     tile of a piece to its largest logit (packed bf16x2 / fp32 max that
+//     propagates NaN) and store the tile's order key to the workspace. They
+//     never fence, never touch a global atomic and never wait on each other.
+//     Pieces are dealt round-robin to the CTAs, request by request, so rows
+//     complete progressively.
+//  2. Publish. The finisher group (4 warps) takes the pieces its consumers
+//     finished, in batches: one GPU-scope fence per batch, then one counter
+//     increment per piece on the piece's row. The increment that completes a
+//     row makes this CTA the row's finisher.
+//  3. Row final (finisher group): the row's top-k (k = 1 for greedy rows) in
+//     (logit desc, index asc) order. The k-th largest tile maximum tau is a
+//     lower bound of the row's k-th largest logit (the k tiles with the
+//     largest maxima hold k logits >= tau), so the top-k lies among the
+//     logits >= tau of the tiles whose maximum is >= tau: about k tiles,
+//     re-read from L2. The head and tail logits outside the aligned body are
+//     always candidates. A row whose ties leave too many candidates falls back
+//     to an exact radix selection over the whole row.
+//  4. Request final (finisher group of the CTA that completes a request's last
+//     row): filter the rows (temperature, softmax over the survivors, top-p,
+//     renormalise), run the accept test token by token with Philox uniforms,
+//     draw the residual or bonus token, write tokens and accept length.
+//     Greedy requests: argmax prefix match.
+// No CTA ever waits for another ("last arriver does the work" counters), so
+// there is no grid-wide barrier to deadlock; the only waits are on this CTA's
+// own shared-memory barriers and they are time-bounded.
+//
+// The method follows "DFlash2 用投机解码给 Qwen 提速" (bml.asia, draft/verify
+// loop and model-card settings) and "无损加速是真的吗？Qwen3.8-27B-DFlash2
+// 如何保证输出与目标模型完全一致" (rytg.cn, section 投机解码如何白嫖速度, step 3,
+// and the lossless definition), with the standard accept rule min(1, p/q),
+// residual max(0, p - q) and bonus token.
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+#include <cstdint>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+
+namespace dflash {
+namespace {
+
+constexpr uint32_t kStatusBadToken = 1u, kStatusBadRow = 2u, kStatusTimeout = 4u,
+                   kStatusBadTemperature = 8u;
+
+struct Smem {
+  alignas(128) unsigned char ring[kStages][kPieceBytes];
+  uint64_t full[kStages];       // ring stage loaded (producer expect_tx + bytes)
+  uint64_t empty[kStages];      // ring stage read (one arrival per consumer warp)
+  uint64_t kfull[kKeyQueue];    // piece's tile keys stored (one arrival per consumer warp)
+  uint64_t kempty[kKeyQueue];   // piece published (finisher leader)
+  int32_t req_of_ord[kMaxB];
+  union {
+    uint32_t key_cache[kKeyCache];
+    struct {
+      int32_t idx[kMaxRowsPerRequest][32];
+      float prob[kMaxRowsPerRequest][32];
+    } lists;
+  } u;
+  uint32_t hist[256];
+  unsigned long long cand[kCandCap];
+  int32_t cand_tiles[kCandTileCap];
+  int32_t done_slots[kKeyQueue];
+  uint32_t warp_red[kConsumerWarps];
+  int n_cand;
+  int n_cand_tiles;
+  int n_done;
+  int n_batch;
+  int flag;
+  int n_samp;
+  uint32_t digit;
+  uint32_t digit_above;
+  int bad_head_tail;
+  int fin_abort;
+};
+
+__device__ __forceinline__ bool sampling_temperature(float t) { return t > 0.0f && t < INFINITY; }
+
+// ---- row geometry ---------------------------------------------------------------
+struct RowBody {
+  const unsigned char* row;  // first logit of the row
+  int head;                  // logits before the first 16-byte boundary
+  int nvec;                  // 16-byte vectors of the body
+  int tail_start;            // first logit after the body
+};
+
+__device__ __forceinline__ RowBody row_body(const unsigned char* row, int V, int esize) {
+  RowBody r;
+  r.row = row;
+  const uint32_t mis = (uint32_t)((uintptr_t)row & 15u);
+  int head = (int)(((16u - mis) & 15u) / (uint32_t)esize);
+  if (head > V) head = V;
+  r.head = head;
+  r.nvec = (int)(((long long)(V - head) * esize) >> 4);
+  r.tail_start = head + r.nvec * (16 / esize);
+  return r;
+}
+
+__device__ __forceinline__ float load_logit(const unsigned char* row, int j, int dtype) {
+  if (dtype == 0) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + j);
+    return __uint_as_float((uint32_t)h << 16);
+  }
+  return __ldg(reinterpret_cast<const float*>(row) + j);
+}
+
+// ---- work enumeration -----------------------------------------------------------
+// Verification: requests are ordered sampling-first (by index), then greedy.
+// A sampling request owns 2*gamma+1 slots (target 0, draft 0, target 1, ...,
+// target gamma); a greedy one owns gamma+1 (its target rows). Rows tasks: slot
+// = row.
+struct SlotInfo {
+  int ord;        // request ordinal (verify) or row (rows tasks)
+  int r;          // row within the request
+  bool sampling;  // request samples (vs greedy)
+  const unsigned char* ptr;
+  int k_eff;
+};
+
+__device__ __forceinline__ SlotInfo slot_info(const Params& p, const Smem& S, int slot) {
+  SlotInfo s;
+  const size_t row_bytes = (size_t)p.geo.V * p.geo.esize;
+  if (p.task == kTaskVerify || p.task == kTaskVerifyGreedy) {
+    const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
+    const int samp_slots = S.n_samp * per_s;
+    if (slot < samp_slots) {
+      s.ord = slot / per_s;
+      s.r = slot - s.ord * per_s;
+      s.sampling = true;
+      const int b = S.req_of_ord[s.ord];
+      const int i = s.r >> 1;
+      if ((s.r & 1) == 0)
+        s.ptr = p.target + ((size_t)b * (p.gamma + 1) + i) * row_bytes;
+      else
+        s.ptr = p.draft + ((size_t)b * p.gamma + i) * row_bytes;
+      s.k_eff = p.top_k;
+    } else {
+      const int s2 = slot - samp_slots;
+      const int g = s2 / per_g;
+      s.ord = S.n_samp + g;
+      s.r = s2 - g * per_g;
+      s.sampling = false;
+      const int b = S.req_of_ord[s.ord];
+      s.ptr = p.target + ((size_t)b * (p.gamma + 1) + s.r) * row_bytes;
+      s.k_eff = 1;
+    }
+  } else {
+    s.ord = slot;
+    s.r = 0;
+    s.sampling = sampling_temperature(__ldg(p.temperature + slot));
+    s.ptr = p.target + (size_t)slot * row_bytes;
+    s.k_eff = s.sampling ? p.top_k : 1;
+  }
+  return s;
+}
+
+__device__ __forceinline__ int active_slots(const Params& p, const Smem& S) {
+  if (p.task == kTaskVerify || p.task == kTaskVerifyGreedy)
+    return S.n_samp * (2 * p.gamma + 1) + (p.B - S.n_samp) * (p.gamma + 1);
+  return p.B;
+}
+
+// Request order (sampling first), built by all threads of the CTA.
+__device__ void build_request_order(const Params& p, Smem& S) {
+  const int t = threadIdx.x;
+  if (p.task != kTaskVerify && p.task != kTaskVerifyGreedy) {
+    if (t == 0) S.n_samp = 0;
+    return;
+  }
+  const int B = p.B;
+  const int chunk = (B + kConsumers - 1) / kConsumers;
+  const int lo = min(B, t * chunk), hi = min(B, lo + chunk);
+  int mine = 0;
+  if (t < kConsumers && p.task == kTaskVerify)
+    for (int b = lo; b < hi; ++b) mine += sampling_temperature(__ldg(p.temperature + b)) ? 1 : 0;
+  // exclusive scan of per-thread counts over the 256 consumer threads
+  const int lane = t & 31, warp = t >> 5;
+  int incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31 && warp < kConsumerWarps) S.warp_red[warp] = (uint32_t)incl;
+  __syncthreads();
+  int warp_base = 0, total = 0;
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    if (w < warp) warp_base += (int)S.warp_red[w];
+    total += (int)S.warp_red[w];
+  }
+  if (t < kConsumers) {
+    int samp_before = warp_base + incl - mine;
+    int greedy_before = lo - samp_before;
+    for (int b = lo; b < hi; ++b) {
+      const bool s = p.task == kTaskVerify && sampling_temperature(__ldg(p.temperature + b));
+      if (s)
+        S.req_of_ord[samp_before++] = b;
+      else
+        S.req_of_ord[total + greedy_before++] = b;
+    }
+  }
+  if (t == 0) S.n_samp = total;
+  __syncthreads();
+}
+
+// ---- finisher-group helpers (128 threads, gt = thread index in the group) --------
+__device__ __forceinline__ int fin_tid() { return (int)threadIdx.x - kFinBase; }
+
+__device__ __forceinline__ uint32_t fin_max_u32(Smem& S, uint32_t v) {
+  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
+  v = warp_max_u32(v);
+  if (lane == 0) S.warp_red[w] = v;
+  fin_sync();
+  uint32_t r = 0;
+#pragma unroll
+  for (int i = 0; i < kFinWarps; ++i) r = max(r, S.warp_red[i]);
+  fin_sync();
+  return r;
+}
+
+// Finds, in S.hist, the digit holding the krem-th largest element (counts
+// from the top); sets S.digit and S.digit_above (elements in larger digits).
+// Run by the group's first warp.
+__device__ __forceinline__ void find_digit(Smem& S, uint32_t krem) {
+  const int gt = fin_tid(), lane = gt & 31;
+  if (gt < 32) {
+    uint32_t c[8];
+    uint32_t s = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      c[i] = S.hist[lane * 8 + i];
+      s += c[i];
+    }
+    uint32_t v = s;  // sum over lanes >= lane
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t n = __shfl_down_sync(0xffffffffu, v, o);
+      if (lane + o < 32) v += n;
+    }
+    const uint32_t above = v - s;
+    const bool here = above < krem && krem <= v;
+    const uint32_t ball = __ballot_sync(0xffffffffu, here);
+    if (here && lane == 31 - __clz(ball)) {
+      uint32_t acc = above;
+      uint32_t d = (uint32_t)lane * 8u;
+      for (int i = 7; i >= 0; --i) {
+        if (acc + c[i] >= krem) {
+          d = (uint32_t)lane * 8u + (uint32_t)i;
+          break;
+        }
+        acc += c[i];
+      }
+      S.digit = d;
+      S.digit_above = acc;
+    }
+    if (ball == 0u && lane == 0) {  // krem exceeds the count: cannot happen for valid k
+      S.digit = 0;
+      S.digit_above = 0;
+    }
+  }
+}
+
+// The k-th largest of n uint32 keys (MSB-first radix select, 8-bit digits).
+// Keys come from the shared cache when it holds them, else from global (L2).
+__device__ uint32_t select_kth_key(Smem& S, const uint32_t* gkeys, int n, bool cached, int k) {
+  const int gt = fin_tid();
+  uint32_t prefix = 0, mask = 0, krem = (uint32_t)k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    S.hist[gt] = 0u;
+    S.hist[gt + kFin] = 0u;
+    fin_sync();
+    for (int i = gt; i < n; i += kFin) {
+      const uint32_t key = cached ? S.u.key_cache[i] : __ldcg(gkeys + i);
+      if ((key & mask) == prefix) atomicAdd(&S.hist[(key >> shift) & 255u], 1u);
+    }
+    fin_sync();
+    find_digit(S, krem);
+    fin_sync();
+    krem -= S.digit_above;
+    prefix |= S.digit << shift;
+    mask |= 255u << shift;
+  }
+  return prefix;
+}
+
+// Visits every logit of a row with key >= tau (head, body, tail), finisher
+// threads in parallel. Used by the exact fallback when the tile filter leaves
+// too many candidates (heavily tied rows).
+template <class F>
+__device__ __forceinline__ void for_each_row_logit(const RowBody& rb, int V, int dtype, uint32_t tau, F&& f) {
+  const int gt = fin_tid();
+  const int esize = dtype == 0 ? 2 : 4;
+  const int per_vec = 16 / esize;
+  for (int j = gt; j < rb.head; j += kFin) {
+    uint32_t k = key_of(load_logit(rb.row, j, dtype));
+    if (k >= tau) f(k, j);
+  }
+  for (int j = rb.tail_start + gt; j < V; j += kFin) {
+    uint32_t k = key_of(load_logit(rb.row, j, dtype));
+    if (k >= tau) f(k, j);
+  }
+  const uint4* body = reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * esize);
+  for (int v = gt; v < rb.nvec; v += kFin) {
+    const uint4 w = __ldg(body + v);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    const int base = rb.head + v * per_vec;
+    if (dtype == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t h = (ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu;
+        const uint32_t k = key_of(__uint_as_float(h << 16));
+        if (k >= tau) f(k, base + e);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t k = key_of(__uint_as_float(ws[e]));
+        if (k >= tau) f(k, base + e);
+      }
+    }
+  }
+}
+
+// ---- row final ----------------------------------------------------------------------
+// Leaves the row's sorted top-k composites in the group's first warp (lane l:
+// rank l in `top_a`) and in the workspace.
+__device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si, unsigned long long& top_a) {
+  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
+  const int V = p.geo.V, dtype = p.dtype;
+  const RowBody rb = row_body(si.ptr, V, p.geo.esize);
+  const int n_tiles = p.geo.tiles;
+  const uint32_t* gkeys = p.tile_keys + (size_t)slot * n_tiles;
+  const bool cached = n_tiles <= kKeyCache;
+  const int k = si.k_eff;
+
+  // tile keys (cache), largest key, head/tail NaN check
+  uint32_t mx = 0u;
+  for (int i = gt; i < n_tiles; i += kFin) {
+    const uint32_t key = __ldcg(gkeys + i);
+    if (cached) S.u.key_cache[i] = key;
+    mx = max(mx, key);
+  }
+  const uint32_t tile_max = fin_max_u32(S, mx);  // includes syncs
+  const int n_edge = rb.head + (V - rb.tail_start);
+  bool edge_nan = false;
+  uint32_t emx = 0u;
+  if (gt < n_edge) {
+    const int j = gt < rb.head ? gt : rb.tail_start + (gt - rb.head);
+    const float x = load_logit(rb.row, j, dtype);
+    edge_nan = isnan(x);
+    emx = key_of(x);
+  }
+  if (gt == 0) S.bad_head_tail = 0;
+  fin_sync();
+  if (edge_nan) S.bad_head_tail = 1;
+  const uint32_t row_max = max(tile_max, fin_max_u32(S, emx));
+  const bool bad = !key_is_finite(row_max) || S.bad_head_tail != 0;
+
+  // tau: the k-th largest tile maximum (0 keeps everything when tiles < k)
+  uint32_t tau = 0u;
+  if (k == 1)
+    tau = tile_max;
+  else if (n_tiles >= k)
+    tau = select_kth_key(S, gkeys, n_tiles, cached, k);
+
+  if (gt == 0) {
+    S.n_cand_tiles = 0;
+    S.n_cand = 0;
+  }
+  fin_sync();
+  for (int i = gt; i < n_tiles; i += kFin) {
+    const uint32_t key = cached ? S.u.key_cache[i] : __ldcg(gkeys + i);
+    if (key >= tau) {
+      const int pos = atomicAdd(&S.n_cand_tiles, 1);
+      if (pos < kCandTileCap) S.cand_tiles[pos] = i;
+    }
+  }
+  fin_sync();
+  const int n_ct = S.n_cand_tiles;
+  bool overflow = n_ct > kCandTileCap;
+  if (!overflow) {
+    // gather: one warp per candidate tile, lane l reads vector (g*8 + l%8) + 256*(l/8)
+    const int esize = p.geo.esize, per_vec = 16 / esize;
+    const uint4* body = reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * esize);
+    for (int c = w; c < n_ct; c += kFinWarps) {
+      const int tile = S.cand_tiles[c];
+      const int piece = tile / kTilesPerPiece, g = tile - piece * kTilesPerPiece;
+      const int v = piece * kVecPerPiece + g * kTileLanes + (lane & 7) + kConsumers * (lane >> 3);
+      if (v < rb.nvec) {
+        const uint4 wv = __ldg(body + v);
+        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+        const int base = rb.head + v * per_vec;
+        for (int e = 0; e < per_vec; ++e) {
+          uint32_t key;
+          if (dtype == 0)
+            key = key_of(__uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16));
+          else
+            key = key_of(__uint_as_float(ws[e]));
+          if (key >= tau) {
+            const int pos = atomicAdd(&S.n_cand, 1);
+            if (pos < kCandCap) S.cand[pos] = composite(key, base + e);
+          }
+        }
+      }
+    }
+    if (gt < n_edge) {  // head and tail logits are always candidates
+      const int j = gt < rb.head ? gt : rb.tail_start + (gt - rb.head);
+      const int pos = atomicAdd(&S.n_cand, 1);
+      if (pos < kCandCap) S.cand[pos] = composite(key_of(load_logit(rb.row, j, dtype)), j);
+    }
+    fin_sync();
+    overflow = S.n_cand > kCandCap;
+  }
+  if (overflow) {
+    // exact fallback: radix-select the k-th largest composite over all logits >= tau
+    unsigned long long prefix = 0ull, mask = 0ull;
+    uint32_t krem = (uint32_t)k;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      S.hist[gt] = 0u;
+      S.hist[gt + kFin] = 0u;
+      fin_sync();
+      for_each_row_logit(rb, V, dtype, tau, [&](uint32_t key, int j) {
+        const unsigned long long c = composite(key, j);
+        if ((c & mask) == prefix) atomicAdd(&S.hist[(uint32_t)(c >> shift) & 255u], 1u);
+      });
+      fin_sync();
+      find_digit(S, krem);
+      fin_sync();
+      krem -= S.digit_above;
+      prefix |= (unsigned long long)S.digit << shift;
+      mask |= 255ull << shift;
+    }
+    if (gt == 0) S.n_cand = 0;
+    fin_sync();
+    const unsigned long long thr = prefix;
+    for_each_row_logit(rb, V, dtype, tau, [&](uint32_t key, int j) {
+      const unsigned long long c = composite(key, j);
+      if (c >= thr) {
+        const int pos = atomicAdd(&S.n_cand, 1);
+        if (pos < kCandCap) S.cand[pos] = c;
+      }
+    });
+    fin_sync();
+  }
+  // sort the (<= 64) candidates in the first warp; ranks < k are the row's top-k
+  const int n_c = min(S.n_cand, kCandCap);
+  if (w == 0) {
+    unsigned long long a = lane < n_c ? S.cand[lane] : 0ull;
+    unsigned long long b = lane + 32 < n_c ? S.cand[lane + 32] : 0ull;
+    warp_sort64_desc(a, b, lane);
+    top_a = a;
+    // workspace copy of ranks < k (k <= 32): the request final reads it
+    const bool valid = lane < k && lane < n_c;
+    p.res_key[(size_t)slot * kMaxTopK + lane] = valid ? composite_key(a) : 0u;
+    p.res_idx[(size_t)slot * kMaxTopK + lane] = valid ? composite_idx(a) : -1;
+    if (lane == 0) p.res_flag[slot] = bad ? 1u : 0u;
+    if (bad && lane == 0 && p.status) atomicOr(p.status, kStatusBadRow);
+  }
+  fin_sync();
+}
+
+// ---- filtering and drawing ---------------------------------------------------------
+// Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
+// over the survivors, top-p cut, renormalisation. Returns this lane's
+// probability (0 outside the kept set) and sets idx to -1 there.
+__device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
+                                             int lane) {
+  const bool in_k = lane < k_eff && idx >= 0;
+  const float x = value_of_key(key);
+  const float z = x / T;
+  const float z0 = __shfl_sync(0xffffffffu, z, 0);
+  const float w = in_k ? expf(z - z0) : 0.0f;
+  bool keep = in_k;
+  if (top_p < 1.0f) {
+    const float W = warp_sum(w);
+    const float pi = w / W;
+    const float incl = warp_inclusive_scan(pi, lane);
+    float before = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) before = 0.0f;
+    keep = keep && (before < top_p);
+  }
+  const float wk = keep ? w : 0.0f;
+  const float Wk = warp_sum(wk);
+  if (!keep) idx = -1;
+  return keep ? wk / Wk : 0.0f;
+}
+
+// Inverse CDF in ascending token order: the smallest token whose cumulative
+// weight exceeds u * total; if rounding leaves none, the last token with
+// positive weight; tokens marked -1 have no weight.
+__device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane) {
+  int32_t key = tok >= 0 ? tok : INT_MAX;
+  float wt = tok >= 0 ? w : 0.0f;
+  warp_sort32_asc(key, wt, lane);
+  const float cum = warp_inclusive_scan(wt, lane);
+  const float total = __shfl_sync(0xffffffffu, cum, 31);
+  const float t = u * total;
+  const uint32_t hit = __ballot_sync(0xffffffffu, wt > 0.0f && t < cum);
+  int chosen;
+  if (hit) {
+    chosen = __ffs(hit) - 1;
+  } else {
+    const uint32_t pos = __ballot_sync(0xffffffffu, wt > 0.0f);
+    chosen = pos ? 31 - __clz(pos) : 0;
+  }
+  const int32_t r = __shfl_sync(0xffffffffu, key, chosen);
+  return r == INT_MAX ? -1 : r;
+}
+
+// ---- request final (verification) --------------------------------------------------
+__device__ void request_final(const Params& p, Smem& S, int ord) {
+  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
+  const int gamma = p.gamma, V = p.geo.V;
+  const int b = S.req_of_ord[ord];
+  const bool sampling = ord < S.n_samp;
+  int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
+  const int32_t* d = p.draft_tokens + (size_t)b * gamma;
+  const int per_s = 2 * gamma + 1, per_g = gamma + 1;
+
+  if (!sampling) {
+    if (w == 0) {
+      const int slot0 = S.n_samp * per_s + (ord - S.n_samp) * per_g;
+      uint32_t st = 0;
+      if (p.task == kTaskVerify && __ldg(p.temperature + b) != 0.0f) st |= kStatusBadTemperature;
+      int n = gamma;  // length of the matching prefix
+      for (int base = 0; base <= gamma; base += 32) {
+        const int i = base + lane;
+        int32_t a = -1;
+        bool mismatch = false;
+        if (i <= gamma) {
+          a = __ldcg(p.res_idx + (size_t)(slot0 + i) * kMaxTopK);
+          if (__ldcg(p.res_flag + slot0 + i)) st |= kStatusBadRow;
+        }
+        if (i < gamma) {
+          const int32_t di = __ldg(d + i);
+          if (di < 0 || di >= V) st |= kStatusBadToken;
+          mismatch = di != a;
+        }
+        const uint32_t mm = __ballot_sync(0xffffffffu, mismatch);
+        if (mm && n == gamma) n = base + __ffs(mm) - 1;
+      }
+      for (int base = 0; base <= gamma; base += 32) {
+        const int i = base + lane;
+        if (i <= gamma) {
+          int32_t v = -1;
+          if (i < n)
+            v = __ldg(d + i);
+          else if (i == n)
+            v = __ldcg(p.res_idx + (size_t)(slot0 + i) * kMaxTopK);
+          out[i] = v;
+        }
+      }
+      st = __reduce_or_sync(0xffffffffu, st);
+      if (lane == 0) {
+        p.out_len[b] = n + 1;
+        if (st && p.status) atomicOr(p.status, st);
+      }
+    }
+    fin_sync();
+    return;
+  }
+
+  // sampling request: filter every row into shared lists (warps in parallel)
+  const int slot0 = ord * per_s;
+  const float T = __ldg(p.temperature + b);
+  for (int r = w; r < per_s; r += kFinWarps) {
+    const size_t s = (size_t)(slot0 + r);
+    uint32_t key = lane < p.top_k ? __ldcg(p.res_key + s * kMaxTopK + lane) : 0u;
+    int32_t idx = lane < p.top_k ? __ldcg(p.res_idx + s * kMaxTopK + lane) : -1;
+    const float pr = filter_lane(key, idx, p.top_k, T, p.top_p, lane);
+    S.u.lists.idx[r][lane] = idx;
+    S.u.lists.prob[r][lane] = pr;
+  }
+  fin_sync();
+  if (w == 0) {
+    uint32_t st = 0;
+    for (int r = lane; r < per_s; r += 32)
+      if (__ldcg(p.res_flag + slot0 + r)) st |= kStatusBadRow;
+    int n = 0;
+    int32_t last = -1;
+    bool rejected = false;
+    for (int i = 0; i < gamma; ++i) {
+      const int32_t di = __ldg(d + i);
+      if (di < 0 || di >= V) st |= kStatusBadToken;
+      const int32_t ti = S.u.lists.idx[2 * i][lane];
+      const float pi = S.u.lists.prob[2 * i][lane];
+      const int32_t qi_idx = S.u.lists.idx[2 * i + 1][lane];
+      const float qi = S.u.lists.prob[2 * i + 1][lane];
+      const uint32_t hp = __ballot_sync(0xffffffffu, ti == di && di >= 0);
+      const uint32_t hq = __ballot_sync(0xffffffffu, qi_idx == di && di >= 0);
+      const float p_d = hp ? __shfl_sync(0xffffffffu, pi, __ffs(hp) - 1) : 0.0f;
+      const float q_d = hq ? __shfl_sync(0xffffffffu, qi, __ffs(hq) - 1) : 0.0f;
+      const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
+      const float u = uniform24(wd.x);
+      const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
+      if (u < ratio) {
+        ++n;
+        continue;
+      }
+      // residual max(0, p - q) over the target's kept tokens
+      float q_of_t = 0.0f;
+      for (int m = 0; m < 32; ++m) {
+        const int32_t qm = S.u.lists.idx[2 * i + 1][m];
+        if (qm == ti && ti >= 0) q_of_t = S.u.lists.prob[2 * i + 1][m];
+      }
+      const float r = ti >= 0 ? fmaxf(pi - q_of_t, 0.0f) : 0.0f;
+      const bool any = __ballot_sync(0xffffffffu, r > 0.0f) != 0u;
+      last = draw_ascending(ti, any ? r : pi, uniform24(wd.y), lane);
+      if (last < 0) last = __shfl_sync(0xffffffffu, ti, 0);
+      rejected = true;
+      break;
+    }
+    if (!rejected) {
+      const int32_t tg = S.u.lists.idx[2 * gamma][lane];
+      const float pg = S.u.lists.prob[2 * gamma][lane];
+      const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)gamma, 0u);
+      last = draw_ascending(tg, pg, uniform24(wd.y), lane);
+      if (last < 0) last = __shfl_sync(0xffffffffu, tg, 0);
+    }
+    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? last : -1);
+    st = __reduce_or_sync(0xffffffffu, st);
+    if (lane == 0) {
+      p.out_len[b] = n + 1;
+      if (st && p.status) atomicOr(p.status, st);
+    }
+  }
+  fin_sync();
+}
+
+// ---- row final of the rows tasks: filtered distribution / one sample ----------------
+__device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long top_a) {
+  const int gt = fin_tid(), lane = gt & 31;
+  if ((gt >> 5) == 0) {
+    const float T = __ldg(p.temperature + r);
+    const bool samp = sampling_temperature(T);
+    const uint32_t st = (!samp && T != 0.0f) ? kStatusBadTemperature : 0u;
+    const int k_eff = samp ? p.top_k : 1;
+    const int n_c = min(S.n_cand, kCandCap);
+    const uint32_t key = (lane < k_eff && lane < n_c) ? composite_key(top_a) : 0u;
+    int32_t idx = (lane < k_eff && lane < n_c) ? composite_idx(top_a) : -1;
+    float pr;
+    if (samp) {
+      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane);
+    } else {
+      pr = lane == 0 ? 1.0f : 0.0f;
+      if (lane != 0) idx = -1;
+    }
+    if (p.task == kTaskFilter) {
+      const int cnt = __popc(__ballot_sync(0xffffffffu, idx >= 0));
+      if (lane < p.top_k) {
+        p.out_idx[(size_t)r * p.top_k + lane] = idx;
+        p.out_prob[(size_t)r * p.top_k + lane] = idx >= 0 ? pr : 0.0f;
+      }
+      if (lane == 0) p.out_count[r] = cnt;
+    } else {
+      int32_t tok;
+      if (samp) {
+        const uint4 wd = step_uniform_words(p.seed, 0u, (uint32_t)(p.row_base + r), 1u);
+        tok = draw_ascending(idx, pr, uniform24(wd.x), lane);
+        if (tok < 0) tok = __shfl_sync(0xffffffffu, idx, 0);
+      } else {
+        tok = __shfl_sync(0xffffffffu, idx, 0);
+      }
+      if (lane == 0) p.out_tokens[r] = tok;
+    }
+    if (lane == 0 && st && p.status) atomicOr(p.status, st);
+  }
+  fin_sync();
+}
+
+// ---- roles ---------------------------------------------------------------------------
+__device__ __forceinline__ void raise_timeout(const Params& p) {
+  atomicExch(p.abort_flag, 1u);
+  if (p.status) atomicOr(p.status, kStatusTimeout);
+}
+
+__device__ void producer(const Params& p, Smem& S, long long total) {
+  const int lane = threadIdx.x & 31;
+  if (lane != 0) return;
+  const volatile uint32_t* abort_flag = p.abort_flag;
+  const int ppr = p.geo.ppr;
+  int it = 0;
+  bool aborted = false;
+  for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it) {
+    const int stage = it % kStages;
+    const uint32_t round = (uint32_t)(it / kStages);
+    if (!mbar_wait(&S.empty[stage], (round & 1u) ^ 1u, abort_flag)) {
+      aborted = true;
+      break;
+    }
+    const int slot = (int)(piece / ppr), pp = (int)(piece - (long long)slot * ppr);
+    const SlotInfo si = slot_info(p, S, slot);
+    const RowBody rb = row_body(si.ptr, p.geo.V, p.geo.esize);
+    const int v0 = pp * kVecPerPiece;
+    const int nvec = max(0, min(kVecPerPiece, rb.nvec - v0));
+    if (nvec > 0) {
+      mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec * 16u);
+      bulk_load(S.ring[stage], rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16, (uint32_t)nvec * 16u,
+                &S.full[stage]);
+    } else {
+      mbar_arrive(&S.full[stage]);
+    }
+  }
+  if (aborted) {
+    // let copies already issued land before the CTA's shared memory goes away
+    const int first = max(0, it - kStages);
+    for (int j = first; j < it; ++j)
+      (void)mbar_wait(&S.full[j % kStages], (uint32_t)((j / kStages) & 1), abort_flag);
+  }
+}
+
+template <int DT>
+__device__ void consumer(const Params& p, Smem& S, long long total) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const volatile uint32_t* abort_flag = p.abort_flag;
+  const int ppr = p.geo.ppr;
+  int it = 0;
+  for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it) {
+    const int stage = it % kStages;
+    const int q = it % kKeyQueue;
+    const int slot = (int)(piece / ppr), pp = (int)(piece - (long long)slot * ppr);
+    const bool landed = mbar_wait(&S.full[stage], (uint32_t)(it / kStages) & 1u, abort_flag);
+    if (!__all_sync(0xffffffffu, landed)) {
+      if (lane == 0) raise_timeout(p);
+      return;
+    }
+    const SlotInfo si = slot_info(p, S, slot);
+    const RowBody rb = row_body(si.ptr, p.geo.V, p.geo.esize);
+    const int nvec = max(0, min(kVecPerPiece, rb.nvec - pp * kVecPerPiece));
+
+    // tile maximum of this thread's 4 vectors, then of its 8-lane group
+    const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
+    float m;
+    if (DT == 0) {
+      __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+#pragma unroll
+      for (int j = 0; j < kVecPerThread; ++j) {
+        const int v = tid + kConsumers * j;
+        if (v < nvec) {
+          const uint4 wv = st4[v];
+          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.x));
+          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.z));
+          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
+        }
+      }
+      m = max_nan(__low2float(m2), __high2float(m2));
+    } else {
+      m = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < kVecPerThread; ++j) {
+        const int v = tid + kConsumers * j;
+        if (v < nvec) {
+          const float4 wv = reinterpret_cast<const float4*>(st4)[v];
+          m = max_nan(m, max_nan(max_nan(wv.x, wv.y), max_nan(wv.z, wv.w)));
+        }
+      }
+    }
+    uint32_t key = key_of(m);
+    key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+    key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+    key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
+    if ((lane & (kTileLanes - 1)) == 0)
+      p.tile_keys[(size_t)slot * p.geo.tiles + pp * kTilesPerPiece + (tid >> 3)] = key;
+    __syncwarp();  // orders the key stores before lane 0's arrival below
+    int ok = 1;
+    if (lane == 0) {
+      // the finisher must have taken queue slot q's previous piece
+      if (!mbar_wait(&S.kempty[q], ((uint32_t)(it / kKeyQueue) & 1u) ^ 1u, abort_flag)) {
+        raise_timeout(p);
+        ok = 0;
+      } else {
+        mbar_arrive(&S.kfull[q]);
+      }
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+  }
+}
+
+__device__ void finisher(const Params& p, Smem& S, long long total) {
+  const int gt = fin_tid();
+  const int ppr = p.geo.ppr;
+  const volatile uint32_t* abort_flag = p.abort_flag;
+  const long long mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  long long q = 0;
+  if (gt == 0) S.fin_abort = 0;
+  fin_sync();
+  while (q < mine) {
+    if (gt == 0) {
+      // batch: the oldest unpublished piece, plus every later one already stored
+      int n = 0;
+      if (mbar_wait(&S.kfull[q % kKeyQueue], (uint32_t)((q / kKeyQueue) & 1), abort_flag)) {
+        n = 1;
+        while (q + n < mine && n < kKeyQueue &&
+               mbar_test_wait(&S.kfull[(q + n) % kKeyQueue], (uint32_t)(((q + n) / kKeyQueue) & 1)))
+          ++n;
+      }
+      if (n == 0) {
+        raise_timeout(p);
+        S.fin_abort = 1;
+      } else {
+        fence_acq_rel_gpu();  // release the batch's tile keys to the other CTAs
+        uint32_t old[kKeyQueue];
+#pragma unroll
+        for (int j = 0; j < kKeyQueue; ++j) {
+          if (j < n) {
+            const long long piece = blockIdx.x + (q + j) * (long long)gridDim.x;
+            const int slot = (int)(piece / ppr);
+            old[j] = atomicAdd(p.row_cnt + slot, 1u);
+          }
+        }
+        int m = 0;
+#pragma unroll
+        for (int j = 0; j < kKeyQueue; ++j) {
+          if (j < n) {
+            const long long piece = blockIdx.x + (q + j) * (long long)gridDim.x;
+            const int slot = (int)(piece / ppr);
+            if (old[j] == (uint32_t)(ppr - 1)) {
+              S.done_slots[m++] = slot;
+              p.row_cnt[slot] = 0u;  // ready for the next call
+            }
+            mbar_arrive(&S.kempty[(q + j) % kKeyQueue]);
+          }
+        }
+        if (m > 0) fence_acq_rel_gpu();  // acquire the other CTAs' keys of the finished rows
+        S.n_done = m;
+        S.n_batch = n;
+      }
+    }
+    fin_sync();
+    if (S.fin_abort) return;
+    const int n_done = S.n_done;
+    q += S.n_batch;
+    for (int j = 0; j < n_done; ++j) {
+      const int slot = S.done_slots[j];
+      const SlotInfo si = slot_info(p, S, slot);
+      unsigned long long top_a = 0ull;
+      row_final(p, S, slot, si, top_a);
+      if (p.task == kTaskFilter || p.task == kTaskSample) {
+        rows_final(p, S, slot, top_a);
+        continue;
+      }
+      // request hand-off: the CTA finishing the request's last row runs its final
+      const int b = S.req_of_ord[si.ord];
+      const int rows = si.sampling ? 2 * p.gamma + 1 : p.gamma + 1;
+      if (gt == 0) {
+        fence_acq_rel_gpu();  // release this row's results
+        const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(rows - 1);
+        if (last) {
+          p.req_cnt[b] = 0u;
+          fence_acq_rel_gpu();  // acquire the request's other rows
+        }
+        S.flag = last ? 1 : 0;
+      }
+      fin_sync();
+      if (S.flag) request_final(p, S, si.ord);
+    }
+    fin_sync();  // S.done_slots / S.n_done are rewritten by the next batch
+  }
+}
+
+// ---- the kernel ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  const int tid = threadIdx.x, warp = tid >> 5;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], kConsumerWarps);
+    }
+    for (int s = 0; s < kKeyQueue; ++s) {
+      mbar_init(&S.kfull[s], kConsumerWarps);
+      mbar_init(&S.kempty[s], 1);
+    }
+    fence_barrier_init();
+  }
+  build_request_order(p, S);  // contains __syncthreads
+  __syncthreads();
+  const long long total = (long long)active_slots(p, S) * p.geo.ppr;
+
+  if (warp < kConsumerWarps)
+    consumer<DT>(p, S, total);
+  else if (warp == kProducerWarp)
+    producer(p, S, total);
+  else
+    finisher(p, S, total);
+}
+
+__global__ void uniforms_kernel(unsigned long long seed, int B, int npos, int stream_id, float* ua, float* ud) {
+  const long long n = (long long)B * npos;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    const int b = (int)(i / npos), pos = (int)(i - (long long)b * npos);
+    const uint4 w = step_uniform_words(seed, (uint32_t)b, (uint32_t)pos, (uint32_t)stream_id);
+    if (ua) ua[i] = uniform24(w.x);
+    if (ud) ud[i] = uniform24(w.y);
+  }
+}
+
+}  // namespace
+
+int sweep_smem_bytes() { return (int)sizeof(Smem); }
+
+int launch_sweep(const Params& p, int grid, void* stream) {
+  const int smem = (int)sizeof(Smem);
+  cudaError_t e;
+  if (p.dtype == 0) {
+    e = cudaFuncSetAttribute(sweep_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    sweep_kernel<0><<<grid, kThreads, smem, (cudaStream_t)stream>>>(p);
+  } else {
+    e = cudaFuncSetAttribute(sweep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return (int)e;
+    sweep_kernel<1><<<grid, kThreads, smem, (cudaStream_t)stream>>>(p);
+  }
+  return (int)cudaGetLastError();
+}
+
+int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* ua, float* ud, void* stream) {
+  const long long n = (long long)B * npos;
+  if (n <= 0) return 0;
+  const int block = 256;
+  const int grid = (int)((n + block - 1) / block < 1024 ? (n + block - 1) / block : 1024);
+  uniforms_kernel<<<grid, block, 0, (cudaStream_t)stream>>>(seed, B, npos, stream_id, ua, ud);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -133,3 +133,14 @@ def make_workload(name: str, data_seed: int = 0, seed: int = 0, B: int | None = 
 def draft_sampling_temperatures(T: np.ndarray, gamma: int) -> np.ndarray:
     """Per-draft-row temperatures [B*gamma]: each request's temperature repeated."""
     return np.repeat(np.asarray(T, np.float32), gamma)
+
+
+def to_torch(a: np.ndarray, device="cuda"):
+    """A generated array as a torch tensor on ``device`` (uint16 bf16 bits
+    become torch.bfloat16 with the same bits)."""
+    import torch
+
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)

@@ -1,0 +1,72 @@
+"""The C-ABI library loads, exports every entry point include/dflash_verify.h
+declares, and rejects bad arguments on the host before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_83_gb300 as dv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "dflash_verify.h")
+
+
+def declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dflash_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    dv.build()
+    return dv.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in dv.EXPORTS, f"binding lacks {n}"
+    assert lib.dflash_abi_version() == 1
+
+
+def test_workspace_sizes(lib):
+    n = lib.dflash_workspace_bytes(32, 7, 248320, dv.DFLASH_BF16, 20, 0.95)
+    assert n > 0 and n % 256 == 0
+    assert lib.dflash_workspace_bytes(0, 7, 248320, 0, 20, 0.95) == 0
+    assert lib.dflash_workspace_bytes(32, 7, 248320, 7, 20, 0.95) == 0
+    assert lib.dflash_workspace_bytes(32, 7, 248320, 0, 64, 0.95) == 0   # top_k > 32
+    assert lib.dflash_rows_workspace_bytes(224, 248320, 0, 20, 0.95) > 0
+    assert lib.dflash_host_staging_bytes(32, 7, 248320, 0) >= 32 * 15 * 248320 * 2
+
+
+def _verify(lib, B=2, gamma=3, V=100, dtype=0, top_k=20, top_p=0.95, ptr=1 << 20):
+    # non-null fake pointers: argument checks run before any CUDA call
+    p = ctypes.c_void_p(ptr)
+    return lib.dflash_verify(p, p, p, B, gamma, V, dtype, p, top_k, top_p, 0, p, p, p, 1 << 30,
+                             None, None)
+
+
+def test_argument_checks_happen_on_the_host(lib):
+    assert _verify(lib, B=0) == dv.ERR_INVALID_ARG
+    assert b"B=0" in lib.dflash_last_error()
+    assert _verify(lib, gamma=0) == dv.ERR_INVALID_ARG
+    assert _verify(lib, gamma=33) == dv.ERR_INVALID_ARG
+    assert _verify(lib, V=0) == dv.ERR_INVALID_ARG
+    assert _verify(lib, dtype=5) == dv.ERR_INVALID_ARG
+    assert _verify(lib, top_p=0.0) == dv.ERR_INVALID_ARG
+    assert _verify(lib, top_p=float("nan")) == dv.ERR_INVALID_ARG
+    assert _verify(lib, top_k=33) == dv.ERR_UNSUPPORTED
+    assert _verify(lib, top_k=0, top_p=0.9) == dv.ERR_UNSUPPORTED      # full-vocab top-p
+    assert _verify(lib, dtype=1, ptr=(1 << 20) + 2) == dv.ERR_INVALID_ARG  # fp32 misaligned
+    n = ctypes.c_void_p(0)
+    assert lib.dflash_verify(n, n, n, 2, 3, 100, 0, n, 20, 0.95, 0, n, n, n, 0, None,
+                             None) == dv.ERR_INVALID_ARG
+    assert lib.dflash_uniforms(0, 0, 3, 0, None, None, None) == dv.ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        dv.load(str(tmp_path / "absent.so"))
