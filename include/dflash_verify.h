@@ -182,6 +182,30 @@ int dflash_sample(const void* logits, int R, int V, int dtype, const float* temp
 int dflash_uniforms(uint64_t seed, int B, int npos, int stream_id, float* out_accept,
                     float* out_draw, void* stream);
 
+/* dflash_verify without a caller-provided workspace, for callers that cannot
+ * allocate device memory: code running under another framework's memory pool
+ * that forbids foreign cudaMalloc calls, plugins loaded into a process whose
+ * allocator they do not own, or paths where an allocation (or the device-wide
+ * synchronisation a cudaFree can cause) is not allowed. The pages describe no
+ * such entry point; it is a convenience of this library.
+ *
+ * Scratch comes from a fixed array of dflash_noalloc_scratch_bytes() bytes
+ * (4 MiB) that the library keeps on every GPU that loads it, until the process
+ * exits. Shapes whose workspace (dflash_workspace_bytes) exceeds it return
+ * DFLASH_ERR_INVALID_ARG with a message naming the sizes. The first call on a
+ * device looks the array up with that device current; make that first call
+ * before any stream capture. Each call clears the array's counters on `stream`
+ * before the kernel runs, and every call on a device shares the one array:
+ * calls that may overlap on the GPU (other streams, other threads) race and
+ * must be ordered by the caller. Nothing here allocates or frees memory.
+ * Arguments and results as for dflash_verify. */
+size_t dflash_noalloc_scratch_bytes(void);
+int dflash_verify_noalloc(const void* target_logits, const void* draft_logits,
+                          const int32_t* draft_tokens, int B, int gamma, int V, int dtype,
+                          const float* temperature, int top_k, float top_p, uint64_t seed,
+                          int32_t* out_tokens, int32_t* out_accept_len, uint32_t* status,
+                          void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,7 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash_verify.so")
-SOURCES = ["dflash_sweep.cu", "dflash_abi.cu"]
+SOURCES = ["dflash_sweep.cu", "dflash_abi.cu", "dflash_noalloc.cu"]
 HEADERS = ["dflash_device.cuh", "dflash_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
@@ -102,6 +102,8 @@ EXPORTS = {
     "dflash_filter": ("i", "piiipifpppp" "zpp"),
     "dflash_sample": ("i", "piiipifQp" "pzpp"),
     "dflash_uniforms": ("i", "Qiiippp"),
+    "dflash_noalloc_scratch_bytes": ("z", ""),
+    "dflash_verify_noalloc": ("i", "pppiiiipifQpppp"),
 }
 _CT = {"i": ctypes.c_int, "p": ctypes.c_void_p, "z": ctypes.c_size_t, "f": ctypes.c_float,
        "Q": ctypes.c_uint64, "s": ctypes.c_char_p, "": None}

@@ -112,6 +112,8 @@ Params base_params(int dtype, int V) {
 
 }  // namespace
 
+void dflash::set_last_error(const char* msg) { snprintf(g_last_error, sizeof g_last_error, "%s", msg); }
+
 extern "C" {
 
 int dflash_abi_version(void) { return DFLASH_ABI_VERSION; }

@@ -126,6 +126,9 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   return L;
 }
 
+// sets the message dflash_last_error() returns on this thread (dflash_abi.cu)
+void set_last_error(const char* msg);
+
 // launches (dflash_sweep.cu); return a cudaError_t value
 int launch_sweep(const Params& p, int grid, void* stream);
 int sweep_smem_bytes();
