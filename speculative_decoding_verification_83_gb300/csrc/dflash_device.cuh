@@ -138,8 +138,18 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
       : "memory");
 }
 
-// named barrier over the finisher group only
+// named barrier over the finals group only
 __device__ __forceinline__ void fin_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// GPU-scope release store / acquire load of a flag word
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // GPU-scope acquire-release fence (orders this thread's, and what it has
 // observed of its CTA's, memory operations against other CTAs)

@@ -14,15 +14,16 @@ namespace dflash {
 // "tile" is what 8 neighbouring consumer lanes read: 32 vectors (256 bf16 or
 // 128 fp32 logits); its largest logit is recorded for the row-level selection.
 //
-// A CTA (one per SM) has three roles: warps 0-7 consume pieces, warp 8 is the
-// producer (bulk copies), warps 9-12 are the finisher group (publishes
-// finished pieces to the other CTAs, runs row and request finals).
+// A CTA (one per SM) has four roles: warps 0-7 consume pieces, warp 8 is the
+// producer (bulk copies), warp 9 publishes finished pieces to the other CTAs,
+// warps 10-13 are the finals group (row and request finals).
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kPublisherWarp = kConsumerWarps + 1;
 constexpr int kFinWarps = 4;
 constexpr int kFin = kFinWarps * 32;
-constexpr int kFinBase = (kConsumerWarps + 1) * 32;
+constexpr int kFinBase = (kConsumerWarps + 2) * 32;
 constexpr int kThreads = kFinBase + kFin;
 constexpr int kPieceBytes = 16384;
 constexpr int kVecPerPiece = kPieceBytes / 16;
@@ -30,7 +31,7 @@ constexpr int kVecPerThread = kVecPerPiece / kConsumers;
 constexpr int kTileLanes = 8;
 constexpr int kTilesPerPiece = kConsumers / kTileLanes;
 constexpr int kStages = 8;       // ring of bulk-copy stages
-constexpr int kKeyQueue = 32;    // pieces the finisher group may lag behind
+constexpr int kKeyQueue = 32;    // pieces the publisher may lag behind
 constexpr int kCtasPerSm = 1;
 
 constexpr int kMaxTopK = 32;     // one kept token per lane of a warp
@@ -81,6 +82,8 @@ struct Params {
   uint32_t* row_cnt;    // [n_slots]
   uint32_t* req_cnt;    // [B]
   uint32_t* abort_flag; // [1]
+  uint32_t* qcnt;       // [3]: rows queued, rows claimed, finals groups done
+  uint32_t* ready;      // [kMaxCounterSlots]: queued row slot + 1, 0 = empty
   uint32_t* tile_keys;  // [n_slots, geo.tiles]
   uint32_t* res_key;    // [n_slots, kMaxTopK]
   int32_t* res_idx;     // [n_slots, kMaxTopK]
@@ -89,7 +92,7 @@ struct Params {
 };
 
 struct WorkspaceLayout {
-  size_t row_cnt, req_cnt, abort_flag, tile_keys, res_key, res_idx, res_flag, total;
+  size_t row_cnt, req_cnt, abort_flag, qcnt, ready, tile_keys, res_key, res_idx, res_flag, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -105,10 +108,10 @@ inline Geometry make_geometry(int V, int esize) {
   return g;
 }
 
-// The hand-off counters live in a fixed header at the start of every
-// workspace, at offsets that do not depend on the call's shape: every call
-// returns the counters it used to zero, so a workspace stays ready for the
-// next call of any shape. The per-row data follows the header.
+// The hand-off counters and the queue of finished rows live in a fixed header
+// at the start of every workspace, at offsets that do not depend on the
+// call's shape: every call returns what it used to zero, so a workspace stays
+// ready for the next call of any shape. The per-row data follows the header.
 constexpr int kMaxCounterSlots = kMaxB * kMaxRowsPerRequest;  // also the rows-task chunk
 
 inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g) {
@@ -118,6 +121,8 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.req_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxB, 256);
   L.row_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
   L.abort_flag = off; off = align_up(off + sizeof(uint32_t), 256);
+  L.qcnt = off;       off = align_up(off + sizeof(uint32_t) * 3, 256);
+  L.ready = off;      off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
   L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
   L.res_key = off;    off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * kMaxTopK, 256);
   L.res_idx = off;    off = align_up(off + sizeof(int32_t) * (size_t)n_slots * kMaxTopK, 256);

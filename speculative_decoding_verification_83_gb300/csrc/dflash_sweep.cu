@@ -1,28 +1,30 @@
 // dflash_sweep.cu -- the draft-verification step as one persistent kernel.
 //
-// Pass structure (one launch, one CTA per SM, three warp roles):
+// Pass structure (one launch, one CTA per SM, four warp roles):
 //  1. Stream. Every row the step needs (target rows of every request, draft
 //     rows of sampling requests) is cut into 16 KB pieces of its aligned body.
 //     The producer warp moves pieces into an 8-stage shared-memory ring with
-//     1-D bulk copies (TMA). The 8 consumer warps reduce every 256-element
-//     tile of a piece to its largest logit (packed bf16x2 / fp32 max that
-//     propagates NaN) and store the tile's order key to the workspace. They
-//     never fence, never touch a global atomic and never wait on each other.
-//     Pieces are dealt round-robin to the CTAs, request by request, so rows
-//     complete progressively.
-//  2. Publish. The finisher group (4 warps) takes the pieces its consumers
-//     finished, in batches: one GPU-scope fence per batch, then one counter
-//     increment per piece on the piece's row. The increment that completes a
-//     row makes this CTA the row's finisher.
-//  3. Row final (finisher group): the row's top-k (k = 1 for greedy rows) in
-//     (logit desc, index asc) order. The k-th largest tile maximum tau is a
-//     lower bound of the row's k-th largest logit (the k tiles with the
-//     largest maxima hold k logits >= tau), so the top-k lies among the
-//     logits >= tau of the tiles whose maximum is >= tau: about k tiles,
-//     re-read from L2. The head and tail logits outside the aligned body are
-//     always candidates. A row whose ties leave too many candidates falls back
-//     to an exact radix selection over the whole row.
-//  4. Request final (finisher group of the CTA that completes a request's last
+//     1-D bulk copies (TMA) and records what each stage holds. The 8 consumer
+//     warps reduce every 256-element tile of a piece to its largest logit
+//     (packed bf16x2 / fp32 max that propagates NaN) and store the tile's
+//     order key to the workspace. They never fence, never touch a global
+//     atomic and never wait on each other. Pieces are dealt round-robin to
+//     the CTAs, request by request, so rows complete progressively.
+//  2. Publish. The publisher warp takes the pieces its consumers finished, in
+//     batches: one GPU-scope fence per batch, then one counter increment per
+//     piece on the piece's row. The increment that completes a row appends
+//     it to a global queue of finished rows; publishing never waits for a
+//     final.
+//  3. Row final (the finals group, 4 warps, of whichever CTA claims the row
+//     next from the queue, so finals spread over all SMs): the row's top-k (k = 1 for greedy
+//     rows) in (logit desc, index asc) order. A lower bound tau of the k-th
+//     largest tile maximum is also a lower bound of the row's k-th largest
+//     logit (the k tiles with the largest maxima hold k logits >= it), so the
+//     top-k lies among the logits >= tau of the tiles whose maximum is >= tau:
+//     about k tiles, re-read from L2. The head and tail logits outside the
+//     aligned body are always candidates. A row whose ties leave too many
+//     candidates falls back to an exact radix selection over the whole row.
+//  4. Request final (finals group of the CTA that completes a request's last
 //     row): filter the rows (temperature, softmax over the survivors, top-p,
 //     renormalise), run the accept test token by token with Philox uniforms,
 //     draw the residual or bonus token, write tokens and accept length.
@@ -53,12 +55,21 @@ namespace {
 constexpr uint32_t kStatusBadToken = 1u, kStatusBadRow = 2u, kStatusTimeout = 4u,
                    kStatusBadTemperature = 8u;
 
+// what the producer loaded into a ring stage (read by the consumers)
+struct PieceDesc {
+  int slot;
+  int pp;    // piece index within the row
+  int nvec;  // 16-byte vectors in the stage
+  int pad;
+};
+
 struct Smem {
   alignas(128) unsigned char ring[kStages][kPieceBytes];
+  PieceDesc desc[kStages];
   uint64_t full[kStages];       // ring stage loaded (producer expect_tx + bytes)
   uint64_t empty[kStages];      // ring stage read (one arrival per consumer warp)
   uint64_t kfull[kKeyQueue];    // piece's tile keys stored (one arrival per consumer warp)
-  uint64_t kempty[kKeyQueue];   // piece published (finisher leader)
+  uint64_t kempty[kKeyQueue];   // piece published (publisher)
   int32_t req_of_ord[kMaxB];
   union {
     uint32_t key_cache[kKeyCache];
@@ -70,18 +81,16 @@ struct Smem {
   uint32_t hist[256];
   unsigned long long cand[kCandCap];
   int32_t cand_tiles[kCandTileCap];
-  int32_t done_slots[kKeyQueue];
+  int fin_slot;
+  int fin_cmd;
   uint32_t warp_red[kConsumerWarps];
   int n_cand;
   int n_cand_tiles;
-  int n_done;
-  int n_batch;
   int flag;
   int n_samp;
   uint32_t digit;
   uint32_t digit_above;
   int bad_head_tail;
-  int fin_abort;
 };
 
 __device__ __forceinline__ bool sampling_temperature(float t) { return t > 0.0f && t < INFINITY; }
@@ -213,7 +222,7 @@ __device__ void build_request_order(const Params& p, Smem& S) {
   __syncthreads();
 }
 
-// ---- finisher-group helpers (128 threads, gt = thread index in the group) --------
+// ---- finals-group helpers (128 threads, gt = thread index in the group) ----------
 __device__ __forceinline__ int fin_tid() { return (int)threadIdx.x - kFinBase; }
 
 __device__ __forceinline__ uint32_t fin_max_u32(Smem& S, uint32_t v) {
@@ -293,7 +302,7 @@ __device__ uint32_t select_kth_key(Smem& S, const uint32_t* gkeys, int n, bool c
   return prefix;
 }
 
-// Visits every logit of a row with key >= tau (head, body, tail), finisher
+// Visits every logit of a row with key >= tau (head, body, tail), finals-group
 // threads in parallel. Used by the exact fallback when the tile filter leaves
 // too many candidates (heavily tied rows).
 template <class F>
@@ -366,12 +375,63 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   const uint32_t row_max = max(tile_max, fin_max_u32(S, emx));
   const bool bad = !key_is_finite(row_max) || S.bad_head_tail != 0;
 
-  // tau: the k-th largest tile maximum (0 keeps everything when tiles < k)
+  // tau: a lower bound of the k-th largest tile maximum (0 keeps everything
+  // when tiles < k). Tile keys within 255 buckets of 2^16 key units below the
+  // largest are counted per bucket; the bucket where the count from the top
+  // reaches k gives tau (exact for bf16 logits, whose keys have zero low 16
+  // bits). When the top k spread wider, an exact radix selection runs.
   uint32_t tau = 0u;
-  if (k == 1)
+  if (k == 1) {
     tau = tile_max;
-  else if (n_tiles >= k)
-    tau = select_kth_key(S, gkeys, n_tiles, cached, k);
+  } else if (n_tiles >= k) {
+    S.hist[gt] = 0u;
+    S.hist[gt + kFin] = 0u;
+    fin_sync();
+    for (int i = gt; i < n_tiles; i += kFin) {
+      const uint32_t key = cached ? S.u.key_cache[i] : __ldcg(gkeys + i);
+      const uint32_t bucket = (tile_max - key) >> 16;
+      if (bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
+    }
+    fin_sync();
+    if (gt < 32) {
+      // inclusive count over buckets 0..b, eight buckets per lane
+      uint32_t c[8], run = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = S.hist[lane * 8 + i];
+        run += c[i];
+      }
+      uint32_t incl = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
+      }
+      const uint32_t before = incl - run;
+      const bool here = before < (uint32_t)k && (uint32_t)k <= incl;
+      if (here) {
+        uint32_t acc = before;
+        int bkt = lane * 8;
+        for (int i = 0; i < 8; ++i) {
+          acc += c[i];
+          if (acc >= (uint32_t)k) {
+            bkt = lane * 8 + i;
+            break;
+          }
+        }
+        S.digit = (uint32_t)bkt;
+      }
+      if (lane == 31 && incl < (uint32_t)k) S.digit = 0xffffffffu;  // top k spread too wide
+    }
+    fin_sync();
+    const uint32_t bkt = S.digit;
+    if (bkt != 0xffffffffu) {
+      const uint32_t span = (bkt + 1u) << 16;
+      tau = tile_max >= span ? tile_max - span + 1u : 0u;
+    } else {
+      tau = select_kth_key(S, gkeys, n_tiles, cached, k);
+    }
+  }
 
   if (gt == 0) {
     S.n_cand_tiles = 0;
@@ -389,17 +449,34 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   const int n_ct = S.n_cand_tiles;
   bool overflow = n_ct > kCandTileCap;
   if (!overflow) {
-    // gather: one warp per candidate tile, lane l reads vector (g*8 + l%8) + 256*(l/8)
+    // gather: the candidate tiles' 32 vectors each, spread over the group with
+    // every load of a round issued before any is used; tile g of piece pc
+    // holds vectors pc*1024 + g*8 + l + 256*j (l < 8, j < 4)
     const int esize = p.geo.esize, per_vec = 16 / esize;
     const uint4* body = reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * esize);
-    for (int c = w; c < n_ct; c += kFinWarps) {
-      const int tile = S.cand_tiles[c];
-      const int piece = tile / kTilesPerPiece, g = tile - piece * kTilesPerPiece;
-      const int v = piece * kVecPerPiece + g * kTileLanes + (lane & 7) + kConsumers * (lane >> 3);
-      if (v < rb.nvec) {
-        const uint4 wv = __ldg(body + v);
-        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-        const int base = rb.head + v * per_vec;
+    const int n_vec_all = n_ct * 32;
+    for (int base = 0; base < n_vec_all; base += kFin * 8) {
+      uint4 wv[8];
+      int vi[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int f = base + u * kFin + gt;
+        vi[u] = -1;
+        if (f < n_vec_all) {
+          const int tile = S.cand_tiles[f >> 5], t = f & 31;
+          const int pc = tile / kTilesPerPiece, g = tile - pc * kTilesPerPiece;
+          const int v = pc * kVecPerPiece + g * kTileLanes + (t & 7) + kConsumers * (t >> 3);
+          if (v < rb.nvec) {
+            vi[u] = v;
+            wv[u] = __ldg(body + v);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (vi[u] < 0) continue;
+        const uint32_t ws[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+        const int ebase = rb.head + vi[u] * per_vec;
         for (int e = 0; e < per_vec; ++e) {
           uint32_t key;
           if (dtype == 0)
@@ -408,7 +485,7 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
             key = key_of(__uint_as_float(ws[e]));
           if (key >= tau) {
             const int pos = atomicAdd(&S.n_cand, 1);
-            if (pos < kCandCap) S.cand[pos] = composite(key, base + e);
+            if (pos < kCandCap) S.cand[pos] = composite(key, ebase + e);
           }
         }
       }
@@ -684,25 +761,47 @@ __device__ __forceinline__ void raise_timeout(const Params& p) {
   if (p.status) atomicOr(p.status, kStatusTimeout);
 }
 
+// A CTA's pieces are blockIdx.x, blockIdx.x + G, ... (G = gridDim.x); their
+// (slot, piece-in-row) pairs advance without divisions.
+struct PieceWalk {
+  int slot, pp, dslot, dpp, ppr;
+  __device__ __forceinline__ PieceWalk(int ppr_) : ppr(ppr_) {
+    slot = (int)(blockIdx.x / (unsigned)ppr_);
+    pp = (int)(blockIdx.x - (unsigned)slot * ppr_);
+    dslot = (int)(gridDim.x / (unsigned)ppr_);
+    dpp = (int)(gridDim.x - (unsigned)dslot * ppr_);
+  }
+  __device__ __forceinline__ void next() {
+    slot += dslot;
+    pp += dpp;
+    if (pp >= ppr) {
+      pp -= ppr;
+      ++slot;
+    }
+  }
+};
+
 __device__ void producer(const Params& p, Smem& S, long long total) {
   const int lane = threadIdx.x & 31;
   if (lane != 0) return;
   const volatile uint32_t* abort_flag = p.abort_flag;
-  const int ppr = p.geo.ppr;
+  PieceWalk w(p.geo.ppr);
   int it = 0;
   bool aborted = false;
-  for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it) {
+  for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it, w.next()) {
     const int stage = it % kStages;
     const uint32_t round = (uint32_t)(it / kStages);
     if (!mbar_wait(&S.empty[stage], (round & 1u) ^ 1u, abort_flag)) {
       aborted = true;
       break;
     }
-    const int slot = (int)(piece / ppr), pp = (int)(piece - (long long)slot * ppr);
-    const SlotInfo si = slot_info(p, S, slot);
+    const SlotInfo si = slot_info(p, S, w.slot);
     const RowBody rb = row_body(si.ptr, p.geo.V, p.geo.esize);
-    const int v0 = pp * kVecPerPiece;
+    const int v0 = w.pp * kVecPerPiece;
     const int nvec = max(0, min(kVecPerPiece, rb.nvec - v0));
+    S.desc[stage].slot = w.slot;
+    S.desc[stage].pp = w.pp;
+    S.desc[stage].nvec = nvec;
     if (nvec > 0) {
       mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec * 16u);
       bulk_load(S.ring[stage], rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16, (uint32_t)nvec * 16u,
@@ -723,20 +822,17 @@ template <int DT>
 __device__ void consumer(const Params& p, Smem& S, long long total) {
   const int tid = threadIdx.x, lane = tid & 31;
   const volatile uint32_t* abort_flag = p.abort_flag;
-  const int ppr = p.geo.ppr;
   int it = 0;
   for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it) {
     const int stage = it % kStages;
     const int q = it % kKeyQueue;
-    const int slot = (int)(piece / ppr), pp = (int)(piece - (long long)slot * ppr);
     const bool landed = mbar_wait(&S.full[stage], (uint32_t)(it / kStages) & 1u, abort_flag);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) raise_timeout(p);
       return;
     }
-    const SlotInfo si = slot_info(p, S, slot);
-    const RowBody rb = row_body(si.ptr, p.geo.V, p.geo.esize);
-    const int nvec = max(0, min(kVecPerPiece, rb.nvec - pp * kVecPerPiece));
+    const PieceDesc dsc = S.desc[stage];
+    const int nvec = dsc.nvec;
 
     // tile maximum of this thread's 4 vectors, then of its 8-lane group
     const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
@@ -773,11 +869,11 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
     __syncwarp();
     if (lane == 0) mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
     if ((lane & (kTileLanes - 1)) == 0)
-      p.tile_keys[(size_t)slot * p.geo.tiles + pp * kTilesPerPiece + (tid >> 3)] = key;
+      p.tile_keys[(size_t)dsc.slot * p.geo.tiles + dsc.pp * kTilesPerPiece + (tid >> 3)] = key;
     __syncwarp();  // orders the key stores before lane 0's arrival below
     int ok = 1;
     if (lane == 0) {
-      // the finisher must have taken queue slot q's previous piece
+      // the publisher must have taken queue slot q's previous piece
       if (!mbar_wait(&S.kempty[q], ((uint32_t)(it / kKeyQueue) & 1u) ^ 1u, abort_flag)) {
         raise_timeout(p);
         ok = 0;
@@ -789,85 +885,128 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
   }
 }
 
-__device__ void finisher(const Params& p, Smem& S, long long total) {
-  const int gt = fin_tid();
+// Publisher (one thread): takes the pieces the consumers finished in batches,
+// releases their tile keys to the other CTAs with one fence per batch, counts
+// them on their rows, and queues every row it completes for the finals group.
+__device__ void publisher(const Params& p, Smem& S, long long total) {
+  if ((threadIdx.x & 31) != 0) return;
   const int ppr = p.geo.ppr;
   const volatile uint32_t* abort_flag = p.abort_flag;
   const long long mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  PieceWalk w(ppr);
+  int tail = 0;
   long long q = 0;
-  if (gt == 0) S.fin_abort = 0;
-  fin_sync();
-  while (q < mine) {
+  bool ok = true;
+  while (q < mine && ok) {
+    int n = 0;
+    if (mbar_wait(&S.kfull[q % kKeyQueue], (uint32_t)((q / kKeyQueue) & 1), abort_flag)) {
+      n = 1;
+      while (q + n < mine && n < kKeyQueue &&
+             mbar_test_wait(&S.kfull[(q + n) % kKeyQueue], (uint32_t)(((q + n) / kKeyQueue) & 1)))
+        ++n;
+    }
+    if (n == 0) {
+      ok = false;
+      break;
+    }
+    fence_acq_rel_gpu();  // release the batch's tile keys to the other CTAs
+    int slots[kKeyQueue];
+    uint32_t old[kKeyQueue];
+#pragma unroll
+    for (int j = 0; j < kKeyQueue; ++j) {
+      if (j < n) {
+        slots[j] = w.slot;
+        old[j] = atomicAdd(p.row_cnt + w.slot, 1u);
+        w.next();
+      }
+    }
+    int done = 0;
+#pragma unroll
+    for (int j = 0; j < kKeyQueue; ++j) {
+      if (j < n) {
+        mbar_arrive(&S.kempty[(q + j) % kKeyQueue]);
+        if (old[j] == (uint32_t)(ppr - 1)) {
+          p.row_cnt[slots[j]] = 0u;  // ready for the next call
+          slots[done++] = slots[j];
+        }
+      }
+    }
+    if (done > 0) {
+      fence_acq_rel_gpu();  // acquire the other CTAs' keys of the finished rows
+      // queue the finished rows for whichever finals group claims them next
+      for (int j = 0; j < done; ++j) {
+        const uint32_t idx = atomicAdd(p.qcnt + 0, 1u);
+        st_release_gpu(p.ready + idx, (uint32_t)slots[j] + 1u);
+      }
+    }
+    q += n;
+  }
+  if (!ok) raise_timeout(p);
+}
+
+// Finals group (4 warps): claims finished rows from the global queue in
+// order (whichever CTA's group is free takes the next one), runs the row
+// final, the request hand-off and, for the last row of a request, its final.
+// The last group to leave resets the queue counters for the next call.
+__device__ void finals(const Params& p, Smem& S, int n_rows) {
+  const int gt = fin_tid();
+  const volatile uint32_t* abort_flag = p.abort_flag;
+  while (true) {
     if (gt == 0) {
-      // batch: the oldest unpublished piece, plus every later one already stored
-      int n = 0;
-      if (mbar_wait(&S.kfull[q % kKeyQueue], (uint32_t)((q / kKeyQueue) & 1), abort_flag)) {
-        n = 1;
-        while (q + n < mine && n < kKeyQueue &&
-               mbar_test_wait(&S.kfull[(q + n) % kKeyQueue], (uint32_t)(((q + n) / kKeyQueue) & 1)))
-          ++n;
-      }
-      if (n == 0) {
-        raise_timeout(p);
-        S.fin_abort = 1;
-      } else {
-        fence_acq_rel_gpu();  // release the batch's tile keys to the other CTAs
-        uint32_t old[kKeyQueue];
-#pragma unroll
-        for (int j = 0; j < kKeyQueue; ++j) {
-          if (j < n) {
-            const long long piece = blockIdx.x + (q + j) * (long long)gridDim.x;
-            const int slot = (int)(piece / ppr);
-            old[j] = atomicAdd(p.row_cnt + slot, 1u);
+      int cmd = 0;  // 0 finish, 1 work, 2 abort
+      const uint32_t idx = atomicAdd(p.qcnt + 1, 1u);
+      if (idx < (uint32_t)n_rows) {
+        uint32_t v = ld_acquire_gpu(p.ready + idx);
+        if (v == 0u) {
+          const unsigned long long t0 = global_timer_ns();
+          while ((v = ld_acquire_gpu(p.ready + idx)) == 0u) {
+            if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(64);
           }
         }
-        int m = 0;
-#pragma unroll
-        for (int j = 0; j < kKeyQueue; ++j) {
-          if (j < n) {
-            const long long piece = blockIdx.x + (q + j) * (long long)gridDim.x;
-            const int slot = (int)(piece / ppr);
-            if (old[j] == (uint32_t)(ppr - 1)) {
-              S.done_slots[m++] = slot;
-              p.row_cnt[slot] = 0u;  // ready for the next call
-            }
-            mbar_arrive(&S.kempty[(q + j) % kKeyQueue]);
-          }
+        if (v != 0u) {
+          p.ready[idx] = 0u;  // empty again for the next call
+          S.fin_slot = (int)(v - 1u);
+          cmd = 1;
+        } else {
+          raise_timeout(p);
+          cmd = 2;
         }
-        if (m > 0) fence_acq_rel_gpu();  // acquire the other CTAs' keys of the finished rows
-        S.n_done = m;
-        S.n_batch = n;
       }
+      S.fin_cmd = cmd;
     }
     fin_sync();
-    if (S.fin_abort) return;
-    const int n_done = S.n_done;
-    q += S.n_batch;
-    for (int j = 0; j < n_done; ++j) {
-      const int slot = S.done_slots[j];
-      const SlotInfo si = slot_info(p, S, slot);
-      unsigned long long top_a = 0ull;
-      row_final(p, S, slot, si, top_a);
-      if (p.task == kTaskFilter || p.task == kTaskSample) {
-        rows_final(p, S, slot, top_a);
-        continue;
-      }
-      // request hand-off: the CTA finishing the request's last row runs its final
-      const int b = S.req_of_ord[si.ord];
-      const int rows = si.sampling ? 2 * p.gamma + 1 : p.gamma + 1;
-      if (gt == 0) {
-        fence_acq_rel_gpu();  // release this row's results
-        const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(rows - 1);
-        if (last) {
-          p.req_cnt[b] = 0u;
-          fence_acq_rel_gpu();  // acquire the request's other rows
-        }
-        S.flag = last ? 1 : 0;
-      }
-      fin_sync();
-      if (S.flag) request_final(p, S, si.ord);
+    if (S.fin_cmd != 1) break;
+    const int slot = S.fin_slot;
+    const SlotInfo si = slot_info(p, S, slot);
+    unsigned long long top_a = 0ull;
+    row_final(p, S, slot, si, top_a);
+    if (p.task == kTaskFilter || p.task == kTaskSample) {
+      rows_final(p, S, slot, top_a);
+      continue;
     }
-    fin_sync();  // S.done_slots / S.n_done are rewritten by the next batch
+    // request hand-off: the group finishing the request's last row runs its final
+    const int b = S.req_of_ord[si.ord];
+    const int rows = si.sampling ? 2 * p.gamma + 1 : p.gamma + 1;
+    if (gt == 0) {
+      fence_acq_rel_gpu();  // release this row's results
+      const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(rows - 1);
+      if (last) {
+        p.req_cnt[b] = 0u;
+        fence_acq_rel_gpu();  // acquire the request's other rows
+      }
+      S.flag = last ? 1 : 0;
+    }
+    fin_sync();
+    if (S.flag) request_final(p, S, si.ord);
+  }
+  if (gt == 0 && S.fin_cmd == 0) {
+    // every group leaves once all rows are claimed; the last one resets
+    if (atomicAdd(p.qcnt + 2, 1u) == gridDim.x - 1u) {
+      p.qcnt[0] = 0u;
+      p.qcnt[1] = 0u;
+      p.qcnt[2] = 0u;
+    }
   }
 }
 
@@ -897,8 +1036,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
     consumer<DT>(p, S, total);
   else if (warp == kProducerWarp)
     producer(p, S, total);
+  else if (warp == kPublisherWarp)
+    publisher(p, S, total);
   else
-    finisher(p, S, total);
+    finals(p, S, active_slots(p, S));
 }
 
 __global__ void uniforms_kernel(unsigned long long seed, int B, int npos, int stream_id, float* ua, float* ud) {
