@@ -83,8 +83,7 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests) {
   p.row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
   p.req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
   p.abort_flag = reinterpret_cast<uint32_t*>(base + L.abort_flag);
-  p.qcnt = reinterpret_cast<uint32_t*>(base + L.qcnt);
-  p.ready = reinterpret_cast<uint32_t*>(base + L.ready);
+  p.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
   p.tile_keys = reinterpret_cast<uint32_t*>(base + L.tile_keys);
   p.res_key = reinterpret_cast<uint32_t*>(base + L.res_key);
   p.res_idx = reinterpret_cast<int32_t*>(base + L.res_idx);

@@ -82,8 +82,7 @@ struct Params {
   uint32_t* row_cnt;    // [n_slots]
   uint32_t* req_cnt;    // [B]
   uint32_t* abort_flag; // [1]
-  uint32_t* qcnt;       // [3]: rows queued, rows claimed, finals groups done
-  uint32_t* ready;      // [kMaxCounterSlots]: queued row slot + 1, 0 = empty
+  unsigned long long* row_best;  // [kMaxCounterSlots]: greedy rows' best (key, index) composite
   uint32_t* tile_keys;  // [n_slots, geo.tiles]
   uint32_t* res_key;    // [n_slots, kMaxTopK]
   int32_t* res_idx;     // [n_slots, kMaxTopK]
@@ -92,7 +91,7 @@ struct Params {
 };
 
 struct WorkspaceLayout {
-  size_t row_cnt, req_cnt, abort_flag, qcnt, ready, tile_keys, res_key, res_idx, res_flag, total;
+  size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_key, res_idx, res_flag, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -108,7 +107,7 @@ inline Geometry make_geometry(int V, int esize) {
   return g;
 }
 
-// The hand-off counters and the queue of finished rows live in a fixed header
+// The hand-off counters and the greedy rows' running argmax live in a fixed header
 // at the start of every workspace, at offsets that do not depend on the
 // call's shape: every call returns what it used to zero, so a workspace stays
 // ready for the next call of any shape. The per-row data follows the header.
@@ -121,8 +120,7 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.req_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxB, 256);
   L.row_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
   L.abort_flag = off; off = align_up(off + sizeof(uint32_t), 256);
-  L.qcnt = off;       off = align_up(off + sizeof(uint32_t) * 3, 256);
-  L.ready = off;      off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
+  L.row_best = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)kMaxCounterSlots, 256);
   L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
   L.res_key = off;    off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * kMaxTopK, 256);
   L.res_idx = off;    off = align_up(off + sizeof(int32_t) * (size_t)n_slots * kMaxTopK, 256);

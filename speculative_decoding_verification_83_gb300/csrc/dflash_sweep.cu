@@ -11,27 +11,28 @@
 //     atomic and never wait on each other. Pieces are dealt round-robin to
 //     the CTAs, request by request, so rows complete progressively.
 //  2. Publish. The publisher warp takes the pieces its consumers finished, in
-//     batches: one GPU-scope fence per batch, then one counter increment per
-//     piece on the piece's row. The increment that completes a row appends
-//     it to a global queue of finished rows; publishing never waits for a
-//     final.
-//  3. Row final (the finals group, 4 warps, of whichever CTA claims the row
-//     next from the queue, so finals spread over all SMs): the row's top-k (k = 1 for greedy
-//     rows) in (logit desc, index asc) order. A lower bound tau of the k-th
-//     largest tile maximum is also a lower bound of the row's k-th largest
-//     logit (the k tiles with the largest maxima hold k logits >= it), so the
-//     top-k lies among the logits >= tau of the tiles whose maximum is >= tau:
-//     about k tiles, re-read from L2. The head and tail logits outside the
-//     aligned body are always candidates. A row whose ties leave too many
-//     candidates falls back to an exact radix selection over the whole row.
-//  4. Request final (finals group of the CTA that completes a request's last
-//     row): filter the rows (temperature, softmax over the survivors, top-p,
-//     renormalise), run the accept test token by token with Philox uniforms,
-//     draw the residual or bonus token, write tokens and accept length.
-//     Greedy requests: argmax prefix match.
-// No CTA ever waits for another ("last arriver does the work" counters), so
-// there is no grid-wide barrier to deadlock; the only waits are on this CTA's
-// own shared-memory barriers and they are time-bounded.
+//     batches: one GPU-scope fence per batch, then a fire-and-forget counter
+//     increment per piece on the piece's row. For greedy rows the consumer
+//     warps also fold each piece's best (logit, lowest index) into the row's
+//     running argmax with a 64-bit max reduction, so greedy rows need no
+//     row final.
+//  3. Row final (the 4-warp finals group of the CTA the row is dealt to: job
+//     j goes to CTA j mod G, in the order rows finish): the row's top-k in
+//     (logit desc, index asc) order. A lower bound tau of the k-th largest
+//     tile maximum is also a lower bound of the row's k-th largest logit (the
+//     k tiles with the largest maxima hold k logits >= it), so the top-k lies
+//     among the logits >= tau of the tiles whose maximum is >= tau: about k
+//     tiles, re-read from L2. The head and tail logits outside the aligned
+//     body are always candidates. A row whose ties leave too many candidates
+//     falls back to an exact radix selection over the whole row.
+//  4. Request final: a sampling request's final runs in the group that
+//     finishes its last row (filter the rows: temperature, softmax over the
+//     survivors, top-p, renormalise; accept test token by token with Philox
+//     uniforms; residual or bonus draw; tokens and accept length). A greedy
+//     request is a job of its own: argmax prefix match on the streamed argmax.
+// A job waits, time-bounded, only for its rows' pieces to be counted; the
+// pieces are counted by publishers, which wait for nothing but their own
+// consumers, so there is no cycle of waits and no grid-wide barrier.
 //
 // The method follows "DFlash2 用投机解码给 Qwen 提速" (bml.asia, draft/verify
 // loop and model-card settings) and "无损加速是真的吗？Qwen3.8-27B-DFlash2
@@ -58,10 +59,11 @@ constexpr uint32_t kStatusBadToken = 1u, kStatusBadRow = 2u, kStatusTimeout = 4u
 // what the producer loaded into a ring stage (read by the consumers)
 struct PieceDesc {
   int slot;
-  int pp;    // piece index within the row
-  int nvec;  // 16-byte vectors in the stage
-  int pad;
+  int pp;      // piece index within the row
+  int nvec;    // 16-byte vectors in the stage
+  int head;    // logits before the row's aligned body; + kDescArgmax for greedy rows
 };
+constexpr int kDescArgmax = 256;  // the consumers track this row's argmax in-stream
 
 struct Smem {
   alignas(128) unsigned char ring[kStages][kPieceBytes];
@@ -594,58 +596,14 @@ __device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u,
   return r == INT_MAX ? -1 : r;
 }
 
-// ---- request final (verification) --------------------------------------------------
+// ---- request final (sampling verification) -------------------------------------------
 __device__ void request_final(const Params& p, Smem& S, int ord) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int gamma = p.gamma, V = p.geo.V;
   const int b = S.req_of_ord[ord];
-  const bool sampling = ord < S.n_samp;
   int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
   const int32_t* d = p.draft_tokens + (size_t)b * gamma;
-  const int per_s = 2 * gamma + 1, per_g = gamma + 1;
-
-  if (!sampling) {
-    if (w == 0) {
-      const int slot0 = S.n_samp * per_s + (ord - S.n_samp) * per_g;
-      uint32_t st = 0;
-      if (p.task == kTaskVerify && __ldg(p.temperature + b) != 0.0f) st |= kStatusBadTemperature;
-      int n = gamma;  // length of the matching prefix
-      for (int base = 0; base <= gamma; base += 32) {
-        const int i = base + lane;
-        int32_t a = -1;
-        bool mismatch = false;
-        if (i <= gamma) {
-          a = __ldcg(p.res_idx + (size_t)(slot0 + i) * kMaxTopK);
-          if (__ldcg(p.res_flag + slot0 + i)) st |= kStatusBadRow;
-        }
-        if (i < gamma) {
-          const int32_t di = __ldg(d + i);
-          if (di < 0 || di >= V) st |= kStatusBadToken;
-          mismatch = di != a;
-        }
-        const uint32_t mm = __ballot_sync(0xffffffffu, mismatch);
-        if (mm && n == gamma) n = base + __ffs(mm) - 1;
-      }
-      for (int base = 0; base <= gamma; base += 32) {
-        const int i = base + lane;
-        if (i <= gamma) {
-          int32_t v = -1;
-          if (i < n)
-            v = __ldg(d + i);
-          else if (i == n)
-            v = __ldcg(p.res_idx + (size_t)(slot0 + i) * kMaxTopK);
-          out[i] = v;
-        }
-      }
-      st = __reduce_or_sync(0xffffffffu, st);
-      if (lane == 0) {
-        p.out_len[b] = n + 1;
-        if (st && p.status) atomicOr(p.status, st);
-      }
-    }
-    fin_sync();
-    return;
-  }
+  const int per_s = 2 * gamma + 1;
 
   // sampling request: filter every row into shared lists (warps in parallel)
   const int slot0 = ord * per_s;
@@ -761,6 +719,11 @@ __device__ __forceinline__ void raise_timeout(const Params& p) {
   if (p.status) atomicOr(p.status, kStatusTimeout);
 }
 
+// Greedy rows of a verification get their argmax in the stream (no row final).
+__device__ __forceinline__ bool in_stream_argmax(const Params& p, const SlotInfo& si) {
+  return (p.task == kTaskVerify || p.task == kTaskVerifyGreedy) && !si.sampling;
+}
+
 // A CTA's pieces are blockIdx.x, blockIdx.x + G, ... (G = gridDim.x); their
 // (slot, piece-in-row) pairs advance without divisions.
 struct PieceWalk {
@@ -802,6 +765,7 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
     S.desc[stage].slot = w.slot;
     S.desc[stage].pp = w.pp;
     S.desc[stage].nvec = nvec;
+    S.desc[stage].head = rb.head + (in_stream_argmax(p, si) ? kDescArgmax : 0);
     if (nvec > 0) {
       mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec * 16u);
       bulk_load(S.ring[stage], rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16, (uint32_t)nvec * 16u,
@@ -866,10 +830,50 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
     key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
     key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
     key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
-    if ((lane & (kTileLanes - 1)) == 0)
-      p.tile_keys[(size_t)dsc.slot * p.geo.tiles + dsc.pp * kTilesPerPiece + (tid >> 3)] = key;
+    if (dsc.head & kDescArgmax) {
+      // greedy row: this warp's best (logit, lowest index) over its 4 tiles
+      uint32_t wmax = max(key, __shfl_xor_sync(0xffffffffu, key, 8));
+      wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, 16));
+      unsigned long long comp = 0ull;
+      if (key == wmax && nvec > 0) {
+        const int head = dsc.head & (kDescArgmax - 1);
+        const int per_vec = DT == 0 ? 8 : 4;
+        int best = INT_MAX;
+        for (int j = 0; j < kVecPerThread; ++j) {
+          const int v = tid + kConsumers * j;
+          if (v >= nvec) break;
+          const uint4 wv = st4[v];
+          const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+          for (int e = 0; e < per_vec; ++e) {
+            const float x = DT == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16)
+                                    : __uint_as_float(ws[e]);
+            if (key_of(x) == wmax) {
+              best = min(best, head + (dsc.pp * kVecPerPiece + v) * per_vec + e);
+              break;
+            }
+          }
+        }
+        // A NaN maximum matches no logit's key: the lane still offers the key
+        // (so the row gets flagged), at the largest index, which loses to any
+        // lane that did find the maximum.
+        comp = composite(wmax, best == INT_MAX ? INT_MAX : best);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const unsigned long long oc = shfl_xor_u64(comp, o);
+        comp = oc > comp ? oc : comp;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
+        if (comp) red_max_gpu(p.row_best + dsc.slot, comp);
+      }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
+      if ((lane & (kTileLanes - 1)) == 0)
+        p.tile_keys[(size_t)dsc.slot * p.geo.tiles + dsc.pp * kTilesPerPiece + (tid >> 3)] = key;
+    }
     __syncwarp();  // orders the key stores before lane 0's arrival below
     int ok = 1;
     if (lane == 0) {
@@ -886,18 +890,17 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
 }
 
 // Publisher (one thread): takes the pieces the consumers finished in batches,
-// releases their tile keys to the other CTAs with one fence per batch, counts
-// them on their rows, and queues every row it completes for the finals group.
+// releases their tile keys (and greedy argmax updates) to the other CTAs with
+// one fence per batch, then counts the pieces on their rows with
+// fire-and-forget reductions, so it never waits for a reply.
 __device__ void publisher(const Params& p, Smem& S, long long total) {
   if ((threadIdx.x & 31) != 0) return;
   const int ppr = p.geo.ppr;
   const volatile uint32_t* abort_flag = p.abort_flag;
   const long long mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   PieceWalk w(ppr);
-  int tail = 0;
   long long q = 0;
-  bool ok = true;
-  while (q < mine && ok) {
+  while (q < mine) {
     int n = 0;
     if (mbar_wait(&S.kfull[q % kKeyQueue], (uint32_t)((q / kKeyQueue) & 1), abort_flag)) {
       n = 1;
@@ -906,88 +909,137 @@ __device__ void publisher(const Params& p, Smem& S, long long total) {
         ++n;
     }
     if (n == 0) {
-      ok = false;
-      break;
+      raise_timeout(p);
+      return;
     }
     fence_acq_rel_gpu();  // release the batch's tile keys to the other CTAs
-    int slots[kKeyQueue];
-    uint32_t old[kKeyQueue];
-#pragma unroll
-    for (int j = 0; j < kKeyQueue; ++j) {
-      if (j < n) {
-        slots[j] = w.slot;
-        old[j] = atomicAdd(p.row_cnt + w.slot, 1u);
-        w.next();
-      }
-    }
-    int done = 0;
-#pragma unroll
-    for (int j = 0; j < kKeyQueue; ++j) {
-      if (j < n) {
-        mbar_arrive(&S.kempty[(q + j) % kKeyQueue]);
-        if (old[j] == (uint32_t)(ppr - 1)) {
-          p.row_cnt[slots[j]] = 0u;  // ready for the next call
-          slots[done++] = slots[j];
-        }
-      }
-    }
-    if (done > 0) {
-      fence_acq_rel_gpu();  // acquire the other CTAs' keys of the finished rows
-      // queue the finished rows for whichever finals group claims them next
-      for (int j = 0; j < done; ++j) {
-        const uint32_t idx = atomicAdd(p.qcnt + 0, 1u);
-        st_release_gpu(p.ready + idx, (uint32_t)slots[j] + 1u);
-      }
+    for (int j = 0; j < n; ++j) {
+      red_add_gpu(p.row_cnt + w.slot, 1u);
+      w.next();
+      mbar_arrive(&S.kempty[(q + j) % kKeyQueue]);
     }
     q += n;
   }
-  if (!ok) raise_timeout(p);
 }
 
-// Finals group (4 warps): claims finished rows from the global queue in
-// order (whichever CTA's group is free takes the next one), runs the row
-// final, the request hand-off and, for the last row of a request, its final.
-// The last group to leave resets the queue counters for the next call.
-__device__ void finals(const Params& p, Smem& S, int n_rows) {
-  const int gt = fin_tid();
+// Waits (bounded) until `n` consecutive rows from `slot0` have all their
+// pieces counted, then returns their counters to zero. Run by one warp.
+__device__ __forceinline__ bool wait_rows(const Params& p, int slot0, int n) {
+  const int lane = threadIdx.x & 31;
   const volatile uint32_t* abort_flag = p.abort_flag;
-  while (true) {
-    if (gt == 0) {
-      int cmd = 0;  // 0 finish, 1 work, 2 abort
-      const uint32_t idx = atomicAdd(p.qcnt + 1, 1u);
-      if (idx < (uint32_t)n_rows) {
-        uint32_t v = ld_acquire_gpu(p.ready + idx);
-        if (v == 0u) {
-          const unsigned long long t0 = global_timer_ns();
-          while ((v = ld_acquire_gpu(p.ready + idx)) == 0u) {
-            if (*abort_flag || global_timer_ns() - t0 > kWaitLimitNs) break;
-            __nanosleep(64);
-          }
-        }
-        if (v != 0u) {
-          p.ready[idx] = 0u;  // empty again for the next call
-          S.fin_slot = (int)(v - 1u);
-          cmd = 1;
-        } else {
-          raise_timeout(p);
-          cmd = 2;
-        }
+  const uint32_t need = (uint32_t)p.geo.ppr;
+  const unsigned long long t0 = global_timer_ns();
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    bool done = i >= n || ld_acquire_gpu(p.row_cnt + slot0 + i) >= need;
+    while (!__all_sync(0xffffffffu, done)) {
+      // the give-up decision is the warp's, so every lane leaves together
+      const bool stop = *abort_flag != 0u || global_timer_ns() - t0 > kWaitLimitNs;
+      if (__any_sync(0xffffffffu, stop)) return false;
+      __nanosleep(64);
+      if (!done) done = ld_acquire_gpu(p.row_cnt + slot0 + i) >= need;
+    }
+  }
+  for (int i = lane; i < n; i += 32) p.row_cnt[slot0 + i] = 0u;  // ready for the next call
+  return true;
+}
+
+// Final of a greedy request: its rows' argmax came from the stream (plus the
+// logits outside each row's aligned body); prefix-match the drafts.
+__device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
+  const int lane = fin_tid() & 31;
+  const int gamma = p.gamma, V = p.geo.V;
+  const int b = S.req_of_ord[ord];
+  const int slot0 = S.n_samp * (2 * gamma + 1) + (ord - S.n_samp) * (gamma + 1);
+  int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
+  const int32_t* d = p.draft_tokens + (size_t)b * gamma;
+  const size_t row_bytes = (size_t)V * p.geo.esize;
+  uint32_t st = 0;
+  if (p.task == kTaskVerify && __ldg(p.temperature + b) != 0.0f) st |= kStatusBadTemperature;
+  int n = gamma;  // length of the matching prefix
+  int32_t am[2] = {-1, -1};  // argmax of rows lane and lane + 32
+  for (int base = 0, u = 0; base <= gamma; base += 32, ++u) {
+    const int i = base + lane;
+    bool mismatch = false;
+    if (i <= gamma) {
+      unsigned long long comp = ld_acquire_gpu_u64(p.row_best + slot0 + i);
+      p.row_best[slot0 + i] = 0ull;  // ready for the next call
+      const RowBody rb = row_body(p.target + ((size_t)b * (gamma + 1) + i) * row_bytes, V, p.geo.esize);
+      bool nan = false;
+      for (int j = 0; j < rb.head; ++j) {
+        const float x = load_logit(rb.row, j, p.dtype);
+        nan |= isnan(x);
+        const unsigned long long c = composite(key_of(x), j);
+        comp = c > comp ? c : comp;
       }
-      S.fin_cmd = cmd;
+      for (int j = rb.tail_start; j < V; ++j) {
+        const float x = load_logit(rb.row, j, p.dtype);
+        nan |= isnan(x);
+        const unsigned long long c = composite(key_of(x), j);
+        comp = c > comp ? c : comp;
+      }
+      if (nan || !key_is_finite(composite_key(comp))) st |= kStatusBadRow;
+      am[u] = composite_idx(comp);
+      if (am[u] < 0 || am[u] >= V) am[u] = 0;
+    }
+    if (i < gamma) {
+      const int32_t di = __ldg(d + i);
+      if (di < 0 || di >= V) st |= kStatusBadToken;
+      mismatch = di != am[u];
+    }
+    const uint32_t mm = __ballot_sync(0xffffffffu, mismatch);
+    if (mm && n == gamma) n = base + __ffs(mm) - 1;
+  }
+  for (int base = 0, u = 0; base <= gamma; base += 32, ++u) {
+    const int i = base + lane;
+    if (i <= gamma) out[i] = i < n ? __ldg(d + i) : (i == n ? am[u] : -1);
+  }
+  st = __reduce_or_sync(0xffffffffu, st);
+  if (lane == 0) {
+    p.out_len[b] = n + 1;
+    if (st && p.status) atomicOr(p.status, st);
+  }
+}
+
+// Finals group (4 warps): works through the jobs dealt to this CTA (job j
+// goes to CTA j mod G, in the order rows finish): first the rows that need a
+// top-k (sampling rows, every row of the rows tasks), then one job per greedy
+// request. A job waits only for its rows' pieces to be counted, never for
+// another final, so no two groups can wait on each other.
+__device__ void finals(const Params& p, Smem& S) {
+  const int gt = fin_tid(), w = gt >> 5;
+  const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
+  const int n_row_jobs = verify ? S.n_samp * (2 * p.gamma + 1) : p.B;
+  const int n_jobs = n_row_jobs + (verify ? p.B - S.n_samp : 0);
+  for (int j = blockIdx.x; j < n_jobs; j += gridDim.x) {
+    const bool row_job = j < n_row_jobs;
+    if (w == 0) {
+      const bool ok = row_job ? wait_rows(p, j, 1)
+                              : wait_rows(p, n_row_jobs + (j - n_row_jobs) * (p.gamma + 1), p.gamma + 1);
+      if (gt == 0) {
+        if (!ok) raise_timeout(p);
+        S.fin_cmd = ok ? 1 : 2;
+      }
+      if (ok) fence_acq_rel_gpu();  // acquire the rows' keys
     }
     fin_sync();
-    if (S.fin_cmd != 1) break;
-    const int slot = S.fin_slot;
+    if (S.fin_cmd != 1) return;
+    if (!row_job) {
+      if (w == 0) greedy_request_final(p, S, S.n_samp + (j - n_row_jobs));
+      fin_sync();
+      continue;
+    }
+    const int slot = j;
     const SlotInfo si = slot_info(p, S, slot);
     unsigned long long top_a = 0ull;
     row_final(p, S, slot, si, top_a);
-    if (p.task == kTaskFilter || p.task == kTaskSample) {
+    if (!verify) {
       rows_final(p, S, slot, top_a);
       continue;
     }
     // request hand-off: the group finishing the request's last row runs its final
     const int b = S.req_of_ord[si.ord];
-    const int rows = si.sampling ? 2 * p.gamma + 1 : p.gamma + 1;
+    const int rows = 2 * p.gamma + 1;
     if (gt == 0) {
       fence_acq_rel_gpu();  // release this row's results
       const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(rows - 1);
@@ -999,14 +1051,6 @@ __device__ void finals(const Params& p, Smem& S, int n_rows) {
     }
     fin_sync();
     if (S.flag) request_final(p, S, si.ord);
-  }
-  if (gt == 0 && S.fin_cmd == 0) {
-    // every group leaves once all rows are claimed; the last one resets
-    if (atomicAdd(p.qcnt + 2, 1u) == gridDim.x - 1u) {
-      p.qcnt[0] = 0u;
-      p.qcnt[1] = 0u;
-      p.qcnt[2] = 0u;
-    }
   }
 }
 
@@ -1039,7 +1083,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
   else if (warp == kPublisherWarp)
     publisher(p, S, total);
   else
-    finals(p, S, active_slots(p, S));
+    finals(p, S);
 }
 
 __global__ void uniforms_kernel(unsigned long long seed, int B, int npos, int stream_id, float* ua, float* ud) {
