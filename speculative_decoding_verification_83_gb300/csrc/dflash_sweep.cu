@@ -800,63 +800,46 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
 
     // tile maximum of this thread's 4 vectors, then of its 8-lane group
     const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
-    float m;
-    if (DT == 0) {
-      __nv_bfloat162 m2 = __floats2bfloat162_rn(-INFINITY, -INFINITY);
+    // maximum of each of this thread's 4 vectors, then of the 4
+    float vm[kVecPerThread];
 #pragma unroll
-      for (int j = 0; j < kVecPerThread; ++j) {
-        const int v = tid + kConsumers * j;
-        if (v < nvec) {
+    for (int j = 0; j < kVecPerThread; ++j) {
+      const int v = tid + kConsumers * j;
+      vm[j] = -INFINITY;
+      if (v < nvec) {
+        if (DT == 0) {
           const uint4 wv = st4[v];
-          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.x));
-          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.z));
-          m2 = __hmax2_nan(m2, *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
-        }
-      }
-      m = max_nan(__low2float(m2), __high2float(m2));
-    } else {
-      m = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < kVecPerThread; ++j) {
-        const int v = tid + kConsumers * j;
-        if (v < nvec) {
+          __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.x),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+          const __nv_bfloat162 b = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.z),
+                                               *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
+          a = __hmax2_nan(a, b);
+          vm[j] = max_nan(__low2float(a), __high2float(a));
+        } else {
           const float4 wv = reinterpret_cast<const float4*>(st4)[v];
-          m = max_nan(m, max_nan(max_nan(wv.x, wv.y), max_nan(wv.z, wv.w)));
+          vm[j] = max_nan(max_nan(wv.x, wv.y), max_nan(wv.z, wv.w));
         }
       }
     }
-    uint32_t key = key_of(m);
+    const float m = max_nan(max_nan(vm[0], vm[1]), max_nan(vm[2], vm[3]));
+    const uint32_t own_key = key_of(m);
+    uint32_t key = own_key;
     key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
     key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
     key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
     if (dsc.head & kDescArgmax) {
-      // greedy row: this warp's best (logit, lowest index) over its 4 tiles
+      // greedy row: this warp's best (logit, lowest vector) over its 4 tiles;
+      // vectors are in logit order, so the lowest vector holding the maximum
+      // holds the lowest-index maximum of the warp
       uint32_t wmax = max(key, __shfl_xor_sync(0xffffffffu, key, 8));
       wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, 16));
       unsigned long long comp = 0ull;
-      if (key == wmax && nvec > 0) {
-        const int head = dsc.head & (kDescArgmax - 1);
-        const int per_vec = DT == 0 ? 8 : 4;
-        int best = INT_MAX;
-        for (int j = 0; j < kVecPerThread; ++j) {
-          const int v = tid + kConsumers * j;
-          if (v >= nvec) break;
-          const uint4 wv = st4[v];
-          const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-          for (int e = 0; e < per_vec; ++e) {
-            const float x = DT == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16)
-                                    : __uint_as_float(ws[e]);
-            if (key_of(x) == wmax) {
-              best = min(best, head + (dsc.pp * kVecPerPiece + v) * per_vec + e);
-              break;
-            }
-          }
-        }
-        // A NaN maximum matches no logit's key: the lane still offers the key
-        // (so the row gets flagged), at the largest index, which loses to any
-        // lane that did find the maximum.
-        comp = composite(wmax, best == INT_MAX ? INT_MAX : best);
+      if (own_key == wmax && nvec > 0) {  // this lane holds the warp's maximum
+        int jf = 0;
+#pragma unroll
+        for (int j = kVecPerThread - 1; j >= 0; --j)
+          if (key_of(vm[j]) == wmax) jf = j;
+        comp = composite(wmax, dsc.pp * kVecPerPiece + tid + kConsumers * jf);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -962,10 +945,27 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
     const int i = base + lane;
     bool mismatch = false;
     if (i <= gamma) {
-      unsigned long long comp = ld_acquire_gpu_u64(p.row_best + slot0 + i);
+      // the stream left (largest key, lowest body vector holding it)
+      const unsigned long long vbest = ld_acquire_gpu_u64(p.row_best + slot0 + i);
       p.row_best[slot0 + i] = 0ull;  // ready for the next call
       const RowBody rb = row_body(p.target + ((size_t)b * (gamma + 1) + i) * row_bytes, V, p.geo.esize);
       bool nan = false;
+      unsigned long long comp = 0ull;
+      if (vbest != 0ull) {
+        const uint32_t vkey = composite_key(vbest);
+        const int v = composite_idx(vbest);
+        const int per_vec = 16 / p.geo.esize;
+        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * p.geo.esize) + v);
+        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+        int e_hit = -1;
+        for (int e = per_vec - 1; e >= 0; --e) {
+          const float x = p.dtype == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16)
+                                       : __uint_as_float(ws[e]);
+          if (key_of(x) == vkey) e_hit = e;
+        }
+        // no logit carries a NaN maximum's canonical key: keep it, flagged below
+        comp = composite(vkey, rb.head + v * per_vec + (e_hit < 0 ? 0 : e_hit));
+      }
       for (int j = 0; j < rb.head; ++j) {
         const float x = load_logit(rb.row, j, p.dtype);
         nan |= isnan(x);
