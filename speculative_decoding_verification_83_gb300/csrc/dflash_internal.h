@@ -9,10 +9,12 @@ namespace dflash {
 
 // ---- fixed tiling -------------------------------------------------------------
 // One "piece" is a 16 KB contiguous run of a row's 16-byte-aligned body, moved
-// into shared memory by one bulk (TMA) copy. 256 consumer threads read it as
-// 1024 16-byte vectors, thread t taking vectors t, t+256, t+512, t+768. A
-// "tile" is what 8 neighbouring consumer lanes read: 32 vectors (256 bf16 or
-// 128 fp32 logits); its largest logit is recorded for the row-level selection.
+// into shared memory by one bulk (TMA) copy and reduced by one consumer warp:
+// lane l reads vectors 32*r + l for r = 0..31, in 8 blocks of 4 rounds. A
+// "tile" is what 8 neighbouring lanes read in one block: vectors
+// 32*(4*blk + rr) + 8*g + l (rr < 4, l < 8) for tile 4*blk + g, i.e. 32
+// vectors (256 bf16 or 128 fp32 logits); its largest logit is recorded for the
+// row-level selection.
 //
 // A CTA (one per SM) has four roles: warps 0-7 consume pieces, warp 8 is the
 // producer (bulk copies), warp 9 publishes finished pieces to the other CTAs,
@@ -27,10 +29,10 @@ constexpr int kFinBase = (kConsumerWarps + 2) * 32;
 constexpr int kThreads = kFinBase + kFin;
 constexpr int kPieceBytes = 16384;
 constexpr int kVecPerPiece = kPieceBytes / 16;
-constexpr int kVecPerThread = kVecPerPiece / kConsumers;
+constexpr int kRoundsPerPiece = kVecPerPiece / 32;   // vectors per lane
 constexpr int kTileLanes = 8;
-constexpr int kTilesPerPiece = kConsumers / kTileLanes;
-constexpr int kStages = 8;       // ring of bulk-copy stages
+constexpr int kTilesPerPiece = kRoundsPerPiece;       // 8 blocks x 4 lane groups
+constexpr int kStages = 12;      // ring of bulk-copy stages
 constexpr int kKeyQueue = 32;    // pieces the publisher may lag behind
 constexpr int kCtasPerSm = 1;
 
@@ -41,6 +43,11 @@ constexpr int kKeyCache = 2048;  // tile keys of one row cached in shared memory
 constexpr int kMaxGamma = 32;
 constexpr int kMaxRowsPerRequest = 2 * kMaxGamma + 1;
 constexpr int kMaxB = 2048;
+
+// body vector (within its piece) of vector t (< 32) of tile `tile`
+inline __host__ __device__ int tile_vector(int tile, int t) {
+  return 32 * (4 * (tile >> 2) + (t >> 3)) + 8 * (tile & 3) + (t & 7);
+}
 
 enum Task : int { kTaskVerify = 0, kTaskVerifyGreedy = 1, kTaskFilter = 2, kTaskSample = 3 };
 

@@ -3,11 +3,11 @@
 // Pass structure (one launch, one CTA per SM, four warp roles):
 //  1. Stream. Every row the step needs (target rows of every request, draft
 //     rows of sampling requests) is cut into 16 KB pieces of its aligned body.
-//     The producer warp moves pieces into an 8-stage shared-memory ring with
-//     1-D bulk copies (TMA) and records what each stage holds. The 8 consumer
-//     warps reduce every 256-element tile of a piece to its largest logit
-//     (packed bf16x2 / fp32 max that propagates NaN) and store the tile's
-//     order key to the workspace. They never fence, never touch a global
+//     The producer warp moves pieces into a 12-stage shared-memory ring with
+//     1-D bulk copies (TMA) and records what each stage holds. Each of the 8
+//     consumer warps takes whole pieces and reduces every 256-element tile of
+//     them to its largest logit (packed bf16x2 / fp32 max that propagates NaN)
+//     and stores the tile's order key to the workspace. They never fence, never touch a global
 //     atomic and never wait on each other. Pieces are dealt round-robin to
 //     the CTAs, request by request, so rows complete progressively.
 //  2. Publish. The publisher warp takes the pieces its consumers finished, in
@@ -69,10 +69,10 @@ struct Smem {
   alignas(128) unsigned char ring[kStages][kPieceBytes];
   PieceDesc desc[kStages];
   uint64_t full[kStages];       // ring stage loaded (producer expect_tx + bytes)
-  uint64_t empty[kStages];      // ring stage read (one arrival per consumer warp)
-  uint64_t kfull[kKeyQueue];    // piece's tile keys stored (one arrival per consumer warp)
+  uint64_t empty[kStages];      // ring stage read (by the piece's consumer warp)
+  uint64_t kfull[kKeyQueue];    // piece's tile keys stored (by the piece's consumer warp)
   uint64_t kempty[kKeyQueue];   // piece published (publisher)
-  int32_t req_of_ord[kMaxB];
+  int16_t req_of_ord[kMaxB];
   union {
     uint32_t key_cache[kKeyCache];
     struct {
@@ -452,8 +452,7 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   bool overflow = n_ct > kCandTileCap;
   if (!overflow) {
     // gather: the candidate tiles' 32 vectors each, spread over the group with
-    // every load of a round issued before any is used; tile g of piece pc
-    // holds vectors pc*1024 + g*8 + l + 256*j (l < 8, j < 4)
+    // every load of a round issued before any is used
     const int esize = p.geo.esize, per_vec = 16 / esize;
     const uint4* body = reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * esize);
     const int n_vec_all = n_ct * 32;
@@ -466,8 +465,8 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
         vi[u] = -1;
         if (f < n_vec_all) {
           const int tile = S.cand_tiles[f >> 5], t = f & 31;
-          const int pc = tile / kTilesPerPiece, g = tile - pc * kTilesPerPiece;
-          const int v = pc * kVecPerPiece + g * kTileLanes + (t & 7) + kConsumers * (t >> 3);
+          const int pc = tile / kTilesPerPiece;
+          const int v = pc * kVecPerPiece + tile_vector(tile - pc * kTilesPerPiece, t);
           if (v < rb.nvec) {
             vi[u] = v;
             wv[u] = __ldg(body + v);
@@ -783,83 +782,88 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
 }
 
 template <int DT>
+__device__ __forceinline__ float vector_max(const uint4& wv) {
+  if (DT == 0) {
+    __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.x),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+    const __nv_bfloat162 b = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.z),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
+    a = __hmax2_nan(a, b);
+    return max_nan(__low2float(a), __high2float(a));
+  }
+  return max_nan(max_nan(__uint_as_float(wv.x), __uint_as_float(wv.y)),
+                 max_nan(__uint_as_float(wv.z), __uint_as_float(wv.w)));
+}
+
+// Consumer warp: reduces whole pieces (this warp takes every 8th piece of the
+// CTA). Per block of 4 rounds, each 8-lane group's maximum is one tile key;
+// for greedy rows the warp instead folds the piece's (largest key, lowest
+// vector holding it) into the row's running argmax.
+template <int DT>
 __device__ void consumer(const Params& p, Smem& S, long long total) {
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const volatile uint32_t* abort_flag = p.abort_flag;
-  int it = 0;
-  for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it) {
-    const int stage = it % kStages;
-    const int q = it % kKeyQueue;
-    const bool landed = mbar_wait(&S.full[stage], (uint32_t)(it / kStages) & 1u, abort_flag);
+  const long long mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  for (long long it = warp; it < mine; it += kConsumerWarps) {
+    const int stage = (int)(it % kStages);
+    const int q = (int)(it % kKeyQueue);
+    const bool landed = mbar_wait(&S.full[stage], (uint32_t)((it / kStages) & 1), abort_flag);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) raise_timeout(p);
       return;
     }
     const PieceDesc dsc = S.desc[stage];
     const int nvec = dsc.nvec;
-
-    // tile maximum of this thread's 4 vectors, then of its 8-lane group
+    const bool argmax = (dsc.head & kDescArgmax) != 0;
     const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
-    // maximum of each of this thread's 4 vectors, then of the 4
-    float vm[kVecPerThread];
+    uint32_t* keys_out = p.tile_keys + (size_t)dsc.slot * p.geo.tiles + dsc.pp * kTilesPerPiece;
+    uint32_t best_key = 0u;  // greedy: this lane's largest key and its lowest vector
+    int best_v = 0;
+#pragma unroll 2
+    for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
+      uint4 wv[4];
 #pragma unroll
-    for (int j = 0; j < kVecPerThread; ++j) {
-      const int v = tid + kConsumers * j;
-      vm[j] = -INFINITY;
-      if (v < nvec) {
-        if (DT == 0) {
-          const uint4 wv = st4[v];
-          __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.x),
-                                         *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-          const __nv_bfloat162 b = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.z),
-                                               *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
-          a = __hmax2_nan(a, b);
-          vm[j] = max_nan(__low2float(a), __high2float(a));
-        } else {
-          const float4 wv = reinterpret_cast<const float4*>(st4)[v];
-          vm[j] = max_nan(max_nan(wv.x, wv.y), max_nan(wv.z, wv.w));
+      for (int rr = 0; rr < 4; ++rr) {
+        const int v = 32 * (4 * blk + rr) + lane;
+        if (v < nvec) wv[rr] = st4[v];
+      }
+      float m = -INFINITY;
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int v = 32 * (4 * blk + rr) + lane;
+        if (v < nvec) {
+          const float vmax = vector_max<DT>(wv[rr]);
+          m = max_nan(m, vmax);
+          if (argmax) {
+            const uint32_t k = key_of(vmax);
+            if (k > best_key) {
+              best_key = k;
+              best_v = v;
+            }
+          }
         }
       }
-    }
-    const float m = max_nan(max_nan(vm[0], vm[1]), max_nan(vm[2], vm[3]));
-    const uint32_t own_key = key_of(m);
-    uint32_t key = own_key;
-    key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
-    key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
-    key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
-    if (dsc.head & kDescArgmax) {
-      // greedy row: this warp's best (logit, lowest vector) over its 4 tiles;
-      // vectors are in logit order, so the lowest vector holding the maximum
-      // holds the lowest-index maximum of the warp
-      uint32_t wmax = max(key, __shfl_xor_sync(0xffffffffu, key, 8));
-      wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, 16));
-      unsigned long long comp = 0ull;
-      if (own_key == wmax && nvec > 0) {  // this lane holds the warp's maximum
-        int jf = 0;
-#pragma unroll
-        for (int j = kVecPerThread - 1; j >= 0; --j)
-          if (key_of(vm[j]) == wmax) jf = j;
-        comp = composite(wmax, dsc.pp * kVecPerPiece + tid + kConsumers * jf);
+      if (!argmax) {
+        uint32_t key = key_of(m);
+        key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+        key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+        key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
+        if ((lane & (kTileLanes - 1)) == 0) keys_out[4 * blk + (lane >> 3)] = key;
       }
+    }
+    if (argmax) {
+      unsigned long long comp = best_key ? composite(best_key, dsc.pp * kVecPerPiece + best_v) : 0ull;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const unsigned long long oc = shfl_xor_u64(comp, o);
         comp = oc > comp ? oc : comp;
       }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
-        if (comp) red_max_gpu(p.row_best + dsc.slot, comp);
-      }
-    } else {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[stage]);  // this warp is done with the stage
-      if ((lane & (kTileLanes - 1)) == 0)
-        p.tile_keys[(size_t)dsc.slot * p.geo.tiles + dsc.pp * kTilesPerPiece + (tid >> 3)] = key;
+      if (lane == 0 && comp) red_max_gpu(p.row_best + dsc.slot, comp);
     }
-    __syncwarp();  // orders the key stores before lane 0's arrival below
+    __syncwarp();  // the stage is read and the keys are stored before lane 0 signals
     int ok = 1;
     if (lane == 0) {
+      mbar_arrive(&S.empty[stage]);
       // the publisher must have taken queue slot q's previous piece
       if (!mbar_wait(&S.kempty[q], ((uint32_t)(it / kKeyQueue) & 1u) ^ 1u, abort_flag)) {
         raise_timeout(p);
@@ -1064,10 +1068,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], kConsumerWarps);
+      mbar_init(&S.empty[s], 1);
     }
     for (int s = 0; s < kKeyQueue; ++s) {
-      mbar_init(&S.kfull[s], kConsumerWarps);
+      mbar_init(&S.kfull[s], 1);
       mbar_init(&S.kempty[s], 1);
     }
     fence_barrier_init();
