@@ -85,7 +85,7 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests) {
   p.abort_flag = reinterpret_cast<uint32_t*>(base + L.abort_flag);
   p.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
   p.tile_keys = reinterpret_cast<uint32_t*>(base + L.tile_keys);
-  p.res_key = reinterpret_cast<uint32_t*>(base + L.res_key);
+  p.res_prob = reinterpret_cast<float*>(base + L.res_prob);
   p.res_idx = reinterpret_cast<int32_t*>(base + L.res_idx);
   p.res_flag = reinterpret_cast<uint32_t*>(base + L.res_flag);
   p.n_slots = n_slots;

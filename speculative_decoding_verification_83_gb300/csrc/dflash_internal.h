@@ -91,14 +91,14 @@ struct Params {
   uint32_t* abort_flag; // [1]
   unsigned long long* row_best;  // [kMaxCounterSlots]: greedy rows' best (key, index) composite
   uint32_t* tile_keys;  // [n_slots, geo.tiles]
-  uint32_t* res_key;    // [n_slots, kMaxTopK]
+  float* res_prob;      // [n_slots, kMaxTopK]: filtered probability (sampling rows)
   int32_t* res_idx;     // [n_slots, kMaxTopK]
   uint32_t* res_flag;   // [n_slots]
   int n_slots;
 };
 
 struct WorkspaceLayout {
-  size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_key, res_idx, res_flag, total;
+  size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_prob, res_idx, res_flag, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -129,7 +129,7 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.abort_flag = off; off = align_up(off + sizeof(uint32_t), 256);
   L.row_best = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)kMaxCounterSlots, 256);
   L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
-  L.res_key = off;    off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * kMaxTopK, 256);
+  L.res_prob = off;   off = align_up(off + sizeof(float) * (size_t)n_slots * kMaxTopK, 256);
   L.res_idx = off;    off = align_up(off + sizeof(int32_t) * (size_t)n_slots * kMaxTopK, 256);
   L.res_flag = off;   off = align_up(off + sizeof(uint32_t) * (size_t)n_slots, 256);
   L.total = off;

@@ -75,9 +75,9 @@ struct Smem {
   int16_t req_of_ord[kMaxB];
   union {
     uint32_t key_cache[kKeyCache];
-    struct {
-      int32_t idx[kMaxRowsPerRequest][32];
-      float prob[kMaxRowsPerRequest][32];
+    struct {  // rows padded to 33 words: lane i reading row 2i hits bank 2i
+      int32_t idx[kMaxRowsPerRequest][33];
+      float prob[kMaxRowsPerRequest][33];
     } lists;
   } u;
   uint32_t hist[256];
@@ -342,6 +342,54 @@ __device__ __forceinline__ void for_each_row_logit(const RowBody& rb, int V, int
   }
 }
 
+// ---- filtering and drawing ---------------------------------------------------------
+// Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
+// over the survivors, top-p cut, renormalisation. Returns this lane's
+// probability (0 outside the kept set) and sets idx to -1 there.
+__device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
+                                             int lane) {
+  const bool in_k = lane < k_eff && idx >= 0;
+  const float x = value_of_key(key);
+  const float z = x / T;
+  const float z0 = __shfl_sync(0xffffffffu, z, 0);
+  const float w = in_k ? expf(z - z0) : 0.0f;
+  bool keep = in_k;
+  if (top_p < 1.0f) {
+    const float W = warp_sum(w);
+    const float pi = w / W;
+    const float incl = warp_inclusive_scan(pi, lane);
+    float before = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) before = 0.0f;
+    keep = keep && (before < top_p);
+  }
+  const float wk = keep ? w : 0.0f;
+  const float Wk = warp_sum(wk);
+  if (!keep) idx = -1;
+  return keep ? wk / Wk : 0.0f;
+}
+
+// Inverse CDF in ascending token order: the smallest token whose cumulative
+// weight exceeds u * total; if rounding leaves none, the last token with
+// positive weight; tokens marked -1 have no weight.
+__device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane) {
+  int32_t key = tok >= 0 ? tok : INT_MAX;
+  float wt = tok >= 0 ? w : 0.0f;
+  warp_sort32_asc(key, wt, lane);
+  const float cum = warp_inclusive_scan(wt, lane);
+  const float total = __shfl_sync(0xffffffffu, cum, 31);
+  const float t = u * total;
+  const uint32_t hit = __ballot_sync(0xffffffffu, wt > 0.0f && t < cum);
+  int chosen;
+  if (hit) {
+    chosen = __ffs(hit) - 1;
+  } else {
+    const uint32_t pos = __ballot_sync(0xffffffffu, wt > 0.0f);
+    chosen = pos ? 31 - __clz(pos) : 0;
+  }
+  const int32_t r = __shfl_sync(0xffffffffu, key, chosen);
+  return r == INT_MAX ? -1 : r;
+}
+
 // ---- row final ----------------------------------------------------------------------
 // Leaves the row's sorted top-k composites in the group's first warp (lane l:
 // rank l in `top_a`) and in the workspace.
@@ -537,65 +585,27 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     unsigned long long b = lane + 32 < n_c ? S.cand[lane + 32] : 0ull;
     warp_sort64_desc(a, b, lane);
     top_a = a;
-    // workspace copy of ranks < k (k <= 32): the request final reads it
-    const bool valid = lane < k && lane < n_c;
-    p.res_key[(size_t)slot * kMaxTopK + lane] = valid ? composite_key(a) : 0u;
-    p.res_idx[(size_t)slot * kMaxTopK + lane] = valid ? composite_idx(a) : -1;
+    if (p.task == kTaskVerify) {
+      // the row's filtered distribution (ranks < k, k <= 32), which the
+      // request final reads
+      const bool valid = lane < k && lane < n_c;
+      int32_t idx = valid ? composite_idx(a) : -1;
+      const float T = __ldg(p.temperature + S.req_of_ord[si.ord]);
+      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T, p.top_p, lane);
+      p.res_idx[(size_t)slot * kMaxTopK + lane] = idx;
+      p.res_prob[(size_t)slot * kMaxTopK + lane] = pr;
+    }
     if (lane == 0) p.res_flag[slot] = bad ? 1u : 0u;
     if (bad && lane == 0 && p.status) atomicOr(p.status, kStatusBadRow);
   }
   fin_sync();
 }
 
-// ---- filtering and drawing ---------------------------------------------------------
-// Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
-// over the survivors, top-p cut, renormalisation. Returns this lane's
-// probability (0 outside the kept set) and sets idx to -1 there.
-__device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
-                                             int lane) {
-  const bool in_k = lane < k_eff && idx >= 0;
-  const float x = value_of_key(key);
-  const float z = x / T;
-  const float z0 = __shfl_sync(0xffffffffu, z, 0);
-  const float w = in_k ? expf(z - z0) : 0.0f;
-  bool keep = in_k;
-  if (top_p < 1.0f) {
-    const float W = warp_sum(w);
-    const float pi = w / W;
-    const float incl = warp_inclusive_scan(pi, lane);
-    float before = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) before = 0.0f;
-    keep = keep && (before < top_p);
-  }
-  const float wk = keep ? w : 0.0f;
-  const float Wk = warp_sum(wk);
-  if (!keep) idx = -1;
-  return keep ? wk / Wk : 0.0f;
-}
-
-// Inverse CDF in ascending token order: the smallest token whose cumulative
-// weight exceeds u * total; if rounding leaves none, the last token with
-// positive weight; tokens marked -1 have no weight.
-__device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane) {
-  int32_t key = tok >= 0 ? tok : INT_MAX;
-  float wt = tok >= 0 ? w : 0.0f;
-  warp_sort32_asc(key, wt, lane);
-  const float cum = warp_inclusive_scan(wt, lane);
-  const float total = __shfl_sync(0xffffffffu, cum, 31);
-  const float t = u * total;
-  const uint32_t hit = __ballot_sync(0xffffffffu, wt > 0.0f && t < cum);
-  int chosen;
-  if (hit) {
-    chosen = __ffs(hit) - 1;
-  } else {
-    const uint32_t pos = __ballot_sync(0xffffffffu, wt > 0.0f);
-    chosen = pos ? 31 - __clz(pos) : 0;
-  }
-  const int32_t r = __shfl_sync(0xffffffffu, key, chosen);
-  return r == INT_MAX ? -1 : r;
-}
-
 // ---- request final (sampling verification) -------------------------------------------
+// The rows arrive filtered (kept tokens and probabilities). One lane per draft
+// position runs the accept test u < p(d)/q(d); the first failing position (or
+// gamma when none fails) is where the residual max(0, p - q) (or the bonus
+// distribution p) is drawn from.
 __device__ void request_final(const Params& p, Smem& S, int ord) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int gamma = p.gamma, V = p.geo.V;
@@ -603,64 +613,49 @@ __device__ void request_final(const Params& p, Smem& S, int ord) {
   int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
   const int32_t* d = p.draft_tokens + (size_t)b * gamma;
   const int per_s = 2 * gamma + 1;
-
-  // sampling request: filter every row into shared lists (warps in parallel)
   const int slot0 = ord * per_s;
-  const float T = __ldg(p.temperature + b);
   for (int r = w; r < per_s; r += kFinWarps) {
     const size_t s = (size_t)(slot0 + r);
-    uint32_t key = lane < p.top_k ? __ldcg(p.res_key + s * kMaxTopK + lane) : 0u;
-    int32_t idx = lane < p.top_k ? __ldcg(p.res_idx + s * kMaxTopK + lane) : -1;
-    const float pr = filter_lane(key, idx, p.top_k, T, p.top_p, lane);
-    S.u.lists.idx[r][lane] = idx;
-    S.u.lists.prob[r][lane] = pr;
+    S.u.lists.idx[r][lane] = __ldcg(p.res_idx + s * kMaxTopK + lane);
+    S.u.lists.prob[r][lane] = __ldcg(p.res_prob + s * kMaxTopK + lane);
   }
   fin_sync();
   if (w == 0) {
     uint32_t st = 0;
     for (int r = lane; r < per_s; r += 32)
       if (__ldcg(p.res_flag + slot0 + r)) st |= kStatusBadRow;
-    int n = 0;
-    int32_t last = -1;
-    bool rejected = false;
-    for (int i = 0; i < gamma; ++i) {
+    bool reject = false;
+    if (lane < gamma) {
+      const int i = lane;
       const int32_t di = __ldg(d + i);
       if (di < 0 || di >= V) st |= kStatusBadToken;
-      const int32_t ti = S.u.lists.idx[2 * i][lane];
-      const float pi = S.u.lists.prob[2 * i][lane];
-      const int32_t qi_idx = S.u.lists.idx[2 * i + 1][lane];
-      const float qi = S.u.lists.prob[2 * i + 1][lane];
-      const uint32_t hp = __ballot_sync(0xffffffffu, ti == di && di >= 0);
-      const uint32_t hq = __ballot_sync(0xffffffffu, qi_idx == di && di >= 0);
-      const float p_d = hp ? __shfl_sync(0xffffffffu, pi, __ffs(hp) - 1) : 0.0f;
-      const float q_d = hq ? __shfl_sync(0xffffffffu, qi, __ffs(hq) - 1) : 0.0f;
-      const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
-      const float u = uniform24(wd.x);
-      const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
-      if (u < ratio) {
-        ++n;
-        continue;
+      float p_d = 0.0f, q_d = 0.0f;
+      for (int m = 0; m < 32; ++m) {
+        if (S.u.lists.idx[2 * i][m] == di) p_d = S.u.lists.prob[2 * i][m];
+        if (S.u.lists.idx[2 * i + 1][m] == di) q_d = S.u.lists.prob[2 * i + 1][m];
       }
+      if (di < 0) p_d = q_d = 0.0f;  // -1 marks dropped entries
+      const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
+      const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
+      reject = !(uniform24(wd.x) < ratio);
+    }
+    const uint32_t rej = __ballot_sync(0xffffffffu, reject);
+    const int n = rej ? __ffs(rej) - 1 : gamma;  // drafts accepted
+    const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)n, 0u);
+    const int row = 2 * n;  // target row of position n (the bonus row when n == gamma)
+    const int32_t ti = S.u.lists.idx[row][lane];
+    const float pi = S.u.lists.prob[row][lane];
+    float wt = pi;
+    if (n < gamma) {
       // residual max(0, p - q) over the target's kept tokens
       float q_of_t = 0.0f;
-      for (int m = 0; m < 32; ++m) {
-        const int32_t qm = S.u.lists.idx[2 * i + 1][m];
-        if (qm == ti && ti >= 0) q_of_t = S.u.lists.prob[2 * i + 1][m];
-      }
+      for (int m = 0; m < 32; ++m)
+        if (ti >= 0 && S.u.lists.idx[row + 1][m] == ti) q_of_t = S.u.lists.prob[row + 1][m];
       const float r = ti >= 0 ? fmaxf(pi - q_of_t, 0.0f) : 0.0f;
-      const bool any = __ballot_sync(0xffffffffu, r > 0.0f) != 0u;
-      last = draw_ascending(ti, any ? r : pi, uniform24(wd.y), lane);
-      if (last < 0) last = __shfl_sync(0xffffffffu, ti, 0);
-      rejected = true;
-      break;
+      if (__ballot_sync(0xffffffffu, r > 0.0f) != 0u) wt = r;
     }
-    if (!rejected) {
-      const int32_t tg = S.u.lists.idx[2 * gamma][lane];
-      const float pg = S.u.lists.prob[2 * gamma][lane];
-      const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)gamma, 0u);
-      last = draw_ascending(tg, pg, uniform24(wd.y), lane);
-      if (last < 0) last = __shfl_sync(0xffffffffu, tg, 0);
-    }
+    int32_t last = draw_ascending(ti, wt, uniform24(wd.y), lane);
+    if (last < 0) last = __shfl_sync(0xffffffffu, ti, 0);
     for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? last : -1);
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
