@@ -61,6 +61,8 @@ def _bind(lib):
     lib.oracle_filter_row_sparse.restype = I
     lib.oracle_verify.argtypes = [P, P, P, I, I, I, I, P, I, F, U64, P, P, P, P, I, I]
     lib.oracle_verify.restype = I
+    lib.oracle_verify_margins.argtypes = [P, P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, I, I]
+    lib.oracle_verify_margins.restype = I
     lib.oracle_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, I, I]
     lib.oracle_verify_greedy.restype = I
     lib.oracle_sample_rows.argtypes = [P, I, I, I, P, I, F, U64, P, P, P, I, I]
@@ -174,12 +176,14 @@ def _ranges(n: int, parts: int):
 
 
 def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads=None,
-           requests=None, lib=None):
+           requests=None, lib=None, split_margins=False):
     """Sampling-mode verification (greedy for requests with temperature 0).
 
     Returns (tokens [B, gamma+1], accept_len [B], margin [B], status).
     ``requests`` (optional iterable of request indices) restricts the work to
     those requests; the other rows of the outputs stay -1 / 0.
+    With ``split_margins`` the third item is the pair (accept margin [B],
+    draw margin [B]): the accept tests and top-p cuts, and the final draw.
     """
     lib = lib or _load()
     X = _contig(target)
@@ -194,6 +198,7 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
     tokens = np.full((B, gamma + 1), -1, np.int32)
     lens = np.zeros(B, np.int32)
     margin = np.full(B, np.inf, np.float64)
+    margin_draw = np.full(B, np.inf, np.float64)
     nthreads = threads or default_threads()
     if requests is None:
         todo = _ranges(B, nthreads * 4)
@@ -202,9 +207,10 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
 
     def run(rng):
         st = np.zeros(1, np.uint32)
-        rc = lib.oracle_verify(_ptr(X), _ptr(Y), _ptr(d), B, gamma, V, dt, _ptr(T), int(top_k),
-                               float(top_p), int(seed), _ptr(tokens), _ptr(lens), _ptr(margin),
-                               _ptr(st), rng[0], rng[1])
+        rc = lib.oracle_verify_margins(_ptr(X), _ptr(Y), _ptr(d), B, gamma, V, dt, _ptr(T),
+                                       int(top_k), float(top_p), int(seed), _ptr(tokens),
+                                       _ptr(lens), _ptr(margin), _ptr(margin_draw), _ptr(st),
+                                       rng[0], rng[1])
         if rc != 0:
             raise RuntimeError(f"oracle_verify failed: {rc}")
         return int(st[0])
@@ -217,7 +223,9 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
     status = 0
     for s in statuses:
         status |= s
-    return tokens, lens, margin, status
+    if split_margins:
+        return tokens, lens, (margin, margin_draw), status
+    return tokens, lens, np.minimum(margin, margin_draw), status
 
 
 def verify_greedy(target, draft_tokens, threads=None, lib=None):

@@ -315,10 +315,11 @@ int oracle_verify_greedy(const void* target, const int32_t* draft_tokens, int B,
   return ORC_OK;
 }
 
-int oracle_verify(const void* target, const void* draft, const int32_t* draft_tokens, int B,
-                  int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
-                  uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, double* margin,
-                  uint32_t* status, int b_begin, int b_end) {
+int oracle_verify_margins(const void* target, const void* draft, const int32_t* draft_tokens,
+                          int B, int gamma, int V, int dtype, const float* temperature, int top_k,
+                          float top_p, uint64_t seed, int32_t* out_tokens,
+                          int32_t* out_accept_len, double* margin_accept, double* margin_draw,
+                          uint32_t* status, int b_begin, int b_end) {
   if (!target || !draft || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
       B < 0 || gamma < 1 || V < 1 || !(top_p > 0.0f))
     return ORC_ERR_INVALID_ARG;
@@ -342,10 +343,12 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
     const char* Yb = (const char*)draft + (size_t)b * (size_t)gamma * row_bytes;
     const int32_t* d = draft_tokens + (size_t)b * gamma;
     int32_t* out = out_tokens + (size_t)b * (gamma + 1);
-    double mg = DBL_MAX;
+    double mg = DBL_MAX;   /* accept tests and top-p cuts */
+    double mgd = DBL_MAX;  /* the final inverse-CDF draw */
     if (!temperature_kind(temperature[b], &st)) {
       greedy_request(Xb, d, gamma, V, dtype, out, out_accept_len + b, &st);
-      if (margin) margin[b] = mg;
+      if (margin_accept) margin_accept[b] = mg;
+      if (margin_draw) margin_draw[b] = mgd;
       continue;
     }
     const double T = (double)temperature[b];
@@ -388,7 +391,7 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
         r[j] = p[j] - q[j] > 0.0 ? p[j] - q[j] : 0.0;
         Zr += r[j];
       }
-      last = draw_ascending(Zr > 0.0 ? r : p, V, u_draw, &mg);
+      last = draw_ascending(Zr > 0.0 ? r : p, V, u_draw, &mgd);
       rejected = 1;
       break;
     }
@@ -399,12 +402,13 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
       } else {
         float u_draw;
         oracle_uniforms(seed, (uint32_t)b, (uint32_t)gamma, 0u, NULL, &u_draw);
-        last = draw_ascending(p, V, u_draw, &mg);
+        last = draw_ascending(p, V, u_draw, &mgd);
       }
     }
     out[n] = last;
     out_accept_len[b] = n + 1;
-    if (margin) margin[b] = mg;
+    if (margin_accept) margin_accept[b] = mg;
+    if (margin_draw) margin_draw[b] = mgd;
   }
   free(p);
   free(q);
@@ -412,6 +416,28 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
   free(x);
   if (status) *status |= st;
   return ORC_OK;
+}
+
+int oracle_verify(const void* target, const void* draft, const int32_t* draft_tokens, int B,
+                  int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
+                  uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, double* margin,
+                  uint32_t* status, int b_begin, int b_end) {
+  if (!margin)
+    return oracle_verify_margins(target, draft, draft_tokens, B, gamma, V, dtype, temperature,
+                                 top_k, top_p, seed, out_tokens, out_accept_len, NULL, NULL,
+                                 status, b_begin, b_end);
+  if (b_begin < 0) b_begin = 0;
+  if (b_end > B) b_end = B;
+  const int n = b_end > b_begin ? b_end - b_begin : 0;
+  double* md = (double*)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1));
+  if (!md) return ORC_ERR_NOMEM;
+  int rc = oracle_verify_margins(target, draft, draft_tokens, B, gamma, V, dtype, temperature,
+                                 top_k, top_p, seed, out_tokens, out_accept_len, margin, md,
+                                 status, b_begin, b_end);
+  for (int i = 0; i < n && rc == ORC_OK; ++i)
+    if (md[b_begin + i] < margin[b_begin + i]) margin[b_begin + i] = md[b_begin + i];
+  free(md);
+  return rc;
 }
 
 int oracle_sample_rows(const void* logits, int R, int V, int dtype, const float* temperature,

@@ -83,6 +83,17 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
                   uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, double* margin,
                   uint32_t* status, int b_begin, int b_end);
 
+/* oracle_verify with the decision margins split: margin_accept ([B],
+ * optional) covers the accept tests and the top-p cuts, margin_draw ([B],
+ * optional) the final residual or bonus draw. Over the full vocabulary the
+ * draw's cumulative weights are a few parts per million apart, so its margin
+ * is small on every row while the accept margins are not. */
+int oracle_verify_margins(const void* target, const void* draft, const int32_t* draft_tokens,
+                          int B, int gamma, int V, int dtype, const float* temperature, int top_k,
+                          float top_p, uint64_t seed, int32_t* out_tokens,
+                          int32_t* out_accept_len, double* margin_accept, double* margin_draw,
+                          uint32_t* status, int b_begin, int b_end);
+
 /* Greedy verification: argmax prefix match, requests [b_begin, b_end). */
 int oracle_verify_greedy(const void* target, const int32_t* draft_tokens, int B, int gamma, int V,
                          int dtype, int32_t* out_tokens, int32_t* out_accept_len,

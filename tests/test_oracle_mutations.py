@@ -20,8 +20,8 @@ MUTATIONS = {
     "accept_test_flipped": ("if (u_acc < (float)ratio) {", "if (u_acc > (float)ratio) {"),
     "residual_sign": ("r[j] = p[j] - q[j] > 0.0 ? p[j] - q[j] : 0.0;",
                       "r[j] = q[j] - p[j] > 0.0 ? q[j] - p[j] : 0.0;"),
-    "residual_dropped": ("last = draw_ascending(Zr > 0.0 ? r : p, V, u_draw, &mg);",
-                         "last = draw_ascending(p, V, u_draw, &mg);"),
+    "residual_dropped": ("last = draw_ascending(Zr > 0.0 ? r : p, V, u_draw, &mgd);",
+                         "last = draw_ascending(p, V, u_draw, &mgd);"),
     "no_renormalise_after_top_p": ("p[t] = p[t] / Wkept;", "p[t] = p[t] / W;"),
     "temperature_multiplies": ("p[t] = exp(e[t].x / T - zmax);", "p[t] = exp(e[t].x * T - zmax);"),
     "tie_break_high_index": ("return (ea->j < eb->j) ? -1 : (ea->j > eb->j) ? 1 : 0;",

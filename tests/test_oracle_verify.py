@@ -277,3 +277,26 @@ def test_sampler_follows_filtered_distribution():
     tok, _, _ = oracle.sample_rows(np.broadcast_to(x, (10, V)), np.zeros(10, np.float32), 20,
                                    0.95, 5)
     assert np.all(tok == np.argmax(x))
+
+
+def test_split_margins_recombine():
+    """The accept/draw margins are a split of the single margin: same outputs,
+    and their minimum is the combined margin (greedy requests keep both open)."""
+    inp = synth.make_workload("tiny_v1024", data_seed=3)
+    B = 6
+    X = np.broadcast_to(inp.target, (B,) + inp.target.shape[1:])
+    Y = np.broadcast_to(inp.draft, (B,) + inp.draft.shape[1:])
+    gamma, V = inp.shape[1], inp.shape[2]
+    # drafts: each request's row argmax for some positions, a random token for others
+    rng = np.random.default_rng(5)
+    d = np.where(rng.random((B, gamma)) < 0.5, np.argmax(inp.draft[0], axis=-1)[None, :],
+                 rng.integers(0, V, (B, gamma))).astype(np.int32)
+    T = np.array([1.0, 0.0, 0.7, 1.0, 0.0, 1.3], np.float32)
+    for k, tp in ((20, 0.95), (0, 1.0)):
+        t1, l1, m, s1 = oracle.verify(X, Y, d, T, k, tp, 11)
+        t2, l2, (ma, md), s2 = oracle.verify(X, Y, d, T, k, tp, 11, split_margins=True)
+        assert np.array_equal(t1, t2) and np.array_equal(l1, l2) and s1 == s2
+        assert np.array_equal(m, np.minimum(ma, md))
+        greedy = T == 0
+        assert np.all(ma[greedy] > 1e300) and np.all(md[greedy] > 1e300)
+        assert np.all(md[~greedy] < 1e300)  # every sampling request draws once
