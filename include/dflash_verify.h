@@ -47,8 +47,9 @@
  *    off); softmax over the survivors; top-p keeps the shortest prefix of
  *    that order whose mass reaches top_p (top_p >= 1: off) and renormalises.
  *    Supported: 1 <= top_k <= DFLASH_MAX_TOP_K with any top_p in (0, 1], or
- *    top-k off with top_p >= 1 (full-vocabulary softmax). Other combinations
- *    return DFLASH_ERR_UNSUPPORTED.
+ *    top-k off with top_p >= 1 (full-vocabulary softmax; dflash_verify and
+ *    dflash_verify_host only). Other combinations return
+ *    DFLASH_ERR_UNSUPPORTED.
  */
 #ifndef DFLASH_VERIFY_H
 #define DFLASH_VERIFY_H
@@ -128,7 +129,9 @@ int dflash_workspace_init(void* workspace, size_t bytes, void* stream);
  * Accept test at position i: u < p_i(d_i) / q_i(d_i) in fp32 (q = 0 with
  * p > 0 accepts; p = q = 0 rejects). The residual and bonus draws take the
  * smallest token index whose cumulative weight (ascending token order)
- * exceeds u * total. 1 <= gamma <= 64, 1 <= V < 2^31, B >= 1. */
+ * exceeds u * total; over the full vocabulary (top-k off, top_p >= 1) the
+ * cumulative weights are carried in float-float and the comparison is taken
+ * on their fp32 roundings. 1 <= gamma <= 32, 1 <= V < 2^31, 1 <= B <= 2048. */
 int dflash_verify(const void* target_logits, const void* draft_logits,
                   const int32_t* draft_tokens, int B, int gamma, int V, int dtype,
                   const float* temperature, int top_k, float top_p, uint64_t seed,

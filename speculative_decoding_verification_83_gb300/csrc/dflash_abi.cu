@@ -48,13 +48,32 @@ int sm_count() {
 
 int esize_of(int dtype) { return dtype == DFLASH_BF16 ? 2 : (dtype == DFLASH_F32 ? 4 : 0); }
 
-// Filter mode of a call: 1 = top-k (1..32) with any top_p, 0 = unsupported,
-// -1 = invalid.
+// Filter mode of a call: 1 = top-k (1..32) with any top_p, 2 = full
+// vocabulary (top-k off, top_p >= 1), 0 = unsupported, -1 = invalid.
+constexpr int kModeTopK = 1, kModeFullVocab = 2;
 int filter_mode(int V, int top_k, float top_p) {
   if (!(top_p > 0.0f) || std::isnan(top_p)) return -1;
   const bool k_on = top_k > 0 && top_k < V;
-  if (k_on && top_k <= DFLASH_MAX_TOP_K) return 1;
+  if (k_on && top_k <= DFLASH_MAX_TOP_K) return kModeTopK;
+  if (!k_on && top_p >= 1.0f) return kModeFullVocab;
   return 0;
+}
+
+// 2^(j/64), j < 64, split into fp32 pairs (hi = nearest float, lo = the rest)
+// for the full-vocabulary draw's exp; computed once in double precision.
+struct Exp2Table {
+  float hi[kExpTable], lo[kExpTable];
+  Exp2Table() {
+    for (int j = 0; j < kExpTable; ++j) {
+      const double v = std::exp2((double)j / kExpTable);
+      hi[j] = (float)v;
+      lo[j] = (float)(v - (double)hi[j]);
+    }
+  }
+};
+const Exp2Table& exp2_table() {
+  static const Exp2Table t;
+  return t;
 }
 
 int check_shape(int B, int gamma, int V, int dtype) {
@@ -72,13 +91,13 @@ int check_aligned(const void* p, int esize, const char* name) {
   return DFLASH_OK;
 }
 
-size_t verify_workspace(int B, int gamma, int V, int dtype) {
+size_t verify_workspace(int B, int gamma, int V, int dtype, bool fullvocab = false) {
   const Geometry g = make_geometry(V, esize_of(dtype));
-  return make_layout(B * (2 * gamma + 1), B, g).total;
+  return make_layout(B * (2 * gamma + 1), B, g, fullvocab).total;
 }
 
-void bind_workspace(Params& p, void* ws, int n_slots, int n_requests) {
-  const WorkspaceLayout L = make_layout(n_slots, n_requests, p.geo);
+void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, bool fullvocab = false) {
+  const WorkspaceLayout L = make_layout(n_slots, n_requests, p.geo, fullvocab);
   unsigned char* base = static_cast<unsigned char*>(ws);
   p.row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
   p.req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
@@ -88,7 +107,37 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests) {
   p.res_prob = reinterpret_cast<float*>(base + L.res_prob);
   p.res_idx = reinterpret_cast<int32_t*>(base + L.res_idx);
   p.res_flag = reinterpret_cast<uint32_t*>(base + L.res_flag);
+  p.fv_draw = fullvocab ? reinterpret_cast<FvDraw*>(base + L.fv_draw) : nullptr;
   p.n_slots = n_slots;
+}
+
+// the full-vocabulary draw's second pass over the rows the accept test left
+int run_fullvocab_draw(const Params& p, void* ws, void* stream) {
+  const WorkspaceLayout L = make_layout(p.n_slots, p.B, p.geo, true);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  FvParams f;
+  memset(&f, 0, sizeof f);
+  f.target = p.target;
+  f.draft = p.draft;
+  f.temperature = p.temperature;
+  f.B = p.B;
+  f.gamma = p.gamma;
+  f.V = p.geo.V;
+  f.dtype = p.dtype;
+  f.n_slices = fv_slices(p.geo.V);
+  f.seed = p.seed;
+  f.out_tokens = p.out_tokens;
+  f.draw = reinterpret_cast<const FvDraw*>(base + L.fv_draw);
+  f.part = reinterpret_cast<float4*>(base + L.fv_part);
+  f.sum = reinterpret_cast<float4*>(base + L.fv_sum);
+  f.last = reinterpret_cast<int2*>(base + L.fv_last);
+  f.abort_flag = p.abort_flag;
+  const Exp2Table& t = exp2_table();
+  memcpy(f.exp_hi, t.hi, sizeof t.hi);
+  memcpy(f.exp_lo, t.lo, sizeof t.lo);
+  const int e = launch_fullvocab_draw(f, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "launching the full-vocabulary draw");
+  return DFLASH_OK;
 }
 
 int run(Params& p, int total_slots, void* stream) {
@@ -125,11 +174,11 @@ size_t dflash_workspace_bytes(int B, int gamma, int V, int dtype, int top_k, flo
   if (B < 1 || B > kMaxB || gamma < 1 || gamma > kMaxGamma || V < 1 || !esize_of(dtype)) return 0;
   const int mode = filter_mode(V, top_k, top_p);
   if (mode <= 0 && !(top_k == 1 && top_p >= 1.0f)) return 0;
-  return verify_workspace(B, gamma, V, dtype);
+  return verify_workspace(B, gamma, V, dtype, mode == kModeFullVocab);
 }
 
 size_t dflash_rows_workspace_bytes(int R, int V, int dtype, int top_k, float top_p) {
-  if (R < 1 || V < 1 || !esize_of(dtype) || filter_mode(V, top_k, top_p) <= 0) return 0;
+  if (R < 1 || V < 1 || !esize_of(dtype) || filter_mode(V, top_k, top_p) != kModeTopK) return 0;
   const int chunk = R < kMaxCounterSlots ? R : kMaxCounterSlots;
   return make_layout(chunk, 1, make_geometry(V, esize_of(dtype))).total;
 }
@@ -155,15 +204,18 @@ int dflash_verify(const void* target_logits, const void* draft_logits, const int
   if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
   if (mode == 0)
     return fail(DFLASH_ERR_UNSUPPORTED,
-                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d, top_k < V)", top_k,
-                (double)top_p, DFLASH_MAX_TOP_K);
+                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d and top_k < V, or top-k "
+                "off with top_p = 1)",
+                top_k, (double)top_p, DFLASH_MAX_TOP_K);
+  const bool fullvocab = mode == kModeFullVocab;
   const int es = esize_of(dtype);
   if ((rc = check_aligned(target_logits, es, "target_logits")) ||
       (rc = check_aligned(draft_logits, es, "draft_logits")))
     return rc;
-  if (workspace_bytes < verify_workspace(B, gamma, V, dtype))
+  const size_t need = verify_workspace(B, gamma, V, dtype, fullvocab);
+  if (workspace_bytes < need)
     return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
-                workspace_bytes, verify_workspace(B, gamma, V, dtype));
+                workspace_bytes, need);
   Params p = base_params(dtype, V);
   p.target = static_cast<const unsigned char*>(target_logits);
   p.draft = static_cast<const unsigned char*>(draft_logits);
@@ -175,12 +227,15 @@ int dflash_verify(const void* target_logits, const void* draft_logits, const int
   p.top_p = top_p >= 1.0f ? 1.0f : top_p;
   p.seed = seed;
   p.task = kTaskVerify;
+  p.fullvocab = fullvocab ? 1 : 0;
   p.out_tokens = out_tokens;
   p.out_len = out_accept_len;
   p.status = status;
-  bind_workspace(p, workspace, B * (2 * gamma + 1), B);
+  bind_workspace(p, workspace, B * (2 * gamma + 1), B, fullvocab);
   // the slot count depends on the device-side temperatures; launch for the maximum
-  return run(p, B * (2 * gamma + 1), stream);
+  rc = run(p, B * (2 * gamma + 1), stream);
+  if (rc || !fullvocab) return rc;
+  return run_fullvocab_draw(p, workspace, stream);
 }
 
 int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
@@ -307,9 +362,9 @@ static int rows_task(int task, const void* logits, int R, int V, int dtype, cons
   if (!logits || !temperature || !workspace) return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
   const int mode = filter_mode(V, top_k, top_p);
   if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
-  if (mode == 0)
+  if (mode != kModeTopK)
     return fail(DFLASH_ERR_UNSUPPORTED,
-                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d, top_k < V)", top_k,
+                "top_k=%d with top_p=%g is not supported here (need 1 <= top_k <= %d, top_k < V)", top_k,
                 (double)top_p, DFLASH_MAX_TOP_K);
   int rc = check_aligned(logits, esize_of(dtype), "logits");
   if (rc) return rc;

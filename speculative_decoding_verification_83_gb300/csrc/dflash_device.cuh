@@ -43,6 +43,14 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   return r;
 }
 
+// 2^x on the special-function unit (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22; results below 2^-126 flush to zero, -inf gives 0)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // ---- Philox4x32-10 (Salmon et al., SC'11) ----------------------------------------
 // Ten rounds; each round multiplies words 0 and 2 by the two round
 // multipliers, mixes the high halves with words 1 and 3 and the key, and the

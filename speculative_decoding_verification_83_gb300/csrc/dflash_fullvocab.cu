@@ -1,0 +1,482 @@
+// dflash_fullvocab.cu -- second pass of the full-vocabulary mode (top-k off,
+// top-p 1): the residual or bonus draw over the whole vocabulary.
+//
+// With no top-k the filtered distributions are the plain softmax
+// p_j = exp(x_j/T - max/T) / S over all V tokens, so the residual
+// max(0, p - q) at the first rejected position spans the vocabulary too (the
+// accept rule min(1, p/q), the residual and the bonus token of standard
+// speculative sampling; "DFlash2 用投机解码给 Qwen 提速", bml.asia, the
+// draft/verify loop, and "无损加速是真的吗？Qwen3.8-27B-DFlash2 如何保证输出与
+// 目标模型完全一致", rytg.cn, section 投机解码如何白嫖速度, step 3). The first
+// pass (the stream in dflash_sweep.cu) ran the accept tests and left, per
+// request, the accepted count n and the row maxima; this pass draws the token
+// at position n by the inverse CDF in ascending token order.
+//
+// Precision. At V = 248320 a token holds a few parts per million of the mass,
+// so the draw compares a cumulative sum with u * total to far better than
+// fp32 resolution: every weight here is a float-float pair (about 44 bits),
+// and exp() is Tang's table-driven method ("Table-driven implementation of
+// the exponential function in IEEE floating-point arithmetic", ACM TOMS 15(2),
+// 1989) evaluated in float-float: exp(a) = 2^m * 2^(j/64) * exp(r) with
+// N = 64 m + j = round(a * 64/ln2), |r| <= ln2/128 and exp(r) - 1 by its
+// Taylor series to r^4, relative error about 1e-9. The decision itself is
+// taken in fp32 like every other decision of the step: the smallest token
+// whose cumulative weight, rounded to fp32, exceeds u * total rounded to fp32.
+// All arithmetic uses explicitly rounded intrinsics, so the per-token weights
+// are bit-identical wherever they are recomputed.
+//
+// Three launches, no waits between CTAs:
+//  1. fv_norm:  per (slice, request), the slice's sums of exp weights of the
+//               target and draft rows -> the normalisers S_x, S_y.
+//  2. fv_slice: per (slice, request), the slice's sum of the residual weights
+//               r_j = max(0, p_j - q_j) and of p_j, and the last token of the
+//               slice with a positive weight.
+//  3. fv_pick:  per request, the slice where the cumulative weight crosses
+//               u * total, then a block scan inside that slice.
+
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+
+namespace dflash {
+namespace {
+
+// ---- float-float arithmetic (Dekker / Knuth error-free transformations) --------------
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return {s, e};
+}
+// requires |a| >= |b| (or a == 0)
+__device__ __forceinline__ ff fast_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  const ff s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ ff ff_neg(ff a) { return {-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+  const float p = __fmul_rn(a.hi, b.hi);
+  float e = __fmaf_rn(a.hi, b.hi, -p);
+  e = __fmaf_rn(a.hi, b.lo, __fmaf_rn(a.lo, b.hi, e));
+  return fast_two_sum(p, e);
+}
+// x * b for a plain float x
+__device__ __forceinline__ ff ff_scale(float x, ff b) {
+  const float p = __fmul_rn(x, b.hi);
+  const float e = __fmaf_rn(x, b.lo, __fmaf_rn(x, b.hi, -p));
+  return {p, e};
+}
+// 1 / a; the remainder 1 - a.hi * RN(1/a.hi) is exact in fp32
+__device__ __forceinline__ ff ff_recip(ff a) {
+  const float r = __frcp_rn(a.hi);
+  const float e = __fmaf_rn(-a.lo, r, __fmaf_rn(-a.hi, r, 1.0f));
+  return fast_two_sum(r, __fmul_rn(e, r));
+}
+// the fp32 value nearest to hi + lo (one correctly rounded addition)
+__device__ __forceinline__ float ff_round(ff a) { return __fadd_rn(a.hi, a.lo); }
+
+__device__ __forceinline__ ff shfl_down_ff(ff a, int o) {
+  return {__shfl_down_sync(0xffffffffu, a.hi, o), __shfl_down_sync(0xffffffffu, a.lo, o)};
+}
+__device__ __forceinline__ ff shfl_up_ff(ff a, int o) {
+  return {__shfl_up_sync(0xffffffffu, a.hi, o), __shfl_up_sync(0xffffffffu, a.lo, o)};
+}
+// warp sum in a fixed tree; the result is valid in lane 0
+__device__ __forceinline__ ff warp_sum_ff(ff a) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const ff b = shfl_down_ff(a, o);
+    if ((threadIdx.x & 31) + o < 32) a = ff_add(a, b);
+  }
+  return a;
+}
+
+// ---- exp in float-float ------------------------------------------------------------
+constexpr double kInvLn2x64 = 92.33248261689366;        // 64 / ln 2
+constexpr double kLn2Div64 = 0.010830424696249145;      // ln 2 / 64
+constexpr float kK_hi = (float)kInvLn2x64;
+constexpr float kK_lo = (float)(kInvLn2x64 - (double)(float)kInvLn2x64);
+constexpr float kL_hi = (float)kLn2Div64;
+constexpr float kL_lo = (float)(kLn2Div64 - (double)(float)kLn2Div64);
+constexpr float kRoundMagic = 12582912.0f;              // 1.5 * 2^23
+
+// exp(a) for a <= 0 (a.hi >= -87: below that the weight is under 2^-125 of
+// the row's largest and is taken as 0). th/tl: 2^(j/64) as fp32 pairs.
+__device__ __forceinline__ ff exp_ff(ff a, const float* th, const float* tl) {
+  if (!(a.hi >= -87.0f)) return {0.0f, 0.0f};
+  // t = a * 64/ln2 as a pair; N = round(t) = 64 m + j
+  const float t_hi = __fmul_rn(a.hi, kK_hi);
+  float t_lo = __fmaf_rn(a.hi, kK_hi, -t_hi);
+  t_lo = __fmaf_rn(a.hi, kK_lo, __fmaf_rn(a.lo, kK_hi, t_lo));
+  const float v = __fadd_rn(t_hi, kRoundMagic);  // |t_hi| < 2^22: v's last bit is N's
+  const int N = __float_as_int(v) - __float_as_int(kRoundMagic);
+  const float Nf = __fsub_rn(v, kRoundMagic);
+  const float g = __fadd_rn(__fsub_rn(t_hi, Nf), t_lo);  // t - N, |g| <= 1/2; t_hi - Nf is exact
+  const float r = __fmaf_rn(g, kL_hi, __fmul_rn(g, kL_lo));  // r = g * ln2/64
+  // exp(r) - 1 = r + r^2 (1/2 + r (1/6 + r/24)) + O(r^5), |r| <= 0.0055
+  const float c4 = __fmaf_rn(r, 1.0f / 24.0f, 1.0f / 6.0f);
+  const float c2 = __fmaf_rn(r, c4, 0.5f);
+  const float P = __fmaf_rn(__fmul_rn(r, r), c2, r);
+  const int j = N & (kExpTable - 1), m = N >> 6;
+  const float Th = th[j], Tl = tl[j];
+  const ff w = fast_two_sum(Th, __fmaf_rn(Th, P, Tl));  // 2^(j/64) (1 + P)
+  const float sc = __int_as_float((m + 127) << 23);      // 2^m, m >= -126
+  return {__fmul_rn(w.hi, sc), __fmul_rn(w.lo, sc)};
+}
+
+__device__ __forceinline__ float fv_load(const unsigned char* row, int j, int dtype) {
+  if (dtype == 0) {
+    const unsigned short h = __ldg(reinterpret_cast<const unsigned short*>(row) + j);
+    return __uint_as_float((uint32_t)h << 16);
+  }
+  return __ldg(reinterpret_cast<const float*>(row) + j);
+}
+
+// ---- per-request context -------------------------------------------------------------
+struct Req {
+  bool live;
+  bool residual;
+  int n;
+  const unsigned char* x;  // target row n
+  const unsigned char* y;  // draft row n (residual)
+  ff inv_t;                // 1 / T
+  ff zmx, zmy;             // row maxima / T
+};
+
+__device__ __forceinline__ Req load_req(const FvParams& f, int b) {
+  Req q;
+  q.live = false;
+  if (*reinterpret_cast<const volatile uint32_t*>(f.abort_flag) != 0u) return q;
+  const FvDraw d = f.draw[b];
+  // a request drawn by the first pass has 0 <= n <= gamma; a residual needs n < gamma
+  if (d.mode != kFvResidual && d.mode != kFvBonus) return q;
+  if (d.n < 0 || d.n > f.gamma || (d.mode == kFvResidual && d.n >= f.gamma)) return q;
+  const float T = __ldg(f.temperature + b);
+  if (!(T > 0.0f) || !(T < INFINITY)) return q;
+  q.live = true;
+  q.residual = d.mode == kFvResidual;
+  q.n = d.n;
+  const size_t row_bytes = (size_t)f.V * (f.dtype == 0 ? 2 : 4);
+  q.x = f.target + ((size_t)b * (f.gamma + 1) + d.n) * row_bytes;
+  q.y = q.residual ? f.draft + ((size_t)b * f.gamma + d.n) * row_bytes : nullptr;
+  const float r = __frcp_rn(T);
+  q.inv_t = fast_two_sum(r, __fmul_rn(__fmaf_rn(-T, r, 1.0f), r));
+  q.zmx = ff_scale(d.mx, q.inv_t);
+  q.zmy = ff_scale(d.my, q.inv_t);
+  return q;
+}
+
+// unnormalised weight exp(x/T - max/T) of logit x
+__device__ __forceinline__ ff weight(float x, ff inv_t, ff zmax, const float* th, const float* tl) {
+  const ff z = ff_scale(x, inv_t);
+  const ff s = two_sum(z.hi, -zmax.hi);
+  const ff a = {s.hi, __fadd_rn(s.lo, __fsub_rn(z.lo, zmax.lo))};
+  return exp_ff(a, th, tl);
+}
+
+struct Norm {
+  ff inv_sx, inv_sy;
+};
+
+// 1/S_x and 1/S_y of request b from the first launch's slice sums, summed in
+// a fixed order (the same in every CTA that needs them). Run by warp 0;
+// the result is written to *out.
+__device__ __forceinline__ void load_norm(const FvParams& f, int b, bool residual, Norm* out) {
+  const int lane = threadIdx.x & 31;
+  ff sx = {0.0f, 0.0f}, sy = {0.0f, 0.0f};
+  const float4* part = f.part + (size_t)b * f.n_slices;
+  for (int s = lane; s < f.n_slices; s += 32) {
+    const float4 v = part[s];
+    sx = ff_add(sx, ff{v.x, v.y});
+    sy = ff_add(sy, ff{v.z, v.w});
+  }
+  sx = warp_sum_ff(sx);
+  sy = warp_sum_ff(sy);
+  if (lane == 0) {
+    out->inv_sx = ff_recip(sx);
+    out->inv_sy = residual ? ff_recip(sy) : ff{0.0f, 0.0f};
+  }
+}
+
+// p_j and r_j = max(0, p_j - q_j) of a token with target logit x and draft
+// logit y (r = 0 for a bonus draw)
+__device__ __forceinline__ void token_weights(const Req& q, const Norm& nm, float x, float y, const float* th,
+                                              const float* tl, ff& p, ff& r) {
+  p = ff_mul(weight(x, q.inv_t, q.zmx, th, tl), nm.inv_sx);
+  r = {0.0f, 0.0f};
+  if (q.residual) {
+    const ff qq = ff_mul(weight(y, q.inv_t, q.zmy, th, tl), nm.inv_sy);
+    const ff d = ff_add(p, ff_neg(qq));
+    if (d.hi > 0.0f) r = d;
+  }
+}
+
+// exclusive warp scan of a pair (fixed order)
+__device__ __forceinline__ ff warp_exclusive_ff(ff v, ff& inclusive) {
+  const int lane = threadIdx.x & 31;
+  ff incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff n = shfl_up_ff(incl, o);
+    if (lane >= o) incl = ff_add(n, incl);
+  }
+  inclusive = incl;
+  ff ex = shfl_up_ff(incl, 1);
+  if (lane == 0) ex = {0.0f, 0.0f};
+  return ex;
+}
+
+// block sum (kFvThreads threads) in a fixed order; valid in thread 0
+__device__ __forceinline__ ff block_sum_ff(ff a, ff* scratch) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  a = warp_sum_ff(a);
+  if (lane == 0) scratch[w] = a;
+  __syncthreads();
+  ff t = {0.0f, 0.0f};
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kFvThreads / 32; ++i) t = ff_add(t, scratch[i]);
+  __syncthreads();
+  return t;
+}
+
+__device__ __forceinline__ void load_table(const FvParams& f, float* th, float* tl) {
+  for (int i = threadIdx.x; i < kExpTable; i += blockDim.x) {
+    th[i] = f.exp_hi[i];
+    tl[i] = f.exp_lo[i];
+  }
+}
+
+// ---- launch 1: slice sums of the exp weights ---------------------------------------------
+__global__ void __launch_bounds__(kFvThreads) fv_norm_kernel(const FvParams f) {
+  __shared__ float th[kExpTable], tl[kExpTable];
+  __shared__ ff scratch[kFvThreads / 32];
+  const int s = blockIdx.x, b = blockIdx.y;
+  const Req q = load_req(f, b);
+  if (!q.live) return;
+  load_table(f, th, tl);
+  __syncthreads();
+  ff sx = {0.0f, 0.0f}, sy = {0.0f, 0.0f};
+  const int j0 = s * kFvSlice + threadIdx.x;
+  const int jn = min(f.V, (s + 1) * kFvSlice);
+  float xs[kFvPerThread], ys[kFvPerThread];
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    const int j = j0 + k * kFvThreads;
+    xs[k] = j < jn ? fv_load(q.x, j, f.dtype) : -INFINITY;
+    ys[k] = (q.residual && j < jn) ? fv_load(q.y, j, f.dtype) : -INFINITY;
+  }
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    sx = ff_add(sx, weight(xs[k], q.inv_t, q.zmx, th, tl));
+    if (q.residual) sy = ff_add(sy, weight(ys[k], q.inv_t, q.zmy, th, tl));
+  }
+  sx = block_sum_ff(sx, scratch);
+  sy = block_sum_ff(sy, scratch);
+  if (threadIdx.x == 0) f.part[(size_t)b * f.n_slices + s] = make_float4(sx.hi, sx.lo, sy.hi, sy.lo);
+}
+
+// ---- launch 2: slice sums of the draw weights ---------------------------------------------
+__global__ void __launch_bounds__(kFvThreads) fv_slice_kernel(const FvParams f) {
+  __shared__ float th[kExpTable], tl[kExpTable];
+  __shared__ ff scratch[kFvThreads / 32];
+  __shared__ Norm nm_s;
+  __shared__ int last_r, last_p;
+  const int s = blockIdx.x, b = blockIdx.y;
+  const Req q = load_req(f, b);
+  if (!q.live) return;
+  load_table(f, th, tl);
+  if (threadIdx.x < 32) load_norm(f, b, q.residual, &nm_s);
+  if (threadIdx.x == 0) {
+    last_r = -1;
+    last_p = -1;
+  }
+  __syncthreads();
+  const Norm nm = nm_s;
+  ff sr = {0.0f, 0.0f}, sp = {0.0f, 0.0f};
+  int lr = -1, lp = -1;
+  const int j0 = s * kFvSlice + threadIdx.x;
+  const int jn = min(f.V, (s + 1) * kFvSlice);
+  float xs[kFvPerThread], ys[kFvPerThread];
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    const int j = j0 + k * kFvThreads;
+    xs[k] = j < jn ? fv_load(q.x, j, f.dtype) : -INFINITY;
+    ys[k] = (q.residual && j < jn) ? fv_load(q.y, j, f.dtype) : -INFINITY;
+  }
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    const int j = j0 + k * kFvThreads;
+    ff p, r;
+    token_weights(q, nm, xs[k], ys[k], th, tl, p, r);
+    sp = ff_add(sp, p);
+    sr = ff_add(sr, r);
+    if (p.hi > 0.0f) lp = j;
+    if (r.hi > 0.0f) lr = j;
+  }
+  if (lr >= 0) atomicMax(&last_r, lr);
+  if (lp >= 0) atomicMax(&last_p, lp);
+  sr = block_sum_ff(sr, scratch);  // its barriers also order the atomics above
+  sp = block_sum_ff(sp, scratch);
+  if (threadIdx.x == 0) {
+    const size_t c = (size_t)b * f.n_slices + s;
+    f.sum[c] = make_float4(sr.hi, sr.lo, sp.hi, sp.lo);
+    f.last[c] = make_int2(last_r, last_p);
+  }
+}
+
+// ---- launch 3: the draw ---------------------------------------------------------------------
+__global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
+  __shared__ float th[kExpTable], tl[kExpTable];
+  __shared__ Norm nm_s;
+  __shared__ ff warp_tot[kFvThreads / 32];
+  __shared__ int sel_slice, use_r, hit, last_any;
+  __shared__ float target_f;
+  __shared__ ff slice_base;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const Req q = load_req(f, b);
+  if (!q.live) return;
+  load_table(f, th, tl);
+  if (tid < 32) load_norm(f, b, q.residual, &nm_s);
+  __syncthreads();
+  const Norm nm = nm_s;
+  const size_t c0 = (size_t)b * f.n_slices;
+
+  if (w == 0) {
+    // totals of both weights (fixed order), then the kind the draw uses: the
+    // residual, or p when there is none (bonus draw, or a residual that is
+    // zero everywhere)
+    ff zr = {0.0f, 0.0f}, zp = {0.0f, 0.0f};
+    int lr = -1, lp = -1;
+    for (int s = lane; s < f.n_slices; s += 32) {
+      const float4 v = f.sum[c0 + s];
+      zr = ff_add(zr, ff{v.x, v.y});
+      zp = ff_add(zp, ff{v.z, v.w});
+      const int2 l = f.last[c0 + s];
+      lr = max(lr, l.x);
+      lp = max(lp, l.y);
+    }
+    zr = warp_sum_ff(zr);
+    zp = warp_sum_ff(zp);
+    const bool resid = __shfl_sync(0xffffffffu, (int)(q.residual && zr.hi > 0.0f), 0) != 0;
+    const ff z = resid ? zr : zp;
+    lr = __reduce_max_sync(0xffffffffu, lr);
+    lp = __reduce_max_sync(0xffffffffu, lp);
+    const float u = uniform24(step_uniform_words(f.seed, (uint32_t)b, (uint32_t)q.n, 0u).y);
+    const float tf = __shfl_sync(0xffffffffu, ff_round(ff_scale(u, z)), 0);
+    // first slice whose cumulative weight (rounded to fp32) exceeds tf
+    ff carry = {0.0f, 0.0f};
+    int found = -1;
+    ff found_base = {0.0f, 0.0f};
+    for (int s0 = 0; s0 < f.n_slices && found < 0; s0 += 32) {
+      const int s = s0 + lane;
+      ff v = {0.0f, 0.0f};
+      if (s < f.n_slices) {
+        const float4 t = f.sum[c0 + s];
+        v = resid ? ff{t.x, t.y} : ff{t.z, t.w};
+      }
+      ff incl;  // scans over the 32 slices of this round
+      const ff excl = ff_add(carry, warp_exclusive_ff(v, incl));
+      const ff cum = ff_add(carry, incl);
+      const uint32_t ball = __ballot_sync(0xffffffffu, s < f.n_slices && tf < ff_round(cum));
+      if (ball) {
+        const int l = __ffs(ball) - 1;
+        found = s0 + l;  // the cumulative weight before it is lane l's excl
+        found_base = {__shfl_sync(0xffffffffu, excl.hi, l), __shfl_sync(0xffffffffu, excl.lo, l)};
+      }
+      carry = {__shfl_sync(0xffffffffu, cum.hi, 31), __shfl_sync(0xffffffffu, cum.lo, 31)};
+    }
+    if (lane == 0) {
+      sel_slice = found;
+      use_r = resid ? 1 : 0;
+      target_f = tf;
+      slice_base = found_base;
+      last_any = resid ? lr : lp;
+      hit = INT_MAX;
+    }
+  }
+  __syncthreads();
+  const int s = sel_slice;
+  int32_t* out = f.out_tokens + (size_t)b * (f.gamma + 1) + q.n;
+  if (s < 0) {  // rounding left no token above u * total: the last with weight
+    if (tid == 0) *out = last_any >= 0 ? last_any : 0;
+    return;
+  }
+  // inside slice s: thread t owns tokens s*kFvSlice + t*kFvPerThread + k, in order
+  const bool resid = use_r != 0;
+  const int jb = s * kFvSlice + tid * kFvPerThread;
+  float xs[kFvPerThread], ys[kFvPerThread];
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    const int j = jb + k;
+    xs[k] = j < f.V ? fv_load(q.x, j, f.dtype) : -INFINITY;
+    ys[k] = (q.residual && j < f.V) ? fv_load(q.y, j, f.dtype) : -INFINITY;
+  }
+  ff wk[kFvPerThread];
+  ff mine = {0.0f, 0.0f};
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    ff p, r;
+    token_weights(q, nm, xs[k], ys[k], th, tl, p, r);
+    wk[k] = resid ? r : p;
+    mine = ff_add(mine, wk[k]);
+  }
+  // exclusive block scan of the threads' sums
+  ff incl;
+  const ff ex = warp_exclusive_ff(mine, incl);
+  if (lane == 31) warp_tot[w] = incl;
+  __syncthreads();
+  ff cum = slice_base;
+  for (int i = 0; i < w; ++i) cum = ff_add(cum, warp_tot[i]);
+  cum = ff_add(cum, ex);
+  const float tf = target_f;
+  int first = INT_MAX;
+#pragma unroll
+  for (int k = 0; k < kFvPerThread; ++k) {
+    cum = ff_add(cum, wk[k]);
+    if (first == INT_MAX && wk[k].hi > 0.0f && tf < ff_round(cum)) first = jb + k;
+  }
+  if (first != INT_MAX) atomicMin(&hit, first);
+  __syncthreads();
+  if (tid == 0) {
+    int j = hit;
+    if (j == INT_MAX) {
+      // the slice sum said the crossing is here but the in-slice order
+      // rounded past it: the slice's last token with weight
+      const int2 l = f.last[c0 + s];
+      j = resid ? l.x : l.y;
+      if (j < 0) j = last_any >= 0 ? last_any : 0;
+    }
+    *out = j;
+  }
+}
+
+}  // namespace
+
+int launch_fullvocab_draw(const FvParams& f, void* stream) {
+  if (f.B <= 0 || f.n_slices <= 0) return 0;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const dim3 grid((unsigned)f.n_slices, (unsigned)f.B);
+  fv_norm_kernel<<<grid, kFvThreads, 0, st>>>(f);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  fv_slice_kernel<<<grid, kFvThreads, 0, st>>>(f);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  fv_pick_kernel<<<f.B, kFvThreads, 0, st>>>(f);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -2,6 +2,8 @@
 // the host side (dflash_abi.cu) and the kernels (dflash_sweep.cu).
 #pragma once
 
+#include <vector_types.h>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -63,6 +65,27 @@ struct Geometry {
   int tiles;     // ppr * kTilesPerPiece
 };
 
+// ---- full-vocabulary mode (top-k off, top-p 1) --------------------------------------
+// The stream reduces each piece of a sampling row to (max, sum of exp) for the
+// accept test; the residual or bonus draw then runs as a second pass over the
+// one or two rows it needs, cut into slices of kFvSlice logits.
+constexpr int kFvSlice = 4096;
+constexpr int kFvThreads = 256;
+constexpr int kFvPerThread = kFvSlice / kFvThreads;
+constexpr int kExpTable = 64;  // 2^(j/64), j < 64, as fp32 pairs
+
+enum FvMode : int { kFvNone = 0, kFvResidual = 1, kFvBonus = 2 };
+
+// what the accept test left for the draw of request b
+struct FvDraw {
+  int n;       // drafts accepted: the token drawn goes to position n
+  int mode;    // FvMode
+  float mx;    // largest logit of target row n
+  float my;    // largest logit of draft row n (residual)
+};
+
+inline int fv_slices(int V) { return (V + kFvSlice - 1) / kFvSlice; }
+
 struct Params {
   // inputs
   const unsigned char* target;  // verify: [B, gamma+1, V]; rows tasks: [R, V]
@@ -76,6 +99,7 @@ struct Params {
   float top_p;
   unsigned long long seed;
   int task;
+  int fullvocab;                // top-k off and top-p 1: softmax over the whole vocabulary
   int row_base;                 // rows tasks: index of this launch's first row
   Geometry geo;
   // outputs
@@ -90,15 +114,34 @@ struct Params {
   uint32_t* req_cnt;    // [B]
   uint32_t* abort_flag; // [1]
   unsigned long long* row_best;  // [kMaxCounterSlots]: greedy rows' best (key, index) composite
-  uint32_t* tile_keys;  // [n_slots, geo.tiles]
+  uint32_t* tile_keys;  // [n_slots, geo.tiles]; full-vocabulary rows: float2 (max, sum) per piece
   float* res_prob;      // [n_slots, kMaxTopK]: filtered probability (sampling rows)
   int32_t* res_idx;     // [n_slots, kMaxTopK]
   uint32_t* res_flag;   // [n_slots]
+  FvDraw* fv_draw;      // [B]: full-vocabulary mode
   int n_slots;
 };
 
+// Second pass of the full-vocabulary draw (dflash_fullvocab.cu).
+struct FvParams {
+  const unsigned char* target;  // [B, gamma+1, V]
+  const unsigned char* draft;   // [B, gamma, V]
+  const float* temperature;     // [B]
+  int B, gamma, V, dtype, n_slices;
+  unsigned long long seed;
+  int32_t* out_tokens;          // [B, gamma+1]
+  const FvDraw* draw;           // [B]
+  float4* part;                 // [B, n_slices]: slice sums of the two rows' exp weights
+  float4* sum;                  // [B, n_slices]: slice sums of the residual and of p
+  int2* last;                   // [B, n_slices]: last token with positive residual / p
+  const uint32_t* abort_flag;
+  float exp_hi[kExpTable];      // 2^(j/64) = exp_hi[j] + exp_lo[j]
+  float exp_lo[kExpTable];
+};
+
 struct WorkspaceLayout {
-  size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_prob, res_idx, res_flag, total;
+  size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_prob, res_idx, res_flag;
+  size_t fv_draw, fv_part, fv_sum, fv_last, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -120,8 +163,7 @@ inline Geometry make_geometry(int V, int esize) {
 // ready for the next call of any shape. The per-row data follows the header.
 constexpr int kMaxCounterSlots = kMaxB * kMaxRowsPerRequest;  // also the rows-task chunk
 
-inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g) {
-  (void)n_requests;
+inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g, bool fullvocab = false) {
   WorkspaceLayout L;
   size_t off = 0;
   L.req_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxB, 256);
@@ -132,6 +174,12 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.res_prob = off;   off = align_up(off + sizeof(float) * (size_t)n_slots * kMaxTopK, 256);
   L.res_idx = off;    off = align_up(off + sizeof(int32_t) * (size_t)n_slots * kMaxTopK, 256);
   L.res_flag = off;   off = align_up(off + sizeof(uint32_t) * (size_t)n_slots, 256);
+  const size_t fv_req = fullvocab ? (size_t)n_requests : 0;
+  const size_t fv_cells = fv_req * (size_t)fv_slices(g.V);
+  L.fv_draw = off;    off = align_up(off + sizeof(FvDraw) * fv_req, 256);
+  L.fv_part = off;    off = align_up(off + 16 * fv_cells, 256);
+  L.fv_sum = off;     off = align_up(off + 16 * fv_cells, 256);
+  L.fv_last = off;    off = align_up(off + 8 * fv_cells, 256);
   L.total = off;
   return L;
 }
@@ -142,6 +190,7 @@ void set_last_error(const char* msg);
 // launches (dflash_sweep.cu); return a cudaError_t value
 int launch_sweep(const Params& p, int grid, void* stream);
 int sweep_smem_bytes();
+int launch_fullvocab_draw(const FvParams& f, void* stream);
 int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* out_accept,
                     float* out_draw, void* stream);
 

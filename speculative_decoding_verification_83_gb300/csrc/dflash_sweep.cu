@@ -61,9 +61,12 @@ struct PieceDesc {
   int slot;
   int pp;      // piece index within the row
   int nvec;    // 16-byte vectors in the stage
-  int head;    // logits before the row's aligned body; + kDescArgmax for greedy rows
+  int head;    // logits before the row's aligned body; + kDescArgmax / kDescStats
+  float scale; // full-vocabulary rows: log2(e) / T
 };
 constexpr int kDescArgmax = 256;  // the consumers track this row's argmax in-stream
+constexpr int kDescStats = 512;   // the consumers reduce the piece to (max, sum of exp)
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct Smem {
   alignas(128) unsigned char ring[kStages][kPieceBytes];
@@ -79,6 +82,11 @@ struct Smem {
       int32_t idx[kMaxRowsPerRequest][33];
       float prob[kMaxRowsPerRequest][33];
     } lists;
+    struct {  // full-vocabulary request final: per row max, sum of exp, bad flag
+      float m[kMaxRowsPerRequest];
+      float s[kMaxRowsPerRequest];
+      int bad[kMaxRowsPerRequest];
+    } fv;
   } u;
   uint32_t hist[256];
   unsigned long long cand[kCandCap];
@@ -759,7 +767,16 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
     S.desc[stage].slot = w.slot;
     S.desc[stage].pp = w.pp;
     S.desc[stage].nvec = nvec;
-    S.desc[stage].head = rb.head + (in_stream_argmax(p, si) ? kDescArgmax : 0);
+    int flags = 0;
+    float scale = 0.0f;
+    if (in_stream_argmax(p, si)) {
+      flags = kDescArgmax;
+    } else if (p.fullvocab && si.sampling) {
+      flags = kDescStats;
+      scale = kLog2e / __ldg(p.temperature + S.req_of_ord[si.ord]);
+    }
+    S.desc[stage].head = rb.head + flags;
+    S.desc[stage].scale = scale;
     if (nvec > 0) {
       mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec * 16u);
       bulk_load(S.ring[stage], rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16, (uint32_t)nvec * 16u,
@@ -790,10 +807,130 @@ __device__ __forceinline__ float vector_max(const uint4& wv) {
                  max_nan(__uint_as_float(wv.z), __uint_as_float(wv.w)));
 }
 
+// Tile keys of a piece: per block of 4 rounds, each 8-lane group's maximum is
+// one tile key. For greedy rows (argmax) the warp instead folds the piece's
+// (largest key, lowest vector holding it) into the row's running argmax.
+template <int DT>
+__device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, int nvec, int slot, int pp,
+                                           bool argmax, int lane) {
+  uint32_t* keys_out = p.tile_keys + (size_t)slot * p.geo.tiles + pp * kTilesPerPiece;
+  uint32_t best_key = 0u;  // greedy: this lane's largest key and its lowest vector
+  int best_v = 0;
+#pragma unroll 2
+  for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
+    uint4 wv[4];
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int v = 32 * (4 * blk + rr) + lane;
+      if (v < nvec) wv[rr] = st4[v];
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int v = 32 * (4 * blk + rr) + lane;
+      if (v < nvec) {
+        const float vmax = vector_max<DT>(wv[rr]);
+        m = max_nan(m, vmax);
+        if (argmax) {
+          const uint32_t k = key_of(vmax);
+          if (k > best_key) {
+            best_key = k;
+            best_v = v;
+          }
+        }
+      }
+    }
+    if (!argmax) {
+      uint32_t key = key_of(m);
+      key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
+      key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
+      key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
+      if ((lane & (kTileLanes - 1)) == 0) keys_out[4 * blk + (lane >> 3)] = key;
+    }
+  }
+  if (argmax) {
+    unsigned long long comp = best_key ? composite(best_key, pp * kVecPerPiece + best_v) : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long oc = shfl_xor_u64(comp, o);
+      comp = oc > comp ? oc : comp;
+    }
+    if (lane == 0 && comp) red_max_gpu(p.row_best + slot, comp);
+  }
+}
+
+// Online (max, sum of exp) of a running set: folds in a block whose largest
+// value is bm and rescales the sum when the maximum grows. An empty set is
+// (-inf, 0).
+__device__ __forceinline__ void stats_raise(float& m, float& s, float bm, float scale) {
+  if (bm > m) {
+    s = m == -INFINITY ? 0.0f : s * ex2_approx((m - bm) * scale);
+    m = bm;
+  }
+}
+// (m, s) of two sets combined
+__device__ __forceinline__ void stats_merge(float& m, float& s, float m2, float s2, float scale) {
+  if (m2 == -INFINITY) return;
+  stats_raise(m, s, m2, scale);
+  s += s2 * ex2_approx((m2 - m) * scale);
+}
+
+// Full-vocabulary rows: a piece's largest logit m and sum of 2^((x - m) *
+// scale) = exp((x - m) / T), written as one float2 per piece (sum NaN when
+// the piece holds a NaN). Precise enough for the accept test; the draw
+// recomputes its sums in float-float.
+template <int DT>
+__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, float scale, float2* out, int lane) {
+  float m = -INFINITY, s = 0.0f;
+  bool nan = false;
+#pragma unroll 2
+  for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
+    uint4 wv[4];
+    float bm = -INFINITY;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int v = 32 * (4 * blk + rr) + lane;
+      if (v < nvec) {
+        wv[rr] = st4[v];
+        bm = max_nan(bm, vector_max<DT>(wv[rr]));
+      }
+    }
+    nan |= isnan(bm);
+    stats_raise(m, s, bm, scale);
+    if (m == -INFINITY) continue;  // nothing above -inf yet
+    // (x - m) first: exact or nearly so for the logits that carry the mass,
+    // and no overflow of m * scale at small temperatures
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int v = 32 * (4 * blk + rr) + lane;
+      if (v >= nvec) continue;
+      const uint32_t ws[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
+      if (DT == 0) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s += ex2_approx((__uint_as_float(ws[e] << 16) - m) * scale);
+          s += ex2_approx((__uint_as_float(ws[e] & 0xffff0000u) - m) * scale);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s += ex2_approx((__uint_as_float(ws[e]) - m) * scale);
+      }
+    }
+  }
+  // combine the lanes
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    stats_merge(m, s, m2, s2, scale);
+  }
+  nan = __any_sync(0xffffffffu, nan);
+  if (lane == 0) *out = make_float2(m, nan ? __int_as_float(0x7fffffff) : s);
+}
+
 // Consumer warp: reduces whole pieces (this warp takes every 8th piece of the
-// CTA). Per block of 4 rounds, each 8-lane group's maximum is one tile key;
-// for greedy rows the warp instead folds the piece's (largest key, lowest
-// vector holding it) into the row's running argmax.
+// CTA) to tile keys, a greedy row's running argmax, or a full-vocabulary
+// row's (max, sum of exp).
 template <int DT>
 __device__ void consumer(const Params& p, Smem& S, long long total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -809,52 +946,12 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
     }
     const PieceDesc dsc = S.desc[stage];
     const int nvec = dsc.nvec;
-    const bool argmax = (dsc.head & kDescArgmax) != 0;
     const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
-    uint32_t* keys_out = p.tile_keys + (size_t)dsc.slot * p.geo.tiles + dsc.pp * kTilesPerPiece;
-    uint32_t best_key = 0u;  // greedy: this lane's largest key and its lowest vector
-    int best_v = 0;
-#pragma unroll 2
-    for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
-      uint4 wv[4];
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int v = 32 * (4 * blk + rr) + lane;
-        if (v < nvec) wv[rr] = st4[v];
-      }
-      float m = -INFINITY;
-#pragma unroll
-      for (int rr = 0; rr < 4; ++rr) {
-        const int v = 32 * (4 * blk + rr) + lane;
-        if (v < nvec) {
-          const float vmax = vector_max<DT>(wv[rr]);
-          m = max_nan(m, vmax);
-          if (argmax) {
-            const uint32_t k = key_of(vmax);
-            if (k > best_key) {
-              best_key = k;
-              best_v = v;
-            }
-          }
-        }
-      }
-      if (!argmax) {
-        uint32_t key = key_of(m);
-        key = max(key, __shfl_xor_sync(0xffffffffu, key, 1));
-        key = max(key, __shfl_xor_sync(0xffffffffu, key, 2));
-        key = max(key, __shfl_xor_sync(0xffffffffu, key, 4));
-        if ((lane & (kTileLanes - 1)) == 0) keys_out[4 * blk + (lane >> 3)] = key;
-      }
-    }
-    if (argmax) {
-      unsigned long long comp = best_key ? composite(best_key, dsc.pp * kVecPerPiece + best_v) : 0ull;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long oc = shfl_xor_u64(comp, o);
-        comp = oc > comp ? oc : comp;
-      }
-      if (lane == 0 && comp) red_max_gpu(p.row_best + dsc.slot, comp);
-    }
+    if (dsc.head & kDescStats)
+      piece_stats<DT>(st4, nvec, dsc.scale,
+                      reinterpret_cast<float2*>(p.tile_keys + (size_t)dsc.slot * p.geo.tiles) + dsc.pp, lane);
+    else
+      piece_keys<DT>(p, st4, nvec, dsc.slot, dsc.pp, (dsc.head & kDescArgmax) != 0, lane);
     __syncwarp();  // the stage is read and the keys are stored before lane 0 signals
     int ok = 1;
     if (lane == 0) {
@@ -997,7 +1094,95 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   if (lane == 0) {
     p.out_len[b] = n + 1;
     if (st && p.status) atomicOr(p.status, st);
+    if (p.fullvocab) p.fv_draw[b] = FvDraw{n, kFvNone, 0.0f, 0.0f};
   }
+}
+
+// Final of a full-vocabulary sampling request (finals group): each row's
+// (max, sum of exp) from its pieces' statistics and the logits outside its
+// aligned body, then the accept test at every draft position at once (lane i:
+// u_i < p_i(d_i) / q_i(d_i)). Emits the accepted drafts and the accept length
+// and leaves the draw at the first rejected position (residual) or at the
+// bonus position to the second pass, with the rows' maxima.
+__device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
+  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
+  const int gamma = p.gamma, V = p.geo.V, per_s = 2 * gamma + 1;
+  const int b = S.req_of_ord[ord];
+  const int slot0 = ord * per_s;
+  const float scale = kLog2e / __ldg(p.temperature + b);  // as the producer computed it
+  for (int r = w; r < per_s; r += kFinWarps) {
+    const SlotInfo si = slot_info(p, S, slot0 + r);
+    const RowBody rb = row_body(si.ptr, V, p.geo.esize);
+    const float2* st = reinterpret_cast<const float2*>(p.tile_keys + (size_t)(slot0 + r) * p.geo.tiles);
+    float m = -INFINITY, sum = 0.0f;
+    bool nan = false;
+    for (int pp = lane; pp < p.geo.ppr; pp += 32) {
+      const float2 v = __ldcg(st + pp);
+      nan |= isnan(v.y);
+      stats_merge(m, sum, v.x, v.y, scale);
+    }
+    const int n_edge = rb.head + (V - rb.tail_start);
+    for (int e = lane; e < n_edge; e += 32) {
+      const int j = e < rb.head ? e : rb.tail_start + (e - rb.head);
+      const float x = load_logit(rb.row, j, p.dtype);
+      nan |= isnan(x);
+      if (!isnan(x)) stats_merge(m, sum, x, 1.0f, scale);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      stats_merge(m, sum, m2, s2, scale);
+    }
+    nan = __any_sync(0xffffffffu, nan);
+    if (lane == 0) {
+      S.u.fv.m[r] = m;
+      S.u.fv.s[r] = sum;
+      S.u.fv.bad[r] = (nan || isnan(sum) || !(fabsf(m) < INFINITY)) ? 1 : 0;
+    }
+  }
+  fin_sync();
+  if (w == 0) {
+    const int32_t* d = p.draft_tokens + (size_t)b * gamma;
+    int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
+    uint32_t st = 0;
+    for (int r = lane; r < per_s; r += 32)
+      if (S.u.fv.bad[r]) st |= kStatusBadRow;
+    bool stop = false;
+    if (lane < gamma) {
+      const int i = lane;
+      const int32_t di = __ldg(d + i);
+      const bool valid = di >= 0 && di < V;
+      if (!valid) st |= kStatusBadToken;
+      if (S.u.fv.bad[2 * i] || S.u.fv.bad[2 * i + 1]) {
+        stop = true;  // a bad row ends the loop at its position
+      } else {
+        float p_d = 0.0f, q_d = 0.0f;  // a token outside the vocabulary has p = q = 0
+        if (valid) {
+          const SlotInfo sx = slot_info(p, S, slot0 + 2 * i);
+          const SlotInfo sy = slot_info(p, S, slot0 + 2 * i + 1);
+          p_d = ex2_approx((load_logit(sx.ptr, di, p.dtype) - S.u.fv.m[2 * i]) * scale) / S.u.fv.s[2 * i];
+          q_d = ex2_approx((load_logit(sy.ptr, di, p.dtype) - S.u.fv.m[2 * i + 1]) * scale) /
+                S.u.fv.s[2 * i + 1];
+        }
+        const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
+        stop = !(uniform24(wd.x) < p_d / q_d);  // q = 0: +inf if p > 0, NaN if p == 0
+      }
+    }
+    const uint32_t ball = __ballot_sync(0xffffffffu, stop);
+    const int n = ball ? __ffs(ball) - 1 : gamma;
+    const bool bad_n = n < gamma ? (S.u.fv.bad[2 * n] || S.u.fv.bad[2 * n + 1]) : S.u.fv.bad[2 * gamma] != 0;
+    const int mode = bad_n ? kFvNone : (n < gamma ? kFvResidual : kFvBonus);
+    // the token at position n is the second pass's (0 when a bad row leaves no draw)
+    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? 0 : -1);
+    st = __reduce_or_sync(0xffffffffu, st);
+    if (lane == 0) {
+      p.out_len[b] = n + 1;
+      p.fv_draw[b] = FvDraw{n, mode, S.u.fv.m[2 * n], n < gamma ? S.u.fv.m[2 * n + 1] : 0.0f};
+      if (st && p.status) atomicOr(p.status, st);
+    }
+  }
+  fin_sync();
 }
 
 // Finals group (4 warps): works through the jobs dealt to this CTA (job j
@@ -1008,13 +1193,24 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
 __device__ void finals(const Params& p, Smem& S) {
   const int gt = fin_tid(), w = gt >> 5;
   const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
-  const int n_row_jobs = verify ? S.n_samp * (2 * p.gamma + 1) : p.B;
-  const int n_jobs = n_row_jobs + (verify ? p.B - S.n_samp : 0);
+  const bool fv = verify && p.fullvocab;
+  const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
+  // row jobs (top-k sampling rows, rows tasks), then request jobs from
+  // request ordinal ord0 on (full-vocabulary sampling requests, greedy ones)
+  const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * per_s : p.B);
+  const int ord0 = fv ? 0 : S.n_samp;
+  const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
   for (int j = blockIdx.x; j < n_jobs; j += gridDim.x) {
     const bool row_job = j < n_row_jobs;
+    const int ord = ord0 + (j - n_row_jobs);
     if (w == 0) {
-      const bool ok = row_job ? wait_rows(p, j, 1)
-                              : wait_rows(p, n_row_jobs + (j - n_row_jobs) * (p.gamma + 1), p.gamma + 1);
+      bool ok;
+      if (row_job)
+        ok = wait_rows(p, j, 1);
+      else if (ord < S.n_samp)
+        ok = wait_rows(p, ord * per_s, per_s);
+      else
+        ok = wait_rows(p, S.n_samp * per_s + (ord - S.n_samp) * per_g, per_g);
       if (gt == 0) {
         if (!ok) raise_timeout(p);
         S.fin_cmd = ok ? 1 : 2;
@@ -1024,8 +1220,12 @@ __device__ void finals(const Params& p, Smem& S) {
     fin_sync();
     if (S.fin_cmd != 1) return;
     if (!row_job) {
-      if (w == 0) greedy_request_final(p, S, S.n_samp + (j - n_row_jobs));
-      fin_sync();
+      if (ord < S.n_samp) {
+        fullvocab_request_final(p, S, ord);
+      } else {
+        if (w == 0) greedy_request_final(p, S, ord);
+        fin_sync();
+      }
       continue;
     }
     const int slot = j;
