@@ -129,7 +129,7 @@ int run_fullvocab_draw(const Params& p, void* ws, void* stream) {
   f.out_tokens = p.out_tokens;
   f.draw = reinterpret_cast<const FvDraw*>(base + L.fv_draw);
   f.part = reinterpret_cast<float4*>(base + L.fv_part);
-  f.sum = reinterpret_cast<float4*>(base + L.fv_sum);
+  f.pos = reinterpret_cast<float4*>(base + L.fv_pos);
   f.last = reinterpret_cast<int2*>(base + L.fv_last);
   f.abort_flag = p.abort_flag;
   const Exp2Table& t = exp2_table();

@@ -25,14 +25,13 @@
 // All arithmetic uses explicitly rounded intrinsics, so the per-token weights
 // are bit-identical wherever they are recomputed.
 //
-// Three launches, no waits between CTAs:
-//  1. fv_norm:  per (slice, request), the slice's sums of exp weights of the
-//               target and draft rows -> the normalisers S_x, S_y.
-//  2. fv_slice: per (slice, request), the slice's sum of the residual weights
-//               r_j = max(0, p_j - q_j) and of p_j, and the last token of the
-//               slice with a positive weight.
-//  3. fv_pick:  per request, the slice where the cumulative weight crosses
-//               u * total, then a block scan inside that slice.
+// Two launches, no waits between CTAs:
+//  1. fv_sums: per (slice, request), the slice's sums of the exp weights of
+//              the target and draft rows (-> the normalisers S_x, S_y), the
+//              same sums over the tokens with p > q (-> the residual's slice
+//              sums), and the slice's last token with weight.
+//  2. fv_pick: per request, the slice where the cumulative weight crosses
+//              u * total, then a block scan inside that slice.
 
 #include <cuda_runtime.h>
 
@@ -153,6 +152,7 @@ struct Req {
   const unsigned char* y;  // draft row n (residual)
   ff inv_t;                // 1 / T
   ff zmx, zmy;             // row maxima / T
+  float sx0, sy0;          // the stream's fp32 normalisers (residual: which side of p = q)
 };
 
 __device__ __forceinline__ Req load_req(const FvParams& f, int b) {
@@ -175,6 +175,8 @@ __device__ __forceinline__ Req load_req(const FvParams& f, int b) {
   q.inv_t = fast_two_sum(r, __fmul_rn(__fmaf_rn(-T, r, 1.0f), r));
   q.zmx = ff_scale(d.mx, q.inv_t);
   q.zmy = ff_scale(d.my, q.inv_t);
+  q.sx0 = d.sx0;
+  q.sy0 = d.sy0;
   return q;
 }
 
@@ -186,13 +188,21 @@ __device__ __forceinline__ ff weight(float x, ff inv_t, ff zmax, const float* th
   return exp_ff(a, th, tl);
 }
 
+// running sum of non-negative pairs: the low parts gather the rounding errors
+// and the pair is renormalised once at the end (acc_done)
+__device__ __forceinline__ void acc_add(ff& acc, ff w) {
+  const ff s = two_sum(acc.hi, w.hi);
+  acc.hi = s.hi;
+  acc.lo = __fadd_rn(acc.lo, __fadd_rn(s.lo, w.lo));
+}
+__device__ __forceinline__ ff acc_done(ff acc) { return fast_two_sum(acc.hi, acc.lo); }
+
 struct Norm {
   ff inv_sx, inv_sy;
 };
 
-// 1/S_x and 1/S_y of request b from the first launch's slice sums, summed in
-// a fixed order (the same in every CTA that needs them). Run by warp 0;
-// the result is written to *out.
+// 1/S_x and 1/S_y of request b from the slice sums, summed in a fixed order
+// (the same wherever they are needed). Run by warp 0; lane 0 writes *out.
 __device__ __forceinline__ void load_norm(const FvParams& f, int b, bool residual, Norm* out) {
   const int lane = threadIdx.x & 31;
   ff sx = {0.0f, 0.0f}, sy = {0.0f, 0.0f};
@@ -208,34 +218,6 @@ __device__ __forceinline__ void load_norm(const FvParams& f, int b, bool residua
     out->inv_sx = ff_recip(sx);
     out->inv_sy = residual ? ff_recip(sy) : ff{0.0f, 0.0f};
   }
-}
-
-// p_j and r_j = max(0, p_j - q_j) of a token with target logit x and draft
-// logit y (r = 0 for a bonus draw)
-__device__ __forceinline__ void token_weights(const Req& q, const Norm& nm, float x, float y, const float* th,
-                                              const float* tl, ff& p, ff& r) {
-  p = ff_mul(weight(x, q.inv_t, q.zmx, th, tl), nm.inv_sx);
-  r = {0.0f, 0.0f};
-  if (q.residual) {
-    const ff qq = ff_mul(weight(y, q.inv_t, q.zmy, th, tl), nm.inv_sy);
-    const ff d = ff_add(p, ff_neg(qq));
-    if (d.hi > 0.0f) r = d;
-  }
-}
-
-// exclusive warp scan of a pair (fixed order)
-__device__ __forceinline__ ff warp_exclusive_ff(ff v, ff& inclusive) {
-  const int lane = threadIdx.x & 31;
-  ff incl = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const ff n = shfl_up_ff(incl, o);
-    if (lane >= o) incl = ff_add(n, incl);
-  }
-  inclusive = incl;
-  ff ex = shfl_up_ff(incl, 1);
-  if (lane == 0) ex = {0.0f, 0.0f};
-  return ex;
 }
 
 // block sum (kFvThreads threads) in a fixed order; valid in thread 0
@@ -258,53 +240,43 @@ __device__ __forceinline__ void load_table(const FvParams& f, float* th, float* 
   }
 }
 
-// ---- launch 1: slice sums of the exp weights ---------------------------------------------
-__global__ void __launch_bounds__(kFvThreads) fv_norm_kernel(const FvParams f) {
-  __shared__ float th[kExpTable], tl[kExpTable];
-  __shared__ ff scratch[kFvThreads / 32];
-  const int s = blockIdx.x, b = blockIdx.y;
-  const Req q = load_req(f, b);
-  if (!q.live) return;
-  load_table(f, th, tl);
-  __syncthreads();
-  ff sx = {0.0f, 0.0f}, sy = {0.0f, 0.0f};
-  const int j0 = s * kFvSlice + threadIdx.x;
-  const int jn = min(f.V, (s + 1) * kFvSlice);
-  float xs[kFvPerThread], ys[kFvPerThread];
+// exclusive warp scan of a pair (fixed order)
+__device__ __forceinline__ ff warp_exclusive_ff(ff v, ff& inclusive) {
+  const int lane = threadIdx.x & 31;
+  ff incl = v;
 #pragma unroll
-  for (int k = 0; k < kFvPerThread; ++k) {
-    const int j = j0 + k * kFvThreads;
-    xs[k] = j < jn ? fv_load(q.x, j, f.dtype) : -INFINITY;
-    ys[k] = (q.residual && j < jn) ? fv_load(q.y, j, f.dtype) : -INFINITY;
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff n = shfl_up_ff(incl, o);
+    if (lane >= o) incl = ff_add(n, incl);
   }
-#pragma unroll
-  for (int k = 0; k < kFvPerThread; ++k) {
-    sx = ff_add(sx, weight(xs[k], q.inv_t, q.zmx, th, tl));
-    if (q.residual) sy = ff_add(sy, weight(ys[k], q.inv_t, q.zmy, th, tl));
-  }
-  sx = block_sum_ff(sx, scratch);
-  sy = block_sum_ff(sy, scratch);
-  if (threadIdx.x == 0) f.part[(size_t)b * f.n_slices + s] = make_float4(sx.hi, sx.lo, sy.hi, sy.lo);
+  inclusive = incl;
+  ff ex = shfl_up_ff(incl, 1);
+  if (lane == 0) ex = {0.0f, 0.0f};
+  return ex;
 }
 
-// ---- launch 2: slice sums of the draw weights ---------------------------------------------
-__global__ void __launch_bounds__(kFvThreads) fv_slice_kernel(const FvParams f) {
+// ---- launch 1: slice sums --------------------------------------------------------------
+// Per (slice, request): S_x and S_y over the slice, and for a residual the
+// same sums over the tokens with p > q, A = sum w_x and B = sum w_y. The
+// residual's slice sum is then A / S_x - B / S_y with the exact normalisers,
+// known only after every slice is summed. Which side of p = q a token is on
+// comes from the stream's fp32 normalisers (w_x S_y0 > w_y S_x0); a token
+// they place wrongly has |p - q| below about 1e-6 p and carries under 1e-11 of
+// the mass.
+__global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   __shared__ float th[kExpTable], tl[kExpTable];
   __shared__ ff scratch[kFvThreads / 32];
-  __shared__ Norm nm_s;
   __shared__ int last_r, last_p;
   const int s = blockIdx.x, b = blockIdx.y;
   const Req q = load_req(f, b);
   if (!q.live) return;
   load_table(f, th, tl);
-  if (threadIdx.x < 32) load_norm(f, b, q.residual, &nm_s);
   if (threadIdx.x == 0) {
     last_r = -1;
     last_p = -1;
   }
   __syncthreads();
-  const Norm nm = nm_s;
-  ff sr = {0.0f, 0.0f}, sp = {0.0f, 0.0f};
+  ff sx = {0.0f, 0.0f}, sy = {0.0f, 0.0f}, ax = {0.0f, 0.0f}, by = {0.0f, 0.0f};
   int lr = -1, lp = -1;
   const int j0 = s * kFvSlice + threadIdx.x;
   const int jn = min(f.V, (s + 1) * kFvSlice);
@@ -315,28 +287,56 @@ __global__ void __launch_bounds__(kFvThreads) fv_slice_kernel(const FvParams f) 
     xs[k] = j < jn ? fv_load(q.x, j, f.dtype) : -INFINITY;
     ys[k] = (q.residual && j < jn) ? fv_load(q.y, j, f.dtype) : -INFINITY;
   }
+  if (q.residual) {
 #pragma unroll
-  for (int k = 0; k < kFvPerThread; ++k) {
-    const int j = j0 + k * kFvThreads;
-    ff p, r;
-    token_weights(q, nm, xs[k], ys[k], th, tl, p, r);
-    sp = ff_add(sp, p);
-    sr = ff_add(sr, r);
-    if (p.hi > 0.0f) lp = j;
-    if (r.hi > 0.0f) lr = j;
+    for (int k = 0; k < kFvPerThread; ++k) {
+      const ff wx = weight(xs[k], q.inv_t, q.zmx, th, tl);
+      const ff wy = weight(ys[k], q.inv_t, q.zmy, th, tl);
+      acc_add(sx, wx);
+      acc_add(sy, wy);
+      if (__fmul_rn(wx.hi, q.sy0) > __fmul_rn(wy.hi, q.sx0)) {
+        acc_add(ax, wx);
+        acc_add(by, wy);
+        lr = j0 + k * kFvThreads;
+      }
+      if (wx.hi > 0.0f) lp = j0 + k * kFvThreads;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < kFvPerThread; ++k) {
+      const ff wx = weight(xs[k], q.inv_t, q.zmx, th, tl);
+      acc_add(sx, wx);
+      if (wx.hi > 0.0f) lp = j0 + k * kFvThreads;
+    }
   }
   if (lr >= 0) atomicMax(&last_r, lr);
   if (lp >= 0) atomicMax(&last_p, lp);
-  sr = block_sum_ff(sr, scratch);  // its barriers also order the atomics above
-  sp = block_sum_ff(sp, scratch);
+  sx = block_sum_ff(acc_done(sx), scratch);  // its barriers also order the atomics above
+  sy = block_sum_ff(acc_done(sy), scratch);
+  ax = block_sum_ff(acc_done(ax), scratch);
+  by = block_sum_ff(acc_done(by), scratch);
   if (threadIdx.x == 0) {
     const size_t c = (size_t)b * f.n_slices + s;
-    f.sum[c] = make_float4(sr.hi, sr.lo, sp.hi, sp.lo);
+    f.part[c] = make_float4(sx.hi, sx.lo, sy.hi, sy.lo);
+    f.pos[c] = make_float4(ax.hi, ax.lo, by.hi, by.lo);
     f.last[c] = make_int2(last_r, last_p);
   }
 }
 
-// ---- launch 3: the draw ---------------------------------------------------------------------
+// ---- launch 2: the draw -----------------------------------------------------------------
+// p_j and r_j = max(0, p_j - q_j) of a token with target logit x and draft
+// logit y (r = 0 for a bonus draw), normalised exactly
+__device__ __forceinline__ void token_weights(const Req& q, const Norm& nm, float x, float y, const float* th,
+                                              const float* tl, ff& p, ff& r) {
+  p = ff_mul(weight(x, q.inv_t, q.zmx, th, tl), nm.inv_sx);
+  r = {0.0f, 0.0f};
+  if (q.residual) {
+    const ff qq = ff_mul(weight(y, q.inv_t, q.zmy, th, tl), nm.inv_sy);
+    const ff d = ff_add(p, ff_neg(qq));
+    if (d.hi > 0.0f) r = d;
+  }
+}
+
 __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   __shared__ float th[kExpTable], tl[kExpTable];
   __shared__ Norm nm_s;
@@ -355,15 +355,23 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   const size_t c0 = (size_t)b * f.n_slices;
 
   if (w == 0) {
-    // totals of both weights (fixed order), then the kind the draw uses: the
-    // residual, or p when there is none (bonus draw, or a residual that is
-    // zero everywhere)
+    // slice sums of the residual (A/S_x - B/S_y, never below 0) and of p
+    // (S_x slice / S_x); the draw uses the residual unless it is zero
+    // everywhere (or this is the bonus draw)
+    auto slice_r = [&](int s) {
+      const float4 v = f.pos[c0 + s];
+      const ff d = ff_add(ff_mul(ff{v.x, v.y}, nm.inv_sx), ff_neg(ff_mul(ff{v.z, v.w}, nm.inv_sy)));
+      return d.hi > 0.0f ? d : ff{0.0f, 0.0f};
+    };
+    auto slice_p = [&](int s) {
+      const float4 v = f.part[c0 + s];
+      return ff_mul(ff{v.x, v.y}, nm.inv_sx);
+    };
     ff zr = {0.0f, 0.0f}, zp = {0.0f, 0.0f};
     int lr = -1, lp = -1;
     for (int s = lane; s < f.n_slices; s += 32) {
-      const float4 v = f.sum[c0 + s];
-      zr = ff_add(zr, ff{v.x, v.y});
-      zp = ff_add(zp, ff{v.z, v.w});
+      if (q.residual) zr = ff_add(zr, slice_r(s));
+      zp = ff_add(zp, slice_p(s));
       const int2 l = f.last[c0 + s];
       lr = max(lr, l.x);
       lp = max(lp, l.y);
@@ -383,10 +391,7 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
     for (int s0 = 0; s0 < f.n_slices && found < 0; s0 += 32) {
       const int s = s0 + lane;
       ff v = {0.0f, 0.0f};
-      if (s < f.n_slices) {
-        const float4 t = f.sum[c0 + s];
-        v = resid ? ff{t.x, t.y} : ff{t.z, t.w};
-      }
+      if (s < f.n_slices) v = resid ? slice_r(s) : slice_p(s);
       ff incl;  // scans over the 32 slices of this round
       const ff excl = ff_add(carry, warp_exclusive_ff(v, incl));
       const ff cum = ff_add(carry, incl);
@@ -453,8 +458,8 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   if (tid == 0) {
     int j = hit;
     if (j == INT_MAX) {
-      // the slice sum said the crossing is here but the in-slice order
-      // rounded past it: the slice's last token with weight
+      // the slice sums put the crossing here but the in-slice order rounded
+      // past it: the slice's last token with weight
       const int2 l = f.last[c0 + s];
       j = resid ? l.x : l.y;
       if (j < 0) j = last_any >= 0 ? last_any : 0;
@@ -469,11 +474,8 @@ int launch_fullvocab_draw(const FvParams& f, void* stream) {
   if (f.B <= 0 || f.n_slices <= 0) return 0;
   const cudaStream_t st = (cudaStream_t)stream;
   const dim3 grid((unsigned)f.n_slices, (unsigned)f.B);
-  fv_norm_kernel<<<grid, kFvThreads, 0, st>>>(f);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return (int)e;
-  fv_slice_kernel<<<grid, kFvThreads, 0, st>>>(f);
-  e = cudaGetLastError();
+  fv_sums_kernel<<<grid, kFvThreads, 0, st>>>(f);
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   fv_pick_kernel<<<f.B, kFvThreads, 0, st>>>(f);
   return (int)cudaGetLastError();

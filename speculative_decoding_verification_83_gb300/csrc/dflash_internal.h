@@ -82,6 +82,8 @@ struct FvDraw {
   int mode;    // FvMode
   float mx;    // largest logit of target row n
   float my;    // largest logit of draft row n (residual)
+  float sx0;   // the stream's (fp32) sum of exp((x - mx) / T) over target row n
+  float sy0;   // the same over draft row n (residual)
 };
 
 inline int fv_slices(int V) { return (V + kFvSlice - 1) / kFvSlice; }
@@ -132,8 +134,8 @@ struct FvParams {
   int32_t* out_tokens;          // [B, gamma+1]
   const FvDraw* draw;           // [B]
   float4* part;                 // [B, n_slices]: slice sums of the two rows' exp weights
-  float4* sum;                  // [B, n_slices]: slice sums of the residual and of p
-  int2* last;                   // [B, n_slices]: last token with positive residual / p
+  float4* pos;                  // [B, n_slices]: the same sums over the tokens with p > q
+  int2* last;                   // [B, n_slices]: last token with p > q / with p > 0
   const uint32_t* abort_flag;
   float exp_hi[kExpTable];      // 2^(j/64) = exp_hi[j] + exp_lo[j]
   float exp_lo[kExpTable];
@@ -141,7 +143,7 @@ struct FvParams {
 
 struct WorkspaceLayout {
   size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_prob, res_idx, res_flag;
-  size_t fv_draw, fv_part, fv_sum, fv_last, total;
+  size_t fv_draw, fv_part, fv_pos, fv_last, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -178,7 +180,7 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   const size_t fv_cells = fv_req * (size_t)fv_slices(g.V);
   L.fv_draw = off;    off = align_up(off + sizeof(FvDraw) * fv_req, 256);
   L.fv_part = off;    off = align_up(off + 16 * fv_cells, 256);
-  L.fv_sum = off;     off = align_up(off + 16 * fv_cells, 256);
+  L.fv_pos = off;     off = align_up(off + 16 * fv_cells, 256);
   L.fv_last = off;    off = align_up(off + 8 * fv_cells, 256);
   L.total = off;
   return L;

@@ -62,7 +62,7 @@ struct PieceDesc {
   int pp;      // piece index within the row
   int nvec;    // 16-byte vectors in the stage
   int head;    // logits before the row's aligned body; + kDescArgmax / kDescStats
-  float scale; // full-vocabulary rows: log2(e) / T
+  int ord;     // request ordinal of the row (verification)
 };
 constexpr int kDescArgmax = 256;  // the consumers track this row's argmax in-stream
 constexpr int kDescStats = 512;   // the consumers reduce the piece to (max, sum of exp)
@@ -768,15 +768,12 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
     S.desc[stage].pp = w.pp;
     S.desc[stage].nvec = nvec;
     int flags = 0;
-    float scale = 0.0f;
-    if (in_stream_argmax(p, si)) {
+    if (in_stream_argmax(p, si))
       flags = kDescArgmax;
-    } else if (p.fullvocab && si.sampling) {
+    else if (p.fullvocab && si.sampling)
       flags = kDescStats;
-      scale = kLog2e / __ldg(p.temperature + S.req_of_ord[si.ord]);
-    }
     S.desc[stage].head = rb.head + flags;
-    S.desc[stage].scale = scale;
+    S.desc[stage].ord = si.ord;
     if (nvec > 0) {
       mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec * 16u);
       bulk_load(S.ring[stage], rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16, (uint32_t)nvec * 16u,
@@ -879,8 +876,13 @@ __device__ __forceinline__ void stats_merge(float& m, float& s, float m2, float 
 // scale) = exp((x - m) / T), written as one float2 per piece (sum NaN when
 // the piece holds a NaN). Precise enough for the accept test; the draw
 // recomputes its sums in float-float.
+// The request's temperature is fetched here, by the consumer warp, not by the
+// producer: a dependent load per piece on the single thread that issues the
+// bulk copies slows the whole stream.
 template <int DT>
-__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, float scale, float2* out, int lane) {
+__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, const float* temperature, float2* out,
+                                            int lane) {
+  const float scale = kLog2e / __ldg(temperature);  // log2(e) / T, as the request final computes it
   float m = -INFINITY, s = 0.0f;
   bool nan = false;
 #pragma unroll 2
@@ -948,7 +950,7 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
     const int nvec = dsc.nvec;
     const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
     if (dsc.head & kDescStats)
-      piece_stats<DT>(st4, nvec, dsc.scale,
+      piece_stats<DT>(st4, nvec, p.temperature + S.req_of_ord[dsc.ord],
                       reinterpret_cast<float2*>(p.tile_keys + (size_t)dsc.slot * p.geo.tiles) + dsc.pp, lane);
     else
       piece_keys<DT>(p, st4, nvec, dsc.slot, dsc.pp, (dsc.head & kDescArgmax) != 0, lane);
@@ -1094,7 +1096,7 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   if (lane == 0) {
     p.out_len[b] = n + 1;
     if (st && p.status) atomicOr(p.status, st);
-    if (p.fullvocab) p.fv_draw[b] = FvDraw{n, kFvNone, 0.0f, 0.0f};
+    if (p.fullvocab) p.fv_draw[b] = FvDraw{n, kFvNone, 0.0f, 0.0f, 0.0f, 0.0f};
   }
 }
 
@@ -1178,7 +1180,8 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
       p.out_len[b] = n + 1;
-      p.fv_draw[b] = FvDraw{n, mode, S.u.fv.m[2 * n], n < gamma ? S.u.fv.m[2 * n + 1] : 0.0f};
+      p.fv_draw[b] = FvDraw{n, mode, S.u.fv.m[2 * n], n < gamma ? S.u.fv.m[2 * n + 1] : 0.0f, S.u.fv.s[2 * n],
+                            n < gamma ? S.u.fv.s[2 * n + 1] : 0.0f};
       if (st && p.status) atomicOr(p.status, st);
     }
   }
