@@ -36,6 +36,14 @@ constexpr int kTileLanes = 8;
 constexpr int kTilesPerPiece = kRoundsPerPiece;       // 8 blocks x 4 lane groups
 constexpr int kStages = 12;      // ring of bulk-copy stages
 constexpr int kKeyQueue = 32;    // pieces the publisher may lag behind
+// Consumer warp w waits for piece it = w + 8 k on stage it % kStages with the
+// phase parity of round it / kStages. That parity names the right phase only
+// if piece it - kStages has already landed, which holds when the warp's own
+// previous piece (it - 8) is no older than it: kStages >= kConsumerWarps.
+// With fewer stages a parity wait can match a phase two rounds old and read
+// a stage before its copy lands. The key queue has the same rule.
+static_assert(kStages >= kConsumerWarps, "ring stages must cover every consumer warp's piece");
+static_assert(kKeyQueue >= kConsumerWarps, "key-queue slots must cover every consumer warp's piece");
 constexpr int kCtasPerSm = 1;
 
 constexpr int kMaxTopK = 32;     // one kept token per lane of a warp
