@@ -401,9 +401,13 @@ __device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u,
 // ---- row final ----------------------------------------------------------------------
 // Leaves the row's sorted top-k composites in the group's first warp (lane l:
 // rank l in `top_a`) and in the workspace.
-__device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si, unsigned long long& top_a) {
+__device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si, unsigned long long& top_a,
+                          float& T_row) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int V = p.geo.V, dtype = p.dtype;
+  // the row's temperature, loaded now and used last: a global load at the
+  // end of the final would add a full round trip to it
+  T_row = __ldg(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
   const RowBody rb = row_body(si.ptr, V, p.geo.esize);
   const int n_tiles = p.geo.tiles;
   const uint32_t* gkeys = p.tile_keys + (size_t)slot * n_tiles;
@@ -598,8 +602,7 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       // request final reads
       const bool valid = lane < k && lane < n_c;
       int32_t idx = valid ? composite_idx(a) : -1;
-      const float T = __ldg(p.temperature + S.req_of_ord[si.ord]);
-      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T, p.top_p, lane);
+      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane);
       p.res_idx[(size_t)slot * kMaxTopK + lane] = idx;
       p.res_prob[(size_t)slot * kMaxTopK + lane] = pr;
     }
@@ -675,10 +678,9 @@ __device__ void request_final(const Params& p, Smem& S, int ord) {
 }
 
 // ---- row final of the rows tasks: filtered distribution / one sample ----------------
-__device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long top_a) {
+__device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long top_a, float T) {
   const int gt = fin_tid(), lane = gt & 31;
   if ((gt >> 5) == 0) {
-    const float T = __ldg(p.temperature + r);
     const bool samp = sampling_temperature(T);
     const uint32_t st = (!samp && T != 0.0f) ? kStatusBadTemperature : 0u;
     const int k_eff = samp ? p.top_k : 1;
@@ -1188,72 +1190,79 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
   fin_sync();
 }
 
-// Finals group (4 warps): works through the jobs dealt to this CTA (job j
-// goes to CTA j mod G, in the order rows finish): first the rows that need a
-// top-k (sampling rows, every row of the rows tasks), then one job per greedy
-// request. A job waits only for its rows' pieces to be counted, never for
-// another final, so no two groups can wait on each other.
-__device__ void finals(const Params& p, Smem& S) {
+// Finals group (4 warps): works through the jobs dealt to this CTA, first
+// the rows that need a top-k (sampling rows, every row of the rows tasks;
+// row job j goes to CTA j mod G, in the order rows finish), then the request
+// jobs (full-vocabulary sampling requests, greedy requests; request job i
+// goes to CTA G - 1 - (i mod G), so the CTAs that drew an extra row job draw
+// a request job last). A job waits only for its rows' pieces to be counted,
+// never for another final, so no two groups can wait on each other.
+__device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord) {
   const int gt = fin_tid(), w = gt >> 5;
   const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
-  const bool fv = verify && p.fullvocab;
   const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
-  // row jobs (top-k sampling rows, rows tasks), then request jobs from
-  // request ordinal ord0 on (full-vocabulary sampling requests, greedy ones)
-  const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * per_s : p.B);
-  const int ord0 = fv ? 0 : S.n_samp;
-  const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
-  for (int j = blockIdx.x; j < n_jobs; j += gridDim.x) {
-    const bool row_job = j < n_row_jobs;
-    const int ord = ord0 + (j - n_row_jobs);
-    if (w == 0) {
-      bool ok;
-      if (row_job)
-        ok = wait_rows(p, j, 1);
-      else if (ord < S.n_samp)
-        ok = wait_rows(p, ord * per_s, per_s);
-      else
-        ok = wait_rows(p, S.n_samp * per_s + (ord - S.n_samp) * per_g, per_g);
-      if (gt == 0) {
-        if (!ok) raise_timeout(p);
-        S.fin_cmd = ok ? 1 : 2;
-      }
-      if (ok) fence_acq_rel_gpu();  // acquire the rows' keys
-    }
-    fin_sync();
-    if (S.fin_cmd != 1) return;
-    if (!row_job) {
-      if (ord < S.n_samp) {
-        fullvocab_request_final(p, S, ord);
-      } else {
-        if (w == 0) greedy_request_final(p, S, ord);
-        fin_sync();
-      }
-      continue;
-    }
-    const int slot = j;
-    const SlotInfo si = slot_info(p, S, slot);
-    unsigned long long top_a = 0ull;
-    row_final(p, S, slot, si, top_a);
-    if (!verify) {
-      rows_final(p, S, slot, top_a);
-      continue;
-    }
-    // request hand-off: the group finishing the request's last row runs its final
-    const int b = S.req_of_ord[si.ord];
-    const int rows = 2 * p.gamma + 1;
+  if (w == 0) {
+    bool ok;
+    if (row_job)
+      ok = wait_rows(p, j, 1);
+    else if (ord < S.n_samp)
+      ok = wait_rows(p, ord * per_s, per_s);
+    else
+      ok = wait_rows(p, S.n_samp * per_s + (ord - S.n_samp) * per_g, per_g);
     if (gt == 0) {
-      fence_acq_rel_gpu();  // release this row's results
-      const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(rows - 1);
-      if (last) {
-        p.req_cnt[b] = 0u;
-        fence_acq_rel_gpu();  // acquire the request's other rows
-      }
-      S.flag = last ? 1 : 0;
+      if (!ok) raise_timeout(p);
+      S.fin_cmd = ok ? 1 : 2;
     }
-    fin_sync();
-    if (S.flag) request_final(p, S, si.ord);
+    if (ok) fence_acq_rel_gpu();  // acquire the rows' keys
   }
+  fin_sync();
+  if (S.fin_cmd != 1) return false;
+  if (!row_job) {
+    if (ord < S.n_samp) {
+      fullvocab_request_final(p, S, ord);
+    } else {
+      if (w == 0) greedy_request_final(p, S, ord);
+      fin_sync();
+    }
+    return true;
+  }
+  const int slot = j;
+  const SlotInfo si = slot_info(p, S, slot);
+  unsigned long long top_a = 0ull;
+  float T_row;
+  row_final(p, S, slot, si, top_a, T_row);
+  if (!verify) {
+    rows_final(p, S, slot, top_a, T_row);
+    return true;
+  }
+  // request hand-off: the group finishing the request's last row runs its final
+  const int b = S.req_of_ord[si.ord];
+  if (gt == 0) {
+    fence_acq_rel_gpu();  // release this row's results
+    const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(per_s - 1);
+    if (last) {
+      p.req_cnt[b] = 0u;
+      fence_acq_rel_gpu();  // acquire the request's other rows
+    }
+    S.flag = last ? 1 : 0;
+  }
+  fin_sync();
+  if (S.flag) request_final(p, S, si.ord);
+  return true;
+}
+
+__device__ void finals(const Params& p, Smem& S) {
+  const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
+  const bool fv = verify && p.fullvocab;
+  // row jobs: top-k sampling rows, or every row of a rows task
+  const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * (2 * p.gamma + 1) : p.B);
+  for (int j = blockIdx.x; j < n_row_jobs; j += gridDim.x)
+    if (!finals_job(p, S, true, j, 0)) return;
+  if (!verify) return;
+  // request jobs from request ordinal ord0 on
+  const int ord0 = fv ? 0 : S.n_samp;
+  for (int i = gridDim.x - 1 - blockIdx.x; i < p.B - ord0; i += gridDim.x)
+    if (!finals_job(p, S, false, 0, ord0 + i)) return;
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
