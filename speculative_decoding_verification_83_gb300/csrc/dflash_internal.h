@@ -37,12 +37,18 @@ constexpr int kTilesPerPiece = kRoundsPerPiece;       // 8 blocks x 4 lane group
 constexpr int kStages = 12;      // ring of bulk-copy stages
 constexpr int kKeyQueue = 32;    // pieces the publisher may lag behind
 // Consumer warp w waits for piece it = w + 8 k on stage it % kStages with the
-// phase parity of round it / kStages. That parity names the right phase only
-// if piece it - kStages has already landed, which holds when the warp's own
-// previous piece (it - 8) is no older than it: kStages >= kConsumerWarps.
-// With fewer stages a parity wait can match a phase two rounds old and read
-// a stage before its copy lands. The key queue has the same rule.
+// phase parity of round it / kStages. A parity wait only tells adjacent
+// phases apart, so it names the right phase only if the stage's previous
+// piece (it - kStages) has landed. Bulk copies can land out of order, so the
+// consumer first waits for that piece to be consumed (the stage's empty
+// barrier). That wait is unambiguous when piece it - 2 kStages was the warp's
+// own, i.e. 2 kStages is a multiple of kConsumerWarps. With fewer stages than
+// warps, or without that first wait, a consumer can read a stage before its
+// copy lands. The key queue is safe with kKeyQueue >= kConsumerWarps: the
+// warp's own previous piece already waited for the publisher to be within
+// kKeyQueue + kConsumerWarps pieces.
 static_assert(kStages >= kConsumerWarps, "ring stages must cover every consumer warp's piece");
+static_assert((2 * kStages) % kConsumerWarps == 0, "piece it - 2 kStages must be the consumer warp's own");
 static_assert(kKeyQueue >= kConsumerWarps, "key-queue slots must cover every consumer warp's piece");
 constexpr int kCtasPerSm = 1;
 

@@ -943,7 +943,16 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
   for (long long it = warp; it < mine; it += kConsumerWarps) {
     const int stage = (int)(it % kStages);
     const int q = (int)(it % kKeyQueue);
-    const bool landed = mbar_wait(&S.full[stage], (uint32_t)((it / kStages) & 1), abort_flag);
+    const uint32_t round = (uint32_t)(it / kStages);
+    // A parity wait only tells adjacent phases apart. Bulk copies may land
+    // out of order, so this stage's previous piece (it - kStages, another
+    // warp's) might not have landed yet, and a full-barrier wait for piece it
+    // would then match the phase before and pass at once. Waiting first for
+    // that piece to be consumed (empty barrier) closes the gap; that wait is
+    // itself unambiguous because piece it - 2 kStages was this warp's own.
+    bool landed = true;
+    if (it >= kStages) landed = mbar_wait(&S.empty[stage], (round & 1u) ^ 1u, abort_flag);
+    landed = landed && mbar_wait(&S.full[stage], round & 1u, abort_flag);
     if (!__all_sync(0xffffffffu, landed)) {
       if (lane == 0) raise_timeout(p);
       return;
