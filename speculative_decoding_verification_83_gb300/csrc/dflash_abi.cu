@@ -102,6 +102,7 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, bool fullv
   p.row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
   p.req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
   p.abort_flag = reinterpret_cast<uint32_t*>(base + L.abort_flag);
+  p.job_cnt = p.abort_flag + 1;
   p.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
   p.tile_keys = reinterpret_cast<uint32_t*>(base + L.tile_keys);
   p.res_prob = reinterpret_cast<float*>(base + L.res_prob);

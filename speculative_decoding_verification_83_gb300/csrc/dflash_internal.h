@@ -129,6 +129,7 @@ struct Params {
   uint32_t* row_cnt;    // [n_slots]
   uint32_t* req_cnt;    // [B]
   uint32_t* abort_flag; // [1]
+  uint32_t* job_cnt;    // [1]: next finals job to hand out (beside the abort flag)
   unsigned long long* row_best;  // [kMaxCounterSlots]: greedy rows' best (key, index) composite
   uint32_t* tile_keys;  // [n_slots, geo.tiles]; full-vocabulary rows: float2 (max, sum) per piece
   float* res_prob;      // [n_slots, kMaxTopK]: filtered probability (sampling rows)
@@ -184,7 +185,7 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   size_t off = 0;
   L.req_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxB, 256);
   L.row_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
-  L.abort_flag = off; off = align_up(off + sizeof(uint32_t), 256);
+  L.abort_flag = off; off = align_up(off + 2 * sizeof(uint32_t), 256);  // abort flag, job counter
   L.row_best = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)kMaxCounterSlots, 256);
   L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
   L.res_prob = off;   off = align_up(off + sizeof(float) * (size_t)n_slots * kMaxTopK, 256);

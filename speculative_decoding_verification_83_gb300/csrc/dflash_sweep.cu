@@ -1199,13 +1199,13 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
   fin_sync();
 }
 
-// Finals group (4 warps): works through the jobs dealt to this CTA, first
-// the rows that need a top-k (sampling rows, every row of the rows tasks;
-// row job j goes to CTA j mod G, in the order rows finish), then the request
-// jobs (full-vocabulary sampling requests, greedy requests; request job i
-// goes to CTA G - 1 - (i mod G), so the CTAs that drew an extra row job draw
-// a request job last). A job waits only for its rows' pieces to be counted,
-// never for another final, so no two groups can wait on each other.
+// Finals group (4 warps): runs finals jobs, which it draws one at a time from
+// a counter in the workspace: first the rows that need a top-k (sampling
+// rows, every row of the rows tasks) in the order rows finish, then the
+// request jobs (full-vocabulary sampling requests, greedy requests). A group
+// draws its next job while it works on the current one, so a job goes to
+// whichever group frees up first. A job waits only for its rows' pieces to be
+// counted, never for another final, so no two groups can wait on each other.
 __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord) {
   const int gt = fin_tid(), w = gt >> 5;
   const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
@@ -1261,17 +1261,31 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
 }
 
 __device__ void finals(const Params& p, Smem& S) {
+  const int gt = fin_tid();
+  constexpr int kDrawer = kFin - 32;  // a thread of the last warp, which issues no fences
   const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
   const bool fv = verify && p.fullvocab;
-  // row jobs: top-k sampling rows, or every row of a rows task
+  // row jobs: top-k sampling rows, or every row of a rows task; then request
+  // jobs from request ordinal ord0 on
   const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * (2 * p.gamma + 1) : p.B);
-  for (int j = blockIdx.x; j < n_row_jobs; j += gridDim.x)
-    if (!finals_job(p, S, true, j, 0)) return;
-  if (!verify) return;
-  // request jobs from request ordinal ord0 on
   const int ord0 = fv ? 0 : S.n_samp;
-  for (int i = gridDim.x - 1 - blockIdx.x; i < p.B - ord0; i += gridDim.x)
-    if (!finals_job(p, S, false, 0, ord0 + i)) return;
+  const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
+  if (gt == kDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);
+  fin_sync();
+  int j = S.fin_slot;
+  while (j < n_jobs) {
+    uint32_t next = 0u;
+    if (gt == kDrawer) next = atomicAdd(p.job_cnt, 1u);  // read only after this job
+    const bool ok = j < n_row_jobs ? finals_job(p, S, true, j, 0)
+                                   : finals_job(p, S, false, 0, ord0 + (j - n_row_jobs));
+    if (!ok) return;  // timed out: the workspace must be prepared again anyway
+    if (gt == kDrawer) S.fin_slot = (int)next;
+    fin_sync();
+    j = S.fin_slot;
+  }
+  // every group's last draw is past the jobs; the very last of all draws
+  // returns the counter to zero for the next call
+  if (gt == kDrawer && j == n_jobs + (int)gridDim.x - 1) *p.job_cnt = 0u;
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
