@@ -148,6 +148,32 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint
 
 // named barrier over the finals group only
 __device__ __forceinline__ void fin_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+// finals-group barrier that also returns whether v held in every thread
+// (bar.red.and on the same named barrier)
+__device__ __forceinline__ bool fin_sync_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, 2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0u;
+}
+// ... or in any thread
+__device__ __forceinline__ bool fin_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0u;
+}
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 // GPU-scope release store / acquire load of a flag word
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {

@@ -347,7 +347,13 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const Req q = load_req(f, b);
-  if (!q.live) return;
+  // every call leaves the workspace at zero (its regions move with the
+  // shape): this launch is the last reader of the request's draw state
+  FvDraw* draw_w = const_cast<FvDraw*>(f.draw) + b;
+  if (!q.live) {
+    if (tid == 0 && *reinterpret_cast<const volatile uint32_t*>(f.abort_flag) == 0u) *draw_w = FvDraw{};
+    return;
+  }
   load_table(f, th, tl);
   if (tid < 32) load_norm(f, b, q.residual, &nm_s);
   __syncthreads();
@@ -415,8 +421,14 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   __syncthreads();
   const int s = sel_slice;
   int32_t* out = f.out_tokens + (size_t)b * (f.gamma + 1) + q.n;
+  for (int c = tid; c < f.n_slices; c += kFvThreads) {  // the slice sums are used up
+    f.part[c0 + c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    f.pos[c0 + c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
+  if (tid == 0) *draw_w = FvDraw{};
   if (s < 0) {  // rounding left no token above u * total: the last with weight
     if (tid == 0) *out = last_any >= 0 ? last_any : 0;
+    for (int c = tid; c < f.n_slices; c += kFvThreads) f.last[c0 + c] = make_int2(0, 0);
     return;
   }
   // inside slice s: thread t owns tokens s*kFvSlice + t*kFvPerThread + k, in order
@@ -466,6 +478,8 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
     }
     *out = j;
   }
+  __syncthreads();
+  for (int c = tid; c < f.n_slices; c += kFvThreads) f.last[c0 + c] = make_int2(0, 0);
 }
 
 }  // namespace

@@ -95,12 +95,11 @@ int dflash_verify_noalloc(const void* target_logits, const void* draft_logits, c
   void* scratch = nullptr;
   int rc = scratch_address(&scratch);
   if (rc) return rc;
-  // The scratch keeps whatever the previous call left. Its counter header must
-  // be zero when the kernel starts (a call that timed out leaves it dirty), so
-  // it is cleared on the call's stream before every launch.
-  const dflash::WorkspaceLayout L =
-      dflash::make_layout(B * (2 * gamma + 1), B, dflash::make_geometry(V, dtype == DFLASH_BF16 ? 2 : 4));
-  cudaError_t e = cudaMemsetAsync(scratch, 0, L.tile_keys, (cudaStream_t)stream);
+  // The scratch keeps whatever the previous call left. Its counters and tile
+  // keys must be zero when the kernel starts (a call that timed out leaves
+  // them dirty), so the part this call uses is cleared on the call's stream
+  // before every launch.
+  cudaError_t e = cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     snprintf(msg, sizeof msg, "dflash_verify_noalloc: clearing the scratch header: %s", cudaGetErrorString(e));
     return noalloc_fail(DFLASH_ERR_CUDA, msg);

@@ -247,6 +247,26 @@ __device__ __forceinline__ uint32_t fin_max_u32(Smem& S, uint32_t v) {
   return r;
 }
 
+// Group-wide maxima of two values at once. No barrier follows the read of
+// S.warp_red: its next writer is past a later group barrier.
+__device__ __forceinline__ void fin_max2_u32(Smem& S, uint32_t a, uint32_t b, uint32_t& ra, uint32_t& rb) {
+  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
+  a = warp_max_u32(a);
+  b = warp_max_u32(b);
+  if (lane == 0) {
+    S.warp_red[w] = a;
+    S.warp_red[kFinWarps + w] = b;
+  }
+  fin_sync();
+  ra = 0u;
+  rb = 0u;
+#pragma unroll
+  for (int i = 0; i < kFinWarps; ++i) {
+    ra = max(ra, S.warp_red[i]);
+    rb = max(rb, S.warp_red[kFinWarps + i]);
+  }
+}
+
 // Finds, in S.hist, the digit holding the krem-th largest element (counts
 // from the top); sets S.digit and S.digit_above (elements in larger digits).
 // Run by the group's first warp.
@@ -401,7 +421,7 @@ __device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u,
 // ---- row final ----------------------------------------------------------------------
 // Leaves the row's sorted top-k composites in the group's first warp (lane l:
 // rank l in `top_a`) and in the workspace.
-__device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si, unsigned long long& top_a,
+__device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si, unsigned long long& top_a,
                           float& T_row) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int V = p.geo.V, dtype = p.dtype;
@@ -414,28 +434,36 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   const bool cached = n_tiles <= kKeyCache;
   const int k = si.k_eff;
 
-  // tile keys (cache), largest key, head/tail NaN check
-  uint32_t mx = 0u;
-  for (int i = gt; i < n_tiles; i += kFin) {
-    const uint32_t key = __ldcg(gkeys + i);
-    if (cached) S.u.key_cache[i] = key;
-    mx = max(mx, key);
-  }
-  const uint32_t tile_max = fin_max_u32(S, mx);  // includes syncs
+  // tile keys (cached) and the logits outside the aligned body, loaded in
+  // one round trip; the edges' maximum is all ones when one of them is NaN
   const int n_edge = rb.head + (V - rb.tail_start);
-  bool edge_nan = false;
-  uint32_t emx = 0u;
-  if (gt < n_edge) {
-    const int j = gt < rb.head ? gt : rb.tail_start + (gt - rb.head);
-    const float x = load_logit(rb.row, j, dtype);
-    edge_nan = isnan(x);
-    emx = key_of(x);
+  const int edge_j = gt < rb.head ? gt : rb.tail_start + (gt - rb.head);
+  const float edge_x = gt < n_edge ? load_logit(rb.row, edge_j, dtype) : 0.0f;
+  // The row is ready when every tile key is written: the keys start the call
+  // at zero (no tile key is zero: a NaN maximum is the canonical NaN) and a
+  // consumer warp stores each one once. So the polls are the final's own key
+  // loads, and no counter, fence or second round trip stands between the
+  // stream and the final.
+  uint32_t mx = 0u;
+  const volatile uint32_t* abort_flag = p.abort_flag;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    bool mine = true;
+    mx = 0u;
+    for (int i = gt; i < n_tiles; i += kFin) {
+      const uint32_t key = ld_relaxed_gpu(gkeys + i);
+      mine = mine && key != 0u;
+      if (cached) S.u.key_cache[i] = key;
+      mx = max(mx, key);
+    }
+    if (fin_sync_and(mine)) break;
+    if (fin_sync_or(*abort_flag != 0u || global_timer_ns() - t0 > kWaitLimitNs)) return false;
+    __nanosleep(128);
   }
-  if (gt == 0) S.bad_head_tail = 0;
-  fin_sync();
-  if (edge_nan) S.bad_head_tail = 1;
-  const uint32_t row_max = max(tile_max, fin_max_u32(S, emx));
-  const bool bad = !key_is_finite(row_max) || S.bad_head_tail != 0;
+  const uint32_t emx = gt < n_edge ? (isnan(edge_x) ? 0xffffffffu : key_of(edge_x)) : 0u;
+  uint32_t tile_max, edge_max;
+  fin_max2_u32(S, mx, emx, tile_max, edge_max);
+  const bool bad = !key_is_finite(max(tile_max, edge_max));
 
   // tau: a lower bound of the k-th largest tile maximum (0 keeps everything
   // when tiles < k). Tile keys within 255 buckets of 2^16 key units below the
@@ -500,11 +528,17 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     S.n_cand = 0;
   }
   fin_sync();
-  for (int i = gt; i < n_tiles; i += kFin) {
-    const uint32_t key = cached ? S.u.key_cache[i] : __ldcg(gkeys + i);
-    if (key >= tau) {
-      const int pos = atomicAdd(&S.n_cand_tiles, 1);
-      if (pos < kCandTileCap) S.cand_tiles[pos] = i;
+  // candidate tiles, one slot reservation per warp and step
+  for (int base = 0; base < n_tiles; base += kFin) {
+    const int i = base + gt;
+    const bool take = i < n_tiles && (cached ? S.u.key_cache[i] : __ldcg(gkeys + i)) >= tau;
+    const uint32_t ball = __ballot_sync(0xffffffffu, take);
+    if (ball) {
+      int first = 0;
+      if (lane == __ffs(ball) - 1) first = atomicAdd(&S.n_cand_tiles, __popc(ball));
+      first = __shfl_sync(0xffffffffu, first, __ffs(ball) - 1);
+      const int pos = first + __popc(ball & ((1u << lane) - 1u));
+      if (take && pos < kCandTileCap) S.cand_tiles[pos] = i;
     }
   }
   fin_sync();
@@ -552,9 +586,8 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       }
     }
     if (gt < n_edge) {  // head and tail logits are always candidates
-      const int j = gt < rb.head ? gt : rb.tail_start + (gt - rb.head);
       const int pos = atomicAdd(&S.n_cand, 1);
-      if (pos < kCandCap) S.cand[pos] = composite(key_of(load_logit(rb.row, j, dtype)), j);
+      if (pos < kCandCap) S.cand[pos] = composite(key_of(edge_x), edge_j);
     }
     fin_sync();
     overflow = S.n_cand > kCandCap;
@@ -609,7 +642,11 @@ __device__ void row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     if (lane == 0) p.res_flag[slot] = bad ? 1u : 0u;
     if (bad && lane == 0 && p.status) atomicOr(p.status, kStatusBadRow);
   }
+  // leave the keys at zero for the next call
+  uint32_t* wkeys = p.tile_keys + (size_t)slot * n_tiles;
+  for (int i = gt; i < n_tiles; i += kFin) wkeys[i] = 0u;
   fin_sync();
+  return true;
 }
 
 // ---- request final (sampling verification) -------------------------------------------
@@ -629,12 +666,18 @@ __device__ void request_final(const Params& p, Smem& S, int ord) {
     const size_t s = (size_t)(slot0 + r);
     S.u.lists.idx[r][lane] = __ldcg(p.res_idx + s * kMaxTopK + lane);
     S.u.lists.prob[r][lane] = __ldcg(p.res_prob + s * kMaxTopK + lane);
+    // every call leaves the workspace at zero: its regions move with the
+    // shape, and another shape's tile keys may lie here next time
+    p.res_idx[s * kMaxTopK + lane] = 0;
+    p.res_prob[s * kMaxTopK + lane] = 0.0f;
   }
   fin_sync();
   if (w == 0) {
     uint32_t st = 0;
-    for (int r = lane; r < per_s; r += 32)
+    for (int r = lane; r < per_s; r += 32) {
       if (__ldcg(p.res_flag + slot0 + r)) st |= kStatusBadRow;
+      p.res_flag[slot0 + r] = 0u;
+    }
     bool reject = false;
     if (lane < gamma) {
       const int i = lane;
@@ -981,6 +1024,15 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
   }
 }
 
+// Rows whose finals wait for their pieces to be counted: greedy rows of a
+// verification (argmax in the stream) and full-vocabulary sampling rows. Rows
+// with a row final (top-k sampling rows, rows tasks) signal readiness through
+// their tile keys instead.
+__device__ __forceinline__ bool counted_slot(const Params& p, const Smem& S, int slot) {
+  if (p.task != kTaskVerify && p.task != kTaskVerifyGreedy) return false;
+  return slot >= S.n_samp * (2 * p.gamma + 1) || p.fullvocab != 0;
+}
+
 // Publisher (one thread): takes the pieces the consumers finished in batches,
 // releases their tile keys (and greedy argmax updates) to the other CTAs with
 // one fence per batch, then counts the pieces on their rows with
@@ -1004,9 +1056,14 @@ __device__ void publisher(const Params& p, Smem& S, long long total) {
       raise_timeout(p);
       return;
     }
-    fence_acq_rel_gpu();  // release the batch's tile keys to the other CTAs
+    // rows whose finals wait on counts: release what the batch's consumers
+    // wrote (greedy argmax, full-vocabulary statistics), then count
+    PieceWalk w2 = w;
+    bool counted = false;
+    for (int j = 0; j < n; ++j, w2.next()) counted = counted || counted_slot(p, S, w2.slot);
+    if (counted) fence_acq_rel_gpu();
     for (int j = 0; j < n; ++j) {
-      red_add_gpu(p.row_cnt + w.slot, 1u);
+      if (counted_slot(p, S, w.slot)) red_add_gpu(p.row_cnt + w.slot, 1u);
       w.next();
       mbar_arrive(&S.kempty[(q + j) % kKeyQueue]);
     }
@@ -1133,6 +1190,8 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
       const float2 v = __ldcg(st + pp);
       nan |= isnan(v.y);
       stats_merge(m, sum, v.x, v.y, scale);
+      // leave the region at zero: rows of later calls take tile keys there
+      const_cast<float2*>(st)[pp] = make_float2(0.0f, 0.0f);
     }
     const int n_edge = rb.head + (V - rb.tail_start);
     for (int e = lane; e < n_edge; e += 32) {
@@ -1210,11 +1269,11 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
   const int gt = fin_tid(), w = gt >> 5;
   const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
   const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
-  if (w == 0) {
+  // a row job's row final waits on the row's tile keys themselves; a request
+  // job waits for its rows' pieces to be counted
+  if (w == 0 && !row_job) {
     bool ok;
-    if (row_job)
-      ok = wait_rows(p, j, 1);
-    else if (ord < S.n_samp)
+    if (ord < S.n_samp)
       ok = wait_rows(p, ord * per_s, per_s);
     else
       ok = wait_rows(p, S.n_samp * per_s + (ord - S.n_samp) * per_g, per_g);
@@ -1222,8 +1281,9 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
       if (!ok) raise_timeout(p);
       S.fin_cmd = ok ? 1 : 2;
     }
-    if (ok) fence_acq_rel_gpu();  // acquire the rows' keys
+    if (ok) fence_acq_rel_gpu();  // acquire what the rows' consumers wrote
   }
+  if (row_job && gt == 0) S.fin_cmd = 1;
   fin_sync();
   if (S.fin_cmd != 1) return false;
   if (!row_job) {
@@ -1239,7 +1299,10 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
   const SlotInfo si = slot_info(p, S, slot);
   unsigned long long top_a = 0ull;
   float T_row;
-  row_final(p, S, slot, si, top_a, T_row);
+  if (!row_final(p, S, slot, si, top_a, T_row)) {
+    if (gt == 0) raise_timeout(p);
+    return false;
+  }
   if (!verify) {
     rows_final(p, S, slot, top_a, T_row);
     return true;
