@@ -100,14 +100,11 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, bool fullv
   const WorkspaceLayout L = make_layout(n_slots, n_requests, p.geo, fullvocab);
   unsigned char* base = static_cast<unsigned char*>(ws);
   p.row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
-  p.req_cnt = reinterpret_cast<uint32_t*>(base + L.req_cnt);
   p.abort_flag = reinterpret_cast<uint32_t*>(base + L.abort_flag);
   p.job_cnt = p.abort_flag + 1;
   p.row_best = reinterpret_cast<unsigned long long*>(base + L.row_best);
   p.tile_keys = reinterpret_cast<uint32_t*>(base + L.tile_keys);
-  p.res_prob = reinterpret_cast<float*>(base + L.res_prob);
-  p.res_idx = reinterpret_cast<int32_t*>(base + L.res_idx);
-  p.res_flag = reinterpret_cast<uint32_t*>(base + L.res_flag);
+  p.res_list = reinterpret_cast<unsigned long long*>(base + L.res_list);
   p.fv_draw = fullvocab ? reinterpret_cast<FvDraw*>(base + L.fv_draw) : nullptr;
   p.n_slots = n_slots;
 }

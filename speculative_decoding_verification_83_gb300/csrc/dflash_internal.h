@@ -127,14 +127,15 @@ struct Params {
   uint32_t* status;
   // workspace (zero-initialised once; counters reset by their last user)
   uint32_t* row_cnt;    // [n_slots]
-  uint32_t* req_cnt;    // [B]
   uint32_t* abort_flag; // [1]
   uint32_t* job_cnt;    // [1]: next finals job to hand out (beside the abort flag)
   unsigned long long* row_best;  // [kMaxCounterSlots]: greedy rows' best (key, index) composite
   uint32_t* tile_keys;  // [n_slots, geo.tiles]; full-vocabulary rows: float2 (max, sum) per piece
-  float* res_prob;      // [n_slots, kMaxTopK]: filtered probability (sampling rows)
-  int32_t* res_idx;     // [n_slots, kMaxTopK]
-  uint32_t* res_flag;   // [n_slots]
+  // [n_slots, kMaxTopK]: a verification sampling row's filtered list, one
+  // word per rank: (token + 2) << 32 | probability bits, the sign bit of
+  // rank 0 set for a bad row. No written word is zero, so the request final
+  // polls the words themselves.
+  unsigned long long* res_list;
   FvDraw* fv_draw;      // [B]: full-vocabulary mode
   int n_slots;
 };
@@ -157,7 +158,7 @@ struct FvParams {
 };
 
 struct WorkspaceLayout {
-  size_t row_cnt, req_cnt, abort_flag, row_best, tile_keys, res_prob, res_idx, res_flag;
+  size_t row_cnt, abort_flag, row_best, tile_keys, res_list;
   size_t fv_draw, fv_part, fv_pos, fv_last, total;
 };
 
@@ -183,14 +184,11 @@ constexpr int kMaxCounterSlots = kMaxB * kMaxRowsPerRequest;  // also the rows-t
 inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g, bool fullvocab = false) {
   WorkspaceLayout L;
   size_t off = 0;
-  L.req_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxB, 256);
   L.row_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
   L.abort_flag = off; off = align_up(off + 2 * sizeof(uint32_t), 256);  // abort flag, job counter
   L.row_best = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)kMaxCounterSlots, 256);
   L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
-  L.res_prob = off;   off = align_up(off + sizeof(float) * (size_t)n_slots * kMaxTopK, 256);
-  L.res_idx = off;    off = align_up(off + sizeof(int32_t) * (size_t)n_slots * kMaxTopK, 256);
-  L.res_flag = off;   off = align_up(off + sizeof(uint32_t) * (size_t)n_slots, 256);
+  L.res_list = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)n_slots * kMaxTopK, 256);
   const size_t fv_req = fullvocab ? (size_t)n_requests : 0;
   const size_t fv_cells = fv_req * (size_t)fv_slices(g.V);
   L.fv_draw = off;    off = align_up(off + sizeof(FvDraw) * fv_req, 256);

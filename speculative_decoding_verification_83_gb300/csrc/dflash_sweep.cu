@@ -6,33 +6,35 @@
 //     The producer warp moves pieces into a 12-stage shared-memory ring with
 //     1-D bulk copies (TMA) and records what each stage holds. Each of the 8
 //     consumer warps takes whole pieces and reduces every 256-element tile of
-//     them to its largest logit (packed bf16x2 / fp32 max that propagates NaN)
-//     and stores the tile's order key to the workspace. They never fence, never touch a global
-//     atomic and never wait on each other. Pieces are dealt round-robin to
-//     the CTAs, request by request, so rows complete progressively.
-//  2. Publish. The publisher warp takes the pieces its consumers finished, in
+//     them to its largest logit (packed bf16x2 / fp32 max that propagates
+//     NaN), storing the tile's order key to the workspace; for greedy rows it
+//     folds the piece's best (logit, lowest index) into the row's running
+//     argmax, and for full-vocabulary rows it reduces the piece to (max, sum
+//     of exp). Consumers never fence and never wait on each other. Pieces are
+//     dealt round-robin to the CTAs, request by request (sampling requests
+//     first), so rows complete progressively.
+//  2. Publish. For the rows whose finals wait on counts (greedy rows,
+//     full-vocabulary rows) the publisher warp takes the finished pieces in
 //     batches: one GPU-scope fence per batch, then a fire-and-forget counter
-//     increment per piece on the piece's row. For greedy rows the consumer
-//     warps also fold each piece's best (logit, lowest index) into the row's
-//     running argmax with a 64-bit max reduction, so greedy rows need no
-//     row final.
-//  3. Row final (the 4-warp finals group of the CTA the row is dealt to: job
-//     j goes to CTA j mod G, in the order rows finish): the row's top-k in
-//     (logit desc, index asc) order. A lower bound tau of the k-th largest
-//     tile maximum is also a lower bound of the row's k-th largest logit (the
-//     k tiles with the largest maxima hold k logits >= it), so the top-k lies
-//     among the logits >= tau of the tiles whose maximum is >= tau: about k
-//     tiles, re-read from L2. The head and tail logits outside the aligned
-//     body are always candidates. A row whose ties leave too many candidates
-//     falls back to an exact radix selection over the whole row.
-//  4. Request final: a sampling request's final runs in the group that
-//     finishes its last row (filter the rows: temperature, softmax over the
-//     survivors, top-p, renormalise; accept test token by token with Philox
-//     uniforms; residual or bonus draw; tokens and accept length). A greedy
-//     request is a job of its own: argmax prefix match on the streamed argmax.
-// A job waits, time-bounded, only for its rows' pieces to be counted; the
-// pieces are counted by publishers, which wait for nothing but their own
-// consumers, so there is no cycle of waits and no grid-wide barrier.
+//     increment per piece.
+//  3. Finals (the 4-warp finals group of every CTA draws jobs from a counter
+//     in the workspace, in the order rows finish). A row final gives a row's
+//     top-k in (logit desc, index asc) order: it polls the row's tile keys
+//     (zero until written), and a lower bound tau of the k-th largest tile
+//     maximum (also a lower bound of the row's k-th largest logit: the k
+//     tiles with the largest maxima hold k logits >= it) leaves about k tiles
+//     to re-read from L2; the head and tail logits outside the aligned body
+//     are always candidates, and a row whose ties leave too many candidates
+//     falls back to an exact radix selection. It then filters the row
+//     (temperature, softmax over the survivors, top-p, renormalise) into
+//     words that are never zero. A sampling request's final polls its rows'
+//     words and runs the accept test at every draft position at once (Philox
+//     uniforms), then the residual or bonus draw. A greedy request's final
+//     prefix-matches the streamed argmax.
+// Every wait is time-bounded; row finals wait only on the stream, and a
+// request final only on row finals drawn before it, so there is no cycle of
+// waits and no grid-wide barrier. Every successful call leaves the workspace
+// at zero.
 //
 // The method follows "DFlash2 用投机解码给 Qwen 提速" (bml.asia, draft/verify
 // loop and model-card settings) and "无损加速是真的吗？Qwen3.8-27B-DFlash2
@@ -636,10 +638,9 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       const bool valid = lane < k && lane < n_c;
       int32_t idx = valid ? composite_idx(a) : -1;
       const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane);
-      p.res_idx[(size_t)slot * kMaxTopK + lane] = idx;
-      p.res_prob[(size_t)slot * kMaxTopK + lane] = pr;
+      const uint32_t lo = __float_as_uint(pr) | ((bad && lane == 0) ? 0x80000000u : 0u);
+      p.res_list[(size_t)slot * kMaxTopK + lane] = ((unsigned long long)(uint32_t)(idx + 2) << 32) | lo;
     }
-    if (lane == 0) p.res_flag[slot] = bad ? 1u : 0u;
     if (bad && lane == 0 && p.status) atomicOr(p.status, kStatusBadRow);
   }
   // leave the keys at zero for the next call
@@ -654,7 +655,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
 // position runs the accept test u < p(d)/q(d); the first failing position (or
 // gamma when none fails) is where the residual max(0, p - q) (or the bonus
 // distribution p) is drawn from.
-__device__ void request_final(const Params& p, Smem& S, int ord) {
+__device__ bool request_final(const Params& p, Smem& S, int ord) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int gamma = p.gamma, V = p.geo.V;
   const int b = S.req_of_ord[ord];
@@ -662,22 +663,33 @@ __device__ void request_final(const Params& p, Smem& S, int ord) {
   const int32_t* d = p.draft_tokens + (size_t)b * gamma;
   const int per_s = 2 * gamma + 1;
   const int slot0 = ord * per_s;
-  for (int r = w; r < per_s; r += kFinWarps) {
-    const size_t s = (size_t)(slot0 + r);
-    S.u.lists.idx[r][lane] = __ldcg(p.res_idx + s * kMaxTopK + lane);
-    S.u.lists.prob[r][lane] = __ldcg(p.res_prob + s * kMaxTopK + lane);
-    // every call leaves the workspace at zero: its regions move with the
-    // shape, and another shape's tile keys may lie here next time
-    p.res_idx[s * kMaxTopK + lane] = 0;
-    p.res_prob[s * kMaxTopK + lane] = 0.0f;
+  // The rows' filtered lists are ready when every word is written (no
+  // written word is zero): the polls are the final's own loads.
+  unsigned long long* words = p.res_list + (size_t)slot0 * kMaxTopK;
+  const int n_words = per_s * kMaxTopK;
+  const volatile uint32_t* abort_flag = p.abort_flag;
+  const unsigned long long t0 = global_timer_ns();
+  for (;;) {
+    bool mine = true;
+    for (int i = gt; i < n_words; i += kFin) {
+      const unsigned long long v = ld_relaxed_gpu_u64(words + i);
+      mine = mine && v != 0ull;
+      const int r = i >> 5, l = i & 31;
+      S.u.lists.idx[r][l] = (int32_t)(uint32_t)(v >> 32) - 2;
+      S.u.lists.prob[r][l] = __uint_as_float((uint32_t)v & 0x7fffffffu);
+      if (l == 0) S.u.lists.idx[r][32] = (int32_t)((uint32_t)v >> 31);  // the row's bad flag
+    }
+    if (fin_sync_and(mine)) break;
+    if (fin_sync_or(*abort_flag != 0u || global_timer_ns() - t0 > kWaitLimitNs)) return false;
+    __nanosleep(128);
   }
-  fin_sync();
+  // every call leaves the workspace at zero: its regions move with the
+  // shape, and another shape's tile keys may lie here next time
+  for (int i = gt; i < n_words; i += kFin) words[i] = 0ull;
   if (w == 0) {
     uint32_t st = 0;
-    for (int r = lane; r < per_s; r += 32) {
-      if (__ldcg(p.res_flag + slot0 + r)) st |= kStatusBadRow;
-      p.res_flag[slot0 + r] = 0u;
-    }
+    for (int r = lane; r < per_s; r += 32)
+      if (S.u.lists.idx[r][32]) st |= kStatusBadRow;
     bool reject = false;
     if (lane < gamma) {
       const int i = lane;
@@ -718,6 +730,7 @@ __device__ void request_final(const Params& p, Smem& S, int ord) {
     }
   }
   fin_sync();
+  return true;
 }
 
 // ---- row final of the rows tasks: filtered distribution / one sample ----------------
@@ -1260,18 +1273,20 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
 
 // Finals group (4 warps): runs finals jobs, which it draws one at a time from
 // a counter in the workspace: first the rows that need a top-k (sampling
-// rows, every row of the rows tasks) in the order rows finish, then the
-// request jobs (full-vocabulary sampling requests, greedy requests). A group
-// draws its next job while it works on the current one, so a job goes to
-// whichever group frees up first. A job waits only for its rows' pieces to be
-// counted, never for another final, so no two groups can wait on each other.
+// rows, every row of the rows tasks) in the order rows finish, then one job
+// per request (sampling requests, then greedy ones). A group draws its next
+// job while it works on the current one, so a job goes to whichever group
+// frees up first. A row final waits only on the stream; a sampling request's
+// final may wait on its rows' finals, which were all drawn before it, so no
+// two groups can wait on each other in a cycle.
 __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord) {
   const int gt = fin_tid(), w = gt >> 5;
-  const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
   const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
-  // a row job's row final waits on the row's tile keys themselves; a request
-  // job waits for its rows' pieces to be counted
-  if (w == 0 && !row_job) {
+  // A row job's row final, and a top-k sampling request's final, wait on the
+  // words they read (tile keys, filtered lists). A full-vocabulary or greedy
+  // request's final waits for its rows' pieces to be counted.
+  const bool counted = !row_job && (ord >= S.n_samp || p.fullvocab);
+  if (w == 0 && counted) {
     bool ok;
     if (ord < S.n_samp)
       ok = wait_rows(p, ord * per_s, per_s);
@@ -1283,44 +1298,28 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
     }
     if (ok) fence_acq_rel_gpu();  // acquire what the rows' consumers wrote
   }
-  if (row_job && gt == 0) S.fin_cmd = 1;
+  if (!counted && gt == 0) S.fin_cmd = 1;
   fin_sync();
   if (S.fin_cmd != 1) return false;
+  bool ok = true;
   if (!row_job) {
-    if (ord < S.n_samp) {
-      fullvocab_request_final(p, S, ord);
-    } else {
+    if (ord >= S.n_samp) {
       if (w == 0) greedy_request_final(p, S, ord);
       fin_sync();
+    } else if (p.fullvocab) {
+      fullvocab_request_final(p, S, ord);
+    } else {
+      ok = request_final(p, S, ord);
     }
-    return true;
+  } else {
+    const SlotInfo si = slot_info(p, S, j);
+    unsigned long long top_a = 0ull;
+    float T_row;
+    ok = row_final(p, S, j, si, top_a, T_row);
+    if (ok && p.task != kTaskVerify && p.task != kTaskVerifyGreedy) rows_final(p, S, j, top_a, T_row);
   }
-  const int slot = j;
-  const SlotInfo si = slot_info(p, S, slot);
-  unsigned long long top_a = 0ull;
-  float T_row;
-  if (!row_final(p, S, slot, si, top_a, T_row)) {
-    if (gt == 0) raise_timeout(p);
-    return false;
-  }
-  if (!verify) {
-    rows_final(p, S, slot, top_a, T_row);
-    return true;
-  }
-  // request hand-off: the group finishing the request's last row runs its final
-  const int b = S.req_of_ord[si.ord];
-  if (gt == 0) {
-    fence_acq_rel_gpu();  // release this row's results
-    const bool last = atomicAdd(p.req_cnt + b, 1u) == (uint32_t)(per_s - 1);
-    if (last) {
-      p.req_cnt[b] = 0u;
-      fence_acq_rel_gpu();  // acquire the request's other rows
-    }
-    S.flag = last ? 1 : 0;
-  }
-  fin_sync();
-  if (S.flag) request_final(p, S, si.ord);
-  return true;
+  if (!ok && gt == 0) raise_timeout(p);
+  return ok;
 }
 
 __device__ void finals(const Params& p, Smem& S) {
@@ -1331,7 +1330,7 @@ __device__ void finals(const Params& p, Smem& S) {
   // row jobs: top-k sampling rows, or every row of a rows task; then request
   // jobs from request ordinal ord0 on
   const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * (2 * p.gamma + 1) : p.B);
-  const int ord0 = fv ? 0 : S.n_samp;
+  const int ord0 = 0;  // every request has a final job (sampling first, then greedy)
   const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
   if (gt == kDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);
   fin_sync();

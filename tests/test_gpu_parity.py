@@ -316,3 +316,35 @@ def test_verify_host_buffers(dv):
                                                         20, 0.95, 8)
     _compare_sampling(out_tok.numpy(), out_len.numpy(), want_tok, want_len, margin)
     assert int(out_st.item()) == want_st
+
+
+def test_workspace_left_zero_across_shapes(dv):
+    """Every call leaves its whole workspace at zero, whatever the shape.
+
+    The workspace regions move with the shape: a larger call's tile keys can
+    lie where a smaller call kept its filtered lists. Row finals treat
+    non-zero tile keys as written, so the next call would see leftovers as
+    finished keys. Calls of several shapes and modes run in turn on one
+    workspace. Each is checked against the oracle, and the workspace must
+    read back as zero after each call."""
+    ws = dv.Workspace(48 << 20, DEV)
+    cases = [(1024, "f32", 20, 0.95), (777, "f32", 20, 0.95), (20000, "f32", 20, 0.95),
+             (5003, "bf16", 7, 0.9), (20000, "f32", 0, 1.0), (1024, "f32", 20, 0.95)]
+    for V, dtype, top_k, top_p in cases:
+        X, Y, _ = synth.make_logits(6, 5, V, dtype, data_seed=V)
+        T = np.array([1.0, 0.0, 0.6, 1.0, 1.5, 0.0], np.float32)
+        B, gamma = 6, 5
+        d, _, _ = oracle.sample_rows(Y.reshape(B * gamma, V), synth.draft_sampling_temperatures(T, gamma),
+                                     top_k, top_p, 3)
+        d = d.reshape(B, gamma)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        tok, ln = dv.verify(_t(X), _t(Y), torch.from_numpy(d).to(DEV), torch.from_numpy(T).to(DEV), top_k,
+                            top_p, 9, status=st, workspace=ws)
+        torch.cuda.synchronize()
+        want_tok, want_len, (m_acc, m_draw), want_st = oracle.verify(X, Y, d, T, top_k, top_p, 9,
+                                                                      split_margins=True)
+        assert int(st.item()) == want_st
+        same = np.all(tok.cpu().numpy() == want_tok, axis=1) & (ln.cpu().numpy() == want_len)
+        for b in np.nonzero(~same)[0]:
+            assert m_acc[b] < MARGIN or m_draw[b] < 2.0 ** -22, f"V={V} request {b}"
+        assert int(torch.count_nonzero(ws.buf).item()) == 0, f"workspace not left at zero after V={V}"
