@@ -10,6 +10,12 @@ block. Inputs rotate over 3 independently generated sets (each about 238 MB,
 together well above the 129 MB L2), so no step finds its logits in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload NAME]
+
+``--workload`` measures another of the step's workloads the same way (for
+example b128_g15_fullvocab_f32: block 16, fp32, top-k off and top-p 1, where a
+call is the stream plus the full-vocabulary draw's second pass); the default
+is the headline above.
 
 N > 1 runs under torch.distributed.run: every rank verifies its own batch (the
 step shards by request, no data exchange), timing is the max over ranks.
@@ -36,6 +42,14 @@ import synth  # noqa: E402
 
 WORKLOAD = "b32_mixed_v248320"
 METRIC = "verified draft-positions/sec and achieved HBM GB/s (B=32, block 8, V=248320)"
+
+
+def metric_for(workload: str) -> str:
+    if workload == WORKLOAD:
+        return METRIC
+    w = synth.WORKLOADS[workload]
+    return (f"verified draft-positions/sec and achieved HBM GB/s (B={w['B']}, block {w['gamma'] + 1}, "
+            f"V={w['V']})")
 UNIT = "verified draft positions/s"
 N_SETS = 3
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_sweep_b32_mixed_v248320.md")
@@ -125,17 +139,23 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
-def algorithmic_bytes(inp) -> int:
+def algorithmic_bytes(inp, accept_len=None) -> int:
     """Logit bytes one step must read: every target row, and the draft rows of
-    requests that sample (greedy requests never read their draft rows)."""
+    requests that sample (greedy requests never read their draft rows). Over
+    the full vocabulary (top-k off, top-p 1) the residual or bonus draw reads
+    its rows once more: two rows after a rejection, one for a bonus token
+    (from the step's accept lengths)."""
     B, gamma, V = inp.shape
     es = 2 if inp.target.dtype == np.uint16 else 4
-    n_samp = int(np.sum(inp.temperature > 0))
-    rows = B * (gamma + 1) + n_samp * gamma
+    samp = inp.temperature > 0
+    rows = B * (gamma + 1) + int(np.sum(samp)) * gamma
+    if inp.top_k <= 0 and inp.top_p >= 1.0 and accept_len is not None:
+        lens = np.asarray(accept_len)[samp]
+        rows += int(np.sum(np.where(lens <= gamma, 2, 1)))
     return rows * V * es
 
 
-def cpu_baseline(inp, d, threads=None):
+def cpu_baseline(inp, d, workload, threads=None):
     """The oracle (as it stands) on the host cores: one full batch."""
     import oracle
 
@@ -146,8 +166,27 @@ def cpu_baseline(inp, d, threads=None):
                   threads=threads)
     dt = time.perf_counter() - t0
     return {"value": B * gamma / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"one {WORKLOAD} batch of {B} requests (fp64 C oracle, {threads} host "
+            "sample": f"one {workload} batch of {B} requests (fp64 C oracle, {threads} host "
                       f"threads), {dt:.2f} s"}
+
+
+def combine_over_ranks(region_ms: float, e2e_s: float, steps: int, per_rank_units: int, device=None):
+    """Whole-job numbers from this rank's timings: the slowest rank's timed
+    region and end-to-end step (max over ranks; every rank verifies its own
+    batch, so the job is as slow as its slowest rank), and the units all
+    ranks processed divided by that time. Needs the default process group
+    when the world has more than one rank."""
+    import torch
+
+    world = 1
+    t = torch.tensor([region_ms, e2e_s], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        world = torch.distributed.get_world_size()
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    region_ms, e2e_s = float(t[0].item()), float(t[1].item())
+    return {"world": world, "region_ms": region_ms, "ms_per_step": region_ms / steps,
+            "value": world * steps * per_rank_units / (region_ms / 1e3),
+            "e2e_s": e2e_s, "e2e_value": world * per_rank_units / e2e_s}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -157,7 +196,7 @@ def run_reference(args):
         return 0
     import oracle
 
-    inp = synth.make_workload(WORKLOAD, data_seed=0, seed=0)
+    inp = synth.make_workload(args.workload, data_seed=0, seed=0)
     B, gamma, V = inp.shape
     d, _, _ = oracle.sample_rows(inp.draft.reshape(B * gamma, V),
                                  synth.draft_sampling_temperatures(inp.temperature, gamma),
@@ -183,11 +222,11 @@ def run_reference(args):
     value = args.steps * n_req * gamma / dt
     sample = f"{n_req} of the {B} requests per step (fp64 C oracle, {threads} host threads)"
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_for(args.workload), "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD, "B": B, "gamma": gamma, "V": V,
-                                        "top_k": 20, "top_p": 0.95},
+        "data": "synthetic", "config": {"workload": args.workload, "B": B, "gamma": gamma, "V": V,
+                                        "top_k": inp.top_k, "top_p": inp.top_p},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -215,10 +254,13 @@ def run_gpu(args):
     # ---- inputs: N_SETS independent batches, resident in HBM
     sets_np, sets_dev = [], []
     for s in range(N_SETS):
-        sets_np.append(synth.make_workload(WORKLOAD, data_seed=1000 * rank + s, seed=s))
+        sets_np.append(synth.make_workload(args.workload, data_seed=1000 * rank + s, seed=s))
     B, gamma, V = sets_np[0].shape
-    dt_code = dv.DFLASH_BF16
-    rows_ws = dv.Workspace(dv.rows_workspace_bytes(B * gamma, V, dt_code, 20, 0.95), dev)
+    bf16 = sets_np[0].target.dtype == np.uint16
+    dt_code = dv.DFLASH_BF16 if bf16 else dv.DFLASH_F32
+    es = 2 if bf16 else 4
+    rows_ws = dv.Workspace(dv.rows_workspace_bytes(B * gamma, V, dt_code, sets_np[0].top_k,
+                                                   sets_np[0].top_p), dev)
     for inp in sets_np:
         X = synth.to_torch(inp.target, dev)
         Y = synth.to_torch(inp.draft, dev)
@@ -275,20 +317,14 @@ def run_gpu(args):
         torch.distributed.barrier()
     region_ms = start.elapsed_time(end)
     launch_ms = np.array([a.elapsed_time(b) for a, b in evs])
-    t_region = torch.tensor([region_ms], device=dev, dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t_region, op=torch.distributed.ReduceOp.MAX)
-    region_ms = float(t_region.item())
-    ms_per_step = region_ms / args.steps
-    value = world * args.steps * B * gamma / (region_ms / 1e3)
 
     # ---- roofline of the kernel (one launch = one step)
-    alg = algorithmic_bytes(sets_np[0])
+    alg = algorithmic_bytes(sets_np[(args.steps - 1) % N_SETS], out_len.cpu().numpy())
     avg_launch_s = float(launch_ms.mean()) / 1e3
     achieved = alg / avg_launch_s / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    traffic = profiled_traffic()
+    traffic = profiled_traffic() if args.workload == WORKLOAD else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
@@ -318,14 +354,13 @@ def run_gpu(args):
         dv.verify_host(hX, hY, hd, hT, top_k, top_p, i, h_tok, h_len, h_st, staging, ws)
     e2e_s = (time.perf_counter() - t0) / n_e2e
     n_samp = int(np.sum(inp.temperature > 0))
-    h2d = (B * (gamma + 1) + n_samp * gamma) * V * 2 + B * gamma * 4 + B * 4
+    h2d = (B * (gamma + 1) + n_samp * gamma) * V * es + B * gamma * 4 + B * 4
     d2h = B * (gamma + 1) * 4 + B * 4 + 4
-    t_e2e = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-    if world > 1:
-        torch.distributed.all_reduce(t_e2e, op=torch.distributed.ReduceOp.MAX)
-    e2e = {"value": world * B * gamma / float(t_e2e.item()), "unit": UNIT,
+    job = combine_over_ranks(region_ms, e2e_s, args.steps, B * gamma, dev)
+    ms_per_step, value = job["ms_per_step"], job["value"]
+    e2e = {"value": job["e2e_value"], "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": float(t_e2e.item()) * 1e3}
+           "ms_per_step": job["e2e_s"] * 1e3}
 
     if rank != 0:
         if world > 1:
@@ -333,13 +368,18 @@ def run_gpu(args):
             torch.distributed.destroy_process_group()
         return 0
     lens = out_len.cpu().numpy()
-    cpu = cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy()) if world == 1 else None
+    cpu = cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy(), args.workload) if world == 1 else None
+    T0 = sets_np[0].temperature
+    temps = ("cycling " + " / ".join(f"{t:g}" + (" (greedy)" if t == 0 else "")
+                                     for t in dict.fromkeys(T0.tolist()))
+             if len(set(T0.tolist())) > 1 else f"{T0[0]:g} for every request")
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": B, "gamma": gamma, "V": V, "top_k": top_k,
-                   "top_p": top_p, "temperatures": "cycling 0 (greedy) / 0.6 / 1.0",
+        "metric": metric_for(args.workload), "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "gamma": gamma, "V": V, "top_k": top_k,
+                   "top_p": top_p, "temperatures": temps,
                    "l2": f"inputs rotate over {N_SETS} sets of "
                          f"{(sets_np[0].target.nbytes + sets_np[0].draft.nbytes) / 1e6:.0f} MB "
                          "(larger than L2 together)",
@@ -364,6 +404,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

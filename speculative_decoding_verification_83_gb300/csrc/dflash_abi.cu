@@ -110,7 +110,7 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, bool fullv
 }
 
 // the full-vocabulary draw's second pass over the rows the accept test left
-int run_fullvocab_draw(const Params& p, void* ws, void* stream) {
+int run_fullvocab_draw(const Params& p, void* ws, void* stream, bool sampler = false) {
   const WorkspaceLayout L = make_layout(p.n_slots, p.B, p.geo, true);
   unsigned char* base = static_cast<unsigned char*>(ws);
   FvParams f;
@@ -130,6 +130,8 @@ int run_fullvocab_draw(const Params& p, void* ws, void* stream) {
   f.pos = reinterpret_cast<float4*>(base + L.fv_pos);
   f.last = reinterpret_cast<int2*>(base + L.fv_last);
   f.abort_flag = p.abort_flag;
+  f.sampler = sampler ? 1 : 0;
+  f.row_base = p.row_base;
   const Exp2Table& t = exp2_table();
   memcpy(f.exp_hi, t.hi, sizeof t.hi);
   memcpy(f.exp_lo, t.lo, sizeof t.lo);
@@ -176,7 +178,13 @@ size_t dflash_workspace_bytes(int B, int gamma, int V, int dtype, int top_k, flo
 }
 
 size_t dflash_rows_workspace_bytes(int R, int V, int dtype, int top_k, float top_p) {
-  if (R < 1 || V < 1 || !esize_of(dtype) || filter_mode(V, top_k, top_p) != kModeTopK) return 0;
+  if (R < 1 || V < 1 || !esize_of(dtype)) return 0;
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode == kModeFullVocab) {  // the sampler over the full vocabulary: rows of kMaxB at a time
+    const int chunk = R < kMaxB ? R : kMaxB;
+    return verify_workspace(chunk, 0, V, dtype, true);
+  }
+  if (mode != kModeTopK) return 0;
   const int chunk = R < kMaxCounterSlots ? R : kMaxCounterSlots;
   return make_layout(chunk, 1, make_geometry(V, esize_of(dtype))).total;
 }
@@ -352,6 +360,40 @@ int dflash_verify_host(const void* target_logits, const void* draft_logits, cons
   return DFLASH_OK;
 }
 
+// The sampler over the full vocabulary (top-k off, top_p = 1) is the full-
+// vocabulary verification with no draft positions: each row is a request
+// whose only row is its bonus row, drawn from the whole softmax (T = 0: the
+// argmax), with the sampler's uniforms. Rows go kMaxB at a time.
+static int sample_fullvocab(const void* logits, int R, int V, int dtype, const float* temperature, uint64_t seed,
+                            int32_t* out_tokens, void* workspace, uint32_t* status, void* stream) {
+  const size_t row_bytes = (size_t)V * esize_of(dtype);
+  for (int r0 = 0; r0 < R; r0 += kMaxB) {
+    const int n = R - r0 < kMaxB ? R - r0 : kMaxB;
+    Params p = base_params(dtype, V);
+    p.target = static_cast<const unsigned char*>(logits) + (size_t)r0 * row_bytes;
+    p.draft = p.target;  // no draft rows are read (gamma = 0)
+    p.draft_tokens = nullptr;
+    p.temperature = temperature + r0;
+    p.B = n;
+    p.gamma = 0;
+    p.top_k = 0;
+    p.top_p = 1.0f;
+    p.seed = seed;
+    p.task = kTaskVerify;
+    p.fullvocab = 1;
+    p.row_base = r0;
+    p.out_tokens = out_tokens + r0;
+    p.out_len = nullptr;
+    p.status = status;
+    bind_workspace(p, workspace, n, n, true);
+    int rc = run(p, n, stream);
+    if (rc) return rc;
+    rc = run_fullvocab_draw(p, workspace, stream, true);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
 static int rows_task(int task, const void* logits, int R, int V, int dtype, const float* temperature, int top_k,
                      float top_p, uint64_t seed, int32_t* out_tokens, int32_t* out_idx, float* out_prob,
                      int32_t* out_count, void* workspace, size_t workspace_bytes, uint32_t* status, void* stream) {
@@ -360,16 +402,19 @@ static int rows_task(int task, const void* logits, int R, int V, int dtype, cons
   if (!logits || !temperature || !workspace) return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
   const int mode = filter_mode(V, top_k, top_p);
   if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
-  if (mode != kModeTopK)
+  if (mode != kModeTopK && !(mode == kModeFullVocab && task == kTaskSample))
     return fail(DFLASH_ERR_UNSUPPORTED,
-                "top_k=%d with top_p=%g is not supported here (need 1 <= top_k <= %d, top_k < V)", top_k,
-                (double)top_p, DFLASH_MAX_TOP_K);
+                "top_k=%d with top_p=%g is not supported here (need 1 <= top_k <= %d and top_k < V; the "
+                "sampler also takes top-k off with top_p = 1)",
+                top_k, (double)top_p, DFLASH_MAX_TOP_K);
   int rc = check_aligned(logits, esize_of(dtype), "logits");
   if (rc) return rc;
   const size_t need = dflash_rows_workspace_bytes(R, V, dtype, top_k, top_p);
   if (workspace_bytes < need)
     return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
                 need);
+  if (mode == kModeFullVocab) return sample_fullvocab(logits, R, V, dtype, temperature, seed, out_tokens,
+                                                      workspace, status, stream);
   Params p = base_params(dtype, V);
   p.temperature = temperature;
   p.gamma = 1;

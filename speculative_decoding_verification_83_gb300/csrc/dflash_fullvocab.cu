@@ -388,7 +388,10 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
     const ff z = resid ? zr : zp;
     lr = __reduce_max_sync(0xffffffffu, lr);
     lp = __reduce_max_sync(0xffffffffu, lp);
-    const float u = uniform24(step_uniform_words(f.seed, (uint32_t)b, (uint32_t)q.n, 0u).y);
+    // verification: word 1 of (position n, request b, stream 0); the sampler:
+    // word 0 of (row, 0, stream 1), rows counted across the call's launches
+    const float u = f.sampler ? uniform24(step_uniform_words(f.seed, 0u, (uint32_t)(f.row_base + b), 1u).x)
+                              : uniform24(step_uniform_words(f.seed, (uint32_t)b, (uint32_t)q.n, 0u).y);
     const float tf = __shfl_sync(0xffffffffu, ff_round(ff_scale(u, z)), 0);
     // first slice whose cumulative weight (rounded to fp32) exceeds tf
     ff carry = {0.0f, 0.0f};

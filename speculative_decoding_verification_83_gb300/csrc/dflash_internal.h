@@ -147,6 +147,8 @@ struct FvParams {
   const float* temperature;     // [B]
   int B, gamma, V, dtype, n_slices;
   unsigned long long seed;
+  int sampler;                  // the filtered sampler's uniforms (counter (row_base + b, 0, 1, 0), word 0)
+  int row_base;
   int32_t* out_tokens;          // [B, gamma+1]
   const FvDraw* draw;           // [B]
   float4* part;                 // [B, n_slices]: slice sums of the two rows' exp weights

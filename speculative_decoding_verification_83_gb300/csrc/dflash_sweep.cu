@@ -725,7 +725,7 @@ __device__ bool request_final(const Params& p, Smem& S, int ord) {
     for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? last : -1);
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
-      p.out_len[b] = n + 1;
+      if (p.out_len) p.out_len[b] = n + 1;
       if (st && p.status) atomicOr(p.status, st);
     }
   }
@@ -1175,7 +1175,7 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   }
   st = __reduce_or_sync(0xffffffffu, st);
   if (lane == 0) {
-    p.out_len[b] = n + 1;
+    if (p.out_len) p.out_len[b] = n + 1;
     if (st && p.status) atomicOr(p.status, st);
     if (p.fullvocab) p.fv_draw[b] = FvDraw{n, kFvNone, 0.0f, 0.0f, 0.0f, 0.0f};
   }
@@ -1262,7 +1262,7 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? 0 : -1);
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
-      p.out_len[b] = n + 1;
+      if (p.out_len) p.out_len[b] = n + 1;
       p.fv_draw[b] = FvDraw{n, mode, S.u.fv.m[2 * n], n < gamma ? S.u.fv.m[2 * n + 1] : 0.0f, S.u.fv.s[2 * n],
                             n < gamma ? S.u.fv.s[2 * n + 1] : 0.0f};
       if (st && p.status) atomicOr(p.status, st);

@@ -169,3 +169,26 @@ def test_fullvocab_full_size_workload(dv):
     d = _draft_tokens(inp.draft, inp.temperature, 100)
     n_bad, total = _check(dv, inp.target, inp.draft, d, inp.temperature, inp.seed)
     assert n_bad <= 1, n_bad
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_sampler_full_vocab_matches_oracle(dv, dtype):
+    """dflash_sample with top-k off and top-p 1: one token per row from the
+    whole softmax (T = 0 rows: the argmax), uniforms of the sampler's stream.
+    More than 2048 rows cross the launches the rows go in."""
+    for R, V in ((2100, 300), (24, 30011)):
+        X, _, _ = synth.make_logits(R, 0, V, dtype, data_seed=R + V)
+        L = X.reshape(R, V)
+        T = np.array([1.0, 0.0, 0.7, 1.3, -1.0], np.float32)[np.arange(R) % 5]
+        for seed in (0, 31):
+            want, margin, want_st = oracle.sample_rows(L, T, 0, 1.0, seed)
+            st = torch.zeros(1, dtype=torch.int32, device=DEV)
+            got = dv.sample_rows(_t(L), torch.from_numpy(T).to(DEV), 0, 1.0, seed, status=st)
+            torch.cuda.synchronize()
+            got = got.cpu().numpy()
+            assert int(st.item()) == want_st == oracle.STATUS_BAD_TEMPERATURE
+            greedy = T <= 0
+            assert np.array_equal(got[greedy], want[greedy])
+            diff = np.nonzero(got != want)[0]
+            assert all(margin[r] < DRAW_MARGIN for r in diff), [(int(r), margin[r]) for r in diff[:5]]
+            assert len(diff) <= 1
