@@ -56,9 +56,13 @@ PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_sweep_b32_mixed_v248320
 CSRC = os.path.join(ROOT, "speculative_decoding_verification_83_gb300", "csrc")
 
 
+# the sources the profiled kernel (sweep_kernel) is built from
+KERNEL_SOURCES = ("dflash_sweep.cu", "dflash_device.cuh", "dflash_internal.h")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(os.listdir(CSRC)):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(CSRC, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]

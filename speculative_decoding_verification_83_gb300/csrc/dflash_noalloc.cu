@@ -10,7 +10,7 @@
 // every GPU that loads the library, from module load until process exit.
 //
 // The array holds kNoAllocScratchBytes (4 MiB): enough for the batched step at
-// B = 32, block 8, V = 248320 in bf16 (about 3.1 MB). Shapes whose workspace
+// B = 32, block 8, V = 248320 in bf16 (about 3.6 MB). Shapes whose workspace
 // would not fit are rejected with DFLASH_ERR_INVALID_ARG.
 
 #include <cuda_runtime.h>
