@@ -804,47 +804,80 @@ struct PieceWalk {
   }
 };
 
+// Producer warp: lane 0 issues the bulk copies, one per piece. The index
+// arithmetic of a piece (slot, request, row pointer, body geometry, flags) is
+// a few hundred cycles of dependent scalar work, which on one thread would
+// cap the stream well below HBM bandwidth; so the warp prepares the next 32
+// pieces in parallel, one per lane, and lane 0 only waits for the stage,
+// writes its descriptor and issues the copy.
 __device__ void producer(const Params& p, Smem& S, long long total) {
   const int lane = threadIdx.x & 31;
-  if (lane != 0) return;
   const volatile uint32_t* abort_flag = p.abort_flag;
-  PieceWalk w(p.geo.ppr);
-  int it = 0;
+  const long long mine = total > blockIdx.x ? (total - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int ppr = p.geo.ppr;
   bool aborted = false;
-  for (long long piece = blockIdx.x; piece < total; piece += gridDim.x, ++it, w.next()) {
-    const int stage = it % kStages;
-    const uint32_t round = (uint32_t)(it / kStages);
-    if (!mbar_wait(&S.empty[stage], (round & 1u) ^ 1u, abort_flag)) {
-      aborted = true;
-      break;
+  long long it = 0;
+  for (long long base = 0; base < mine && !aborted; base += 32) {
+    // lane l: piece base + l of this CTA
+    const unsigned char* src = nullptr;
+    int slot = 0, pp = 0, nvec = 0, head = 0, ord = 0;
+    if (base + lane < mine) {
+      const long long piece = blockIdx.x + (base + lane) * (long long)gridDim.x;
+      slot = (int)(piece / ppr);
+      pp = (int)(piece - (long long)slot * ppr);
+      const SlotInfo si = slot_info(p, S, slot);
+      const RowBody rb = row_body(si.ptr, p.geo.V, p.geo.esize);
+      const int v0 = pp * kVecPerPiece;
+      nvec = max(0, min(kVecPerPiece, rb.nvec - v0));
+      int flags = 0;
+      if (in_stream_argmax(p, si))
+        flags = kDescArgmax;
+      else if (p.fullvocab && si.sampling)
+        flags = kDescStats;
+      head = rb.head + flags;
+      ord = si.ord;
+      src = rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16;
     }
-    const SlotInfo si = slot_info(p, S, w.slot);
-    const RowBody rb = row_body(si.ptr, p.geo.V, p.geo.esize);
-    const int v0 = w.pp * kVecPerPiece;
-    const int nvec = max(0, min(kVecPerPiece, rb.nvec - v0));
-    S.desc[stage].slot = w.slot;
-    S.desc[stage].pp = w.pp;
-    S.desc[stage].nvec = nvec;
-    int flags = 0;
-    if (in_stream_argmax(p, si))
-      flags = kDescArgmax;
-    else if (p.fullvocab && si.sampling)
-      flags = kDescStats;
-    S.desc[stage].head = rb.head + flags;
-    S.desc[stage].ord = si.ord;
-    if (nvec > 0) {
-      mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec * 16u);
-      bulk_load(S.ring[stage], rb.row + (size_t)rb.head * p.geo.esize + (size_t)v0 * 16, (uint32_t)nvec * 16u,
-                &S.full[stage]);
-    } else {
-      mbar_arrive(&S.full[stage]);
+    const int n = (int)min(32ll, mine - base);
+    for (int j = 0; j < n; ++j, ++it) {
+      const unsigned char* src_j = reinterpret_cast<const unsigned char*>(
+          __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(src), j));
+      const int slot_j = __shfl_sync(0xffffffffu, slot, j);
+      const int pp_j = __shfl_sync(0xffffffffu, pp, j);
+      const int nvec_j = __shfl_sync(0xffffffffu, nvec, j);
+      const int head_j = __shfl_sync(0xffffffffu, head, j);
+      const int ord_j = __shfl_sync(0xffffffffu, ord, j);
+      int ok = 1;
+      if (lane == 0) {
+        const int stage = (int)(it % kStages);
+        const uint32_t round = (uint32_t)(it / kStages);
+        if (!mbar_wait(&S.empty[stage], (round & 1u) ^ 1u, abort_flag)) {
+          ok = 0;
+        } else {
+          S.desc[stage].slot = slot_j;
+          S.desc[stage].pp = pp_j;
+          S.desc[stage].nvec = nvec_j;
+          S.desc[stage].head = head_j;
+          S.desc[stage].ord = ord_j;
+          if (nvec_j > 0) {
+            mbar_arrive_expect_tx(&S.full[stage], (uint32_t)nvec_j * 16u);
+            bulk_load(S.ring[stage], src_j, (uint32_t)nvec_j * 16u, &S.full[stage]);
+          } else {
+            mbar_arrive(&S.full[stage]);
+          }
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) {
+        aborted = true;
+        break;
+      }
     }
   }
-  if (aborted) {
+  if (aborted && lane == 0) {
     // let copies already issued land before the CTA's shared memory goes away
-    const int first = max(0, it - kStages);
-    for (int j = first; j < it; ++j)
-      (void)mbar_wait(&S.full[j % kStages], (uint32_t)((j / kStages) & 1), abort_flag);
+    const long long first = it > kStages ? it - kStages : 0;
+    for (long long q = first; q < it; ++q)
+      (void)mbar_wait(&S.full[q % kStages], (uint32_t)((q / kStages) & 1), abort_flag);
   }
 }
 
