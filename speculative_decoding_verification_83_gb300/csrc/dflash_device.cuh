@@ -180,6 +180,33 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
   return v;
 }
 
+// Read-only load issued where it is written: a plain read-only load may be
+// sunk by the compiler to its first use, which in a long function can put a
+// full memory round trip (several microseconds while HBM is saturated) on the
+// critical path at the end.
+__device__ __forceinline__ float ld_nc_now(const float* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ int32_t ld_nc_now(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ unsigned short ld_nc_now(const unsigned short* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint4 ld_nc_now(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 // GPU-scope release store / acquire load of a flag word
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -208,81 +235,15 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
 // ---- warp collectives ---------------------------------------------------------------
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
 __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
   return v;
 }
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
   uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
   uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);
   return ((unsigned long long)hi << 32) | lo;
-}
-
-// Bitonic sort of 64 composites held two per lane (element e = lane + 32*r),
-// descending: afterwards lane l holds ranks l (a) and l + 32 (b).
-__device__ __forceinline__ void warp_sort64_desc(unsigned long long& a, unsigned long long& b, int lane) {
-#pragma unroll
-  for (int size = 2; size <= 64; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      if (stride == 32) {
-        // partners are the two registers of one lane; size == 64: all descending
-        unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
-        a = hi;
-        b = lo;
-      } else {
-        const bool lower = (lane & stride) == 0;
-        {
-          const int e = lane;
-          const bool desc = (e & size) == 0;
-          unsigned long long o = shfl_xor_u64(a, stride);
-          unsigned long long mx = a > o ? a : o, mn = a > o ? o : a;
-          a = (lower == desc) ? mx : mn;
-        }
-        {
-          const int e = lane + 32;
-          const bool desc = (e & size) == 0;
-          unsigned long long o = shfl_xor_u64(b, stride);
-          unsigned long long mx = b > o ? b : o, mn = b > o ? o : b;
-          b = (lower == desc) ? mx : mn;
-        }
-      }
-    }
-  }
-}
-
-// Bitonic sort of 32 (key, weight) pairs across a warp, ascending by key.
-__device__ __forceinline__ void warp_sort32_asc(int32_t& key, float& w, int lane) {
-#pragma unroll
-  for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      const bool lower = (lane & stride) == 0;
-      const bool asc = (lane & size) == 0 || size == 32;
-      int32_t ok = __shfl_xor_sync(0xffffffffu, key, stride);
-      float ow = __shfl_xor_sync(0xffffffffu, w, stride);
-      const bool take_small = (lower == asc);
-      const bool other_smaller = ok < key;
-      if (take_small == other_smaller && ok != key) {
-        key = ok;
-        w = ow;
-      }
-    }
-  }
 }
 
 }  // namespace dflash

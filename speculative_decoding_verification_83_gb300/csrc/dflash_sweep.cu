@@ -90,8 +90,8 @@ struct Smem {
       int bad[kMaxRowsPerRequest];
     } fv;
   } u;
-  uint32_t hist[256];
-  unsigned long long cand[kCandCap];
+  alignas(16) uint32_t hist[256];              // also a warp's 32-float scratch
+  alignas(16) unsigned long long cand[kCandCap];  // also a warp's draw scratch
   int32_t cand_tiles[kCandTileCap];
   int fin_slot;
   int fin_cmd;
@@ -236,17 +236,13 @@ __device__ void build_request_order(const Params& p, Smem& S) {
 
 // ---- finals-group helpers (128 threads, gt = thread index in the group) ----------
 __device__ __forceinline__ int fin_tid() { return (int)threadIdx.x - kFinBase; }
-
-__device__ __forceinline__ uint32_t fin_max_u32(Smem& S, uint32_t v) {
-  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
-  v = warp_max_u32(v);
-  if (lane == 0) S.warp_red[w] = v;
-  fin_sync();
-  uint32_t r = 0;
-#pragma unroll
-  for (int i = 0; i < kFinWarps; ++i) r = max(r, S.warp_red[i]);
-  fin_sync();
-  return r;
+// The thread that draws the group's finals jobs (one of the last warp, which
+// issues no fences). A group draws its next job once the current one is
+// ready to run, so jobs go to the groups that are actually working through
+// theirs rather than to those still waiting for a row.
+constexpr int kFinDrawer = kFin - 32;
+__device__ __forceinline__ void draw_next_job(const Params& p, uint32_t& next) {
+  if (fin_tid() == kFinDrawer) next = atomicAdd(p.job_cnt, 1u);  // read only when the job ends
 }
 
 // Group-wide maxima of two values at once. No barrier follows the read of
@@ -337,8 +333,9 @@ __device__ uint32_t select_kth_key(Smem& S, const uint32_t* gkeys, int n, bool c
 // Visits every logit of a row with key >= tau (head, body, tail), finals-group
 // threads in parallel. Used by the exact fallback when the tile filter leaves
 // too many candidates (heavily tied rows).
-template <class F>
-__device__ __forceinline__ void for_each_row_logit(const RowBody& rb, int V, int dtype, uint32_t tau, F&& f) {
+template <int DT, class F>
+__device__ __forceinline__ void for_each_row_logit(const RowBody& rb, int V, uint32_t tau, F&& f) {
+  constexpr int dtype = DT;
   const int gt = fin_tid();
   const int esize = dtype == 0 ? 2 : 4;
   const int per_vec = 16 / esize;
@@ -372,64 +369,142 @@ __device__ __forceinline__ void for_each_row_logit(const RowBody& rb, int V, int
   }
 }
 
+// Largest of a 16-byte vector of logits (NaN if one is NaN).
+template <int DT>
+__device__ __forceinline__ float vector_max(const uint4& wv) {
+  if (DT == 0) {
+    __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.x),
+                                   *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
+    const __nv_bfloat162 b = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.z),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
+    a = __hmax2_nan(a, b);
+    return max_nan(__low2float(a), __high2float(a));
+  }
+  return max_nan(max_nan(__uint_as_float(wv.x), __uint_as_float(wv.y)),
+                 max_nan(__uint_as_float(wv.z), __uint_as_float(wv.w)));
+}
+
 // ---- filtering and drawing ---------------------------------------------------------
+// The warp-wide steps of the finals (sums, prefix sums, sorts) go through a
+// small shared-memory scratch with independent loads rather than through
+// shuffle networks: while the stream keeps the SM's shared-memory pipe busy
+// with bulk copies and consumer loads, each shuffle of a dependent chain waits
+// a long time, and a sorting network is dozens of them in a row.
+
+// Total of the 32 values in sc (16-byte aligned), added in lane order, and in
+// `before` the part added before this lane's value. Every lane adds in the
+// same order, so all lanes get the same total.
+__device__ __forceinline__ float scratch_sums(const float* sc, int lane, float& before) {
+  const float4* s4 = reinterpret_cast<const float4*>(sc);
+  float total = 0.0f;
+  before = 0.0f;
+#pragma unroll 1
+  for (int q = 0; q < 8; ++q) {
+    const float4 v = s4[q];
+    const float e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (4 * q + i == lane) before = total;
+      total += e[i];
+    }
+  }
+  return total;
+}
+
 // Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
 // over the survivors, top-p cut, renormalisation. Returns this lane's
-// probability (0 outside the kept set) and sets idx to -1 there.
+// probability (0 outside the kept set) and sets idx to -1 there. sc: 32 floats
+// of warp scratch.
 __device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
-                                             int lane) {
+                                             int lane, float* sc) {
   const bool in_k = lane < k_eff && idx >= 0;
-  const float x = value_of_key(key);
-  const float z = x / T;
-  const float z0 = __shfl_sync(0xffffffffu, z, 0);
+  const float z = value_of_key(key) / T;
+  if (lane == 0) sc[0] = z;
+  __syncwarp();
+  const float z0 = sc[0];  // the largest
+  __syncwarp();
   const float w = in_k ? expf(z - z0) : 0.0f;
   bool keep = in_k;
+  float before;
   if (top_p < 1.0f) {
-    const float W = warp_sum(w);
-    const float pi = w / W;
-    const float incl = warp_inclusive_scan(pi, lane);
-    float before = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) before = 0.0f;
-    keep = keep && (before < top_p);
+    sc[lane] = w;
+    __syncwarp();
+    const float W = scratch_sums(sc, lane, before);
+    __syncwarp();
+    keep = keep && (before / W < top_p);  // mass of the higher ranks
   }
   const float wk = keep ? w : 0.0f;
-  const float Wk = warp_sum(wk);
+  sc[lane] = wk;
+  __syncwarp();
+  const float Wk = scratch_sums(sc, lane, before);
+  __syncwarp();
   if (!keep) idx = -1;
   return keep ? wk / Wk : 0.0f;
 }
 
 // Inverse CDF in ascending token order: the smallest token whose cumulative
 // weight exceeds u * total; if rounding leaves none, the last token with
-// positive weight; tokens marked -1 have no weight.
-__device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane) {
-  int32_t key = tok >= 0 ? tok : INT_MAX;
-  float wt = tok >= 0 ? w : 0.0f;
-  warp_sort32_asc(key, wt, lane);
-  const float cum = warp_inclusive_scan(wt, lane);
-  const float total = __shfl_sync(0xffffffffu, cum, 31);
+// positive weight; tokens marked -1 have no weight. The lanes are put in
+// token order by rank (ties, only among the -1 marks, by lane); sk, sw: 32
+// words each of warp scratch, 16-byte aligned.
+__device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane, int32_t* sk,
+                                                  float* sw) {
+  const int32_t key = tok >= 0 ? tok : INT_MAX;
+  const float wt = tok >= 0 ? w : 0.0f;
+  sk[lane] = key;
+  __syncwarp();
+  int r = 0;
+  const int4* k4 = reinterpret_cast<const int4*>(sk);
+#pragma unroll 1
+  for (int q = 0; q < 8; ++q) {
+    const int4 v = k4[q];
+    const int32_t e[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r += (e[i] < key || (e[i] == key && 4 * q + i < lane)) ? 1 : 0;
+  }
+  __syncwarp();
+  sk[r] = key;
+  sw[r] = wt;
+  __syncwarp();
+  // lane l now stands for rank l
+  const float wl = sw[lane];
+  float before;
+  const float total = scratch_sums(sw, lane, before);
+  const float cum = before + wl;
   const float t = u * total;
-  const uint32_t hit = __ballot_sync(0xffffffffu, wt > 0.0f && t < cum);
+  const uint32_t hit = __ballot_sync(0xffffffffu, wl > 0.0f && t < cum);
   int chosen;
   if (hit) {
     chosen = __ffs(hit) - 1;
   } else {
-    const uint32_t pos = __ballot_sync(0xffffffffu, wt > 0.0f);
+    const uint32_t pos = __ballot_sync(0xffffffffu, wl > 0.0f);
     chosen = pos ? 31 - __clz(pos) : 0;
   }
-  const int32_t r = __shfl_sync(0xffffffffu, key, chosen);
-  return r == INT_MAX ? -1 : r;
+  const int32_t res = sk[chosen];
+  __syncwarp();
+  return res == INT_MAX ? -1 : res;
+}
+
+// Body vector of the f-th gathered vector: f / 32 picks the candidate tile,
+// f % 32 the vector within it.
+__device__ __forceinline__ int candidate_vector(const Smem& S, int f) {
+  const int tile = S.cand_tiles[f >> 5];
+  const int pc = tile / kTilesPerPiece;
+  return pc * kVecPerPiece + tile_vector(tile - pc * kTilesPerPiece, f & 31);
 }
 
 // ---- row final ----------------------------------------------------------------------
 // Leaves the row's sorted top-k composites in the group's first warp (lane l:
 // rank l in `top_a`) and in the workspace.
+template <int DT>
 __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si, unsigned long long& top_a,
-                          float& T_row) {
+                          float& T_row, uint32_t& next) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
-  const int V = p.geo.V, dtype = p.dtype;
+  const int V = p.geo.V;
+  constexpr int dtype = DT;  // the kernel's logit type
   // the row's temperature, loaded now and used last: a global load at the
   // end of the final would add a full round trip to it
-  T_row = __ldg(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
+  T_row = ld_nc_now(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
   const RowBody rb = row_body(si.ptr, V, p.geo.esize);
   const int n_tiles = p.geo.tiles;
   const uint32_t* gkeys = p.tile_keys + (size_t)slot * n_tiles;
@@ -440,7 +515,13 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   // one round trip; the edges' maximum is all ones when one of them is NaN
   const int n_edge = rb.head + (V - rb.tail_start);
   const int edge_j = gt < rb.head ? gt : rb.tail_start + (gt - rb.head);
-  const float edge_x = gt < n_edge ? load_logit(rb.row, edge_j, dtype) : 0.0f;
+  float edge_x = 0.0f;
+  if (gt < n_edge) {  // inline-assembly loads stay here, ahead of the poll
+    if (DT == 0)
+      edge_x = __uint_as_float((uint32_t)ld_nc_now(reinterpret_cast<const unsigned short*>(rb.row) + edge_j) << 16);
+    else
+      edge_x = ld_nc_now(reinterpret_cast<const float*>(rb.row) + edge_j);
+  }
   // The row is ready when every tile key is written: the keys start the call
   // at zero (no tile key is zero: a NaN maximum is the canonical NaN) and a
   // consumer warp stores each one once. So the polls are the final's own key
@@ -462,6 +543,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     if (fin_sync_or(*abort_flag != 0u || global_timer_ns() - t0 > kWaitLimitNs)) return false;
     __nanosleep(128);
   }
+  draw_next_job(p, next);
   const uint32_t emx = gt < n_edge ? (isnan(edge_x) ? 0xffffffffu : key_of(edge_x)) : 0u;
   uint32_t tile_max, edge_max;
   fin_max2_u32(S, mx, emx, tile_max, edge_max);
@@ -493,13 +575,20 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
         c[i] = S.hist[lane * 8 + i];
         run += c[i];
       }
-      uint32_t incl = run;
+      // the lanes' runs through shared memory (hist[0..31], read above)
+      __syncwarp();
+      S.hist[lane] = run;
+      __syncwarp();
+      uint32_t before = 0;
+      const uint4* h4 = reinterpret_cast<const uint4*>(S.hist);
+#pragma unroll 1
+      for (int q = 0; q < 8; ++q) {
+        const uint4 v = h4[q];
+        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t nb = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += nb;
+        for (int i = 0; i < 4; ++i) before += 4 * q + i < lane ? e[i] : 0u;
       }
-      const uint32_t before = incl - run;
+      const uint32_t incl = before + run;
       const bool here = before < (uint32_t)k && (uint32_t)k <= incl;
       if (here) {
         uint32_t acc = before;
@@ -530,26 +619,29 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     S.n_cand = 0;
   }
   fin_sync();
-  // candidate tiles, one slot reservation per warp and step
-  for (int base = 0; base < n_tiles; base += kFin) {
-    const int i = base + gt;
-    const bool take = i < n_tiles && (cached ? S.u.key_cache[i] : __ldcg(gkeys + i)) >= tau;
-    const uint32_t ball = __ballot_sync(0xffffffffu, take);
-    if (ball) {
-      int first = 0;
-      if (lane == __ffs(ball) - 1) first = atomicAdd(&S.n_cand_tiles, __popc(ball));
-      first = __shfl_sync(0xffffffffu, first, __ffs(ball) - 1);
-      const int pos = first + __popc(ball & ((1u << lane) - 1u));
-      if (take && pos < kCandTileCap) S.cand_tiles[pos] = i;
+  // candidate tiles: each thread marks its tiles (every kFin-th) in a mask
+  // and reserves their slots with one atomic
+  for (int base = 0; base < n_tiles; base += kFin * 32) {
+    uint32_t mask = 0u;
+#pragma unroll 8
+    for (int u = 0; u < 32; ++u) {
+      const int i = base + u * kFin + gt;
+      if (i < n_tiles && (cached ? S.u.key_cache[i] : __ldcg(gkeys + i)) >= tau) mask |= 1u << u;
+    }
+    if (mask) {
+      int pos = atomicAdd(&S.n_cand_tiles, __popc(mask));
+      for (; mask; mask &= mask - 1u, ++pos)
+        if (pos < kCandTileCap) S.cand_tiles[pos] = base + (__ffs(mask) - 1) * kFin + gt;
     }
   }
   fin_sync();
   const int n_ct = S.n_cand_tiles;
   bool overflow = n_ct > kCandTileCap;
   if (!overflow) {
-    // gather: the candidate tiles' 32 vectors each, spread over the group with
-    // every load of a round issued before any is used
-    const int esize = p.geo.esize, per_vec = 16 / esize;
+    // gather: the candidate tiles' 32 vectors each, spread over the group,
+    // every load of a round issued before any is used (inline-assembly loads,
+    // which the compiler keeps where they stand)
+    constexpr int esize = DT == 0 ? 2 : 4, per_vec = 16 / esize;
     const uint4* body = reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * esize);
     const int n_vec_all = n_ct * 32;
     for (int base = 0; base < n_vec_all; base += kFin * 8) {
@@ -560,12 +652,10 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
         const int f = base + u * kFin + gt;
         vi[u] = -1;
         if (f < n_vec_all) {
-          const int tile = S.cand_tiles[f >> 5], t = f & 31;
-          const int pc = tile / kTilesPerPiece;
-          const int v = pc * kVecPerPiece + tile_vector(tile - pc * kTilesPerPiece, t);
+          const int v = candidate_vector(S, f);
           if (v < rb.nvec) {
             vi[u] = v;
-            wv[u] = __ldg(body + v);
+            wv[u] = ld_nc_now(body + v);
           }
         }
       }
@@ -574,6 +664,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
         if (vi[u] < 0) continue;
         const uint32_t ws[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
         const int ebase = rb.head + vi[u] * per_vec;
+#pragma unroll
         for (int e = 0; e < per_vec; ++e) {
           uint32_t key;
           if (dtype == 0)
@@ -602,7 +693,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       S.hist[gt] = 0u;
       S.hist[gt + kFin] = 0u;
       fin_sync();
-      for_each_row_logit(rb, V, dtype, tau, [&](uint32_t key, int j) {
+      for_each_row_logit<DT>(rb, V, tau, [&](uint32_t key, int j) {
         const unsigned long long c = composite(key, j);
         if ((c & mask) == prefix) atomicAdd(&S.hist[(uint32_t)(c >> shift) & 255u], 1u);
       });
@@ -616,7 +707,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     if (gt == 0) S.n_cand = 0;
     fin_sync();
     const unsigned long long thr = prefix;
-    for_each_row_logit(rb, V, dtype, tau, [&](uint32_t key, int j) {
+    for_each_row_logit<DT>(rb, V, tau, [&](uint32_t key, int j) {
       const unsigned long long c = composite(key, j);
       if (c >= thr) {
         const int pos = atomicAdd(&S.n_cand, 1);
@@ -628,16 +719,31 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   // sort the (<= 64) candidates in the first warp; ranks < k are the row's top-k
   const int n_c = min(S.n_cand, kCandCap);
   if (w == 0) {
-    unsigned long long a = lane < n_c ? S.cand[lane] : 0ull;
-    unsigned long long b = lane + 32 < n_c ? S.cand[lane + 32] : 0ull;
-    warp_sort64_desc(a, b, lane);
+    // by rank: the composites are distinct (each carries its logit's index),
+    // so a composite's rank is the number of larger ones
+    const unsigned long long a0 = lane < n_c ? S.cand[lane] : 0ull;
+    const unsigned long long b0 = lane + 32 < n_c ? S.cand[lane + 32] : 0ull;
+    int ra = 0, rb = 0;
+    const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(S.cand);
+#pragma unroll 1
+    for (int m = 0; m < n_c; m += 2) {
+      const ulonglong2 v = c2[m >> 1];
+      ra += (v.x > a0 ? 1 : 0) + (m + 1 < n_c && v.y > a0 ? 1 : 0);
+      rb += (v.x > b0 ? 1 : 0) + (m + 1 < n_c && v.y > b0 ? 1 : 0);
+    }
+    __syncwarp();
+    if (lane < n_c) S.cand[ra] = a0;
+    if (lane + 32 < n_c) S.cand[rb] = b0;
+    __syncwarp();
+    const unsigned long long a = lane < n_c ? S.cand[lane] : 0ull;
     top_a = a;
     if (p.task == kTaskVerify) {
       // the row's filtered distribution (ranks < k, k <= 32), which the
       // request final reads
       const bool valid = lane < k && lane < n_c;
       int32_t idx = valid ? composite_idx(a) : -1;
-      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane);
+      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane,
+                                   reinterpret_cast<float*>(S.hist));
       const uint32_t lo = __float_as_uint(pr) | ((bad && lane == 0) ? 0x80000000u : 0u);
       p.res_list[(size_t)slot * kMaxTopK + lane] = ((unsigned long long)(uint32_t)(idx + 2) << 32) | lo;
     }
@@ -655,7 +761,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
 // position runs the accept test u < p(d)/q(d); the first failing position (or
 // gamma when none fails) is where the residual max(0, p - q) (or the bonus
 // distribution p) is drawn from.
-__device__ bool request_final(const Params& p, Smem& S, int ord) {
+__device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int gamma = p.gamma, V = p.geo.V;
   const int b = S.req_of_ord[ord];
@@ -667,6 +773,8 @@ __device__ bool request_final(const Params& p, Smem& S, int ord) {
   // written word is zero): the polls are the final's own loads.
   unsigned long long* words = p.res_list + (size_t)slot0 * kMaxTopK;
   const int n_words = per_s * kMaxTopK;
+  // the drafts, loaded before the wait (after it they would add a round trip)
+  const int32_t d_lane = (w == 0 && lane < gamma) ? ld_nc_now(d + lane) : -1;
   const volatile uint32_t* abort_flag = p.abort_flag;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
@@ -683,6 +791,7 @@ __device__ bool request_final(const Params& p, Smem& S, int ord) {
     if (fin_sync_or(*abort_flag != 0u || global_timer_ns() - t0 > kWaitLimitNs)) return false;
     __nanosleep(128);
   }
+  draw_next_job(p, next);
   // every call leaves the workspace at zero: its regions move with the
   // shape, and another shape's tile keys may lie here next time
   for (int i = gt; i < n_words; i += kFin) words[i] = 0ull;
@@ -693,9 +802,10 @@ __device__ bool request_final(const Params& p, Smem& S, int ord) {
     bool reject = false;
     if (lane < gamma) {
       const int i = lane;
-      const int32_t di = __ldg(d + i);
+      const int32_t di = d_lane;
       if (di < 0 || di >= V) st |= kStatusBadToken;
       float p_d = 0.0f, q_d = 0.0f;
+#pragma unroll 1
       for (int m = 0; m < 32; ++m) {
         if (S.u.lists.idx[2 * i][m] == di) p_d = S.u.lists.prob[2 * i][m];
         if (S.u.lists.idx[2 * i + 1][m] == di) q_d = S.u.lists.prob[2 * i + 1][m];
@@ -715,14 +825,17 @@ __device__ bool request_final(const Params& p, Smem& S, int ord) {
     if (n < gamma) {
       // residual max(0, p - q) over the target's kept tokens
       float q_of_t = 0.0f;
+#pragma unroll 1
       for (int m = 0; m < 32; ++m)
         if (ti >= 0 && S.u.lists.idx[row + 1][m] == ti) q_of_t = S.u.lists.prob[row + 1][m];
       const float r = ti >= 0 ? fmaxf(pi - q_of_t, 0.0f) : 0.0f;
       if (__ballot_sync(0xffffffffu, r > 0.0f) != 0u) wt = r;
     }
-    int32_t last = draw_ascending(ti, wt, uniform24(wd.y), lane);
+    int32_t last = draw_ascending(ti, wt, uniform24(wd.y), lane, reinterpret_cast<int32_t*>(S.cand),
+                                  reinterpret_cast<float*>(S.cand) + 32);
     if (last < 0) last = __shfl_sync(0xffffffffu, ti, 0);
-    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? last : -1);
+    // gamma <= 32: a position i < n is this lane's own (i == lane)
+    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? d_lane : (i == n ? last : -1);
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
       if (p.out_len) p.out_len[b] = n + 1;
@@ -745,7 +858,7 @@ __device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long t
     int32_t idx = (lane < k_eff && lane < n_c) ? composite_idx(top_a) : -1;
     float pr;
     if (samp) {
-      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane);
+      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane, reinterpret_cast<float*>(S.hist));
     } else {
       pr = lane == 0 ? 1.0f : 0.0f;
       if (lane != 0) idx = -1;
@@ -761,7 +874,8 @@ __device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long t
       int32_t tok;
       if (samp) {
         const uint4 wd = step_uniform_words(p.seed, 0u, (uint32_t)(p.row_base + r), 1u);
-        tok = draw_ascending(idx, pr, uniform24(wd.x), lane);
+        tok = draw_ascending(idx, pr, uniform24(wd.x), lane, reinterpret_cast<int32_t*>(S.cand),
+                             reinterpret_cast<float*>(S.cand) + 32);
         if (tok < 0) tok = __shfl_sync(0xffffffffu, idx, 0);
       } else {
         tok = __shfl_sync(0xffffffffu, idx, 0);
@@ -881,19 +995,6 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
   }
 }
 
-template <int DT>
-__device__ __forceinline__ float vector_max(const uint4& wv) {
-  if (DT == 0) {
-    __nv_bfloat162 a = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.x),
-                                   *reinterpret_cast<const __nv_bfloat162*>(&wv.y));
-    const __nv_bfloat162 b = __hmax2_nan(*reinterpret_cast<const __nv_bfloat162*>(&wv.z),
-                                         *reinterpret_cast<const __nv_bfloat162*>(&wv.w));
-    a = __hmax2_nan(a, b);
-    return max_nan(__low2float(a), __high2float(a));
-  }
-  return max_nan(max_nan(__uint_as_float(wv.x), __uint_as_float(wv.y)),
-                 max_nan(__uint_as_float(wv.z), __uint_as_float(wv.w)));
-}
 
 // Tile keys of a piece: per block of 4 rounds, each 8-lane group's maximum is
 // one tile key. For greedy rows (argmax) the warp instead folds the piece's
@@ -1141,6 +1242,7 @@ __device__ __forceinline__ bool wait_rows(const Params& p, int slot0, int n) {
 
 // Final of a greedy request: its rows' argmax came from the stream (plus the
 // logits outside each row's aligned body); prefix-match the drafts.
+template <int DT>
 __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   const int lane = fin_tid() & 31;
   const int gamma = p.gamma, V = p.geo.V;
@@ -1149,8 +1251,11 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
   const int32_t* d = p.draft_tokens + (size_t)b * gamma;
   const size_t row_bytes = (size_t)V * p.geo.esize;
+  // inputs loaded first, so none of them adds a round trip at the end
+  const float T_b = p.task == kTaskVerify ? ld_nc_now(p.temperature + b) : 0.0f;  // greedy task: no temperatures
+  const int32_t d_lane = lane < gamma ? ld_nc_now(d + lane) : -1;
   uint32_t st = 0;
-  if (p.task == kTaskVerify && __ldg(p.temperature + b) != 0.0f) st |= kStatusBadTemperature;
+  if (p.task == kTaskVerify && T_b != 0.0f) st |= kStatusBadTemperature;
   int n = gamma;  // length of the matching prefix
   int32_t am[2] = {-1, -1};  // argmax of rows lane and lane + 32
   for (int base = 0, u = 0; base <= gamma; base += 32, ++u) {
@@ -1171,7 +1276,7 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
         const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
         int e_hit = -1;
         for (int e = per_vec - 1; e >= 0; --e) {
-          const float x = p.dtype == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16)
+          const float x = DT == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16)
                                        : __uint_as_float(ws[e]);
           if (key_of(x) == vkey) e_hit = e;
         }
@@ -1179,13 +1284,13 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
         comp = composite(vkey, rb.head + v * per_vec + (e_hit < 0 ? 0 : e_hit));
       }
       for (int j = 0; j < rb.head; ++j) {
-        const float x = load_logit(rb.row, j, p.dtype);
+        const float x = load_logit(rb.row, j, DT);
         nan |= isnan(x);
         const unsigned long long c = composite(key_of(x), j);
         comp = c > comp ? c : comp;
       }
       for (int j = rb.tail_start; j < V; ++j) {
-        const float x = load_logit(rb.row, j, p.dtype);
+        const float x = load_logit(rb.row, j, DT);
         nan |= isnan(x);
         const unsigned long long c = composite(key_of(x), j);
         comp = c > comp ? c : comp;
@@ -1194,8 +1299,8 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
       am[u] = composite_idx(comp);
       if (am[u] < 0 || am[u] >= V) am[u] = 0;
     }
-    if (i < gamma) {
-      const int32_t di = __ldg(d + i);
+    if (i < gamma) {  // gamma <= 32: i == lane
+      const int32_t di = d_lane;
       if (di < 0 || di >= V) st |= kStatusBadToken;
       mismatch = di != am[u];
     }
@@ -1204,7 +1309,7 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   }
   for (int base = 0, u = 0; base <= gamma; base += 32, ++u) {
     const int i = base + lane;
-    if (i <= gamma) out[i] = i < n ? __ldg(d + i) : (i == n ? am[u] : -1);
+    if (i <= gamma) out[i] = i < n ? d_lane : (i == n ? am[u] : -1);
   }
   st = __reduce_or_sync(0xffffffffu, st);
   if (lane == 0) {
@@ -1220,12 +1325,14 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
 // u_i < p_i(d_i) / q_i(d_i)). Emits the accepted drafts and the accept length
 // and leaves the draw at the first rejected position (residual) or at the
 // bonus position to the second pass, with the rows' maxima.
+template <int DT>
 __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int gamma = p.gamma, V = p.geo.V, per_s = 2 * gamma + 1;
   const int b = S.req_of_ord[ord];
   const int slot0 = ord * per_s;
-  const float scale = kLog2e / __ldg(p.temperature + b);  // as the producer computed it
+  const float scale = kLog2e / ld_nc_now(p.temperature + b);  // as the producer computed it
+  const int32_t d_lane = (w == 0 && lane < gamma) ? ld_nc_now(p.draft_tokens + (size_t)b * gamma + lane) : -1;
   for (int r = w; r < per_s; r += kFinWarps) {
     const SlotInfo si = slot_info(p, S, slot0 + r);
     const RowBody rb = row_body(si.ptr, V, p.geo.esize);
@@ -1242,7 +1349,7 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     const int n_edge = rb.head + (V - rb.tail_start);
     for (int e = lane; e < n_edge; e += 32) {
       const int j = e < rb.head ? e : rb.tail_start + (e - rb.head);
-      const float x = load_logit(rb.row, j, p.dtype);
+      const float x = load_logit(rb.row, j, DT);
       nan |= isnan(x);
       if (!isnan(x)) stats_merge(m, sum, x, 1.0f, scale);
     }
@@ -1261,7 +1368,6 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
   }
   fin_sync();
   if (w == 0) {
-    const int32_t* d = p.draft_tokens + (size_t)b * gamma;
     int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
     uint32_t st = 0;
     for (int r = lane; r < per_s; r += 32)
@@ -1269,7 +1375,7 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     bool stop = false;
     if (lane < gamma) {
       const int i = lane;
-      const int32_t di = __ldg(d + i);
+      const int32_t di = d_lane;
       const bool valid = di >= 0 && di < V;
       if (!valid) st |= kStatusBadToken;
       if (S.u.fv.bad[2 * i] || S.u.fv.bad[2 * i + 1]) {
@@ -1279,8 +1385,8 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
         if (valid) {
           const SlotInfo sx = slot_info(p, S, slot0 + 2 * i);
           const SlotInfo sy = slot_info(p, S, slot0 + 2 * i + 1);
-          p_d = ex2_approx((load_logit(sx.ptr, di, p.dtype) - S.u.fv.m[2 * i]) * scale) / S.u.fv.s[2 * i];
-          q_d = ex2_approx((load_logit(sy.ptr, di, p.dtype) - S.u.fv.m[2 * i + 1]) * scale) /
+          p_d = ex2_approx((load_logit(sx.ptr, di, DT) - S.u.fv.m[2 * i]) * scale) / S.u.fv.s[2 * i];
+          q_d = ex2_approx((load_logit(sy.ptr, di, DT) - S.u.fv.m[2 * i + 1]) * scale) /
                 S.u.fv.s[2 * i + 1];
         }
         const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
@@ -1292,7 +1398,7 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     const bool bad_n = n < gamma ? (S.u.fv.bad[2 * n] || S.u.fv.bad[2 * n + 1]) : S.u.fv.bad[2 * gamma] != 0;
     const int mode = bad_n ? kFvNone : (n < gamma ? kFvResidual : kFvBonus);
     // the token at position n is the second pass's (0 when a bad row leaves no draw)
-    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? __ldg(d + i) : (i == n ? 0 : -1);
+    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? d_lane : (i == n ? 0 : -1);
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
       if (p.out_len) p.out_len[b] = n + 1;
@@ -1308,11 +1414,12 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
 // a counter in the workspace: first the rows that need a top-k (sampling
 // rows, every row of the rows tasks) in the order rows finish, then one job
 // per request (sampling requests, then greedy ones). A group draws its next
-// job while it works on the current one, so a job goes to whichever group
-// frees up first. A row final waits only on the stream; a sampling request's
+// job while it works on the current one (once that one's inputs are ready),
+// so a job goes to whichever group frees up first. A row final waits only on the stream; a sampling request's
 // final may wait on its rows' finals, which were all drawn before it, so no
 // two groups can wait on each other in a cycle.
-__device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord) {
+template <int DT>
+__device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord, uint32_t& next) {
   const int gt = fin_tid(), w = gt >> 5;
   const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
   // A row job's row final, and a top-k sampling request's final, wait on the
@@ -1320,11 +1427,9 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
   // request's final waits for its rows' pieces to be counted.
   const bool counted = !row_job && (ord >= S.n_samp || p.fullvocab);
   if (w == 0 && counted) {
-    bool ok;
-    if (ord < S.n_samp)
-      ok = wait_rows(p, ord * per_s, per_s);
-    else
-      ok = wait_rows(p, S.n_samp * per_s + (ord - S.n_samp) * per_g, per_g);
+    const bool samp = ord < S.n_samp;
+    const bool ok = wait_rows(p, samp ? ord * per_s : S.n_samp * per_s + (ord - S.n_samp) * per_g,
+                              samp ? per_s : per_g);
     if (gt == 0) {
       if (!ok) raise_timeout(p);
       S.fin_cmd = ok ? 1 : 2;
@@ -1334,30 +1439,31 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
   if (!counted && gt == 0) S.fin_cmd = 1;
   fin_sync();
   if (S.fin_cmd != 1) return false;
+  if (counted) draw_next_job(p, next);  // the others draw when their polls succeed
   bool ok = true;
   if (!row_job) {
     if (ord >= S.n_samp) {
-      if (w == 0) greedy_request_final(p, S, ord);
+      if (w == 0) greedy_request_final<DT>(p, S, ord);
       fin_sync();
     } else if (p.fullvocab) {
-      fullvocab_request_final(p, S, ord);
+      fullvocab_request_final<DT>(p, S, ord);
     } else {
-      ok = request_final(p, S, ord);
+      ok = request_final(p, S, ord, next);
     }
   } else {
     const SlotInfo si = slot_info(p, S, j);
     unsigned long long top_a = 0ull;
     float T_row;
-    ok = row_final(p, S, j, si, top_a, T_row);
+    ok = row_final<DT>(p, S, j, si, top_a, T_row, next);
     if (ok && p.task != kTaskVerify && p.task != kTaskVerifyGreedy) rows_final(p, S, j, top_a, T_row);
   }
   if (!ok && gt == 0) raise_timeout(p);
   return ok;
 }
 
+template <int DT>
 __device__ void finals(const Params& p, Smem& S) {
   const int gt = fin_tid();
-  constexpr int kDrawer = kFin - 32;  // a thread of the last warp, which issues no fences
   const bool verify = p.task == kTaskVerify || p.task == kTaskVerifyGreedy;
   const bool fv = verify && p.fullvocab;
   // row jobs: top-k sampling rows, or every row of a rows task; then request
@@ -1365,22 +1471,21 @@ __device__ void finals(const Params& p, Smem& S) {
   const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * (2 * p.gamma + 1) : p.B);
   const int ord0 = 0;  // every request has a final job (sampling first, then greedy)
   const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
-  if (gt == kDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);
+  if (gt == kFinDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);
   fin_sync();
   int j = S.fin_slot;
   while (j < n_jobs) {
-    uint32_t next = 0u;
-    if (gt == kDrawer) next = atomicAdd(p.job_cnt, 1u);  // read only after this job
-    const bool ok = j < n_row_jobs ? finals_job(p, S, true, j, 0)
-                                   : finals_job(p, S, false, 0, ord0 + (j - n_row_jobs));
+    uint32_t next = 0u;  // drawn by the job once it is ready to run
+    const bool ok = j < n_row_jobs ? finals_job<DT>(p, S, true, j, 0, next)
+                                   : finals_job<DT>(p, S, false, 0, ord0 + (j - n_row_jobs), next);
     if (!ok) return;  // timed out: the workspace must be prepared again anyway
-    if (gt == kDrawer) S.fin_slot = (int)next;
+    if (gt == kFinDrawer) S.fin_slot = (int)next;
     fin_sync();
     j = S.fin_slot;
   }
   // every group's last draw is past the jobs; the very last of all draws
   // returns the counter to zero for the next call
-  if (gt == kDrawer && j == n_jobs + (int)gridDim.x - 1) *p.job_cnt = 0u;
+  if (gt == kFinDrawer && j == n_jobs + (int)gridDim.x - 1) *p.job_cnt = 0u;
 }
 
 // ---- the kernel ---------------------------------------------------------------------------
@@ -1412,7 +1517,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
   else if (warp == kPublisherWarp)
     publisher(p, S, total);
   else
-    finals(p, S);
+    finals<DT>(p, S);
 }
 
 __global__ void uniforms_kernel(unsigned long long seed, int B, int npos, int stream_id, float* ua, float* ud) {
