@@ -53,6 +53,7 @@ static_assert(kKeyQueue >= kConsumerWarps, "key-queue slots must cover every con
 constexpr int kCtasPerSm = 1;
 
 constexpr int kMaxTopK = 32;     // one kept token per lane of a warp
+constexpr int kListWords = kMaxTopK + 1;  // a row's filtered list, then its draft token's probability
 constexpr int kCandCap = 64;     // candidates sorted in registers (2 per lane)
 constexpr int kCandTileCap = 128;
 constexpr int kKeyCache = 2048;  // tile keys of one row cached in shared memory
@@ -131,10 +132,11 @@ struct Params {
   uint32_t* job_cnt;    // [1]: next finals job to hand out (beside the abort flag)
   unsigned long long* row_best;  // [kMaxCounterSlots]: greedy rows' best (key, index) composite
   uint32_t* tile_keys;  // [n_slots, geo.tiles]; full-vocabulary rows: float2 (max, sum) per piece
-  // [n_slots, kMaxTopK]: a verification sampling row's filtered list, one
+  // [n_slots, kListWords]: a verification sampling row's filtered list, one
   // word per rank: (token + 2) << 32 | probability bits, the sign bit of
-  // rank 0 set for a bad row. No written word is zero, so the request final
-  // polls the words themselves.
+  // rank 0 set for a bad row; then 1 << 32 | the probability the row gives
+  // its position's draft token (0 when not kept, and for the bonus row). No
+  // written word is zero, so the request final polls the words themselves.
   unsigned long long* res_list;
   FvDraw* fv_draw;      // [B]: full-vocabulary mode
   int n_slots;
@@ -190,7 +192,7 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.abort_flag = off; off = align_up(off + 2 * sizeof(uint32_t), 256);  // abort flag, job counter
   L.row_best = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)kMaxCounterSlots, 256);
   L.tile_keys = off;  off = align_up(off + sizeof(uint32_t) * (size_t)n_slots * g.tiles, 256);
-  L.res_list = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)n_slots * kMaxTopK, 256);
+  L.res_list = off;   off = align_up(off + sizeof(unsigned long long) * (size_t)n_slots * kListWords, 256);
   const size_t fv_req = fullvocab ? (size_t)n_requests : 0;
   const size_t fv_cells = fv_req * (size_t)fv_slices(g.V);
   L.fv_draw = off;    off = align_up(off + sizeof(FvDraw) * fv_req, 256);

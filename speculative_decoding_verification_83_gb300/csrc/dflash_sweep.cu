@@ -505,6 +505,11 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   // the row's temperature, loaded now and used last: a global load at the
   // end of the final would add a full round trip to it
   T_row = ld_nc_now(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
+  // a verification row's position's draft token (target row 2i and draft row
+  // 2i + 1 of a request are position i's; the bonus row has none)
+  const int32_t d_row = (p.task == kTaskVerify && si.r < 2 * p.gamma)
+                            ? ld_nc_now(p.draft_tokens + (size_t)S.req_of_ord[si.ord] * p.gamma + (si.r >> 1))
+                            : -1;
   const RowBody rb = row_body(si.ptr, V, p.geo.esize);
   const int n_tiles = p.geo.tiles;
   const uint32_t* gkeys = p.tile_keys + (size_t)slot * n_tiles;
@@ -745,7 +750,12 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane,
                                    reinterpret_cast<float*>(S.hist));
       const uint32_t lo = __float_as_uint(pr) | ((bad && lane == 0) ? 0x80000000u : 0u);
-      p.res_list[(size_t)slot * kMaxTopK + lane] = ((unsigned long long)(uint32_t)(idx + 2) << 32) | lo;
+      unsigned long long* list = p.res_list + (size_t)slot * kListWords;
+      list[lane] = ((unsigned long long)(uint32_t)(idx + 2) << 32) | lo;
+      // the probability of the position's draft token, for the accept test
+      const uint32_t hit = __ballot_sync(0xffffffffu, idx >= 0 && idx == d_row);
+      const float pd = hit ? __shfl_sync(0xffffffffu, pr, __ffs(hit) - 1) : 0.0f;
+      if (lane == 0) list[kMaxTopK] = (1ull << 32) | __float_as_uint(pd);
     }
     if (bad && lane == 0 && p.status) atomicOr(p.status, kStatusBadRow);
   }
@@ -755,6 +765,10 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   fin_sync();
   return true;
 }
+
+// Home slot of a token in a 64-slot table (Fibonacci hashing).
+__device__ __forceinline__ uint32_t token_slot(int32_t t) { return ((uint32_t)t * 2654435761u) >> 26; }
+static_assert(2 * kMaxTopK == 64, "token_slot hashes into 64 slots");
 
 // ---- request final (sampling verification) -------------------------------------------
 // The rows arrive filtered (kept tokens and probabilities). One lane per draft
@@ -771,8 +785,8 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
   const int slot0 = ord * per_s;
   // The rows' filtered lists are ready when every word is written (no
   // written word is zero): the polls are the final's own loads.
-  unsigned long long* words = p.res_list + (size_t)slot0 * kMaxTopK;
-  const int n_words = per_s * kMaxTopK;
+  unsigned long long* words = p.res_list + (size_t)slot0 * kListWords;
+  const int n_words = per_s * kListWords;
   // the drafts, loaded before the wait (after it they would add a round trip)
   const int32_t d_lane = (w == 0 && lane < gamma) ? ld_nc_now(d + lane) : -1;
   const volatile uint32_t* abort_flag = p.abort_flag;
@@ -782,10 +796,11 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
     for (int i = gt; i < n_words; i += kFin) {
       const unsigned long long v = ld_relaxed_gpu_u64(words + i);
       mine = mine && v != 0ull;
-      const int r = i >> 5, l = i & 31;
-      S.u.lists.idx[r][l] = (int32_t)(uint32_t)(v >> 32) - 2;
+      const int r = i / kListWords, l = i - r * kListWords;
+      // column 32: the prob. of the row's draft token (prob) and the row's bad flag (idx)
       S.u.lists.prob[r][l] = __uint_as_float((uint32_t)v & 0x7fffffffu);
-      if (l == 0) S.u.lists.idx[r][32] = (int32_t)((uint32_t)v >> 31);  // the row's bad flag
+      if (l < kMaxTopK) S.u.lists.idx[r][l] = (int32_t)(uint32_t)(v >> 32) - 2;
+      if (l == 0) S.u.lists.idx[r][32] = (int32_t)((uint32_t)v >> 31);
     }
     if (fin_sync_and(mine)) break;
     if (fin_sync_or(*abort_flag != 0u || global_timer_ns() - t0 > kWaitLimitNs)) return false;
@@ -799,39 +814,63 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
     uint32_t st = 0;
     for (int r = lane; r < per_s; r += 32)
       if (S.u.lists.idx[r][32]) st |= kStatusBadRow;
+    // lane l: position l's uniforms (accept: word x, draw: word y)
+    uint4 wd = make_uint4(0u, 0u, 0u, 0u);
+    if (lane <= gamma) wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)lane, 0u);
     bool reject = false;
     if (lane < gamma) {
-      const int i = lane;
       const int32_t di = d_lane;
       if (di < 0 || di >= V) st |= kStatusBadToken;
-      float p_d = 0.0f, q_d = 0.0f;
-#pragma unroll 1
-      for (int m = 0; m < 32; ++m) {
-        if (S.u.lists.idx[2 * i][m] == di) p_d = S.u.lists.prob[2 * i][m];
-        if (S.u.lists.idx[2 * i + 1][m] == di) q_d = S.u.lists.prob[2 * i + 1][m];
-      }
-      if (di < 0) p_d = q_d = 0.0f;  // -1 marks dropped entries
-      const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
+      // p(d) and q(d), found by the rows' finals (0 when the token is not kept)
+      const float p_d = S.u.lists.prob[2 * lane][32], q_d = S.u.lists.prob[2 * lane + 1][32];
       const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
       reject = !(uniform24(wd.x) < ratio);
     }
     const uint32_t rej = __ballot_sync(0xffffffffu, reject);
     const int n = rej ? __ffs(rej) - 1 : gamma;  // drafts accepted
-    const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)n, 0u);
+    uint32_t u_draw = __shfl_sync(0xffffffffu, wd.y, n & 31);
+    if (n >= 32) u_draw = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)n, 0u).y;  // gamma = 32, all kept
     const int row = 2 * n;  // target row of position n (the bonus row when n == gamma)
     const int32_t ti = S.u.lists.idx[row][lane];
     const float pi = S.u.lists.prob[row][lane];
     float wt = pi;
     if (n < gamma) {
-      // residual max(0, p - q) over the target's kept tokens
+      // residual max(0, p - q) over the target's kept tokens: q from the
+      // draft row's list through a 64-slot open-addressing table (S.cand as
+      // scratch: keys, then values)
+      int32_t* hk = reinterpret_cast<int32_t*>(S.cand);
+      float* hv = reinterpret_cast<float*>(S.cand) + 2 * kMaxTopK;
+      hk[lane] = -1;
+      hk[lane + kMaxTopK] = -1;
+      __syncwarp();
+      const int32_t dt = S.u.lists.idx[row + 1][lane];
+      if (dt >= 0) {
+        uint32_t h = token_slot(dt);
+        for (int probe = 0; probe < 2 * kMaxTopK; ++probe, h = (h + 1u) & (2 * kMaxTopK - 1)) {
+          if (atomicCAS(&hk[h], -1, dt) == -1) {
+            hv[h] = S.u.lists.prob[row + 1][lane];
+            break;
+          }
+        }
+      }
+      __syncwarp();
       float q_of_t = 0.0f;
-#pragma unroll 1
-      for (int m = 0; m < 32; ++m)
-        if (ti >= 0 && S.u.lists.idx[row + 1][m] == ti) q_of_t = S.u.lists.prob[row + 1][m];
+      if (ti >= 0) {
+        uint32_t h = token_slot(ti);
+        for (int probe = 0; probe < 2 * kMaxTopK; ++probe, h = (h + 1u) & (2 * kMaxTopK - 1)) {
+          const int32_t key = hk[h];
+          if (key == ti) {
+            q_of_t = hv[h];
+            break;
+          }
+          if (key == -1) break;
+        }
+      }
+      __syncwarp();  // the table's slots are the draw's scratch next
       const float r = ti >= 0 ? fmaxf(pi - q_of_t, 0.0f) : 0.0f;
       if (__ballot_sync(0xffffffffu, r > 0.0f) != 0u) wt = r;
     }
-    int32_t last = draw_ascending(ti, wt, uniform24(wd.y), lane, reinterpret_cast<int32_t*>(S.cand),
+    int32_t last = draw_ascending(ti, wt, uniform24(u_draw), lane, reinterpret_cast<int32_t*>(S.cand),
                                   reinterpret_cast<float*>(S.cand) + 32);
     if (last < 0) last = __shfl_sync(0xffffffffu, ti, 0);
     // gamma <= 32: a position i < n is this lane's own (i == lane)
