@@ -385,11 +385,10 @@ __device__ __forceinline__ float vector_max(const uint4& wv) {
 }
 
 // ---- filtering and drawing ---------------------------------------------------------
-// The warp-wide steps of the finals (sums, prefix sums, sorts) go through a
-// small shared-memory scratch with independent loads rather than through
-// shuffle networks: while the stream keeps the SM's shared-memory pipe busy
-// with bulk copies and consumer loads, each shuffle of a dependent chain waits
-// a long time, and a sorting network is dozens of them in a row.
+// Sorts in the finals place each element by its rank (independent loads from
+// a small shared scratch) rather than through a sorting network, which is
+// dozens of dependent shuffle steps; sums and prefix sums over a warp are
+// five shuffle steps each.
 
 // Total of the 32 values in sc (16-byte aligned), added in lane order, and in
 // `before` the part added before this lane's value. Every lane adds in the
@@ -411,33 +410,41 @@ __device__ __forceinline__ float scratch_sums(const float* sc, int lane, float& 
   return total;
 }
 
+// Warp-wide sum (butterfly: every lane gets the same total) and inclusive
+// prefix sum of a float. Short shuffle chains: five dependent steps each.
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  return v;
+}
+
 // Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
 // over the survivors, top-p cut, renormalisation. Returns this lane's
-// probability (0 outside the kept set) and sets idx to -1 there. sc: 32 floats
-// of warp scratch.
+// probability (0 outside the kept set) and sets idx to -1 there.
 __device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
-                                             int lane, float* sc) {
+                                             int lane) {
   const bool in_k = lane < k_eff && idx >= 0;
   const float z = value_of_key(key) / T;
-  if (lane == 0) sc[0] = z;
-  __syncwarp();
-  const float z0 = sc[0];  // the largest
-  __syncwarp();
+  const float z0 = __shfl_sync(0xffffffffu, z, 0);  // the largest
   const float w = in_k ? expf(z - z0) : 0.0f;
   bool keep = in_k;
-  float before;
   if (top_p < 1.0f) {
-    sc[lane] = w;
-    __syncwarp();
-    const float W = scratch_sums(sc, lane, before);
-    __syncwarp();
-    keep = keep && (before / W < top_p);  // mass of the higher ranks
+    const float W = warp_sum(w);
+    const float incl = warp_inclusive_scan(w / W, lane);
+    float before = __shfl_up_sync(0xffffffffu, incl, 1);  // mass of the higher ranks
+    if (lane == 0) before = 0.0f;
+    keep = keep && (before < top_p);
   }
   const float wk = keep ? w : 0.0f;
-  sc[lane] = wk;
-  __syncwarp();
-  const float Wk = scratch_sums(sc, lane, before);
-  __syncwarp();
+  const float Wk = warp_sum(wk);
   if (!keep) idx = -1;
   return keep ? wk / Wk : 0.0f;
 }
@@ -491,6 +498,21 @@ __device__ __forceinline__ int candidate_vector(const Smem& S, int f) {
   const int tile = S.cand_tiles[f >> 5];
   const int pc = tile / kTilesPerPiece;
   return pc * kVecPerPiece + tile_vector(tile - pc * kTilesPerPiece, f & 31);
+}
+
+// Exclusive prefix over the warp of a count c (0 <= c < 128), from one
+// ballot per bit, and the warp's total.
+__device__ __forceinline__ int warp_exclusive_count(int c, int lane, int& total) {
+  const uint32_t below = (1u << lane) - 1u;
+  int pre = 0;
+  total = 0;
+#pragma unroll
+  for (int b = 0; b < 7; ++b) {
+    const uint32_t m = __ballot_sync(0xffffffffu, (c >> b) & 1);
+    pre += __popc(m & below) << b;
+    total += __popc(m) << b;
+  }
+  return pre;
 }
 
 // ---- row final ----------------------------------------------------------------------
@@ -566,10 +588,19 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     S.hist[gt] = 0u;
     S.hist[gt + kFin] = 0u;
     fin_sync();
-    for (int i = gt; i < n_tiles; i += kFin) {
-      const uint32_t key = cached ? S.u.key_cache[i] : __ldcg(gkeys + i);
-      const uint32_t bucket = (tile_max - key) >> 16;
-      if (bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
+    // (the cached and uncached loops are separate: a branch inside one loop
+    // keeps the compiler from overlapping the iterations' loads)
+    if (cached) {
+#pragma unroll 4
+      for (int i = gt; i < n_tiles; i += kFin) {
+        const uint32_t bucket = (tile_max - S.u.key_cache[i]) >> 16;
+        if (bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
+      }
+    } else {
+      for (int i = gt; i < n_tiles; i += kFin) {
+        const uint32_t bucket = (tile_max - __ldcg(gkeys + i)) >> 16;
+        if (bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
+      }
     }
     fin_sync();
     if (gt < 32) {
@@ -580,20 +611,13 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
         c[i] = S.hist[lane * 8 + i];
         run += c[i];
       }
-      // the lanes' runs through shared memory (hist[0..31], read above)
-      __syncwarp();
-      S.hist[lane] = run;
-      __syncwarp();
-      uint32_t before = 0;
-      const uint4* h4 = reinterpret_cast<const uint4*>(S.hist);
-#pragma unroll 1
-      for (int q = 0; q < 8; ++q) {
-        const uint4 v = h4[q];
-        const uint32_t e[4] = {v.x, v.y, v.z, v.w};
+      uint32_t incl = run;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) before += 4 * q + i < lane ? e[i] : 0u;
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t nb = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += nb;
       }
-      const uint32_t incl = before + run;
+      const uint32_t before = incl - run;
       const bool here = before < (uint32_t)k && (uint32_t)k <= incl;
       if (here) {
         uint32_t acc = before;
@@ -624,20 +648,27 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     S.n_cand = 0;
   }
   fin_sync();
-  // candidate tiles: each thread marks its tiles (every kFin-th) in a mask
-  // and reserves their slots with one atomic
+  // candidate tiles: each thread marks its tiles (every kFin-th) in a mask;
+  // a warp reserves its slots with one atomic (shared atomics on one address
+  // serialise) and places its lanes by a prefix of their counts
   for (int base = 0; base < n_tiles; base += kFin * 32) {
     uint32_t mask = 0u;
+    const int n_u = min(32, (n_tiles - base - gt + kFin - 1) / kFin);  // this thread's tiles here
+    if (cached) {
 #pragma unroll 8
-    for (int u = 0; u < 32; ++u) {
-      const int i = base + u * kFin + gt;
-      if (i < n_tiles && (cached ? S.u.key_cache[i] : __ldcg(gkeys + i)) >= tau) mask |= 1u << u;
+      for (int u = 0; u < n_u; ++u)
+        if (S.u.key_cache[base + u * kFin + gt] >= tau) mask |= 1u << u;
+    } else {
+      for (int u = 0; u < n_u; ++u)
+        if (__ldcg(gkeys + base + u * kFin + gt) >= tau) mask |= 1u << u;
     }
-    if (mask) {
-      int pos = atomicAdd(&S.n_cand_tiles, __popc(mask));
-      for (; mask; mask &= mask - 1u, ++pos)
-        if (pos < kCandTileCap) S.cand_tiles[pos] = base + (__ffs(mask) - 1) * kFin + gt;
-    }
+    int wtotal;
+    const int pre = warp_exclusive_count(__popc(mask), lane, wtotal);
+    int first = 0;
+    if (lane == 0 && wtotal) first = atomicAdd(&S.n_cand_tiles, wtotal);
+    int pos = __shfl_sync(0xffffffffu, first, 0) + pre;
+    for (; mask; mask &= mask - 1u, ++pos)
+      if (pos < kCandTileCap) S.cand_tiles[pos] = base + (__ffs(mask) - 1) * kFin + gt;
   }
   fin_sync();
   const int n_ct = S.n_cand_tiles;
@@ -747,8 +778,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       // request final reads
       const bool valid = lane < k && lane < n_c;
       int32_t idx = valid ? composite_idx(a) : -1;
-      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane,
-                                   reinterpret_cast<float*>(S.hist));
+      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane);
       const uint32_t lo = __float_as_uint(pr) | ((bad && lane == 0) ? 0x80000000u : 0u);
       unsigned long long* list = p.res_list + (size_t)slot * kListWords;
       list[lane] = ((unsigned long long)(uint32_t)(idx + 2) << 32) | lo;
@@ -897,7 +927,7 @@ __device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long t
     int32_t idx = (lane < k_eff && lane < n_c) ? composite_idx(top_a) : -1;
     float pr;
     if (samp) {
-      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane, reinterpret_cast<float*>(S.hist));
+      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane);
     } else {
       pr = lane == 0 ? 1.0f : 0.0f;
       if (lane != 0) idx = -1;

@@ -348,3 +348,36 @@ def test_workspace_left_zero_across_shapes(dv):
         for b in np.nonzero(~same)[0]:
             assert m_acc[b] < MARGIN or m_draw[b] < 2.0 ** -22, f"V={V} request {b}"
         assert int(torch.count_nonzero(ws.buf).item()) == 0, f"workspace not left at zero after V={V}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_verify_narrow_and_wide_top_tiles(dv, dtype):
+    """Row finals find the k-th largest tile maximum by counting tile maxima in
+    a window of buckets below the row's largest, or, when the k largest spread
+    wider than that window, by a full histogram. Rows of both kinds, in one
+    batch, against the oracle: a row is 'wide' when 20 spikes 100, 95, ..., 5
+    sit in separate tiles above Gaussian logits."""
+    B, gamma, V = 6, 3, 50000
+    X, Y, _ = synth.make_logits(B, gamma, V, "f32", data_seed=123, sigma_d=0.3)
+    X = X.copy()
+    Y = Y.copy()
+    rng = np.random.default_rng(5)
+    for b in (1, 3, 4):
+        for i in range(gamma + 1):
+            pos = rng.choice(V // 300, size=20, replace=False) * 300 + 7
+            X[b, i, pos] = np.arange(100, 0, -5, dtype=np.float32)
+            if i < gamma:
+                Y[b, i, pos] = X[b, i, pos] - 0.5
+    if dtype == "bf16":
+        X, Y = synth.f32_to_bf16_bits(X), synth.f32_to_bf16_bits(Y)
+    T = np.array([1.0, 1.0, 0.7, 1.3, 0.0, 1.0], np.float32)
+    d, _, _ = oracle.sample_rows(Y.reshape(B * gamma, V), synth.draft_sampling_temperatures(T, gamma),
+                                 20, 0.95, 9)
+    d = d.reshape(B, gamma)
+    n_bad = 0
+    for seed in (1, 2, 3):
+        want_tok, want_len, margin, want_st = oracle.verify(X, Y, d, T, 20, 0.95, seed)
+        tok, ln, st = _run_verify(dv, X, Y, d, T, 20, 0.95, seed)
+        assert st == want_st
+        n_bad += _compare_sampling(tok, ln, want_tok, want_len, margin)
+    assert n_bad <= 1
