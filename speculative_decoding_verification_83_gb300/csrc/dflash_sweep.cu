@@ -515,6 +515,8 @@ __device__ __forceinline__ int warp_exclusive_count(int c, int lane, int& total)
   return pre;
 }
 
+static_assert(sizeof(decltype(Smem::u)) >= sizeof(uint4) * 8 * kFin, "the gather's stage fits the union");
+
 // ---- row final ----------------------------------------------------------------------
 // Leaves the row's sorted top-k composites in the group's first warp (lane l:
 // rank l in `top_a`) and in the workspace.
@@ -676,41 +678,56 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   if (!overflow) {
     // gather: the candidate tiles' 32 vectors each, spread over the group,
     // every load of a round issued before any is used (inline-assembly loads,
-    // which the compiler keeps where they stand)
+    // which the compiler keeps where they stand).
     constexpr int esize = DT == 0 ? 2 : 4, per_vec = 16 / esize;
     const uint4* body = reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * esize);
     const int n_vec_all = n_ct * 32;
+    // The round's vectors wait in shared memory (the key cache is done with,
+    // each thread has its own slots), so the marking below is a rolled loop:
+    // its code is fetched once and run eight times, where an unrolled one is
+    // fetched line by line once per row final.
+    uint4* stage = reinterpret_cast<uint4*>(&S.u);  // [8][kFin]
     for (int base = 0; base < n_vec_all; base += kFin * 8) {
       uint4 wv[8];
-      int vi[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int f = base + u * kFin + gt;
-        vi[u] = -1;
+        wv[u] = make_uint4(0u, 0u, 0u, 0u);
         if (f < n_vec_all) {
           const int v = candidate_vector(S, f);
-          if (v < rb.nvec) {
-            vi[u] = v;
-            wv[u] = ld_nc_now(body + v);
-          }
+          if (v < rb.nvec) wv[u] = ld_nc_now(body + v);
         }
       }
 #pragma unroll
+      for (int u = 0; u < 8; ++u) stage[u * kFin + gt] = wv[u];
+      // marks of the logits at or above tau (bit per_vec u + e), without branches per logit
+      unsigned long long cm = 0ull;
+#pragma unroll 1
       for (int u = 0; u < 8; ++u) {
-        if (vi[u] < 0) continue;
-        const uint32_t ws[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
-        const int ebase = rb.head + vi[u] * per_vec;
+        const int f = base + u * kFin + gt;
+        if (f >= n_vec_all) break;
+        if (candidate_vector(S, f) >= rb.nvec) continue;
+        const uint4 x = stage[u * kFin + gt];
+        const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
+        uint32_t m = 0u;
 #pragma unroll
         for (int e = 0; e < per_vec; ++e) {
-          uint32_t key;
-          if (dtype == 0)
-            key = key_of(__uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16));
-          else
-            key = key_of(__uint_as_float(ws[e]));
-          if (key >= tau) {
-            const int pos = atomicAdd(&S.n_cand, 1);
-            if (pos < kCandCap) S.cand[pos] = composite(key, ebase + e);
-          }
+          const uint32_t key = dtype == 0 ? key_of(__uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16))
+                                          : key_of(__uint_as_float(ws[e]));
+          m |= (key >= tau ? 1u : 0u) << e;
+        }
+        cm |= (unsigned long long)m << (u * per_vec);
+      }
+      if (cm) {  // few threads: one slot reservation, then the marked logits
+        int pos = atomicAdd(&S.n_cand, __popcll(cm));
+        for (; cm; cm &= cm - 1ull, ++pos) {
+          const int bit = __ffsll(cm) - 1, u = bit / per_vec, e = bit - u * per_vec;
+          const uint4 x = stage[u * kFin + gt];
+          const int q = dtype == 0 ? e >> 1 : e;
+          const uint32_t word = q == 0 ? x.x : q == 1 ? x.y : q == 2 ? x.z : x.w;
+          const uint32_t key = key_of(__uint_as_float(dtype == 0 ? (word >> ((e & 1) * 16)) << 16 : word));
+          const int v = candidate_vector(S, base + u * kFin + gt);
+          if (pos < kCandCap) S.cand[pos] = composite(key, rb.head + v * per_vec + e);
         }
       }
     }
