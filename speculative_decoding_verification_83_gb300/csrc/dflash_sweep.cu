@@ -1581,16 +1581,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5;
 
-  if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+  // the mbarriers, one per thread of the warps that load no temperatures
+  // (the consumer threads' loads of the request order are in flight meanwhile)
+  static_assert(kThreads - kConsumers >= 2 * (kStages + kKeyQueue), "one thread per mbarrier");
+  {
+    const int b = tid - kConsumers;
+    if (b >= 0 && b < 2 * (kStages + kKeyQueue)) {
+      uint64_t* bar = b < kStages ? &S.full[b]
+                      : b < 2 * kStages ? &S.empty[b - kStages]
+                      : b < 2 * kStages + kKeyQueue ? &S.kfull[b - 2 * kStages]
+                                                    : &S.kempty[b - 2 * kStages - kKeyQueue];
+      mbar_init(bar, 1);
+      fence_barrier_init();
     }
-    for (int s = 0; s < kKeyQueue; ++s) {
-      mbar_init(&S.kfull[s], 1);
-      mbar_init(&S.kempty[s], 1);
-    }
-    fence_barrier_init();
   }
   build_request_order(p, S);  // contains __syncthreads
   __syncthreads();
