@@ -61,10 +61,15 @@ KERNEL_SOURCES = ("dflash_sweep.cu", "dflash_device.cuh", "dflash_internal.h")
 
 
 def kernel_source_hash() -> str:
+    """Hash of the profiled kernel's code: comments and the amount of white
+    space do not count, so editing a comment keeps a profile valid."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(CSRC, f)) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(f.encode() + " ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -27,10 +27,12 @@
 //     are always candidates, and a row whose ties leave too many candidates
 //     falls back to an exact radix selection. It then filters the row
 //     (temperature, softmax over the survivors, top-p, renormalise) into
-//     words that are never zero. A sampling request's final polls its rows'
+//     words that are never zero, plus one with the probability it gives the
+//     position's draft token. A sampling request's final polls its rows'
 //     words and runs the accept test at every draft position at once (Philox
 //     uniforms), then the residual or bonus draw. A greedy request's final
-//     prefix-matches the streamed argmax.
+//     prefix-matches the streamed argmax. A group draws its next job once the
+//     current one's inputs are ready.
 // Every wait is time-bounded; row finals wait only on the stream, and a
 // request final only on row finals drawn before it, so there is no cycle of
 // waits and no grid-wide barrier. Every successful call leaves the workspace
