@@ -92,7 +92,7 @@ struct Smem {
       int bad[kMaxRowsPerRequest];
     } fv;
   } u;
-  alignas(16) uint32_t hist[256];              // also a warp's 32-float scratch
+  alignas(16) uint32_t hist[256];              // a row final's tau histogram
   alignas(16) unsigned long long cand[kCandCap];  // also a warp's draw scratch
   int32_t cand_tiles[kCandTileCap];
   int fin_slot;
