@@ -836,8 +836,11 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
   // written word is zero): the polls are the final's own loads.
   unsigned long long* words = p.res_list + (size_t)slot0 * kListWords;
   const int n_words = per_s * kListWords;
-  // the drafts, loaded before the wait (after it they would add a round trip)
+  // the drafts, loaded before the wait (after it they would add a round trip),
+  // and lane l's counter-based words for position l (accept: x, draw: y)
   const int32_t d_lane = (w == 0 && lane < gamma) ? ld_nc_now(d + lane) : -1;
+  uint4 wd = make_uint4(0u, 0u, 0u, 0u);
+  if (w == 0 && lane <= gamma) wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)lane, 0u);
   const volatile uint32_t* abort_flag = p.abort_flag;
   const unsigned long long t0 = global_timer_ns();
   for (;;) {
@@ -863,9 +866,6 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
     uint32_t st = 0;
     for (int r = lane; r < per_s; r += 32)
       if (S.u.lists.idx[r][32]) st |= kStatusBadRow;
-    // lane l: position l's uniforms (accept: word x, draw: word y)
-    uint4 wd = make_uint4(0u, 0u, 0u, 0u);
-    if (lane <= gamma) wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)lane, 0u);
     bool reject = false;
     if (lane < gamma) {
       const int32_t di = d_lane;
@@ -1089,10 +1089,11 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
 // (largest key, lowest vector holding it) into the row's running argmax.
 template <int DT>
 __device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, int nvec, int slot, int pp,
-                                           bool argmax, int lane) {
+                                           bool argmax, int head, int lane) {
   uint32_t* keys_out = p.tile_keys + (size_t)slot * p.geo.tiles + pp * kTilesPerPiece;
-  uint32_t best_key = 0u;  // greedy: this lane's largest key and its lowest vector
+  uint32_t best_key = 0u;  // greedy: this lane's largest key, its lowest vector and that vector
   int best_v = 0;
+  uint4 best_w = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 2
   for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
     uint4 wv[4];
@@ -1113,6 +1114,7 @@ __device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, in
           if (k > best_key) {
             best_key = k;
             best_v = v;
+            best_w = wv[rr];
           }
         }
       }
@@ -1126,7 +1128,18 @@ __device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, in
     }
   }
   if (argmax) {
-    unsigned long long comp = best_key ? composite(best_key, pp * kVecPerPiece + best_v) : 0ull;
+    // the lowest logit of the best vector that holds its key (none does for a
+    // NaN maximum: its first logit stands in, and the row is flagged bad)
+    constexpr int per_vec = DT == 0 ? 8 : 4;
+    const uint32_t ws[4] = {best_w.x, best_w.y, best_w.z, best_w.w};
+    int e_hit = 0;
+#pragma unroll
+    for (int e = per_vec - 1; e >= 0; --e) {
+      const float x = DT == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16) : __uint_as_float(ws[e]);
+      if (key_of(x) == best_key) e_hit = e;
+    }
+    unsigned long long comp =
+        best_key ? composite(best_key, head + (pp * kVecPerPiece + best_v) * per_vec + e_hit) : 0ull;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const unsigned long long oc = shfl_xor_u64(comp, o);
@@ -1242,7 +1255,8 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
       piece_stats<DT>(st4, nvec, p.temperature + S.req_of_ord[dsc.ord],
                       reinterpret_cast<float2*>(p.tile_keys + (size_t)dsc.slot * p.geo.tiles) + dsc.pp, lane);
     else
-      piece_keys<DT>(p, st4, nvec, dsc.slot, dsc.pp, (dsc.head & kDescArgmax) != 0, lane);
+      piece_keys<DT>(p, st4, nvec, dsc.slot, dsc.pp, (dsc.head & kDescArgmax) != 0, dsc.head & (kDescArgmax - 1),
+                     lane);
     __syncwarp();  // the stage is read and the keys are stored before lane 0 signals
     int ok = 1;
     if (lane == 0) {
@@ -1350,27 +1364,12 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
     const int i = base + lane;
     bool mismatch = false;
     if (i <= gamma) {
-      // the stream left (largest key, lowest body vector holding it)
+      // the stream left (largest key, lowest logit of the body holding it)
       const unsigned long long vbest = ld_acquire_gpu_u64(p.row_best + slot0 + i);
       p.row_best[slot0 + i] = 0ull;  // ready for the next call
       const RowBody rb = row_body(p.target + ((size_t)b * (gamma + 1) + i) * row_bytes, V, p.geo.esize);
       bool nan = false;
-      unsigned long long comp = 0ull;
-      if (vbest != 0ull) {
-        const uint32_t vkey = composite_key(vbest);
-        const int v = composite_idx(vbest);
-        const int per_vec = 16 / p.geo.esize;
-        const uint4 wv = __ldg(reinterpret_cast<const uint4*>(rb.row + (size_t)rb.head * p.geo.esize) + v);
-        const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
-        int e_hit = -1;
-        for (int e = per_vec - 1; e >= 0; --e) {
-          const float x = DT == 0 ? __uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16)
-                                       : __uint_as_float(ws[e]);
-          if (key_of(x) == vkey) e_hit = e;
-        }
-        // no logit carries a NaN maximum's canonical key: keep it, flagged below
-        comp = composite(vkey, rb.head + v * per_vec + (e_hit < 0 ? 0 : e_hit));
-      }
+      unsigned long long comp = vbest;
       for (int j = 0; j < rb.head; ++j) {
         const float x = load_logit(rb.row, j, DT);
         nan |= isnan(x);
