@@ -63,6 +63,8 @@ def _bind(lib):
     lib.oracle_verify.restype = I
     lib.oracle_verify_margins.argtypes = [P, P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, I, I]
     lib.oracle_verify_margins.restype = I
+    lib.oracle_verify_det_margins.argtypes = [P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, I, I]
+    lib.oracle_verify_det_margins.restype = I
     lib.oracle_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, I, I]
     lib.oracle_verify_greedy.restype = I
     lib.oracle_sample_rows.argtypes = [P, I, I, I, P, I, F, U64, P, P, P, I, I]
@@ -223,6 +225,48 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
     status = 0
     for s in statuses:
         status |= s
+    if split_margins:
+        return tokens, lens, (margin, margin_draw), status
+    return tokens, lens, np.minimum(margin, margin_draw), status
+
+
+def verify_det(target, draft_tokens, temperature, top_k, top_p, seed, threads=None, lib=None,
+               split_margins=False):
+    """Verification of deterministic drafts (q = the point mass at each draft
+    token; no draft logits). Returns (tokens, accept_len, margin, status) as
+    ``verify``."""
+    lib = lib or _load()
+    X = _contig(target)
+    d = _contig(draft_tokens, np.int32)
+    T = _contig(temperature, np.float32)
+    B, g1, V = X.shape
+    gamma = g1 - 1
+    assert d.shape == (B, gamma) and T.shape == (B,)
+    dt = _dtype_code(X)
+    tokens = np.full((B, gamma + 1), -1, np.int32)
+    lens = np.zeros(B, np.int32)
+    margin = np.full(B, np.inf, np.float64)
+    margin_draw = np.full(B, np.inf, np.float64)
+    nthreads = threads or default_threads()
+    todo = _ranges(B, nthreads * 4)
+
+    def run(rng):
+        st = np.zeros(1, np.uint32)
+        rc = lib.oracle_verify_det_margins(_ptr(X), _ptr(d), B, gamma, V, dt, _ptr(T), int(top_k),
+                                           float(top_p), int(seed), _ptr(tokens), _ptr(lens),
+                                           _ptr(margin), _ptr(margin_draw), _ptr(st), rng[0], rng[1])
+        if rc != 0:
+            raise RuntimeError(f"oracle_verify_det failed: {rc}")
+        return int(st[0])
+
+    if nthreads <= 1 or len(todo) <= 1:
+        statuses = [run(r) for r in todo]
+    else:
+        with ThreadPoolExecutor(nthreads) as ex:
+            statuses = list(ex.map(run, todo))
+    status = 0
+    for st_ in statuses:
+        status |= st_
     if split_margins:
         return tokens, lens, (margin, margin_draw), status
     return tokens, lens, np.minimum(margin, margin_draw), status

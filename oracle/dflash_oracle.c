@@ -418,6 +418,101 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
   return ORC_OK;
 }
 
+/* Verification of deterministic drafts: the drafter's distribution at
+ * position i is the point mass at d_i (q = delta_d), as for a greedy drafter
+ * (bml.asia, the speculative-decoding listing's drafter) or a path selector
+ * (rytg.cn, the lightweight-selector paragraph). The rule is the general one with that q: accept d_i when
+ * u < min(1, p_i(d_i) / 1), and at the first rejection draw from the
+ * normalised residual max(0, p_i - delta_{d_i}), which is p_i with d_i taken
+ * out; when every draft is accepted, the bonus token from p_gamma. No draft
+ * logits are read. */
+int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, int B, int gamma,
+                              int V, int dtype, const float* temperature, int top_k, float top_p,
+                              uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
+                              double* margin_accept, double* margin_draw, uint32_t* status,
+                              int b_begin, int b_end) {
+  if (!target || !draft_tokens || !temperature || !out_tokens || !out_accept_len || B < 0 ||
+      gamma < 1 || V < 1 || !(top_p > 0.0f))
+    return ORC_ERR_INVALID_ARG;
+  if (b_begin < 0) b_begin = 0;
+  if (b_end > B) b_end = B;
+  const size_t row_bytes = (size_t)V * elem_size(dtype);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* r = (double*)malloc(sizeof(double) * (size_t)V);
+  double* x = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!p || !r || !x) {
+    free(p);
+    free(r);
+    free(x);
+    return ORC_ERR_NOMEM;
+  }
+  uint32_t st = 0;
+  for (int b = b_begin; b < b_end; ++b) {
+    const char* Xb = (const char*)target + (size_t)b * (size_t)(gamma + 1) * row_bytes;
+    const int32_t* d = draft_tokens + (size_t)b * gamma;
+    int32_t* out = out_tokens + (size_t)b * (gamma + 1);
+    double mg = DBL_MAX, mgd = DBL_MAX;
+    if (!temperature_kind(temperature[b], &st)) {
+      greedy_request(Xb, d, gamma, V, dtype, out, out_accept_len + b, &st);
+      if (margin_accept) margin_accept[b] = mg;
+      if (margin_draw) margin_draw[b] = mgd;
+      continue;
+    }
+    const double T = (double)temperature[b];
+    for (int i = 0; i <= gamma; ++i) {
+      for (int j = 0; j < V; ++j) x[j] = logit_at(Xb + (size_t)i * row_bytes, dtype, (size_t)j);
+      if (row_is_bad(x, V)) st |= ORC_STATUS_BAD_ROW;
+    }
+    for (int i = 0; i < gamma; ++i)
+      if (d[i] < 0 || d[i] >= V) st |= ORC_STATUS_BAD_TOKEN;
+    for (int t = 0; t <= gamma; ++t) out[t] = -1;
+    int n = 0, rejected = 0;
+    int32_t last = -1;
+    for (int i = 0; i < gamma; ++i) {
+      if (filter_dense(Xb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, p, &mg) < 0) {
+        last = oracle_argmax_row(Xb + (size_t)i * row_bytes, V, dtype, NULL);
+        rejected = 1;
+        break;
+      }
+      const int32_t tok = d[i];
+      const double p_d = (tok >= 0 && tok < V) ? p[tok] : 0.0;
+      float u_acc, u_draw;
+      oracle_uniforms(seed, (uint32_t)b, (uint32_t)i, 0u, &u_acc, &u_draw);
+      update_margin(&mg, (double)u_acc, p_d);
+      if (u_acc < (float)p_d) { /* q(d) = 1: the ratio is p(d) */
+        out[n++] = tok;
+        continue;
+      }
+      double Zr = 0.0;
+      for (int j = 0; j < V; ++j) {
+        r[j] = j == tok ? 0.0 : p[j];
+        Zr += r[j];
+      }
+      last = draw_ascending(Zr > 0.0 ? r : p, V, u_draw, &mgd);
+      rejected = 1;
+      break;
+    }
+    if (!rejected) {
+      if (filter_dense(Xb + (size_t)gamma * row_bytes, V, dtype, T, top_k, top_p, p, &mg) < 0) {
+        last = oracle_argmax_row(Xb + (size_t)gamma * row_bytes, V, dtype, NULL);
+      } else {
+        float u_draw;
+        oracle_uniforms(seed, (uint32_t)b, (uint32_t)gamma, 0u, NULL, &u_draw);
+        last = draw_ascending(p, V, u_draw, &mgd);
+      }
+    }
+    out[n] = last;
+    out_accept_len[b] = n + 1;
+    if (margin_accept) margin_accept[b] = mg;
+    if (margin_draw) margin_draw[b] = mgd;
+  }
+  free(p);
+  free(r);
+  free(x);
+  if (status) *status |= st;
+  return ORC_OK;
+}
+
 int oracle_verify(const void* target, const void* draft, const int32_t* draft_tokens, int B,
                   int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
                   uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, double* margin,

@@ -94,6 +94,16 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
                           int32_t* out_accept_len, double* margin_accept, double* margin_draw,
                           uint32_t* status, int b_begin, int b_end);
 
+/* Verification of deterministic drafts (q = the point mass at d_i): accept
+ * d_i when u < p_i(d_i); at the first rejection draw from p_i with d_i taken
+ * out; otherwise the bonus token from p_gamma. No draft logits. Arguments and
+ * outputs as oracle_verify_margins without `draft`. */
+int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, int B, int gamma,
+                              int V, int dtype, const float* temperature, int top_k, float top_p,
+                              uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
+                              double* margin_accept, double* margin_draw, uint32_t* status,
+                              int b_begin, int b_end);
+
 /* Greedy verification: argmax prefix match, requests [b_begin, b_end). */
 int oracle_verify_greedy(const void* target, const int32_t* draft_tokens, int B, int gamma, int V,
                          int dtype, int32_t* out_tokens, int32_t* out_accept_len,
