@@ -488,7 +488,9 @@ int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, i
         r[j] = j == tok ? 0.0 : p[j];
         Zr += r[j];
       }
-      last = draw_ascending(Zr > 0.0 ? r : p, V, u_draw, &mgd);
+      /* after a rejection p(d) < 1, so Zr = 1 - p(d) > 0; p is only a guard */
+      const double* w = Zr > 0.0 ? r : p;
+      last = draw_ascending(w, V, u_draw, &mgd);
       rejected = 1;
       break;
     }

@@ -14,6 +14,7 @@ import pytest
 import oracle
 import test_oracle_filter as F
 import test_oracle_philox as P
+import test_oracle_det as DD
 import test_oracle_verify as VV
 
 MUTATIONS = {
@@ -38,6 +39,11 @@ MUTATIONS = {
                      "*u_accept = (float)((double)(w[0] >> 9) / 16777216.0);"),
     "greedy_wrong_position": ("while (n < gamma && d[n] == argmax[n]) {",
                               "while (n < gamma && d[n] == argmax[n > 0 ? n - 1 : 0]) {"),
+    "det_residual_keeps_draft": ("r[j] = j == tok ? 0.0 : p[j];", "r[j] = p[j];"),
+    "det_accept_uses_draw_uniform": (
+        "oracle_uniforms(seed, (uint32_t)b, (uint32_t)i, 0u, &u_acc, &u_draw);\n      update_margin(&mg, (double)u_acc, p_d);",
+        "oracle_uniforms(seed, (uint32_t)b, (uint32_t)i, 0u, &u_draw, &u_acc);\n      update_margin(&mg, (double)u_acc, p_d);"),
+    "det_accept_slack": ("if (u_acc < (float)p_d) {", "if (u_acc < (float)p_d + 0.02f) {"),
 }
 
 
@@ -54,6 +60,8 @@ def _pin_checks(curand_pin):
         ("law_closed_form", lambda: VV.test_sampling_law_closed_form(*VV.LAW_CASES[1])),
         ("identical_draft", VV.test_identical_draft_is_always_accepted),
         ("uniforms_uniform", P.test_uniforms_are_uniform_and_independent),
+        ("det_point_mass", lambda: DD.test_det_equals_general_rule_with_point_mass_drafts(20, 0.95)),
+        ("det_law", lambda: DD.test_det_accept_length_and_token_laws(*DD.DET_LAW_CASES[3])),
     ]
 
 
