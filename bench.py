@@ -10,12 +10,14 @@ block. Inputs rotate over 3 independently generated sets (each about 238 MB,
 together well above the 129 MB L2), so no step finds its logits in L2.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-                  [--workload NAME]
+                  [--workload NAME] [--drafts sampled|det]
 
 ``--workload`` measures another of the step's workloads the same way (for
 example b128_g15_fullvocab_f32: block 16, fp32, top-k off and top-p 1, where a
 call is the stream plus the full-vocabulary draw's second pass); the default
-is the headline above.
+is the headline above. ``--drafts det`` verifies deterministic drafts (each
+draft row's argmax, as a greedy drafter proposes them) through
+dflash_verify_det, which reads no draft logits.
 
 N > 1 runs under torch.distributed.run: every rank verifies its own batch (the
 step shards by request, no data exchange), timing is the max over ranks.
@@ -44,12 +46,15 @@ WORKLOAD = "b32_mixed_v248320"
 METRIC = "verified draft-positions/sec and achieved HBM GB/s (B=32, block 8, V=248320)"
 
 
-def metric_for(workload: str) -> str:
-    if workload == WORKLOAD:
+def metric_for(workload: str, det: bool = False) -> str:
+    if workload == WORKLOAD and not det:
         return METRIC
     w = synth.WORKLOADS[workload]
     return (f"verified draft-positions/sec and achieved HBM GB/s (B={w['B']}, block {w['gamma'] + 1}, "
-            f"V={w['V']})")
+            f"V={w['V']}" + (", deterministic drafts)" if det else ")"))
+
+
+DET_DRAFTS = "deterministic: the argmax of each draft row (q = the point mass at the draft)"
 UNIT = "verified draft positions/s"
 N_SETS = 3
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_sweep_b32_mixed_v248320.md")
@@ -148,31 +153,36 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
-def algorithmic_bytes(inp, accept_len=None) -> int:
+def algorithmic_bytes(inp, accept_len=None, det=False) -> int:
     """Logit bytes one step must read: every target row, and the draft rows of
-    requests that sample (greedy requests never read their draft rows). Over
-    the full vocabulary (top-k off, top-p 1) the residual or bonus draw reads
-    its rows once more: two rows after a rejection, one for a bonus token
-    (from the step's accept lengths)."""
+    requests that sample (greedy requests never read their draft rows, nor
+    does the verification of deterministic drafts). Over the full vocabulary
+    (top-k off, top-p 1) the residual or bonus draw reads its rows once more:
+    two rows after a rejection, one for a bonus token (from the step's accept
+    lengths)."""
     B, gamma, V = inp.shape
     es = 2 if inp.target.dtype == np.uint16 else 4
     samp = inp.temperature > 0
-    rows = B * (gamma + 1) + int(np.sum(samp)) * gamma
+    rows = B * (gamma + 1) + (0 if det else int(np.sum(samp)) * gamma)
     if inp.top_k <= 0 and inp.top_p >= 1.0 and accept_len is not None:
         lens = np.asarray(accept_len)[samp]
         rows += int(np.sum(np.where(lens <= gamma, 2, 1)))
     return rows * V * es
 
 
-def cpu_baseline(inp, d, workload, threads=None):
+def cpu_baseline(inp, d, workload, threads=None, det=False):
     """The oracle (as it stands) on the host cores: one full batch."""
     import oracle
 
     B, gamma, V = inp.shape
     threads = threads or oracle.default_threads()
     t0 = time.perf_counter()
-    oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, inp.seed,
-                  threads=threads)
+    if det:
+        oracle.verify_det(inp.target, d, inp.temperature, inp.top_k, inp.top_p, inp.seed,
+                          threads=threads)
+    else:
+        oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, inp.seed,
+                      threads=threads)
     dt = time.perf_counter() - t0
     return {"value": B * gamma / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"one {workload} batch of {B} requests (fp64 C oracle, {threads} host "
@@ -207,35 +217,46 @@ def run_reference(args):
 
     inp = synth.make_workload(args.workload, data_seed=0, seed=0)
     B, gamma, V = inp.shape
-    d, _, _ = oracle.sample_rows(inp.draft.reshape(B * gamma, V),
-                                 synth.draft_sampling_temperatures(inp.temperature, gamma),
-                                 inp.top_k, inp.top_p, 1000)
-    d = d.reshape(B, gamma)
+    det = args.drafts == "det"
+    if det:
+        d = np.argmax(synth.to_float(inp.draft), axis=-1).astype(np.int32)
+    else:
+        d, _, _ = oracle.sample_rows(inp.draft.reshape(B * gamma, V),
+                                     synth.draft_sampling_temperatures(inp.temperature, gamma),
+                                     inp.top_k, inp.top_p, 1000)
+        d = d.reshape(B, gamma)
     threads = oracle.default_threads()
+
+    def verify(seed, order):
+        if det:
+            Xs = np.ascontiguousarray(inp.target[order])
+            return oracle.verify_det(Xs, d[order], inp.temperature[order], inp.top_k, inp.top_p,
+                                     seed, threads=threads)
+        return oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, seed,
+                             threads=threads, requests=order)
+
     # size each step so that warmup + steps stay within about two minutes
     t0 = time.perf_counter()
-    oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, 0,
-                  threads=threads, requests=[1])
+    verify(0, [1])
     per_req = max(1e-3, time.perf_counter() - t0)
     budget = 120.0 / max(1, args.steps + args.warmup)
     n_req = int(max(1, min(B, budget / per_req)))
     order = [b % B for b in range(1, 1 + n_req)]  # starts with a sampling request
     for _ in range(args.warmup):
-        oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, 0,
-                      threads=threads, requests=order)
+        verify(0, order)
     t0 = time.perf_counter()
     for s in range(args.steps):
-        oracle.verify(inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, s,
-                      threads=threads, requests=order)
+        verify(s, order)
     dt = time.perf_counter() - t0
     value = args.steps * n_req * gamma / dt
     sample = f"{n_req} of the {B} requests per step (fp64 C oracle, {threads} host threads)"
     line = {
-        "impl": "reference", "metric": metric_for(args.workload), "value": value, "unit": UNIT, "n_gpus": world,
+        "impl": "reference", "metric": metric_for(args.workload, det), "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": args.workload, "B": B, "gamma": gamma, "V": V,
-                                        "top_k": inp.top_k, "top_p": inp.top_p},
+                                        "top_k": inp.top_k, "top_p": inp.top_p,
+                                        "drafts": DET_DRAFTS if det else "sampled from q"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -280,6 +301,15 @@ def run_gpu(args):
                            workspace=rows_ws).view(B, gamma).contiguous()
         sets_dev.append((X, Y, d, T))
     torch.cuda.synchronize()
+    det = args.drafts == "det"
+    if det:
+        # a greedy drafter's proposals: each draft row's argmax (the sampler at T = 0)
+        zeros = torch.zeros(B * gamma, dtype=torch.float32, device=dev)
+        for s, (X, Y, d, T) in enumerate(sets_dev):
+            d_det = dv.sample_rows(Y.view(B * gamma, V), zeros, sets_np[s].top_k, sets_np[s].top_p, 0,
+                                   workspace=rows_ws).view(B, gamma).contiguous()
+            sets_dev[s] = (X, Y, d_det, T)
+        torch.cuda.synchronize()
     top_k, top_p = sets_np[0].top_k, sets_np[0].top_p
     ws = dv.Workspace(dv.workspace_bytes(B, gamma, V, dt_code, top_k, top_p), dev)
     out_tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
@@ -289,10 +319,11 @@ def run_gpu(args):
     sp = stream.cuda_stream
     calls = []
     for s, (X, Y, d, T) in enumerate(sets_dev):
-        calls.append((X.data_ptr(), Y.data_ptr(), d.data_ptr(), B, gamma, V, dt_code, T.data_ptr(),
-                      top_k, top_p, s + 1, out_tok.data_ptr(), out_len.data_ptr(), ws.ptr, ws.nbytes,
-                      status.data_ptr(), sp))
-    fn = lib.dflash_verify
+        logits = (X.data_ptr(),) if det else (X.data_ptr(), Y.data_ptr())
+        calls.append(logits + (d.data_ptr(), B, gamma, V, dt_code, T.data_ptr(),
+                               top_k, top_p, s + 1, out_tok.data_ptr(), out_len.data_ptr(), ws.ptr,
+                               ws.nbytes, status.data_ptr(), sp))
+    fn = lib.dflash_verify_det if det else lib.dflash_verify
 
     def step(i):
         rc = fn(*calls[i % N_SETS])
@@ -328,12 +359,12 @@ def run_gpu(args):
     launch_ms = np.array([a.elapsed_time(b) for a, b in evs])
 
     # ---- roofline of the kernel (one launch = one step)
-    alg = algorithmic_bytes(sets_np[(args.steps - 1) % N_SETS], out_len.cpu().numpy())
+    alg = algorithmic_bytes(sets_np[(args.steps - 1) % N_SETS], out_len.cpu().numpy(), det)
     avg_launch_s = float(launch_ms.mean()) / 1e3
     achieved = alg / avg_launch_s / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    traffic = profiled_traffic() if args.workload == WORKLOAD else None
+    traffic = profiled_traffic() if args.workload == WORKLOAD and not det else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
@@ -356,15 +387,34 @@ def run_gpu(args):
     staging = torch.empty(dv.host_staging_bytes(B, gamma, V, dt_code), dtype=torch.uint8,
                           device=dev)
     n_e2e = max(3, min(50, args.steps))
+    if det:
+        # through the Python binding: pinned inputs copied in, dflash_verify_det,
+        # tokens and lengths copied back, on the bench stream
+        eX = torch.empty_like(sets_dev[0][0])
+        ed = torch.empty_like(sets_dev[0][2])
+        eT = torch.empty_like(sets_dev[0][3])
+
+        def e2e_step(i):
+            eX.copy_(hX, non_blocking=True)
+            ed.copy_(hd, non_blocking=True)
+            eT.copy_(hT, non_blocking=True)
+            t_, l_ = dv.verify_det(eX, ed, eT, top_k, top_p, i, out_tokens=out_tok, out_accept_len=out_len,
+                                   workspace=ws, stream=stream)
+            h_tok.copy_(t_, non_blocking=True)
+            h_len.copy_(l_, non_blocking=True)
+            stream.synchronize()
+    else:
+        def e2e_step(i):
+            dv.verify_host(hX, hY, hd, hT, top_k, top_p, i, h_tok, h_len, h_st, staging, ws)
     for i in range(2):
-        dv.verify_host(hX, hY, hd, hT, top_k, top_p, i, h_tok, h_len, h_st, staging, ws)
+        e2e_step(i)
     t0 = time.perf_counter()
     for i in range(n_e2e):
-        dv.verify_host(hX, hY, hd, hT, top_k, top_p, i, h_tok, h_len, h_st, staging, ws)
+        e2e_step(i)
     e2e_s = (time.perf_counter() - t0) / n_e2e
-    n_samp = int(np.sum(inp.temperature > 0))
+    n_samp = 0 if det else int(np.sum(inp.temperature > 0))
     h2d = (B * (gamma + 1) + n_samp * gamma) * V * es + B * gamma * 4 + B * 4
-    d2h = B * (gamma + 1) * 4 + B * 4 + 4
+    d2h = B * (gamma + 1) * 4 + B * 4 + (0 if det else 4)
     job = combine_over_ranks(region_ms, e2e_s, args.steps, B * gamma, dev)
     ms_per_step, value = job["ms_per_step"], job["value"]
     e2e = {"value": job["e2e_value"], "unit": UNIT,
@@ -377,18 +427,20 @@ def run_gpu(args):
             torch.distributed.destroy_process_group()
         return 0
     lens = out_len.cpu().numpy()
-    cpu = cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy(), args.workload) if world == 1 else None
+    cpu = (cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy(), args.workload, det=det)
+           if world == 1 else None)
     T0 = sets_np[0].temperature
     temps = ("cycling " + " / ".join(f"{t:g}" + (" (greedy)" if t == 0 else "")
                                      for t in dict.fromkeys(T0.tolist()))
              if len(set(T0.tolist())) > 1 else f"{T0[0]:g} for every request")
     line = {
-        "metric": metric_for(args.workload), "value": value, "unit": UNIT, "n_gpus": world,
+        "metric": metric_for(args.workload, det), "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if bf16 else "f32", "data": "synthetic",
         "config": {"workload": args.workload, "B": B, "gamma": gamma, "V": V, "top_k": top_k,
                    "top_p": top_p, "temperatures": temps,
+                   "drafts": DET_DRAFTS if det else "sampled from q by the library's sampler",
                    "l2": f"inputs rotate over {N_SETS} sets of "
                          f"{(sets_np[0].target.nbytes + sets_np[0].draft.nbytes) / 1e6:.0f} MB "
                          "(larger than L2 together)",
@@ -414,6 +466,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--drafts", default="sampled", choices=["sampled", "det"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -148,6 +148,27 @@ int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
                          int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
                          uint32_t* status, void* stream);
 
+/* Verification of deterministic drafts: the drafter proposes d_i with
+ * certainty, as a greedy drafter does ("DFlash2 用投机解码给 Qwen 提速",
+ * bml.asia: the drafter of the speculative-decoding listing) or a path
+ * selector does (rytg.cn, section "轻量选择器": one coherent path picked
+ * from the top-16 candidates per position). Its distribution is then the
+ * point mass q_i = delta_{d_i}, and the standard rule with that q reads:
+ * accept d_i when u < p_i(d_i) (fp32); at the first rejection draw from p_i
+ * with d_i taken out (max(0, p_i - delta_{d_i}), renormalised); when every
+ * draft is accepted draw the bonus token from p_gamma. The output follows the
+ * target distribution whatever the drafts are. No draft logits are read, so
+ * a sampling request reads gamma + 1 rows instead of 2 gamma + 1.
+ * Arguments, uniforms, draws, greedy requests (T == 0), outputs and status
+ * bits as for dflash_verify without draft_logits; workspace_bytes >=
+ * dflash_workspace_bytes(...) of the same shape and filter. Top-k must be on
+ * (1 <= top_k <= DFLASH_MAX_TOP_K, top_k < V): the full-vocabulary filter
+ * returns DFLASH_ERR_UNSUPPORTED here. */
+int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, int B, int gamma,
+                      int V, int dtype, const float* temperature, int top_k, float top_p,
+                      uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
+                      void* workspace, size_t workspace_bytes, uint32_t* status, void* stream);
+
 /* dflash_verify with [host] inputs and outputs: copies the logits (the draft
  * rows of sampling requests only), drafts and temperatures into the caller's
  * [device] staging buffer, verifies, copies tokens, accept lengths and the

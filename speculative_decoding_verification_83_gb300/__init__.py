@@ -96,6 +96,7 @@ EXPORTS = {
     "dflash_rows_workspace_bytes": ("z", "iiiif"),
     "dflash_workspace_init": ("i", "pzp"),
     "dflash_verify": ("i", "pppiiiipifQppp" "zpp"),
+    "dflash_verify_det": ("i", "ppiiiipifQpppzpp"),
     "dflash_verify_greedy": ("i", "ppiiiipppzpp"),
     "dflash_host_staging_bytes": ("z", "iiii"),
     "dflash_verify_host": ("i", "pppiiiipifQppppzpzp"),
@@ -234,6 +235,30 @@ def verify(target, draft, draft_tokens, temperature, top_k: int, top_p: float, s
     return out_tokens, out_accept_len
 
 
+def verify_det(target, draft_tokens, temperature, top_k: int, top_p: float, seed: int,
+               out_tokens=None, out_accept_len=None, status=None, workspace=None, stream=None):
+    """dflash_verify_det (deterministic drafts, no draft logits) on torch CUDA
+    tensors. Returns (out_tokens, out_accept_len)."""
+    torch = _torch()
+    B, g1, V = target.shape
+    gamma = g1 - 1
+    dt = _dtype_code(target)
+    dev = target.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = _workspace_for(workspace_bytes(B, gamma, V, dt, top_k, top_p), dev, workspace)
+    rc = load().dflash_verify_det(
+        _dev(target, "target"), _dev(draft_tokens, "draft_tokens", torch.int32), B, gamma, V, dt,
+        _dev(temperature, "temperature", torch.float32), int(top_k), float(top_p),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(out_accept_len, "out_accept_len", torch.int32), ws.ptr, ws.nbytes,
+        None if status is None else _dev(status, "status", torch.int32), _stream_ptr(stream, dev))
+    _check(rc)
+    return out_tokens, out_accept_len
+
+
 def verify_greedy(target, draft_tokens, out_tokens=None, out_accept_len=None, status=None,
                   workspace=None, stream=None):
     torch = _torch()
@@ -334,7 +359,7 @@ def verify_host(target, draft, draft_tokens, temperature, top_k, top_p, seed, ou
 
 
 __all__ = [
-    "build", "load", "verify", "verify_greedy", "filter_rows", "sample_rows", "uniforms",
+    "build", "load", "verify", "verify_det", "verify_greedy", "filter_rows", "sample_rows", "uniforms",
     "verify_host", "Workspace", "workspace_bytes", "rows_workspace_bytes", "host_staging_bytes",
     "DFlashError", "LIB_PATH", "EXPORTS",
 ]

@@ -244,6 +244,44 @@ int dflash_verify(const void* target_logits, const void* draft_logits, const int
   return run_fullvocab_draw(p, workspace, stream);
 }
 
+int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
+                      int dtype, const float* temperature, int top_k, float top_p, uint64_t seed,
+                      int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                      uint32_t* status, void* stream) {
+  int rc = check_shape(B, gamma, V, dtype);
+  if (rc) return rc;
+  if (!target_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len || !workspace)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
+  if (mode != kModeTopK)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "top_k=%d with top_p=%g is not supported for deterministic drafts (need 1 <= top_k <= %d "
+                "and top_k < V)",
+                top_k, (double)top_p, DFLASH_MAX_TOP_K);
+  if ((rc = check_aligned(target_logits, esize_of(dtype), "target_logits"))) return rc;
+  const size_t need = verify_workspace(B, gamma, V, dtype);
+  if (workspace_bytes < need)
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, need);
+  Params p = base_params(dtype, V);
+  p.target = static_cast<const unsigned char*>(target_logits);
+  p.draft_tokens = draft_tokens;
+  p.temperature = temperature;
+  p.B = B;
+  p.gamma = gamma;
+  p.top_k = top_k;
+  p.top_p = top_p >= 1.0f ? 1.0f : top_p;
+  p.seed = seed;
+  p.task = kTaskVerify;
+  p.det = 1;
+  p.out_tokens = out_tokens;
+  p.out_len = out_accept_len;
+  p.status = status;
+  bind_workspace(p, workspace, B * (gamma + 1), B);
+  return run(p, B * (gamma + 1), stream);
+}
+
 int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
                          int dtype, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                          size_t workspace_bytes, uint32_t* status, void* stream) {

@@ -106,7 +106,7 @@ inline int fv_slices(int V) { return (V + kFvSlice - 1) / kFvSlice; }
 struct Params {
   // inputs
   const unsigned char* target;  // verify: [B, gamma+1, V]; rows tasks: [R, V]
-  const unsigned char* draft;   // verify: [B, gamma, V]
+  const unsigned char* draft;   // verify: [B, gamma, V]; unused with deterministic drafts
   const int32_t* draft_tokens;  // [B, gamma]
   const float* temperature;     // [B] or [R]
   int B;                        // requests (verify) or rows (rows tasks)
@@ -117,6 +117,7 @@ struct Params {
   unsigned long long seed;
   int task;
   int fullvocab;                // top-k off and top-p 1: softmax over the whole vocabulary
+  int det;                      // verify: deterministic drafts (q = point mass at the draft; no draft rows)
   int row_base;                 // rows tasks: index of this launch's first row
   Geometry geo;
   // outputs

@@ -140,8 +140,9 @@ __device__ __forceinline__ float load_logit(const unsigned char* row, int j, int
 // ---- work enumeration -----------------------------------------------------------
 // Verification: requests are ordered sampling-first (by index), then greedy.
 // A sampling request owns 2*gamma+1 slots (target 0, draft 0, target 1, ...,
-// target gamma); a greedy one owns gamma+1 (its target rows). Rows tasks: slot
-// = row.
+// target gamma), or with deterministic drafts gamma+1 (its target rows: the
+// drafter's distribution is a point mass, so no draft row is read); a greedy
+// one owns gamma+1 (its target rows). Rows tasks: slot = row.
 struct SlotInfo {
   int ord;        // request ordinal (verify) or row (rows tasks)
   int r;          // row within the request
@@ -150,25 +151,32 @@ struct SlotInfo {
   int k_eff;
 };
 
+// slots of a sampling request
+__device__ __forceinline__ int samp_slots(const Params& p) { return p.det ? p.gamma + 1 : 2 * p.gamma + 1; }
+// position of row r of a sampling request (target row i, or draft row i)
+__device__ __forceinline__ int samp_position(const Params& p, int r) { return p.det ? r : r >> 1; }
+// row of a sampling request holding position i's target logits
+__device__ __forceinline__ int samp_target_row(const Params& p, int i) { return p.det ? i : 2 * i; }
+
 __device__ __forceinline__ SlotInfo slot_info(const Params& p, const Smem& S, int slot) {
   SlotInfo s;
   const size_t row_bytes = (size_t)p.geo.V * p.geo.esize;
   if (p.task == kTaskVerify || p.task == kTaskVerifyGreedy) {
-    const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
-    const int samp_slots = S.n_samp * per_s;
-    if (slot < samp_slots) {
+    const int per_s = samp_slots(p), per_g = p.gamma + 1;
+    const int samp_end = S.n_samp * per_s;
+    if (slot < samp_end) {
       s.ord = slot / per_s;
       s.r = slot - s.ord * per_s;
       s.sampling = true;
       const int b = S.req_of_ord[s.ord];
-      const int i = s.r >> 1;
-      if ((s.r & 1) == 0)
+      const int i = samp_position(p, s.r);
+      if (p.det || (s.r & 1) == 0)
         s.ptr = p.target + ((size_t)b * (p.gamma + 1) + i) * row_bytes;
       else
         s.ptr = p.draft + ((size_t)b * p.gamma + i) * row_bytes;
       s.k_eff = p.top_k;
     } else {
-      const int s2 = slot - samp_slots;
+      const int s2 = slot - samp_end;
       const int g = s2 / per_g;
       s.ord = S.n_samp + g;
       s.r = s2 - g * per_g;
@@ -189,7 +197,7 @@ __device__ __forceinline__ SlotInfo slot_info(const Params& p, const Smem& S, in
 
 __device__ __forceinline__ int active_slots(const Params& p, const Smem& S) {
   if (p.task == kTaskVerify || p.task == kTaskVerifyGreedy)
-    return S.n_samp * (2 * p.gamma + 1) + (p.B - S.n_samp) * (p.gamma + 1);
+    return S.n_samp * samp_slots(p) + (p.B - S.n_samp) * (p.gamma + 1);
   return p.B;
 }
 
@@ -532,9 +540,11 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   // end of the final would add a full round trip to it
   T_row = ld_nc_now(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
   // a verification row's position's draft token (target row 2i and draft row
-  // 2i + 1 of a request are position i's; the bonus row has none)
-  const int32_t d_row = (p.task == kTaskVerify && si.r < 2 * p.gamma)
-                            ? ld_nc_now(p.draft_tokens + (size_t)S.req_of_ord[si.ord] * p.gamma + (si.r >> 1))
+  // 2i + 1 of a request, or target row i with deterministic drafts, are
+  // position i's; the bonus row has none)
+  const int pos = samp_position(p, si.r);
+  const int32_t d_row = (p.task == kTaskVerify && pos < p.gamma)
+                            ? ld_nc_now(p.draft_tokens + (size_t)S.req_of_ord[si.ord] * p.gamma + pos)
                             : -1;
   const RowBody rb = row_body(si.ptr, V, p.geo.esize);
   const int n_tiles = p.geo.tiles;
@@ -823,14 +833,15 @@ static_assert(2 * kMaxTopK == 64, "token_slot hashes into 64 slots");
 // The rows arrive filtered (kept tokens and probabilities). One lane per draft
 // position runs the accept test u < p(d)/q(d); the first failing position (or
 // gamma when none fails) is where the residual max(0, p - q) (or the bonus
-// distribution p) is drawn from.
+// distribution p) is drawn from. With deterministic drafts q is the point
+// mass at d: the test is u < p(d) and the residual is p with d taken out.
 __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
   const int gamma = p.gamma, V = p.geo.V;
   const int b = S.req_of_ord[ord];
   int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
   const int32_t* d = p.draft_tokens + (size_t)b * gamma;
-  const int per_s = 2 * gamma + 1;
+  const int per_s = samp_slots(p);
   const int slot0 = ord * per_s;
   // The rows' filtered lists are ready when every word is written (no
   // written word is zero): the polls are the final's own loads.
@@ -871,7 +882,8 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
       const int32_t di = d_lane;
       if (di < 0 || di >= V) st |= kStatusBadToken;
       // p(d) and q(d), found by the rows' finals (0 when the token is not kept)
-      const float p_d = S.u.lists.prob[2 * lane][32], q_d = S.u.lists.prob[2 * lane + 1][32];
+      const float p_d = S.u.lists.prob[samp_target_row(p, lane)][32];
+      const float q_d = p.det ? 1.0f : S.u.lists.prob[2 * lane + 1][32];
       const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
       reject = !(uniform24(wd.x) < ratio);
     }
@@ -879,11 +891,16 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
     const int n = rej ? __ffs(rej) - 1 : gamma;  // drafts accepted
     uint32_t u_draw = __shfl_sync(0xffffffffu, wd.y, n & 31);
     if (n >= 32) u_draw = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)n, 0u).y;  // gamma = 32, all kept
-    const int row = 2 * n;  // target row of position n (the bonus row when n == gamma)
+    const int row = samp_target_row(p, n);  // target row of position n (the bonus row when n == gamma)
     const int32_t ti = S.u.lists.idx[row][lane];
     const float pi = S.u.lists.prob[row][lane];
     float wt = pi;
-    if (n < gamma) {
+    if (n < gamma && p.det) {
+      // residual p - delta_d: the target's kept tokens other than the draft
+      const int32_t dn = __shfl_sync(0xffffffffu, d_lane, n);
+      const float r = (ti >= 0 && ti != dn) ? pi : 0.0f;
+      if (__ballot_sync(0xffffffffu, r > 0.0f) != 0u) wt = r;
+    } else if (n < gamma) {
       // residual max(0, p - q) over the target's kept tokens: q from the
       // draft row's list through a 64-slot open-addressing table (S.cand as
       // scratch: keys, then values)
@@ -1279,7 +1296,7 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
 // their tile keys instead.
 __device__ __forceinline__ bool counted_slot(const Params& p, const Smem& S, int slot) {
   if (p.task != kTaskVerify && p.task != kTaskVerifyGreedy) return false;
-  return slot >= S.n_samp * (2 * p.gamma + 1) || p.fullvocab != 0;
+  return slot >= S.n_samp * samp_slots(p) || p.fullvocab != 0;
 }
 
 // Publisher (one thread): takes the pieces the consumers finished in batches,
@@ -1349,7 +1366,7 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   const int lane = fin_tid() & 31;
   const int gamma = p.gamma, V = p.geo.V;
   const int b = S.req_of_ord[ord];
-  const int slot0 = S.n_samp * (2 * gamma + 1) + (ord - S.n_samp) * (gamma + 1);
+  const int slot0 = S.n_samp * samp_slots(p) + (ord - S.n_samp) * (gamma + 1);
   int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
   const int32_t* d = p.draft_tokens + (size_t)b * gamma;
   const size_t row_bytes = (size_t)V * p.geo.esize;
@@ -1508,7 +1525,7 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
 template <int DT>
 __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord, uint32_t& next) {
   const int gt = fin_tid(), w = gt >> 5;
-  const int per_s = 2 * p.gamma + 1, per_g = p.gamma + 1;
+  const int per_s = samp_slots(p), per_g = p.gamma + 1;
   // A row job's row final, and a top-k sampling request's final, wait on the
   // words they read (tile keys, filtered lists). A full-vocabulary or greedy
   // request's final waits for its rows' pieces to be counted.
@@ -1555,7 +1572,7 @@ __device__ void finals(const Params& p, Smem& S) {
   const bool fv = verify && p.fullvocab;
   // row jobs: top-k sampling rows, or every row of a rows task; then request
   // jobs from request ordinal ord0 on
-  const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * (2 * p.gamma + 1) : p.B);
+  const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * samp_slots(p) : p.B);
   const int ord0 = 0;  // every request has a final job (sampling first, then greedy)
   const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
   if (gt == kFinDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);

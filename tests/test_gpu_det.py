@@ -1,0 +1,193 @@
+"""GPU parity of the verification of deterministic drafts (q = point mass at d).
+
+The CUDA path (dflash_verify_det through the C ABI) against the oracle's
+verify_det, with the bars of the general verification: greedy requests and
+status words bit-exact, sampled tokens and accept lengths equal on every
+request whose oracle decision margin is at least 1e-4. Drafts come from a
+greedy drafter (the argmax of each draft row, as the drafter of the
+speculative-decoding listing on bml.asia does), mixed with uniform tokens that
+often fall outside the kept set.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+MARGIN = 1e-4
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def dv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import speculative_decoding_verification_83_gb300 as m
+
+    m.build()
+    m.load()
+    return m
+
+
+def _t(a):
+    return synth.to_torch(a, DEV)
+
+
+def _greedy_drafts(inp, mix_seed=None, frac_random=0.25):
+    d = np.argmax(synth.to_float(inp.draft), axis=-1).astype(np.int32)
+    if mix_seed is not None:
+        rng = np.random.default_rng(mix_seed)
+        V = inp.shape[2]
+        d = np.where(rng.random(d.shape) < frac_random, rng.integers(0, V, d.shape), d).astype(np.int32)
+    return d
+
+
+def _run_det(dv, X, d, T, top_k, top_p, seed, workspace=None):
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    tok, ln = dv.verify_det(_t(X), torch.from_numpy(np.ascontiguousarray(d)).to(DEV),
+                            torch.from_numpy(np.ascontiguousarray(T, np.float32)).to(DEV), top_k,
+                            top_p, seed, status=st, workspace=workspace)
+    torch.cuda.synchronize()
+    return tok.cpu().numpy(), ln.cpu().numpy(), int(st.item())
+
+
+def _compare(tok, ln, want_tok, want_len, margin):
+    same = np.all(tok == want_tok, axis=1) & (ln == want_len)
+    bad = np.nonzero(~same)[0]
+    for b in bad:
+        assert margin[b] < MARGIN, (
+            f"request {b}: gpu {tok[b].tolist()} len {ln[b]} vs oracle {want_tok[b].tolist()} "
+            f"len {want_len[b]}, margin {margin[b]:.3g}")
+    return len(bad)
+
+
+@pytest.mark.parametrize("V", [1024, 777, 20000])
+def test_det_small_many_seeds(dv, V):
+    n_bad = total = 0
+    for data_seed in range(5):
+        inp = synth.make_workload("tiny_v1024", data_seed=data_seed, B=9, V=V)
+        T = np.array([1.0, 0.0, 0.6, 1.0, 1.5, 0.0, 0.8, 1.0, 2.0], np.float32)
+        d = _greedy_drafts(inp, mix_seed=data_seed)
+        for seed in (data_seed, 1000 + data_seed):
+            want_tok, want_len, margin, want_st = oracle.verify_det(inp.target, d, T, inp.top_k,
+                                                                    inp.top_p, seed)
+            tok, ln, st = _run_det(dv, inp.target, d, T, inp.top_k, inp.top_p, seed)
+            assert st == want_st
+            n_bad += _compare(tok, ln, want_tok, want_len, margin)
+            total += len(ln)
+    assert n_bad <= max(1, total // 1000)
+
+
+@pytest.mark.parametrize("gamma", [1, 2, 15, 32])
+def test_det_gamma_range(dv, gamma):
+    inp = synth.make_workload("b8_v248320", data_seed=gamma, B=4, V=4099, gamma=gamma)
+    T = np.array([1.0, 0.0, 0.7, 1.0], np.float32)
+    d = _greedy_drafts(inp, mix_seed=gamma, frac_random=0.1)
+    want_tok, want_len, margin, _ = oracle.verify_det(inp.target, d, T, inp.top_k, inp.top_p, 3)
+    tok, ln, _ = _run_det(dv, inp.target, d, T, inp.top_k, inp.top_p, 3)
+    _compare(tok, ln, want_tok, want_len, margin)
+
+
+@pytest.mark.parametrize("filt", [(20, 0.95), (5, 0.9), (1, 1.0), (32, 1.0)])
+def test_det_filters(dv, filt):
+    top_k, top_p = filt
+    inp = synth.make_workload("tiny_v1024", data_seed=11, B=12, V=5003)
+    T = synth.cycle_temperatures(12)
+    d = _greedy_drafts(inp, mix_seed=4)
+    for seed in (1, 2):
+        want_tok, want_len, margin, want_st = oracle.verify_det(inp.target, d, T, top_k, top_p, seed)
+        tok, ln, st = _run_det(dv, inp.target, d, T, top_k, top_p, seed)
+        assert st == want_st
+        _compare(tok, ln, want_tok, want_len, margin)
+
+
+def test_det_full_size_b32_mixed(dv):
+    """The B=32 mixed bf16 workload (block 8, V=248320) with greedy-drafter
+    drafts, every request against the oracle."""
+    inp = synth.make_workload("b32_mixed_v248320", data_seed=0, seed=0)
+    d = _greedy_drafts(inp, mix_seed=1, frac_random=0.1)
+    want_tok, want_len, margin, want_st = oracle.verify_det(inp.target, d, inp.temperature,
+                                                            inp.top_k, inp.top_p, inp.seed)
+    tok, ln, st = _run_det(dv, inp.target, d, inp.temperature, inp.top_k, inp.top_p, inp.seed)
+    assert st == want_st == 0
+    n_bad = _compare(tok, ln, want_tok, want_len, margin)
+    assert n_bad <= 1
+    g = inp.temperature == 0
+    assert np.array_equal(tok[g], want_tok[g]) and np.array_equal(ln[g], want_len[g])
+    # the drafts were accepted at some positions and rejected at others
+    assert 1 < ln[~g].mean() < inp.shape[1] + 1
+
+
+def test_det_equals_general_path_on_point_mass_drafts(dv):
+    """On the GPU, the general verification fed draft logits whose filtered
+    distribution is exactly the point mass at d (d at 0, the rest at -1e4)
+    takes the same decisions as the deterministic-draft path, bit for bit:
+    q(d) = 1, so p/q = p(d), and max(0, p - q) is p without d."""
+    B, gamma, V = 16, 7, 30011
+    X, _, _ = synth.make_logits(B, gamma, V, "f32", data_seed=21)
+    rng = np.random.default_rng(8)
+    am = np.argmax(X[:, :gamma], axis=-1)
+    d = np.where(rng.random((B, gamma)) < 0.6, am, rng.integers(0, V, (B, gamma))).astype(np.int32)
+    Y = np.full((B, gamma, V), -1.0e4, np.float32)
+    bi, ii = np.meshgrid(np.arange(B), np.arange(gamma), indexing="ij")
+    Y[bi, ii, d] = 0.0
+    T = synth.cycle_temperatures(B)
+    for seed in (5, 6, 7):
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        t1, l1 = dv.verify(_t(X), _t(Y), torch.from_numpy(d).to(DEV), torch.from_numpy(T).to(DEV), 20,
+                           0.95, seed, status=st)
+        t2, l2, st2 = _run_det(dv, X, d, T, 20, 0.95, seed)
+        assert int(st.item()) == st2 == 0
+        assert np.array_equal(t1.cpu().numpy(), t2) and np.array_equal(l1.cpu().numpy(), l2)
+
+
+def test_det_status_bits_and_rejected_filters(dv):
+    inp = synth.make_workload("tiny_v1024", data_seed=2, B=4, V=3001)
+    T = np.array([1.0, 1.0, -1.0, np.nan], np.float32)
+    d = _greedy_drafts(inp)
+    d[0, 0] = 3001
+    d[1, 3] = -5
+    X = inp.target.copy()
+    X[1, 6, 17] = np.nan
+    want_tok, want_len, margin, want_st = oracle.verify_det(X, d, T, inp.top_k, inp.top_p, 1)
+    tok, ln, st = _run_det(dv, X, d, T, inp.top_k, inp.top_p, 1)
+    assert st == want_st == (oracle.STATUS_BAD_TOKEN | oracle.STATUS_BAD_ROW
+                             | oracle.STATUS_BAD_TEMPERATURE)
+    assert np.all((tok >= -1) & (tok < 3001)) and np.all((ln >= 1) & (ln <= 8))
+    for b in (0, 2, 3):
+        assert np.array_equal(tok[b], want_tok[b]) and ln[b] == want_len[b]
+    # the full-vocabulary filter and top-k beyond 32 are refused for deterministic drafts
+    for k, tp in ((0, 1.0), (64, 0.95)):
+        with pytest.raises(dv.DFlashError) as e:
+            _run_det(dv, X, d, np.ones(4, np.float32), k, tp, 1)
+        assert e.value.code == 2
+
+
+def test_det_workspace_left_zero_across_modes(dv):
+    """Deterministic-draft calls and general calls of other shapes take turns
+    on one workspace; each agrees with the oracle and leaves it at zero."""
+    ws = dv.Workspace(48 << 20, DEV)
+    for V, dtype, det in [(1024, "f32", True), (20000, "f32", False), (5003, "bf16", True),
+                          (777, "f32", False), (20000, "f32", True)]:
+        B, gamma = 6, 5
+        X, Y, _ = synth.make_logits(B, gamma, V, dtype, data_seed=V + det)
+        T = np.array([1.0, 0.0, 0.6, 1.0, 1.5, 0.0], np.float32)
+        dd, _, _ = oracle.sample_rows(Y.reshape(B * gamma, V), synth.draft_sampling_temperatures(T, gamma),
+                                      20, 0.95, 3)
+        dd = dd.reshape(B, gamma)
+        if det:
+            tok, ln, st = _run_det(dv, X, dd, T, 20, 0.95, 9, workspace=ws)
+            want_tok, want_len, margin, want_st = oracle.verify_det(X, dd, T, 20, 0.95, 9)
+        else:
+            s = torch.zeros(1, dtype=torch.int32, device=DEV)
+            t_, l_ = dv.verify(_t(X), _t(Y), torch.from_numpy(dd).to(DEV), torch.from_numpy(T).to(DEV), 20,
+                               0.95, 9, status=s, workspace=ws)
+            torch.cuda.synchronize()
+            tok, ln, st = t_.cpu().numpy(), l_.cpu().numpy(), int(s.item())
+            want_tok, want_len, margin, want_st = oracle.verify(X, Y, dd, T, 20, 0.95, 9)
+        assert st == want_st
+        _compare(tok, ln, want_tok, want_len, margin)
+        assert int(torch.count_nonzero(ws.buf).item()) == 0, f"workspace not left at zero after V={V}"
