@@ -62,7 +62,7 @@ CSRC = os.path.join(ROOT, "speculative_decoding_verification_83_gb300", "csrc")
 
 
 # the sources the profiled kernel (sweep_kernel) is built from
-KERNEL_SOURCES = ("dflash_sweep.cu", "dflash_device.cuh", "dflash_internal.h")
+KERNEL_SOURCES = ("dflash_sweep.cu", "dflash_rule.cuh", "dflash_device.cuh", "dflash_internal.h")
 
 
 def kernel_source_hash() -> str:

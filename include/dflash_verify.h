@@ -182,6 +182,57 @@ int dflash_verify_host(const void* target_logits, const void* draft_logits,
                        void* staging, size_t staging_bytes, void* workspace,
                        size_t workspace_bytes, void* stream);
 
+/* ---- Vocabulary-sharded verification ----------------------------------------
+ * When each rank holds a slice of the vocabulary of every logits row (a
+ * vocabulary-parallel LM head under tensor parallelism, as the target runs in
+ * the TP=4 measurement of "DFlash2 用投机解码给 Qwen 提速" (bml.asia, the
+ * 8xRTX 3090 paragraph) and in the --tp-size 8 launch command of "你的大模型
+ * 为啥突然快了，下一代投机解码 DFlash 拆给你看" (xiaodao.ai), the step needs
+ * one exchange: every rank reduces its shard to a record (per row its k
+ * largest (logit, token) pairs and its largest logit), the ranks all-gather
+ * the records, and every rank verifies from the gathered records with
+ * identical uniforms. The union of
+ * the shards' top k of a row holds the row's global top k, so the outputs
+ * (tokens, accept lengths, status bits) equal dflash_verify's on the whole
+ * rows, bit for bit, whenever k >= top_k.
+ *
+ * A record is dflash_candidates_words(B, gamma, k) 32-bit words: the target
+ * rows' [B*(gamma+1), k] candidate logits (fp32 bits; -inf past the shard's
+ * tokens), their [B*(gamma+1), k] global token ids (int32; -1 there), the
+ * target rows' largest logits [B*(gamma+1)] (fp32; NaN when the shard row
+ * holds a NaN), then the same three arrays for the draft rows [B*gamma].
+ * Candidates are in (logit desc, token asc) order. 0 for invalid arguments
+ * (1 <= k <= DFLASH_MAX_TOP_K). */
+size_t dflash_candidates_words(int B, int gamma, int k);
+
+/* Device workspace dflash_shard_candidates needs (0 if invalid; needs
+ * k < V_shard). */
+size_t dflash_shard_workspace_bytes(int B, int gamma, int V_shard, int dtype, int k);
+
+/* One rank's record. target_shard [device] [B, gamma+1, V_shard] and
+ * draft_shard [device] [B, gamma, V_shard] (dtype) hold the logits of tokens
+ * vocab_offset .. vocab_offset + V_shard - 1 of every row; record [device]
+ * (4-byte aligned) receives dflash_candidates_words(B, gamma, k) words.
+ * Draft rows of greedy requests are read like the others (any finite values
+ * will do). Needs 1 <= k <= DFLASH_MAX_TOP_K, k < V_shard. Raises no status
+ * bits: whether a row is bad is decided from all shards' records. */
+int dflash_shard_candidates(const void* target_shard, const void* draft_shard, int B, int gamma,
+                            int V_shard, int dtype, int vocab_offset, int k, uint32_t* record,
+                            void* workspace, size_t workspace_bytes, uint32_t* status,
+                            void* stream);
+
+/* Verification from the records of n_shards shards that cover [0, V)
+ * without overlap. records [device] [n_shards, dflash_candidates_words(B,
+ * gamma, k)], in any shard order. Needs 1 <= top_k <= k and top_k < V,
+ * n_shards * k <= 256. Other arguments, outputs, uniforms and status bits as
+ * for dflash_verify (no workspace). The full-vocabulary filter (top-k off)
+ * returns DFLASH_ERR_UNSUPPORTED. */
+int dflash_verify_candidates(const uint32_t* records, int n_shards, int k,
+                             const int32_t* draft_tokens, int B, int gamma, int V,
+                             const float* temperature, int top_k, float top_p, uint64_t seed,
+                             int32_t* out_tokens, int32_t* out_accept_len, uint32_t* status,
+                             void* stream);
+
 /* Filtered distribution of R rows: for row r, the kept tokens in (logit
  * desc, index asc) order, out_idx[r, 0..n-1], their probabilities
  * out_prob[r, 0..n-1] (fp32) and n = out_count[r] (slots n..top_k-1 hold -1

@@ -18,8 +18,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash_verify.so")
-SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_abi.cu", "dflash_noalloc.cu"]
-HEADERS = ["dflash_device.cuh", "dflash_internal.h"]
+SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_candidates.cu", "dflash_abi.cu", "dflash_noalloc.cu"]
+HEADERS = ["dflash_device.cuh", "dflash_internal.h", "dflash_rule.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
@@ -103,6 +103,10 @@ EXPORTS = {
     "dflash_filter": ("i", "piiipifpppp" "zpp"),
     "dflash_sample": ("i", "piiipifQp" "pzpp"),
     "dflash_uniforms": ("i", "Qiiippp"),
+    "dflash_candidates_words": ("z", "iii"),
+    "dflash_shard_workspace_bytes": ("z", "iiiii"),
+    "dflash_shard_candidates": ("i", "ppiiiiiippzpp"),
+    "dflash_verify_candidates": ("i", "piipiiipifQpppp"),
     "dflash_noalloc_scratch_bytes": ("z", ""),
     "dflash_verify_noalloc": ("i", "pppiiiipifQpppp"),
 }
@@ -280,6 +284,94 @@ def verify_greedy(target, draft_tokens, out_tokens=None, out_accept_len=None, st
     return out_tokens, out_accept_len
 
 
+# ---- vocabulary-sharded verification -------------------------------------------------
+def candidates_words(B: int, gamma: int, k: int) -> int:
+    """32-bit words of one shard's candidate record (dflash_candidates_words)."""
+    n = load().dflash_candidates_words(B, gamma, k)
+    if n == 0:
+        raise DFlashError(ERR_INVALID_ARG, f"invalid record shape B={B} gamma={gamma} k={k}")
+    return n
+
+
+def shard_candidates(target_shard, draft_shard, vocab_offset: int, k: int, record=None, status=None,
+                     workspace=None, stream=None):
+    """dflash_shard_candidates: this rank's record (int32 tensor of
+    candidates_words(B, gamma, k) words) from its vocabulary shard of the
+    target [B, gamma+1, V_shard] and draft [B, gamma, V_shard] logits."""
+    torch = _torch()
+    B, g1, Vs = target_shard.shape
+    gamma = g1 - 1
+    if tuple(draft_shard.shape) != (B, gamma, Vs) or draft_shard.dtype != target_shard.dtype:
+        raise ValueError("draft_shard must be [B, gamma, V_shard] with the target's dtype")
+    dt = _dtype_code(target_shard)
+    dev = target_shard.device
+    words = candidates_words(B, gamma, k)
+    if record is None:
+        record = torch.empty((words,), dtype=torch.int32, device=dev)
+    if record.numel() < words:
+        raise ValueError(f"record of {record.numel()} words < {words} needed")
+    nbytes = load().dflash_shard_workspace_bytes(B, gamma, Vs, dt, k)
+    if nbytes == 0:
+        raise DFlashError(ERR_INVALID_ARG, f"k={k} must be in [1, 32] and below the shard's V={Vs}")
+    ws = _workspace_for(nbytes, dev, workspace)
+    rc = load().dflash_shard_candidates(
+        _dev(target_shard, "target_shard"), _dev(draft_shard, "draft_shard"), B, gamma, Vs, dt, int(vocab_offset),
+        int(k), _dev(record, "record", torch.int32), ws.ptr, ws.nbytes,
+        None if status is None else _dev(status, "status", torch.int32), _stream_ptr(stream, dev))
+    _check(rc)
+    return record
+
+
+def gather_records(record, group=None):
+    """The step's one exchange: every rank's record, gathered into a
+    [world, words] tensor in rank order (torch.distributed all-gather into
+    the rows of one buffer; any backend)."""
+    torch = _torch()
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    out = torch.empty((world, record.numel()), dtype=record.dtype, device=record.device)
+    dist.all_gather(list(out.unbind(0)), record.contiguous(), group=group)
+    return out
+
+
+def verify_candidates(records, k: int, draft_tokens, temperature, V: int, top_k: int, top_p: float, seed: int,
+                      out_tokens=None, out_accept_len=None, status=None, stream=None):
+    """dflash_verify_candidates on gathered records [n_shards, words]."""
+    torch = _torch()
+    n_shards = records.shape[0]
+    B, gamma = draft_tokens.shape
+    dev = records.device
+    if not records.is_contiguous() or records.shape[1] != candidates_words(B, gamma, k):
+        raise ValueError("records must be a contiguous [n_shards, candidates_words(B, gamma, k)] tensor")
+    if out_tokens is None:
+        out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    rc = load().dflash_verify_candidates(
+        _dev(records, "records", torch.int32), n_shards, int(k),
+        _dev(draft_tokens, "draft_tokens", torch.int32), B, gamma, int(V),
+        _dev(temperature, "temperature", torch.float32), int(top_k), float(top_p),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(out_accept_len, "out_accept_len", torch.int32),
+        None if status is None else _dev(status, "status", torch.int32), _stream_ptr(stream, dev))
+    _check(rc)
+    return out_tokens, out_accept_len
+
+
+def verify_vocab_sharded(target_shard, draft_shard, vocab_offset: int, V: int, draft_tokens, temperature,
+                         top_k: int, top_p: float, seed: int, group=None, status=None, workspace=None,
+                         stream=None):
+    """One verification step with the vocabulary split across the ranks of
+    `group`: this rank's record, the all-gather, then the verification from
+    every shard's candidates (identical on every rank)."""
+    record = shard_candidates(target_shard, draft_shard, vocab_offset, top_k, status=status,
+                              workspace=workspace, stream=stream)
+    records = gather_records(record, group)
+    return verify_candidates(records, top_k, draft_tokens, temperature, V, top_k, top_p, seed,
+                             status=status, stream=stream)
+
+
 def rows_workspace_bytes(R, V, dtype_code, top_k, top_p) -> int:
     n = load().dflash_rows_workspace_bytes(R, V, dtype_code, top_k, top_p)
     if n == 0:
@@ -359,7 +451,8 @@ def verify_host(target, draft, draft_tokens, temperature, top_k, top_p, seed, ou
 
 
 __all__ = [
-    "build", "load", "verify", "verify_det", "verify_greedy", "filter_rows", "sample_rows", "uniforms",
+    "build", "load", "verify", "verify_det", "verify_greedy", "shard_candidates", "gather_records",
+    "verify_candidates", "verify_vocab_sharded", "candidates_words", "filter_rows", "sample_rows", "uniforms",
     "verify_host", "Workspace", "workspace_bytes", "rows_workspace_bytes", "host_staging_bytes",
     "DFlashError", "LIB_PATH", "EXPORTS",
 ]

@@ -499,6 +499,119 @@ int dflash_sample(const void* logits, int R, int V, int dtype, const float* temp
                    nullptr, workspace, workspace_bytes, status, stream);
 }
 
+size_t dflash_candidates_words(int B, int gamma, int k) {
+  if (B < 1 || B > kMaxB || gamma < 1 || gamma > kMaxGamma || k < 1 || k > DFLASH_MAX_TOP_K) return 0;
+  return candidate_layout(B, gamma, k).words;
+}
+
+size_t dflash_shard_workspace_bytes(int B, int gamma, int V_shard, int dtype, int k) {
+  if (B < 1 || B > kMaxB || gamma < 1 || gamma > kMaxGamma || k < 1 || k > DFLASH_MAX_TOP_K || k >= V_shard)
+    return 0;
+  return dflash_rows_workspace_bytes(B * (gamma + 1), V_shard, dtype, k, 1.0f);
+}
+
+// one candidates pass over R rows of a vocabulary shard
+static int candidates_pass(const void* logits, int R, int V_shard, int dtype, int vocab_offset, int k,
+                           float* out_logit, int32_t* out_token, float* out_max, void* workspace, uint32_t* status,
+                           void* stream) {
+  Params p = base_params(dtype, V_shard);
+  p.gamma = 1;
+  p.top_k = k;
+  p.top_p = 1.0f;
+  p.task = kTaskCandidates;
+  p.vocab_offset = vocab_offset;
+  p.status = status;
+  const int chunk = R < kMaxCounterSlots ? R : kMaxCounterSlots;
+  bind_workspace(p, workspace, chunk, 1);
+  const size_t row_bytes = (size_t)V_shard * esize_of(dtype);
+  for (int r0 = 0; r0 < R; r0 += chunk) {
+    const int n = R - r0 < chunk ? R - r0 : chunk;
+    p.target = static_cast<const unsigned char*>(logits) + (size_t)r0 * row_bytes;
+    p.B = n;
+    p.row_base = r0;
+    p.out_prob = out_logit + (size_t)r0 * k;
+    p.out_idx = out_token + (size_t)r0 * k;
+    p.out_rowmax = out_max + r0;
+    const int rc = run(p, n, stream);
+    if (rc) return rc;
+  }
+  return DFLASH_OK;
+}
+
+int dflash_shard_candidates(const void* target_shard, const void* draft_shard, int B, int gamma, int V_shard,
+                            int dtype, int vocab_offset, int k, uint32_t* record, void* workspace,
+                            size_t workspace_bytes, uint32_t* status, void* stream) {
+  int rc = check_shape(B, gamma, V_shard, dtype);
+  if (rc) return rc;
+  if (!target_shard || !draft_shard || !record || !workspace)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if (k < 1 || k > DFLASH_MAX_TOP_K || k >= V_shard)
+    return fail(DFLASH_ERR_INVALID_ARG, "k=%d must be in [1, %d] and below the shard's V=%d", k, DFLASH_MAX_TOP_K,
+                V_shard);
+  if (vocab_offset < 0 || (long long)vocab_offset + V_shard > 0x7fffffffLL)
+    return fail(DFLASH_ERR_INVALID_ARG, "vocab_offset=%d puts the shard's tokens outside [0, 2^31)", vocab_offset);
+  const int es = esize_of(dtype);
+  if ((rc = check_aligned(target_shard, es, "target_shard")) || (rc = check_aligned(draft_shard, es, "draft_shard")))
+    return rc;
+  if (((uintptr_t)record) % 4u) return fail(DFLASH_ERR_INVALID_ARG, "record is not 4-byte aligned");
+  const size_t need = dflash_shard_workspace_bytes(B, gamma, V_shard, dtype, k);
+  if (workspace_bytes < need)
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
+                need);
+  const CandidateLayout L = candidate_layout(B, gamma, k);
+  float* f = reinterpret_cast<float*>(record);
+  int32_t* t = reinterpret_cast<int32_t*>(record);
+  rc = candidates_pass(target_shard, B * (gamma + 1), V_shard, dtype, vocab_offset, k, f + L.t_logit, t + L.t_token,
+                       f + L.t_max, workspace, status, stream);
+  if (rc) return rc;
+  return candidates_pass(draft_shard, B * gamma, V_shard, dtype, vocab_offset, k, f + L.d_logit, t + L.d_token,
+                         f + L.d_max, workspace, status, stream);
+}
+
+int dflash_verify_candidates(const uint32_t* records, int n_shards, int k, const int32_t* draft_tokens, int B,
+                             int gamma, int V, const float* temperature, int top_k, float top_p, uint64_t seed,
+                             int32_t* out_tokens, int32_t* out_accept_len, uint32_t* status, void* stream) {
+  if (B < 1 || B > kMaxB) return fail(DFLASH_ERR_INVALID_ARG, "B=%d outside [1, %d]", B, kMaxB);
+  if (gamma < 1 || gamma > kMaxGamma)
+    return fail(DFLASH_ERR_INVALID_ARG, "gamma=%d outside [1, %d]", gamma, kMaxGamma);
+  if (V < 1) return fail(DFLASH_ERR_INVALID_ARG, "V=%d must be >= 1", V);
+  if (!records || !draft_tokens || !temperature || !out_tokens || !out_accept_len)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if (((uintptr_t)records) % 4u) return fail(DFLASH_ERR_INVALID_ARG, "records are not 4-byte aligned");
+  if (k < 1 || k > DFLASH_MAX_TOP_K) return fail(DFLASH_ERR_INVALID_ARG, "k=%d outside [1, %d]", k, DFLASH_MAX_TOP_K);
+  if (n_shards < 1 || (long long)n_shards * k > kMaxShardCand)
+    return fail(DFLASH_ERR_INVALID_ARG, "n_shards=%d with k=%d: need 1 <= n_shards * k <= %d", n_shards, k,
+                kMaxShardCand);
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
+  if (mode != kModeTopK || top_k > k)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "top_k=%d with top_p=%g is not supported from shard candidates (need 1 <= top_k <= k = %d and "
+                "top_k < V)",
+                top_k, (double)top_p, k);
+  CandParams c;
+  memset(&c, 0, sizeof c);
+  c.L = candidate_layout(B, gamma, k);
+  c.records = records;
+  c.words = c.L.words;
+  c.n_shards = n_shards;
+  c.k = k;
+  c.draft_tokens = draft_tokens;
+  c.temperature = temperature;
+  c.B = B;
+  c.gamma = gamma;
+  c.V = V;
+  c.top_k = top_k;
+  c.top_p = top_p >= 1.0f ? 1.0f : top_p;
+  c.seed = seed;
+  c.out_tokens = out_tokens;
+  c.out_len = out_accept_len;
+  c.status = status;
+  const int e = launch_verify_candidates(c, stream);
+  if (e) return cuda_fail((cudaError_t)e, "launching the verification from shard candidates");
+  return DFLASH_OK;
+}
+
 int dflash_uniforms(uint64_t seed, int B, int npos, int stream_id, float* out_accept, float* out_draw, void* stream) {
   if (B < 1 || npos < 1 || (!out_accept && !out_draw))
     return fail(DFLASH_ERR_INVALID_ARG, "bad uniforms arguments");

@@ -66,7 +66,7 @@ inline __host__ __device__ int tile_vector(int tile, int t) {
   return 32 * (4 * (tile >> 2) + (t >> 3)) + 8 * (tile & 3) + (t & 7);
 }
 
-enum Task : int { kTaskVerify = 0, kTaskVerifyGreedy = 1, kTaskFilter = 2, kTaskSample = 3 };
+enum Task : int { kTaskVerify = 0, kTaskVerifyGreedy = 1, kTaskFilter = 2, kTaskSample = 3, kTaskCandidates = 4 };
 
 // Row geometry: the head (elements before the first 16-byte boundary) and
 // tail (after the last one) are read with plain loads by the row-final stage;
@@ -119,6 +119,7 @@ struct Params {
   int fullvocab;                // top-k off and top-p 1: softmax over the whole vocabulary
   int det;                      // verify: deterministic drafts (q = point mass at the draft; no draft rows)
   int row_base;                 // rows tasks: index of this launch's first row
+  int vocab_offset;             // candidates task: token id of the shard's first logit
   Geometry geo;
   // outputs
   int32_t* out_tokens;
@@ -126,6 +127,7 @@ struct Params {
   int32_t* out_idx;
   float* out_prob;
   int32_t* out_count;
+  float* out_rowmax;            // candidates task: each row's largest logit (NaN if it holds one)
   uint32_t* status;
   // workspace (zero-initialised once; counters reset by their last user)
   uint32_t* row_cnt;    // [n_slots]
@@ -160,6 +162,44 @@ struct FvParams {
   const uint32_t* abort_flag;
   float exp_hi[kExpTable];      // 2^(j/64) = exp_hi[j] + exp_lo[j]
   float exp_lo[kExpTable];
+};
+
+// ---- vocabulary-shard candidates ----------------------------------------------------
+// A shard's record for a batch (B requests, gamma drafts, k candidates per
+// row), 32-bit words: the target rows' [B * (gamma+1), k] candidate logits
+// (fp32 bits, -inf past the shard's tokens), their [B * (gamma+1), k] global
+// token ids (-1 there), the target rows' maxima [B * (gamma+1)] (fp32), then
+// the same three arrays for the draft rows [B * gamma].
+constexpr int kMaxShardCand = 256;  // shards x k candidates merged per row
+struct CandidateLayout {
+  size_t t_logit, t_token, t_max, d_logit, d_token, d_max, words;
+};
+inline CandidateLayout candidate_layout(int B, int gamma, int k) {
+  CandidateLayout L;
+  const size_t rt = (size_t)B * (gamma + 1), rd = (size_t)B * gamma;
+  L.t_logit = 0;
+  L.t_token = L.t_logit + rt * k;
+  L.t_max = L.t_token + rt * k;
+  L.d_logit = L.t_max + rt;
+  L.d_token = L.d_logit + rd * k;
+  L.d_max = L.d_token + rd * k;
+  L.words = L.d_max + rd;
+  return L;
+}
+
+struct CandParams {
+  const uint32_t* records;      // [n_shards, words]
+  size_t words;                 // one record's words
+  CandidateLayout L;
+  int n_shards, k;              // shards, candidates per shard and row
+  const int32_t* draft_tokens;  // [B, gamma]
+  const float* temperature;     // [B]
+  int B, gamma, V, top_k;
+  float top_p;
+  unsigned long long seed;
+  int32_t* out_tokens;          // [B, gamma+1]
+  int32_t* out_len;             // [B]
+  uint32_t* status;
 };
 
 struct WorkspaceLayout {
@@ -213,5 +253,6 @@ int sweep_smem_bytes();
 int launch_fullvocab_draw(const FvParams& f, void* stream);
 int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* out_accept,
                     float* out_draw, void* stream);
+int launch_verify_candidates(const CandParams& c, void* stream);  // dflash_candidates.cu
 
 }  // namespace dflash

@@ -53,12 +53,11 @@
 
 #include "dflash_device.cuh"
 #include "dflash_internal.h"
+#include "dflash_rule.cuh"
 
 namespace dflash {
 namespace {
 
-constexpr uint32_t kStatusBadToken = 1u, kStatusBadRow = 2u, kStatusTimeout = 4u,
-                   kStatusBadTemperature = 8u;
 
 // what the producer loaded into a ring stage (read by the consumers)
 struct PieceDesc {
@@ -107,8 +106,6 @@ struct Smem {
   int bad_head_tail;
 };
 
-__device__ __forceinline__ bool sampling_temperature(float t) { return t > 0.0f && t < INFINITY; }
-
 // ---- row geometry ---------------------------------------------------------------
 struct RowBody {
   const unsigned char* row;  // first logit of the row
@@ -155,8 +152,6 @@ struct SlotInfo {
 __device__ __forceinline__ int samp_slots(const Params& p) { return p.det ? p.gamma + 1 : 2 * p.gamma + 1; }
 // position of row r of a sampling request (target row i, or draft row i)
 __device__ __forceinline__ int samp_position(const Params& p, int r) { return p.det ? r : r >> 1; }
-// row of a sampling request holding position i's target logits
-__device__ __forceinline__ int samp_target_row(const Params& p, int i) { return p.det ? i : 2 * i; }
 
 __device__ __forceinline__ SlotInfo slot_info(const Params& p, const Smem& S, int slot) {
   SlotInfo s;
@@ -188,7 +183,7 @@ __device__ __forceinline__ SlotInfo slot_info(const Params& p, const Smem& S, in
   } else {
     s.ord = slot;
     s.r = 0;
-    s.sampling = sampling_temperature(__ldg(p.temperature + slot));
+    s.sampling = p.task == kTaskCandidates || sampling_temperature(__ldg(p.temperature + slot));
     s.ptr = p.target + (size_t)slot * row_bytes;
     s.k_eff = s.sampling ? p.top_k : 1;
   }
@@ -394,114 +389,6 @@ __device__ __forceinline__ float vector_max(const uint4& wv) {
                  max_nan(__uint_as_float(wv.z), __uint_as_float(wv.w)));
 }
 
-// ---- filtering and drawing ---------------------------------------------------------
-// Sorts in the finals place each element by its rank (independent loads from
-// a small shared scratch) rather than through a sorting network, which is
-// dozens of dependent shuffle steps; sums and prefix sums over a warp are
-// five shuffle steps each.
-
-// Total of the 32 values in sc (16-byte aligned), added in lane order, and in
-// `before` the part added before this lane's value. Every lane adds in the
-// same order, so all lanes get the same total.
-__device__ __forceinline__ float scratch_sums(const float* sc, int lane, float& before) {
-  const float4* s4 = reinterpret_cast<const float4*>(sc);
-  float total = 0.0f;
-  before = 0.0f;
-#pragma unroll 1
-  for (int q = 0; q < 8; ++q) {
-    const float4 v = s4[q];
-    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (4 * q + i == lane) before = total;
-      total += e[i];
-    }
-  }
-  return total;
-}
-
-// Warp-wide sum (butterfly: every lane gets the same total) and inclusive
-// prefix sum of a float. Short shuffle chains: five dependent steps each.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
-
-// Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
-// over the survivors, top-p cut, renormalisation. Returns this lane's
-// probability (0 outside the kept set) and sets idx to -1 there.
-__device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
-                                             int lane) {
-  const bool in_k = lane < k_eff && idx >= 0;
-  const float z = value_of_key(key) / T;
-  const float z0 = __shfl_sync(0xffffffffu, z, 0);  // the largest
-  const float w = in_k ? expf(z - z0) : 0.0f;
-  bool keep = in_k;
-  if (top_p < 1.0f) {
-    const float W = warp_sum(w);
-    const float incl = warp_inclusive_scan(w / W, lane);
-    float before = __shfl_up_sync(0xffffffffu, incl, 1);  // mass of the higher ranks
-    if (lane == 0) before = 0.0f;
-    keep = keep && (before < top_p);
-  }
-  const float wk = keep ? w : 0.0f;
-  const float Wk = warp_sum(wk);
-  if (!keep) idx = -1;
-  return keep ? wk / Wk : 0.0f;
-}
-
-// Inverse CDF in ascending token order: the smallest token whose cumulative
-// weight exceeds u * total; if rounding leaves none, the last token with
-// positive weight; tokens marked -1 have no weight. The lanes are put in
-// token order by rank (ties, only among the -1 marks, by lane); sk, sw: 32
-// words each of warp scratch, 16-byte aligned.
-__device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane, int32_t* sk,
-                                                  float* sw) {
-  const int32_t key = tok >= 0 ? tok : INT_MAX;
-  const float wt = tok >= 0 ? w : 0.0f;
-  sk[lane] = key;
-  __syncwarp();
-  int r = 0;
-  const int4* k4 = reinterpret_cast<const int4*>(sk);
-#pragma unroll 1
-  for (int q = 0; q < 8; ++q) {
-    const int4 v = k4[q];
-    const int32_t e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) r += (e[i] < key || (e[i] == key && 4 * q + i < lane)) ? 1 : 0;
-  }
-  __syncwarp();
-  sk[r] = key;
-  sw[r] = wt;
-  __syncwarp();
-  // lane l now stands for rank l
-  const float wl = sw[lane];
-  float before;
-  const float total = scratch_sums(sw, lane, before);
-  const float cum = before + wl;
-  const float t = u * total;
-  const uint32_t hit = __ballot_sync(0xffffffffu, wl > 0.0f && t < cum);
-  int chosen;
-  if (hit) {
-    chosen = __ffs(hit) - 1;
-  } else {
-    const uint32_t pos = __ballot_sync(0xffffffffu, wl > 0.0f);
-    chosen = pos ? 31 - __clz(pos) : 0;
-  }
-  const int32_t res = sk[chosen];
-  __syncwarp();
-  return res == INT_MAX ? -1 : res;
-}
-
 // Body vector of the f-th gathered vector: f / 32 picks the candidate tile,
 // f % 32 the vector within it.
 __device__ __forceinline__ int candidate_vector(const Smem& S, int f) {
@@ -538,7 +425,9 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   constexpr int dtype = DT;  // the kernel's logit type
   // the row's temperature, loaded now and used last: a global load at the
   // end of the final would add a full round trip to it
-  T_row = ld_nc_now(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
+  T_row = p.task == kTaskCandidates  // no temperatures: raw logits out
+              ? 1.0f
+              : ld_nc_now(p.temperature + (p.task == kTaskVerify ? S.req_of_ord[si.ord] : slot));
   // a verification row's position's draft token (target row 2i and draft row
   // 2i + 1 of a request, or target row i with deterministic drafts, are
   // position i's; the bonus row has none)
@@ -816,7 +705,18 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       const float pd = hit ? __shfl_sync(0xffffffffu, pr, __ffs(hit) - 1) : 0.0f;
       if (lane == 0) list[kMaxTopK] = (1ull << 32) | __float_as_uint(pd);
     }
-    if (bad && lane == 0 && p.status) atomicOr(p.status, kStatusBadRow);
+    if (p.task == kTaskCandidates) {
+      // a vocabulary shard's top k as (logit, global token), then its largest
+      // logit: whether the whole row is bad is decided once the shards meet
+      const bool valid = lane < k && lane < n_c;
+      if (lane < k) {
+        p.out_prob[(size_t)slot * k + lane] = valid ? value_of_key(composite_key(a)) : -INFINITY;
+        p.out_idx[(size_t)slot * k + lane] = valid ? composite_idx(a) + p.vocab_offset : -1;
+      }
+      if (lane == 0) p.out_rowmax[slot] = value_of_key(max(tile_max, edge_max));
+    } else if (bad && lane == 0 && p.status) {
+      atomicOr(p.status, kStatusBadRow);
+    }
   }
   // leave the keys at zero for the next call
   uint32_t* wkeys = p.tile_keys + (size_t)slot * n_tiles;
@@ -824,10 +724,6 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   fin_sync();
   return true;
 }
-
-// Home slot of a token in a 64-slot table (Fibonacci hashing).
-__device__ __forceinline__ uint32_t token_slot(int32_t t) { return ((uint32_t)t * 2654435761u) >> 26; }
-static_assert(2 * kMaxTopK == 64, "token_slot hashes into 64 slots");
 
 // ---- request final (sampling verification) -------------------------------------------
 // The rows arrive filtered (kept tokens and probabilities). One lane per draft
@@ -873,80 +769,9 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
   // every call leaves the workspace at zero: its regions move with the
   // shape, and another shape's tile keys may lie here next time
   for (int i = gt; i < n_words; i += kFin) words[i] = 0ull;
-  if (w == 0) {
-    uint32_t st = 0;
-    for (int r = lane; r < per_s; r += 32)
-      if (S.u.lists.idx[r][32]) st |= kStatusBadRow;
-    bool reject = false;
-    if (lane < gamma) {
-      const int32_t di = d_lane;
-      if (di < 0 || di >= V) st |= kStatusBadToken;
-      // p(d) and q(d), found by the rows' finals (0 when the token is not kept)
-      const float p_d = S.u.lists.prob[samp_target_row(p, lane)][32];
-      const float q_d = p.det ? 1.0f : S.u.lists.prob[2 * lane + 1][32];
-      const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
-      reject = !(uniform24(wd.x) < ratio);
-    }
-    const uint32_t rej = __ballot_sync(0xffffffffu, reject);
-    const int n = rej ? __ffs(rej) - 1 : gamma;  // drafts accepted
-    uint32_t u_draw = __shfl_sync(0xffffffffu, wd.y, n & 31);
-    if (n >= 32) u_draw = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)n, 0u).y;  // gamma = 32, all kept
-    const int row = samp_target_row(p, n);  // target row of position n (the bonus row when n == gamma)
-    const int32_t ti = S.u.lists.idx[row][lane];
-    const float pi = S.u.lists.prob[row][lane];
-    float wt = pi;
-    if (n < gamma && p.det) {
-      // residual p - delta_d: the target's kept tokens other than the draft
-      const int32_t dn = __shfl_sync(0xffffffffu, d_lane, n);
-      const float r = (ti >= 0 && ti != dn) ? pi : 0.0f;
-      if (__ballot_sync(0xffffffffu, r > 0.0f) != 0u) wt = r;
-    } else if (n < gamma) {
-      // residual max(0, p - q) over the target's kept tokens: q from the
-      // draft row's list through a 64-slot open-addressing table (S.cand as
-      // scratch: keys, then values)
-      int32_t* hk = reinterpret_cast<int32_t*>(S.cand);
-      float* hv = reinterpret_cast<float*>(S.cand) + 2 * kMaxTopK;
-      hk[lane] = -1;
-      hk[lane + kMaxTopK] = -1;
-      __syncwarp();
-      const int32_t dt = S.u.lists.idx[row + 1][lane];
-      if (dt >= 0) {
-        uint32_t h = token_slot(dt);
-        for (int probe = 0; probe < 2 * kMaxTopK; ++probe, h = (h + 1u) & (2 * kMaxTopK - 1)) {
-          if (atomicCAS(&hk[h], -1, dt) == -1) {
-            hv[h] = S.u.lists.prob[row + 1][lane];
-            break;
-          }
-        }
-      }
-      __syncwarp();
-      float q_of_t = 0.0f;
-      if (ti >= 0) {
-        uint32_t h = token_slot(ti);
-        for (int probe = 0; probe < 2 * kMaxTopK; ++probe, h = (h + 1u) & (2 * kMaxTopK - 1)) {
-          const int32_t key = hk[h];
-          if (key == ti) {
-            q_of_t = hv[h];
-            break;
-          }
-          if (key == -1) break;
-        }
-      }
-      __syncwarp();  // the table's slots are the draw's scratch next
-      const float r = ti >= 0 ? fmaxf(pi - q_of_t, 0.0f) : 0.0f;
-      if (__ballot_sync(0xffffffffu, r > 0.0f) != 0u) wt = r;
-    }
-    int32_t last = draw_ascending(ti, wt, uniform24(u_draw), lane, reinterpret_cast<int32_t*>(S.cand),
-                                  reinterpret_cast<float*>(S.cand) + 32);
-    if (last < 0) last = __shfl_sync(0xffffffffu, ti, 0);
-    // gamma <= 32: a position i < n is this lane's own (i == lane)
-    for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? d_lane : (i == n ? last : -1);
-    st = __reduce_or_sync(0xffffffffu, st);
-    if (lane == 0) {
-      if (p.out_len) p.out_len[b] = n + 1;
-      if (st && p.status) atomicOr(p.status, st);
-    }
-  }
+  if (w == 0)
+    sampling_rule(S.u.lists.idx, S.u.lists.prob, per_s, p.det != 0, gamma, V, d_lane, wd, p.seed, b, lane,
+                  S.cand, out, p.out_len, p.status);
   fin_sync();
   return true;
 }
@@ -1559,7 +1384,7 @@ __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int or
     unsigned long long top_a = 0ull;
     float T_row;
     ok = row_final<DT>(p, S, j, si, top_a, T_row, next);
-    if (ok && p.task != kTaskVerify && p.task != kTaskVerifyGreedy) rows_final(p, S, j, top_a, T_row);
+    if (ok && (p.task == kTaskFilter || p.task == kTaskSample)) rows_final(p, S, j, top_a, T_row);
   }
   if (!ok && gt == 0) raise_timeout(p);
   return ok;

@@ -94,7 +94,7 @@ def cycle_temperatures(B: int, cycle=(0.0, 0.6, 1.0)) -> np.ndarray:
     return np.array([cycle[b % len(cycle)] for b in range(B)], np.float32)
 
 
-# The five workloads of the step (shapes, storage types, filters).
+# The workloads of the step (shapes, storage types, filters).
 WORKLOADS = {
     # tiny CPU-checkable case: greedy and sampling on one request
     "tiny_v1024": dict(B=1, gamma=7, V=1024, dtype=F32, sigma_d=0.5, temperature=1.0,
@@ -108,6 +108,11 @@ WORKLOADS = {
     # concurrency 32, temperatures cycling greedy / 0.6 / 1.0
     "b32_mixed_v248320": dict(B=32, gamma=7, V=248320, dtype=BF16, sigma_d=(0.3, 1.5),
                               temperature=(0.0, 0.6, 1.0), top_k=20, top_p=0.95),
+    # the same concurrency-32 mix at blocks of 4 and 16 (3 and 15 verified drafts)
+    "b32_mixed_g3_v248320": dict(B=32, gamma=3, V=248320, dtype=BF16, sigma_d=(0.3, 1.5),
+                                 temperature=(0.0, 0.6, 1.0), top_k=20, top_p=0.95),
+    "b32_mixed_g15_v248320": dict(B=32, gamma=15, V=248320, dtype=BF16, sigma_d=(0.3, 1.5),
+                                  temperature=(0.0, 0.6, 1.0), top_k=20, top_p=0.95),
     # block 16, fp32, top-k off and top-p 1: full-vocabulary softmax and residual
     "b128_g15_fullvocab_f32": dict(B=128, gamma=15, V=248320, dtype=F32, sigma_d=0.5,
                                    temperature=1.0, top_k=0, top_p=1.0),

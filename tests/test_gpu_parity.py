@@ -230,7 +230,8 @@ def test_verify_gamma_range(dv, gamma):
     _compare_sampling(tok, ln, want_tok, want_len, margin)
 
 
-@pytest.mark.parametrize("name", ["b1_v248320", "b8_v248320", "b32_mixed_v248320"])
+@pytest.mark.parametrize("name", ["b1_v248320", "b8_v248320", "b32_mixed_v248320", "b32_mixed_g3_v248320",
+                                  "b32_mixed_g15_v248320"])
 def test_verify_full_size_workloads(dv, name):
     """The full-size bf16 workloads, every request checked against the oracle."""
     seeds = [0, 1, 2] if name == "b1_v248320" else [0]
