@@ -166,6 +166,24 @@ def _dev(t, name, dtype=None):
     return t.data_ptr()
 
 
+def _shape(t, shape, name):
+    """Every buffer the library reads or writes must have the shape the call's
+    sizes imply: a short tensor would let a kernel run past its end."""
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _on(device, **tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the call's logits on {device}")
+
+
+def _status_ok(status):
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold one int32 word")
+
+
 def _stream_ptr(stream, device):
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream(device)
@@ -228,6 +246,13 @@ def verify(target, draft, draft_tokens, temperature, top_k: int, top_p: float, s
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
         out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _shape(draft_tokens, (B, gamma), "draft_tokens")
+    _shape(temperature, (B,), "temperature")
+    _shape(out_tokens, (B, gamma + 1), "out_tokens")
+    _shape(out_accept_len, (B,), "out_accept_len")
+    _status_ok(status)
+    _on(dev, draft=draft, draft_tokens=draft_tokens, temperature=temperature, out_tokens=out_tokens,
+        out_accept_len=out_accept_len, status=status)
     ws = _workspace_for(workspace_bytes(B, gamma, V, dt, top_k, top_p), dev, workspace)
     rc = load().dflash_verify(
         _dev(target, "target"), _dev(draft, "draft"), _dev(draft_tokens, "draft_tokens", torch.int32),
@@ -252,6 +277,13 @@ def verify_det(target, draft_tokens, temperature, top_k: int, top_p: float, seed
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
         out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _shape(draft_tokens, (B, gamma), "draft_tokens")
+    _shape(temperature, (B,), "temperature")
+    _shape(out_tokens, (B, gamma + 1), "out_tokens")
+    _shape(out_accept_len, (B,), "out_accept_len")
+    _status_ok(status)
+    _on(dev, draft_tokens=draft_tokens, temperature=temperature, out_tokens=out_tokens,
+        out_accept_len=out_accept_len, status=status)
     ws = _workspace_for(workspace_bytes(B, gamma, V, dt, top_k, top_p), dev, workspace)
     rc = load().dflash_verify_det(
         _dev(target, "target"), _dev(draft_tokens, "draft_tokens", torch.int32), B, gamma, V, dt,
@@ -274,6 +306,11 @@ def verify_greedy(target, draft_tokens, out_tokens=None, out_accept_len=None, st
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
         out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _shape(draft_tokens, (B, gamma), "draft_tokens")
+    _shape(out_tokens, (B, gamma + 1), "out_tokens")
+    _shape(out_accept_len, (B,), "out_accept_len")
+    _status_ok(status)
+    _on(dev, draft_tokens=draft_tokens, out_tokens=out_tokens, out_accept_len=out_accept_len, status=status)
     ws = _workspace_for(workspace_bytes(B, gamma, V, dt, 1, 1.0), dev, workspace)
     rc = load().dflash_verify_greedy(
         _dev(target, "target"), _dev(draft_tokens, "draft_tokens", torch.int32), B, gamma, V, dt,
@@ -310,6 +347,8 @@ def shard_candidates(target_shard, draft_shard, vocab_offset: int, k: int, recor
         record = torch.empty((words,), dtype=torch.int32, device=dev)
     if record.numel() < words:
         raise ValueError(f"record of {record.numel()} words < {words} needed")
+    _status_ok(status)
+    _on(dev, draft_shard=draft_shard, record=record, status=status)
     nbytes = load().dflash_shard_workspace_bytes(B, gamma, Vs, dt, k)
     if nbytes == 0:
         raise DFlashError(ERR_INVALID_ARG, f"k={k} must be in [1, 32] and below the shard's V={Vs}")
@@ -348,6 +387,12 @@ def verify_candidates(records, k: int, draft_tokens, temperature, V: int, top_k:
         out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
     if out_accept_len is None:
         out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _shape(temperature, (B,), "temperature")
+    _shape(out_tokens, (B, gamma + 1), "out_tokens")
+    _shape(out_accept_len, (B,), "out_accept_len")
+    _status_ok(status)
+    _on(dev, draft_tokens=draft_tokens, temperature=temperature, out_tokens=out_tokens,
+        out_accept_len=out_accept_len, status=status)
     rc = load().dflash_verify_candidates(
         _dev(records, "records", torch.int32), n_shards, int(k),
         _dev(draft_tokens, "draft_tokens", torch.int32), B, gamma, int(V),
@@ -386,6 +431,9 @@ def filter_rows(logits, temperature, top_k: int, top_p: float, status=None, work
     R, V = logits.shape
     dt = _dtype_code(logits)
     dev = logits.device
+    _shape(temperature, (R,), "temperature")
+    _status_ok(status)
+    _on(dev, temperature=temperature, status=status)
     idx = torch.empty((R, top_k), dtype=torch.int32, device=dev)
     prob = torch.empty((R, top_k), dtype=torch.float32, device=dev)
     cnt = torch.empty((R,), dtype=torch.int32, device=dev)
@@ -405,6 +453,9 @@ def sample_rows(logits, temperature, top_k: int, top_p: float, seed: int, status
     R, V = logits.shape
     dt = _dtype_code(logits)
     dev = logits.device
+    _shape(temperature, (R,), "temperature")
+    _status_ok(status)
+    _on(dev, temperature=temperature, status=status)
     out = torch.empty((R,), dtype=torch.int32, device=dev)
     ws = _workspace_for(rows_workspace_bytes(R, V, dt, top_k, top_p), dev, workspace)
     rc = load().dflash_sample(
@@ -435,11 +486,21 @@ def verify_host(target, draft, draft_tokens, temperature, top_k, top_p, seed, ou
     B, g1, V = target.shape
     gamma = g1 - 1
     dt = _dtype_code(target)
-    for t, n in ((target, "target"), (draft, "draft"), (draft_tokens, "draft_tokens"),
-                 (temperature, "temperature"), (out_tokens, "out_tokens"),
-                 (out_accept_len, "out_accept_len"), (out_status, "out_status")):
+    torch = _torch()
+    for t, n, shape, dtype in ((target, "target", (B, gamma + 1, V), target.dtype),
+                               (draft, "draft", (B, gamma, V), target.dtype),
+                               (draft_tokens, "draft_tokens", (B, gamma), torch.int32),
+                               (temperature, "temperature", (B,), torch.float32),
+                               (out_tokens, "out_tokens", (B, gamma + 1), torch.int32),
+                               (out_accept_len, "out_accept_len", (B,), torch.int32),
+                               (out_status, "out_status", (1,), torch.int32)):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{n} must be a contiguous host tensor")
+        _shape(t, shape, n)
+        if t.dtype != dtype:
+            raise TypeError(f"{n} must be {dtype}, got {t.dtype}")
+    if not staging.is_cuda or staging.dtype != torch.uint8:
+        raise ValueError("staging must be a uint8 CUDA tensor")
     rc = load().dflash_verify_host(
         target.data_ptr(), draft.data_ptr(), draft_tokens.data_ptr(), B, gamma, V, dt,
         temperature.data_ptr(), int(top_k), float(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF,
