@@ -161,9 +161,10 @@ int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
  * a sampling request reads gamma + 1 rows instead of 2 gamma + 1.
  * Arguments, uniforms, draws, greedy requests (T == 0), outputs and status
  * bits as for dflash_verify without draft_logits; workspace_bytes >=
- * dflash_workspace_bytes(...) of the same shape and filter. Top-k must be on
- * (1 <= top_k <= DFLASH_MAX_TOP_K, top_k < V): the full-vocabulary filter
- * returns DFLASH_ERR_UNSUPPORTED here. */
+ * dflash_workspace_bytes(...) of the same shape and filter. Filters as for
+ * dflash_verify: top-k on (1 <= top_k <= DFLASH_MAX_TOP_K, top_k < V) with any
+ * top_p, or the full-vocabulary softmax (top-k off, top_p = 1), where the
+ * residual p without d is drawn over the whole vocabulary in float-float. */
 int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, int B, int gamma,
                       int V, int dtype, const float* temperature, int top_k, float top_p,
                       uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,

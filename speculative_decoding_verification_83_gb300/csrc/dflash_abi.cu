@@ -254,13 +254,14 @@ int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, in
     return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
   const int mode = filter_mode(V, top_k, top_p);
   if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
-  if (mode != kModeTopK)
+  if (mode == 0)
     return fail(DFLASH_ERR_UNSUPPORTED,
                 "top_k=%d with top_p=%g is not supported for deterministic drafts (need 1 <= top_k <= %d "
-                "and top_k < V)",
+                "and top_k < V, or top-k off with top_p = 1)",
                 top_k, (double)top_p, DFLASH_MAX_TOP_K);
+  const bool fullvocab = mode == kModeFullVocab;
   if ((rc = check_aligned(target_logits, esize_of(dtype), "target_logits"))) return rc;
-  const size_t need = verify_workspace(B, gamma, V, dtype);
+  const size_t need = verify_workspace(B, gamma, V, dtype, fullvocab);
   if (workspace_bytes < need)
     return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, need);
@@ -275,11 +276,14 @@ int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, in
   p.seed = seed;
   p.task = kTaskVerify;
   p.det = 1;
+  p.fullvocab = fullvocab ? 1 : 0;
   p.out_tokens = out_tokens;
   p.out_len = out_accept_len;
   p.status = status;
-  bind_workspace(p, workspace, B * (gamma + 1), B);
-  return run(p, B * (gamma + 1), stream);
+  bind_workspace(p, workspace, B * (gamma + 1), B, fullvocab);
+  rc = run(p, B * (gamma + 1), stream);
+  if (rc || !fullvocab) return rc;
+  return run_fullvocab_draw(p, workspace, stream);  // reads target rows only: no residual mode here
 }
 
 int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,

@@ -153,6 +153,7 @@ struct Req {
   ff inv_t;                // 1 / T
   ff zmx, zmy;             // row maxima / T
   float sx0, sy0;          // the stream's fp32 normalisers (residual: which side of p = q)
+  int excl;                // token with no weight in this draw (-1: none)
 };
 
 __device__ __forceinline__ Req load_req(const FvParams& f, int b) {
@@ -177,6 +178,7 @@ __device__ __forceinline__ Req load_req(const FvParams& f, int b) {
   q.zmy = ff_scale(d.my, q.inv_t);
   q.sx0 = d.sx0;
   q.sy0 = d.sy0;
+  q.excl = d.mode == kFvBonus ? d.excl : -1;
   return q;
 }
 
@@ -304,7 +306,8 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   } else {
 #pragma unroll
     for (int k = 0; k < kFvPerThread; ++k) {
-      const ff wx = weight(xs[k], q.inv_t, q.zmx, th, tl);
+      ff wx = weight(xs[k], q.inv_t, q.zmx, th, tl);
+      if (j0 + k * kFvThreads == q.excl) wx = {0.0f, 0.0f};  // p without the deterministic draft
       acc_add(sx, wx);
       if (wx.hi > 0.0f) lp = j0 + k * kFvThreads;
     }
@@ -450,6 +453,7 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   for (int k = 0; k < kFvPerThread; ++k) {
     ff p, r;
     token_weights(q, nm, xs[k], ys[k], th, tl, p, r);
+    if (jb + k == q.excl) p = {0.0f, 0.0f};
     wk[k] = resid ? r : p;
     mine = ff_add(mine, wk[k]);
   }

@@ -99,6 +99,7 @@ struct FvDraw {
   float my;    // largest logit of draft row n (residual)
   float sx0;   // the stream's (fp32) sum of exp((x - mx) / T) over target row n
   float sy0;   // the same over draft row n (residual)
+  int excl;    // a token the draw leaves out (a deterministic draft's residual), -1 for none
 };
 
 inline int fv_slices(int V) { return (V + kFvSlice - 1) / kFvSlice; }

@@ -1244,7 +1244,7 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
   if (lane == 0) {
     if (p.out_len) p.out_len[b] = n + 1;
     if (st && p.status) atomicOr(p.status, st);
-    if (p.fullvocab) p.fv_draw[b] = FvDraw{n, kFvNone, 0.0f, 0.0f, 0.0f, 0.0f};
+    if (p.fullvocab) p.fv_draw[b] = FvDraw{n, kFvNone, 0.0f, 0.0f, 0.0f, 0.0f, -1};
   }
 }
 
@@ -1257,7 +1257,8 @@ __device__ void greedy_request_final(const Params& p, Smem& S, int ord) {
 template <int DT>
 __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
   const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
-  const int gamma = p.gamma, V = p.geo.V, per_s = 2 * gamma + 1;
+  const int gamma = p.gamma, V = p.geo.V, per_s = samp_slots(p);
+  const bool det = p.det != 0;  // deterministic drafts: target rows only, q(d) = 1
   const int b = S.req_of_ord[ord];
   const int slot0 = ord * per_s;
   const float scale = kLog2e / ld_nc_now(p.temperature + b);  // as the producer computed it
@@ -1304,19 +1305,23 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     bool stop = false;
     if (lane < gamma) {
       const int i = lane;
+      const int ti = det ? i : 2 * i;  // position i's target row
       const int32_t di = d_lane;
       const bool valid = di >= 0 && di < V;
       if (!valid) st |= kStatusBadToken;
-      if (S.u.fv.bad[2 * i] || S.u.fv.bad[2 * i + 1]) {
+      if (S.u.fv.bad[ti] || (!det && S.u.fv.bad[2 * i + 1])) {
         stop = true;  // a bad row ends the loop at its position
       } else {
-        float p_d = 0.0f, q_d = 0.0f;  // a token outside the vocabulary has p = q = 0
+        // a token outside the vocabulary has p = q = 0; a deterministic draft has q = 1
+        float p_d = 0.0f, q_d = det ? 1.0f : 0.0f;
         if (valid) {
-          const SlotInfo sx = slot_info(p, S, slot0 + 2 * i);
-          const SlotInfo sy = slot_info(p, S, slot0 + 2 * i + 1);
-          p_d = ex2_approx((load_logit(sx.ptr, di, DT) - S.u.fv.m[2 * i]) * scale) / S.u.fv.s[2 * i];
-          q_d = ex2_approx((load_logit(sy.ptr, di, DT) - S.u.fv.m[2 * i + 1]) * scale) /
-                S.u.fv.s[2 * i + 1];
+          const SlotInfo sx = slot_info(p, S, slot0 + ti);
+          p_d = ex2_approx((load_logit(sx.ptr, di, DT) - S.u.fv.m[ti]) * scale) / S.u.fv.s[ti];
+          if (!det) {
+            const SlotInfo sy = slot_info(p, S, slot0 + 2 * i + 1);
+            q_d = ex2_approx((load_logit(sy.ptr, di, DT) - S.u.fv.m[2 * i + 1]) * scale) /
+                  S.u.fv.s[2 * i + 1];
+          }
         }
         const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
         stop = !(uniform24(wd.x) < p_d / q_d);  // q = 0: +inf if p > 0, NaN if p == 0
@@ -1324,15 +1329,21 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     }
     const uint32_t ball = __ballot_sync(0xffffffffu, stop);
     const int n = ball ? __ffs(ball) - 1 : gamma;
-    const bool bad_n = n < gamma ? (S.u.fv.bad[2 * n] || S.u.fv.bad[2 * n + 1]) : S.u.fv.bad[2 * gamma] != 0;
-    const int mode = bad_n ? kFvNone : (n < gamma ? kFvResidual : kFvBonus);
+    const int tn = det ? n : 2 * n;  // position n's target row (the bonus row when n == gamma)
+    const bool resid = n < gamma && !det;
+    const bool bad_n = S.u.fv.bad[tn] || (resid && S.u.fv.bad[2 * n + 1]);
+    // a deterministic draft's residual is p without d: the bonus-style draw
+    // over target row n with d left out
+    const int mode = bad_n ? kFvNone : (resid ? kFvResidual : kFvBonus);
+    const int32_t d_n = __shfl_sync(0xffffffffu, d_lane, n & 31);
+    const int excl = det && n < gamma ? d_n : -1;
     // the token at position n is the second pass's (0 when a bad row leaves no draw)
     for (int i = lane; i <= gamma; i += 32) out[i] = i < n ? d_lane : (i == n ? 0 : -1);
     st = __reduce_or_sync(0xffffffffu, st);
     if (lane == 0) {
       if (p.out_len) p.out_len[b] = n + 1;
-      p.fv_draw[b] = FvDraw{n, mode, S.u.fv.m[2 * n], n < gamma ? S.u.fv.m[2 * n + 1] : 0.0f, S.u.fv.s[2 * n],
-                            n < gamma ? S.u.fv.s[2 * n + 1] : 0.0f};
+      p.fv_draw[b] = FvDraw{n, mode, S.u.fv.m[tn], resid ? S.u.fv.m[2 * n + 1] : 0.0f, S.u.fv.s[tn],
+                            resid ? S.u.fv.s[2 * n + 1] : 0.0f, excl};
       if (st && p.status) atomicOr(p.status, st);
     }
   }

@@ -159,15 +159,15 @@ def test_det_status_bits_and_rejected_filters(dv):
     assert np.all((tok >= -1) & (tok < 3001)) and np.all((ln >= 1) & (ln <= 8))
     for b in (0, 2, 3):
         assert np.array_equal(tok[b], want_tok[b]) and ln[b] == want_len[b]
-    # the full-vocabulary filter and top-k beyond 32 are refused for
-    # deterministic drafts by the entry point itself, before any launch
+    # top-p over the whole vocabulary (top-k off, top_p < 1) and top-k
+    # beyond 32 are refused by the entry point itself, before any launch
     ws = dv.Workspace(dv.workspace_bytes(4, 7, 3001, dv.DFLASH_F32, 0, 1.0), DEV)
     Xd, dd = _t(X), torch.from_numpy(d).to(DEV)
     Td = torch.ones(4, dtype=torch.float32, device=DEV)
     out_t = torch.full((4, 8), -7, dtype=torch.int32, device=DEV)
     out_l = torch.zeros(4, dtype=torch.int32, device=DEV)
     lib = dv.load()
-    for k, tp in ((0, 1.0), (64, 0.95)):
+    for k, tp in ((0, 0.9), (64, 0.95)):
         rc = lib.dflash_verify_det(Xd.data_ptr(), dd.data_ptr(), 4, 7, 3001, dv.DFLASH_F32, Td.data_ptr(),
                                    k, tp, 1, out_t.data_ptr(), out_l.data_ptr(), ws.ptr, ws.nbytes, None,
                                    torch.cuda.current_stream().cuda_stream)
@@ -202,3 +202,98 @@ def test_det_workspace_left_zero_across_modes(dv):
         assert st == want_st
         _compare(tok, ln, want_tok, want_len, margin)
         assert int(torch.count_nonzero(ws.buf).item()) == 0, f"workspace not left at zero after V={V}"
+
+
+# ---------------------------------------------------------------- full vocabulary
+# Top-k off and top_p = 1: p is the softmax over all V tokens; a rejected
+# deterministic draft's residual is p without d, drawn over the whole
+# vocabulary in float-float like the general full-vocabulary draw. The bars
+# are that mode's: a mismatch only where the oracle's accept margin is below
+# 1e-4 or its draw margin below 2^-22 (about two fp32 ulps of u * total).
+ACCEPT_MARGIN = 1e-4
+DRAW_MARGIN = 2.0 ** -22
+
+
+def _check_det_fv(dv, X, d, T, seed, ws=None):
+    want_tok, want_len, (m_acc, m_draw), want_st = oracle.verify_det(X, d, T, 0, 1.0, seed, split_margins=True)
+    tok, ln, st = _run_det(dv, X, d, T, 0, 1.0, seed, workspace=ws)
+    assert st == want_st
+    g = ~((T > 0) & np.isfinite(T))
+    assert np.array_equal(tok[g], want_tok[g]) and np.array_equal(ln[g], want_len[g])
+    same = np.all(tok == want_tok, axis=1) & (ln == want_len)
+    bad = np.nonzero(~same)[0]
+    for b in bad:
+        assert m_acc[b] < ACCEPT_MARGIN or m_draw[b] < DRAW_MARGIN, (
+            f"request {b}: gpu {tok[b].tolist()} len {ln[b]} vs oracle {want_tok[b].tolist()} "
+            f"len {want_len[b]}, margins {m_acc[b]:.3g} / {m_draw[b]:.3g}")
+    return len(bad), tok, ln
+
+
+def _mixed_drafts(Y, seed, frac_random=0.3):
+    d = np.argmax(synth.to_float(Y), axis=-1).astype(np.int32)
+    rng = np.random.default_rng(seed)
+    V = Y.shape[2]
+    return np.where(rng.random(d.shape) < frac_random, rng.integers(0, V, d.shape), d).astype(np.int32)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("V,gamma", [(1024, 7), (777, 7), (20000, 15), (4097, 3), (1, 2), (33, 32)])
+def test_det_fullvocab_small(dv, dtype, V, gamma):
+    n_bad = 0
+    for data_seed in range(3):
+        X, Y, _ = synth.make_logits(9, gamma, V, dtype, data_seed=data_seed, sigma_d=0.5)
+        T = np.array([1.0, 0.0, 0.6, 1.0, 1.5, 0.0, 0.8, 1.0, 2.0], np.float32)
+        d = _mixed_drafts(Y, 60 + data_seed)
+        for seed in (data_seed, 555 + data_seed):
+            nb, _, _ = _check_det_fv(dv, X, d, T, seed)
+            n_bad += nb
+    assert n_bad <= 1
+
+
+def test_det_fullvocab_full_size(dv):
+    """Block 16, V = 248320, fp32, top-k off, top-p 1, 16 requests with
+    greedy-drafter drafts (a tenth replaced by uniform tokens)."""
+    X, Y, _ = synth.make_logits(16, 15, 248320, "f32", data_seed=7, sigma_d=0.5)
+    T = np.ones(16, np.float32)
+    d = _mixed_drafts(Y, 8, frac_random=0.1)
+    n_bad, tok, ln = _check_det_fv(dv, X, d, T, 3)
+    assert n_bad <= 1
+    # a rejected draft is never the token drawn in its place
+    for b in range(16):
+        n = ln[b] - 1
+        if n < 15:
+            assert tok[b, n] != d[b, n]
+
+
+def test_det_fullvocab_status_and_workspace(dv):
+    """Bad rows, tokens and temperatures set the same status bits as the
+    oracle, and full-vocabulary and top-k calls share one workspace, which
+    each leaves at zero."""
+    B, gamma, V = 5, 4, 6007
+    X, Y, _ = synth.make_logits(B, gamma, V, "f32", data_seed=41)
+    X = X.copy()
+    T = np.array([1.0, 1.0, 1.0, -2.0, 1.0], np.float32)
+    d = _mixed_drafts(Y, 2)
+    d[0, 1] = V
+    X[1, 3, 100] = np.nan
+    want_tok, want_len, (m_acc, m_draw), want_st = oracle.verify_det(X, d, T, 0, 1.0, 6, split_margins=True)
+    ws = dv.Workspace(48 << 20, DEV)
+    tok, ln, st = _run_det(dv, X, d, T, 0, 1.0, 6, workspace=ws)
+    assert st == want_st == (oracle.STATUS_BAD_TOKEN | oracle.STATUS_BAD_ROW
+                             | oracle.STATUS_BAD_TEMPERATURE)
+    assert np.all((tok >= -1) & (tok < V)) and np.all((ln >= 1) & (ln <= gamma + 1))
+    # the greedy request (bad temperature) exactly; request 2 (no bad input)
+    # within the draw's bars
+    assert np.array_equal(tok[3], want_tok[3]) and ln[3] == want_len[3]
+    assert (np.array_equal(tok[2], want_tok[2]) and ln[2] == want_len[2]) or \
+        m_acc[2] < ACCEPT_MARGIN or m_draw[2] < DRAW_MARGIN
+    assert int(torch.count_nonzero(ws.buf).item()) == 0
+    X2, Y2, _ = synth.make_logits(B, gamma, V, "f32", data_seed=42)
+    T2 = np.array([1.0, 0.0, 0.6, 1.0, 1.5], np.float32)
+    d2 = _mixed_drafts(Y2, 3)
+    for top_k, top_p in ((20, 0.95), (0, 1.0)):
+        if top_k:
+            _run_det(dv, X2, d2, T2, top_k, top_p, 1, workspace=ws)
+        else:
+            _check_det_fv(dv, X2, d2, T2, 1, ws=ws)
+        assert int(torch.count_nonzero(ws.buf).item()) == 0
