@@ -58,6 +58,12 @@ DET_DRAFTS = "deterministic: the argmax of each draft row (q = the point mass at
 UNIT = "verified draft positions/s"
 N_SETS = 3
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "verify_sweep_b32_mixed_v248320.md")
+
+
+def profile_summary(workload: str, det: bool = False) -> str:
+    """The committed ncu summary of sweep_kernel on a workload (with
+    deterministic drafts: the _det summary)."""
+    return os.path.join(ROOT, "profiles", f"verify_sweep_{workload}{'_det' if det else ''}.md")
 CSRC = os.path.join(ROOT, "speculative_decoding_verification_83_gb300", "csrc")
 
 
@@ -78,11 +84,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source."""
+def profiled_traffic(path: str = PROFILE_SUMMARY):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel source."""
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
@@ -364,7 +370,7 @@ def run_gpu(args):
     achieved = alg / avg_launch_s / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
-    traffic = profiled_traffic() if args.workload == WORKLOAD and not det else None
+    traffic = profiled_traffic(profile_summary(args.workload, det))
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
