@@ -106,6 +106,14 @@ size_t dflash_rows_workspace_bytes(int R, int V, int dtype, int top_k, float top
  * synchronised). */
 int dflash_workspace_init(void* workspace, size_t bytes, void* stream);
 
+/* Cancels the calls on a workspace: sets its abort flag on `stream`. Every
+ * bounded wait of a call on this workspace that starts after the flag is set
+ * (in stream order), or that runs meanwhile on another stream, gives up at
+ * once: the call ORs DFLASH_STATUS_TIMEOUT into its status word, lets its
+ * issued copies land, and returns with unspecified outputs. The workspace
+ * must be prepared again (dflash_workspace_init) before its next use. */
+int dflash_workspace_cancel(void* workspace, size_t bytes, void* stream);
+
 /* Batched verification (sampling, with greedy requests mixed in).
  *
  * target_logits [device] [B, gamma+1, V] dtype: target logits at the gamma

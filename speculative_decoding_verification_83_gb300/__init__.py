@@ -95,6 +95,7 @@ EXPORTS = {
     "dflash_workspace_bytes": ("z", "iiiiif"),
     "dflash_rows_workspace_bytes": ("z", "iiiif"),
     "dflash_workspace_init": ("i", "pzp"),
+    "dflash_workspace_cancel": ("i", "pzp"),
     "dflash_verify": ("i", "pppiiiipifQppp" "zpp"),
     "dflash_verify_det": ("i", "ppiiiipifQpppzpp"),
     "dflash_verify_greedy": ("i", "ppiiiipppzpp"),
@@ -210,6 +211,12 @@ class Workspace:
     def reset(self, stream=None):
         _check(load().dflash_workspace_init(self.buf.data_ptr(), self.nbytes,
                                             _stream_ptr(stream, self.buf.device)))
+
+    def cancel(self, stream=None):
+        """dflash_workspace_cancel: calls on this workspace give up their waits
+        and report DFLASH_STATUS_TIMEOUT; reset() before the next use."""
+        _check(load().dflash_workspace_cancel(self.buf.data_ptr(), self.nbytes,
+                                              _stream_ptr(stream, self.buf.device)))
 
     @property
     def ptr(self):

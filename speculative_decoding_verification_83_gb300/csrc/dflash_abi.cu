@@ -197,6 +197,18 @@ int dflash_workspace_init(void* workspace, size_t bytes, void* stream) {
   return DFLASH_OK;
 }
 
+int dflash_workspace_cancel(void* workspace, size_t bytes, void* stream) {
+  // the abort flag sits in the workspace's fixed header, at the same offset
+  // for every shape
+  const size_t off = make_layout(1, 1, make_geometry(1, 4)).abort_flag;
+  if (!workspace || bytes < off + sizeof(uint32_t))
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes has no abort flag", bytes);
+  cudaError_t e = cudaMemsetAsync(static_cast<unsigned char*>(workspace) + off, 1, sizeof(uint32_t),
+                                  (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "setting the abort flag");
+  return DFLASH_OK;
+}
+
 int dflash_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
                   int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
                   uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,

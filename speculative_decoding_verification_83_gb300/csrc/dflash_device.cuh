@@ -136,6 +136,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
   }
 }
+// Waits (bounded by time only) for the phase of `bar` with `parity`: the bulk
+// copies a CTA issued must land before its shared memory goes away, whatever
+// the abort flag says.
+__device__ __forceinline__ bool mbar_wait_landed(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0u && global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
 // both addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {

@@ -104,6 +104,7 @@ struct Smem {
   uint32_t digit;
   uint32_t digit_above;
   int bad_head_tail;
+  int cancelled;  // the workspace's abort flag was set before the call
 };
 
 // ---- row geometry ---------------------------------------------------------------
@@ -199,6 +200,7 @@ __device__ __forceinline__ int active_slots(const Params& p, const Smem& S) {
 // Request order (sampling first), built by all threads of the CTA.
 __device__ void build_request_order(const Params& p, Smem& S) {
   const int t = threadIdx.x;
+  if (t == 0) S.cancelled = *reinterpret_cast<const volatile uint32_t*>(p.abort_flag) != 0u ? 1 : 0;
   if (p.task != kTaskVerify && p.task != kTaskVerifyGreedy) {
     if (t == 0) S.n_samp = 0;
     return;
@@ -917,11 +919,14 @@ __device__ void producer(const Params& p, Smem& S, long long total) {
       }
     }
   }
-  if (aborted && lane == 0) {
-    // let copies already issued land before the CTA's shared memory goes away
+  if (lane == 0) {
+    // Every copy issued must land before the CTA's shared memory goes away,
+    // also when the consumers stopped early (abort or timeout, possibly after
+    // the last copy was issued). Only the last kStages can be in flight; in
+    // a call that ran through, they have landed already.
     const long long first = it > kStages ? it - kStages : 0;
     for (long long q = first; q < it; ++q)
-      (void)mbar_wait(&S.full[q % kStages], (uint32_t)((q / kStages) & 1), abort_flag);
+      (void)mbar_wait_landed(&S.full[q % kStages], (uint32_t)((q / kStages) & 1));
   }
 }
 
@@ -1451,6 +1456,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
   }
   build_request_order(p, S);  // contains __syncthreads
   __syncthreads();
+  if (S.cancelled) {  // a cancelled workspace: report, and leave before any copy is issued
+    if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+    return;
+  }
   const long long total = (long long)active_slots(p, S) * p.geo.ppr;
 
   if (warp < kConsumerWarps)
