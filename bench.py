@@ -176,6 +176,12 @@ def algorithmic_bytes(inp, accept_len=None, det=False) -> int:
     return rows * V * es
 
 
+def launches_per_step(top_k: int, top_p: float) -> int:
+    """Kernel launches of one verification call: the stream kernel, plus the
+    full-vocabulary draw's two launches when top-k is off and top-p is 1."""
+    return 3 if top_k <= 0 and top_p >= 1.0 else 1
+
+
 def cpu_baseline(inp, d, workload, threads=None, det=False):
     """The oracle (as it stands) on the host cores: one full batch."""
     import oracle
@@ -454,7 +460,7 @@ def run_gpu(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step(top_k, top_p),
         "clocks": clk,
         "mean_accept_len_last_step": float(lens.mean()),
     }

@@ -31,3 +31,8 @@ def test_profile_lookup_names():
     assert bench.profile_summary("b32_mixed_v248320") == bench.PROFILE_SUMMARY
     assert bench.profile_summary("b32_mixed_v248320", det=True).endswith("verify_sweep_b32_mixed_v248320_det.md")
     assert bench.profiled_traffic(bench.profile_summary("no_such_workload")) is None
+
+
+def test_launches_per_step():
+    assert bench.launches_per_step(20, 0.95) == 1
+    assert bench.launches_per_step(0, 1.0) == 3
