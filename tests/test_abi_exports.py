@@ -70,3 +70,9 @@ def test_argument_checks_happen_on_the_host(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         dv.load(str(tmp_path / "absent.so"))
+
+
+def test_cancel_refuses_a_buffer_without_the_header(lib):
+    assert lib.dflash_workspace_cancel(None, 1 << 20, None) == dv.ERR_INVALID_ARG
+    assert lib.dflash_workspace_cancel(ctypes.c_void_p(256), 64, None) == dv.ERR_INVALID_ARG
+    assert b"abort flag" in lib.dflash_last_error()
