@@ -61,9 +61,9 @@ def _bind(lib):
     lib.oracle_filter_row_sparse.restype = I
     lib.oracle_verify.argtypes = [P, P, P, I, I, I, I, P, I, F, U64, P, P, P, P, I, I]
     lib.oracle_verify.restype = I
-    lib.oracle_verify_margins.argtypes = [P, P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, I, I]
+    lib.oracle_verify_margins.argtypes = [P, P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, P, I, I]
     lib.oracle_verify_margins.restype = I
-    lib.oracle_verify_det_margins.argtypes = [P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, I, I]
+    lib.oracle_verify_det_margins.argtypes = [P, P, I, I, I, I, P, I, F, U64, P, P, P, P, P, P, I, I]
     lib.oracle_verify_det_margins.restype = I
     lib.oracle_verify_greedy.argtypes = [P, P, I, I, I, I, P, P, P, I, I]
     lib.oracle_verify_greedy.restype = I
@@ -178,7 +178,7 @@ def _ranges(n: int, parts: int):
 
 
 def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads=None,
-           requests=None, lib=None, split_margins=False):
+           requests=None, lib=None, split_margins=False, cut_margin=False):
     """Sampling-mode verification (greedy for requests with temperature 0).
 
     Returns (tokens [B, gamma+1], accept_len [B], margin [B], status).
@@ -186,6 +186,8 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
     those requests; the other rows of the outputs stay -1 / 0.
     With ``split_margins`` the third item is the pair (accept margin [B],
     draw margin [B]): the accept tests and top-p cuts, and the final draw.
+    With ``cut_margin`` it is the triple (accept [B], cut [B], draw [B]):
+    the accept tests alone, the top-p cuts, and the final draw.
     """
     lib = lib or _load()
     X = _contig(target)
@@ -201,6 +203,7 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
     lens = np.zeros(B, np.int32)
     margin = np.full(B, np.inf, np.float64)
     margin_draw = np.full(B, np.inf, np.float64)
+    margin_cut = np.full(B, np.inf, np.float64)
     nthreads = threads or default_threads()
     if requests is None:
         todo = _ranges(B, nthreads * 4)
@@ -211,7 +214,8 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
         st = np.zeros(1, np.uint32)
         rc = lib.oracle_verify_margins(_ptr(X), _ptr(Y), _ptr(d), B, gamma, V, dt, _ptr(T),
                                        int(top_k), float(top_p), int(seed), _ptr(tokens),
-                                       _ptr(lens), _ptr(margin), _ptr(margin_draw), _ptr(st),
+                                       _ptr(lens), _ptr(margin), _ptr(margin_draw),
+                                       _ptr(margin_cut) if cut_margin else None, _ptr(st),
                                        rng[0], rng[1])
         if rc != 0:
             raise RuntimeError(f"oracle_verify failed: {rc}")
@@ -225,13 +229,15 @@ def verify(target, draft, draft_tokens, temperature, top_k, top_p, seed, threads
     status = 0
     for s in statuses:
         status |= s
+    if cut_margin:
+        return tokens, lens, (margin, margin_cut, margin_draw), status
     if split_margins:
         return tokens, lens, (margin, margin_draw), status
     return tokens, lens, np.minimum(margin, margin_draw), status
 
 
 def verify_det(target, draft_tokens, temperature, top_k, top_p, seed, threads=None, lib=None,
-               split_margins=False):
+               split_margins=False, cut_margin=False):
     """Verification of deterministic drafts (q = the point mass at each draft
     token; no draft logits). Returns (tokens, accept_len, margin, status) as
     ``verify``."""
@@ -247,6 +253,7 @@ def verify_det(target, draft_tokens, temperature, top_k, top_p, seed, threads=No
     lens = np.zeros(B, np.int32)
     margin = np.full(B, np.inf, np.float64)
     margin_draw = np.full(B, np.inf, np.float64)
+    margin_cut = np.full(B, np.inf, np.float64)
     nthreads = threads or default_threads()
     todo = _ranges(B, nthreads * 4)
 
@@ -254,7 +261,8 @@ def verify_det(target, draft_tokens, temperature, top_k, top_p, seed, threads=No
         st = np.zeros(1, np.uint32)
         rc = lib.oracle_verify_det_margins(_ptr(X), _ptr(d), B, gamma, V, dt, _ptr(T), int(top_k),
                                            float(top_p), int(seed), _ptr(tokens), _ptr(lens),
-                                           _ptr(margin), _ptr(margin_draw), _ptr(st), rng[0], rng[1])
+                                           _ptr(margin), _ptr(margin_draw),
+                                           _ptr(margin_cut) if cut_margin else None, _ptr(st), rng[0], rng[1])
         if rc != 0:
             raise RuntimeError(f"oracle_verify_det failed: {rc}")
         return int(st[0])
@@ -267,6 +275,8 @@ def verify_det(target, draft_tokens, temperature, top_k, top_p, seed, threads=No
     status = 0
     for st_ in statuses:
         status |= st_
+    if cut_margin:
+        return tokens, lens, (margin, margin_cut, margin_draw), status
     if split_margins:
         return tokens, lens, (margin, margin_draw), status
     return tokens, lens, np.minimum(margin, margin_draw), status

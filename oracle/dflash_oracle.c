@@ -315,11 +315,24 @@ int oracle_verify_greedy(const void* target, const int32_t* draft_tokens, int B,
   return ORC_OK;
 }
 
+/* A request's margins: with margin_cut given, the accept tests' and the
+ * top-p cuts' apart; without it, margin_accept holds the smaller of the two. */
+static void store_margins(int b, double accept, double cut, double draw, double* margin_accept,
+                          double* margin_cut, double* margin_draw) {
+  if (margin_cut) {
+    margin_cut[b] = cut;
+    if (margin_accept) margin_accept[b] = accept;
+  } else if (margin_accept) {
+    margin_accept[b] = accept < cut ? accept : cut;
+  }
+  if (margin_draw) margin_draw[b] = draw;
+}
+
 int oracle_verify_margins(const void* target, const void* draft, const int32_t* draft_tokens,
                           int B, int gamma, int V, int dtype, const float* temperature, int top_k,
                           float top_p, uint64_t seed, int32_t* out_tokens,
                           int32_t* out_accept_len, double* margin_accept, double* margin_draw,
-                          uint32_t* status, int b_begin, int b_end) {
+                          double* margin_cut, uint32_t* status, int b_begin, int b_end) {
   if (!target || !draft || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
       B < 0 || gamma < 1 || V < 1 || !(top_p > 0.0f))
     return ORC_ERR_INVALID_ARG;
@@ -343,12 +356,12 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
     const char* Yb = (const char*)draft + (size_t)b * (size_t)gamma * row_bytes;
     const int32_t* d = draft_tokens + (size_t)b * gamma;
     int32_t* out = out_tokens + (size_t)b * (gamma + 1);
-    double mg = DBL_MAX;   /* accept tests and top-p cuts */
+    double mg = DBL_MAX;   /* accept tests */
+    double mgc = DBL_MAX;  /* top-p cuts */
     double mgd = DBL_MAX;  /* the final inverse-CDF draw */
     if (!temperature_kind(temperature[b], &st)) {
       greedy_request(Xb, d, gamma, V, dtype, out, out_accept_len + b, &st);
-      if (margin_accept) margin_accept[b] = mg;
-      if (margin_draw) margin_draw[b] = mgd;
+      store_margins(b, mg, mgc, mgd, margin_accept, margin_cut, margin_draw);
       continue;
     }
     const double T = (double)temperature[b];
@@ -367,8 +380,8 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
     int32_t last = -1;
     int rejected = 0;
     for (int i = 0; i < gamma; ++i) {
-      int np = filter_dense(Xb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, p, &mg);
-      int nq = filter_dense(Yb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, q, &mg);
+      int np = filter_dense(Xb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, p, &mgc);
+      int nq = filter_dense(Yb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, q, &mgc);
       if (np < 0 || nq < 0) { /* bad row: output unspecified, keep it in range */
         last = oracle_argmax_row(Xb + (size_t)i * row_bytes, V, dtype, NULL);
         rejected = 1;
@@ -396,7 +409,7 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
       break;
     }
     if (!rejected) {
-      int np = filter_dense(Xb + (size_t)gamma * row_bytes, V, dtype, T, top_k, top_p, p, &mg);
+      int np = filter_dense(Xb + (size_t)gamma * row_bytes, V, dtype, T, top_k, top_p, p, &mgc);
       if (np < 0) {
         last = oracle_argmax_row(Xb + (size_t)gamma * row_bytes, V, dtype, NULL);
       } else {
@@ -407,8 +420,7 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
     }
     out[n] = last;
     out_accept_len[b] = n + 1;
-    if (margin_accept) margin_accept[b] = mg;
-    if (margin_draw) margin_draw[b] = mgd;
+    store_margins(b, mg, mgc, mgd, margin_accept, margin_cut, margin_draw);
   }
   free(p);
   free(q);
@@ -429,8 +441,8 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
 int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, int B, int gamma,
                               int V, int dtype, const float* temperature, int top_k, float top_p,
                               uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
-                              double* margin_accept, double* margin_draw, uint32_t* status,
-                              int b_begin, int b_end) {
+                              double* margin_accept, double* margin_draw, double* margin_cut,
+                              uint32_t* status, int b_begin, int b_end) {
   if (!target || !draft_tokens || !temperature || !out_tokens || !out_accept_len || B < 0 ||
       gamma < 1 || V < 1 || !(top_p > 0.0f))
     return ORC_ERR_INVALID_ARG;
@@ -451,11 +463,10 @@ int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, i
     const char* Xb = (const char*)target + (size_t)b * (size_t)(gamma + 1) * row_bytes;
     const int32_t* d = draft_tokens + (size_t)b * gamma;
     int32_t* out = out_tokens + (size_t)b * (gamma + 1);
-    double mg = DBL_MAX, mgd = DBL_MAX;
+    double mg = DBL_MAX, mgc = DBL_MAX, mgd = DBL_MAX;  /* accept tests, top-p cuts, the draw */
     if (!temperature_kind(temperature[b], &st)) {
       greedy_request(Xb, d, gamma, V, dtype, out, out_accept_len + b, &st);
-      if (margin_accept) margin_accept[b] = mg;
-      if (margin_draw) margin_draw[b] = mgd;
+      store_margins(b, mg, mgc, mgd, margin_accept, margin_cut, margin_draw);
       continue;
     }
     const double T = (double)temperature[b];
@@ -469,7 +480,7 @@ int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, i
     int n = 0, rejected = 0;
     int32_t last = -1;
     for (int i = 0; i < gamma; ++i) {
-      if (filter_dense(Xb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, p, &mg) < 0) {
+      if (filter_dense(Xb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, p, &mgc) < 0) {
         last = oracle_argmax_row(Xb + (size_t)i * row_bytes, V, dtype, NULL);
         rejected = 1;
         break;
@@ -495,7 +506,7 @@ int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, i
       break;
     }
     if (!rejected) {
-      if (filter_dense(Xb + (size_t)gamma * row_bytes, V, dtype, T, top_k, top_p, p, &mg) < 0) {
+      if (filter_dense(Xb + (size_t)gamma * row_bytes, V, dtype, T, top_k, top_p, p, &mgc) < 0) {
         last = oracle_argmax_row(Xb + (size_t)gamma * row_bytes, V, dtype, NULL);
       } else {
         float u_draw;
@@ -505,8 +516,7 @@ int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, i
     }
     out[n] = last;
     out_accept_len[b] = n + 1;
-    if (margin_accept) margin_accept[b] = mg;
-    if (margin_draw) margin_draw[b] = mgd;
+    store_margins(b, mg, mgc, mgd, margin_accept, margin_cut, margin_draw);
   }
   free(p);
   free(r);
@@ -521,7 +531,7 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
                   uint32_t* status, int b_begin, int b_end) {
   if (!margin)
     return oracle_verify_margins(target, draft, draft_tokens, B, gamma, V, dtype, temperature,
-                                 top_k, top_p, seed, out_tokens, out_accept_len, NULL, NULL,
+                                 top_k, top_p, seed, out_tokens, out_accept_len, NULL, NULL, NULL,
                                  status, b_begin, b_end);
   if (b_begin < 0) b_begin = 0;
   if (b_end > B) b_end = B;
@@ -529,7 +539,7 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
   double* md = (double*)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1));
   if (!md) return ORC_ERR_NOMEM;
   int rc = oracle_verify_margins(target, draft, draft_tokens, B, gamma, V, dtype, temperature,
-                                 top_k, top_p, seed, out_tokens, out_accept_len, margin, md,
+                                 top_k, top_p, seed, out_tokens, out_accept_len, margin, md, NULL,
                                  status, b_begin, b_end);
   for (int i = 0; i < n && rc == ORC_OK; ++i)
     if (md[b_begin + i] < margin[b_begin + i]) margin[b_begin + i] = md[b_begin + i];

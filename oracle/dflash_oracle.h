@@ -83,16 +83,19 @@ int oracle_verify(const void* target, const void* draft, const int32_t* draft_to
                   uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, double* margin,
                   uint32_t* status, int b_begin, int b_end);
 
-/* oracle_verify with the decision margins split: margin_accept ([B],
- * optional) covers the accept tests and the top-p cuts, margin_draw ([B],
- * optional) the final residual or bonus draw. Over the full vocabulary the
- * draw's cumulative weights are a few parts per million apart, so its margin
- * is small on every row while the accept margins are not. */
+/* oracle_verify with the decision margins split: margin_draw ([B], optional)
+ * covers the final residual or bonus draw; margin_cut ([B], optional) the
+ * top-p cuts of every row the request filters (the mass before a token
+ * grows along the sorted order, so the smallest gap is at the cut itself);
+ * margin_accept ([B], optional) the accept tests, and also the cuts when
+ * margin_cut is NULL. Over the full vocabulary neighbouring cumulative
+ * weights are a few parts per million apart, so the draw's and the cuts'
+ * margins are small on every row while the accept margins are not. */
 int oracle_verify_margins(const void* target, const void* draft, const int32_t* draft_tokens,
                           int B, int gamma, int V, int dtype, const float* temperature, int top_k,
                           float top_p, uint64_t seed, int32_t* out_tokens,
                           int32_t* out_accept_len, double* margin_accept, double* margin_draw,
-                          uint32_t* status, int b_begin, int b_end);
+                          double* margin_cut, uint32_t* status, int b_begin, int b_end);
 
 /* Verification of deterministic drafts (q = the point mass at d_i): accept
  * d_i when u < p_i(d_i); at the first rejection draw from p_i with d_i taken
@@ -101,8 +104,8 @@ int oracle_verify_margins(const void* target, const void* draft, const int32_t* 
 int oracle_verify_det_margins(const void* target, const int32_t* draft_tokens, int B, int gamma,
                               int V, int dtype, const float* temperature, int top_k, float top_p,
                               uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
-                              double* margin_accept, double* margin_draw, uint32_t* status,
-                              int b_begin, int b_end);
+                              double* margin_accept, double* margin_draw, double* margin_cut,
+                              uint32_t* status, int b_begin, int b_end);
 
 /* Greedy verification: argmax prefix match, requests [b_begin, b_end). */
 int oracle_verify_greedy(const void* target, const int32_t* draft_tokens, int B, int gamma, int V,

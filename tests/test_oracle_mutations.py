@@ -15,6 +15,7 @@ import oracle
 import test_oracle_filter as F
 import test_oracle_philox as P
 import test_oracle_det as DD
+import test_oracle_margins as MM
 import test_oracle_verify as VV
 
 MUTATIONS = {
@@ -44,6 +45,9 @@ MUTATIONS = {
         "oracle_uniforms(seed, (uint32_t)b, (uint32_t)i, 0u, &u_acc, &u_draw);\n      update_margin(&mg, (double)u_acc, p_d);",
         "oracle_uniforms(seed, (uint32_t)b, (uint32_t)i, 0u, &u_draw, &u_acc);\n      update_margin(&mg, (double)u_acc, p_d);"),
     "det_accept_slack": ("if (u_acc < (float)p_d) {", "if (u_acc < (float)p_d + 0.02f) {"),
+    "cut_margin_into_accept": ("      int nq = filter_dense(Yb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, q, &mgc);",
+                               "      int nq = filter_dense(Yb + (size_t)i * row_bytes, V, dtype, T, top_k, top_p, q, &mg);"),
+    "margins_not_split": ("  if (margin_cut) {\n    margin_cut[b] = cut;", "  if (0) {\n    margin_cut[b] = cut;"),
 }
 
 
@@ -62,6 +66,8 @@ def _pin_checks(curand_pin):
         ("uniforms_uniform", P.test_uniforms_are_uniform_and_independent),
         ("det_point_mass", lambda: DD.test_det_equals_general_rule_with_point_mass_drafts(20, 0.95)),
         ("det_law", lambda: DD.test_det_accept_length_and_token_laws(*DD.DET_LAW_CASES[3])),
+        ("cut_margin", lambda: MM.test_cut_margin_closed_form(4, 0.6)),
+        ("accept_margin", MM.test_accept_margin_alone_is_the_uniforms_gap),
     ]
 
 
