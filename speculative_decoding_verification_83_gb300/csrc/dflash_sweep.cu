@@ -36,7 +36,13 @@
 // Every wait is time-bounded; row finals wait only on the stream, and a
 // request final only on row finals drawn before it, so there is no cycle of
 // waits and no grid-wide barrier. Every successful call leaves the workspace
-// at zero.
+// at zero. A CTA that finds the workspace's abort flag set in its prologue
+// (a cancelled workspace) reports a timeout and returns before any copy;
+// otherwise the producer waits for its last copies to land before it returns.
+//
+// The same kernel serves deterministic drafts (sampling requests stream their
+// target rows only) and, as rows tasks, the filtered rows, the sampler and a
+// vocabulary shard's top-k candidates.
 //
 // The method follows "DFlash2 用投机解码给 Qwen 提速" (bml.asia, draft/verify
 // loop and model-card settings) and "无损加速是真的吗？Qwen3.8-27B-DFlash2
