@@ -471,7 +471,7 @@ static int rows_task(int task, const void* logits, int R, int V, int dtype, cons
                                                       workspace, status, stream);
   Params p = base_params(dtype, V);
   p.temperature = temperature;
-  p.gamma = 1;
+  p.gamma = 1;  // unused by the rows tasks (a row is its own slot); any valid value
   p.top_k = top_k;
   p.top_p = top_p >= 1.0f ? 1.0f : top_p;
   p.seed = seed;
@@ -531,7 +531,7 @@ static int candidates_pass(const void* logits, int R, int V_shard, int dtype, in
                            float* out_logit, int32_t* out_token, float* out_max, void* workspace, uint32_t* status,
                            void* stream) {
   Params p = base_params(dtype, V_shard);
-  p.gamma = 1;
+  p.gamma = 1;  // unused by the rows tasks (a row is its own slot); any valid value
   p.top_k = k;
   p.top_p = 1.0f;
   p.task = kTaskCandidates;
