@@ -240,7 +240,7 @@ def verify_det(target, draft_tokens, temperature, top_k, top_p, seed, threads=No
                split_margins=False, cut_margin=False):
     """Verification of deterministic drafts (q = the point mass at each draft
     token; no draft logits). Returns (tokens, accept_len, margin, status) as
-    ``verify``."""
+    ``verify``, with the same ``split_margins`` and ``cut_margin`` options."""
     lib = lib or _load()
     X = _contig(target)
     d = _contig(draft_tokens, np.int32)
