@@ -206,6 +206,34 @@ def cpu_baseline(inp, d, workload, threads=None, det=False, min_s=10.0, max_batc
                       f"{threads} host threads), {dt:.1f} s"}
 
 
+def accept_report(sets_np, lens_by_set, det=False):
+    """Accept lengths of the timed steps (each input set's batch; its seed is
+    fixed, so every step on it gives the same lengths): their histogram over
+    1..gamma+1 and mean, next to the closed-form mean sum_i prod_{j<i} alpha_j
+    with alpha_j = sum min(p_j, q_j) from the oracle's filtered distributions
+    of the same rows (greedy requests enter with their own length, which is
+    not random). With deterministic drafts q is the point mass at the draft,
+    so alpha_j = p_j(d_j)."""
+    import oracle
+
+    B, gamma, V = sets_np[0].shape
+    lens = np.concatenate(lens_by_set)
+    hist = np.bincount(lens, minlength=gamma + 2)[1:gamma + 2]
+    closed = []
+    for inp, ln in zip(sets_np, lens_by_set):
+        if det:
+            return {"hist": hist.tolist(), "mean": float(lens.mean()), "closed_form_mean": None,
+                    "requests": int(lens.size)}
+        alpha = oracle.accept_rates(inp.target, inp.draft, inp.temperature, inp.top_k, inp.top_p)
+        e = oracle.expected_accept_len(np.nan_to_num(alpha, nan=0.0))
+        samp = inp.temperature > 0
+        closed.append(np.where(samp, e, ln))
+    closed = np.concatenate(closed)
+    return {"hist": hist.tolist(), "mean": float(lens.mean()), "closed_form_mean": float(closed.mean()),
+            "requests": int(lens.size),
+            "note": "closed form over the drafts' distribution: the sampled drafts are one draw of it"}
+
+
 def combine_over_ranks(region_ms: float, e2e_s: float, steps: int, per_rank_units: int, device=None):
     """Whole-job numbers from this rank's timings: the slowest rank's timed
     region and end-to-end step (max over ranks; every rank verifies its own
@@ -353,41 +381,59 @@ def run_gpu(args):
     if int(status.item()) != 0:
         raise RuntimeError(f"status word {int(status.item())} after warm-up")
 
-    # ---- timed region: K steps back to back, one event pair per launch
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
+    # ---- timed region: K steps back to back (no event between launches, so
+    # each launch may overlap the end of the one before it: programmatic
+    # dependent launch), bracketed by one event pair on the launching stream
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     time.sleep(0.3)
+    # a spin kernel ahead of the start event keeps the device busy while the
+    # host enqueues the K calls, so the region times the device, not the
+    # host's first launch (it ends before the start event is recorded)
+    torch.cuda._sleep(int(2e6))
     start.record(stream)
     for i in range(args.steps):
-        evs[i][0].record(stream)
         step(i)
-        evs[i][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
     clk = clocks.stop()
     if world > 1:
         torch.distributed.barrier()
     region_ms = start.elapsed_time(end)
-    launch_ms = np.array([a.elapsed_time(b) for a, b in evs])
 
-    # ---- roofline of the kernel (one launch = one step)
-    alg = algorithmic_bytes(sets_np[(args.steps - 1) % N_SETS], out_len.cpu().numpy(), det)
-    avg_launch_s = float(launch_ms.mean()) / 1e3
+    # ---- roofline of the kernel: algorithmic bytes of one call over the
+    # average call duration in the timed region (one call = one launch of the
+    # stream kernel; plus the two draw launches over the full vocabulary)
+    lens_by_set = []
+    for s in range(N_SETS):  # the outputs of each input set (its seed is fixed, so every step on it gives these)
+        step(s)
+        torch.cuda.synchronize()
+        lens_by_set.append(out_len.cpu().numpy().copy())
+    alg = algorithmic_bytes(sets_np[(args.steps - 1) % N_SETS], lens_by_set[(args.steps - 1) % N_SETS], det)
+    avg_launch_s = region_ms / args.steps / 1e3
     achieved = alg / avg_launch_s / 1e9
     peaks, peak_kind = measured_peaks()
     peak = float(peaks.get("hbm_gbs", 6800.0))
     traffic = profiled_traffic(profile_summary(args.workload, det))
+    # an isolated call (an event pair around each of a few launches, which
+    # rules out overlap with the launch before): for reference, not timed above
+    n_iso = min(200, max(20, args.steps))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_iso)]
+    for i in range(n_iso):
+        evs[i][0].record(stream)
+        step(i)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    iso_ms = np.array([a.elapsed_time(b) for a, b in evs])
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_us": avg_launch_s * 1e6,
-                "p50_launch_us": float(np.median(launch_ms)) * 1e3}
+                "isolated_launch_us_p50": float(np.median(iso_ms)) * 1e3}
 
     # ---- end to end through the host-buffer entry point (pinned host memory)
     inp = sets_np[0]
@@ -443,9 +489,12 @@ def run_gpu(args):
             torch.distributed.barrier()
             torch.distributed.destroy_process_group()
         return 0
-    lens = out_len.cpu().numpy()
-    cpu = (cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy(), args.workload, det=det)
-           if world == 1 else None)
+    cpu, accept = None, None
+    if world == 1:
+        cpu = cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy(), args.workload, det=det)
+        cpu["single_core"] = cpu_baseline(sets_np[0], sets_dev[0][2].cpu().numpy(), args.workload, threads=1,
+                                          det=det, min_s=5.0, max_batches=2)
+        accept = accept_report(sets_np, lens_by_set, det)
     T0 = sets_np[0].temperature
     temps = ("cycling " + " / ".join(f"{t:g}" + (" (greedy)" if t == 0 else "")
                                      for t in dict.fromkeys(T0.tolist()))
@@ -467,7 +516,7 @@ def run_gpu(args):
         "e2e": e2e,
         "gpu_launches": args.steps * launches_per_step(top_k, top_p),
         "clocks": clk,
-        "mean_accept_len_last_step": float(lens.mean()),
+        "accept_len": accept,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -171,6 +171,47 @@ def filter_row_sparse(row: np.ndarray, temperature: float, top_k: int, top_p: fl
     return idx[:n].copy(), prob[:n].copy()
 
 
+def accept_rates(target, draft, temperature, top_k, top_p, threads=None, lib=None):
+    """Per (request, draft position) probability that the draft token is
+    accepted when it is a sample of q: alpha = sum_v min(p(v), q(v)) over the
+    filtered target and draft distributions (standard speculative sampling;
+    the accept rule of "DFlash2 用投机解码给 Qwen 提速", bml.asia, the
+    draft/verify loop). Greedy requests (temperature 0) get NaN: their accept
+    length is the argmax prefix match, not a random variable. Returns [B, gamma]."""
+    lib = lib or _load()
+    X = _contig(target)
+    Y = _contig(draft)
+    T = np.asarray(temperature, np.float32)
+    B, g1, V = X.shape
+    gamma = g1 - 1
+    alpha = np.full((B, gamma), np.nan, np.float64)
+    jobs = [(b, i) for b in range(B) if T[b] > 0 and np.isfinite(T[b]) for i in range(gamma)]
+
+    def run(job):
+        b, i = job
+        p = filter_row(X[b, i], float(T[b]), top_k, top_p, lib=lib)
+        q = filter_row(Y[b, i], float(T[b]), top_k, top_p, lib=lib)
+        alpha[b, i] = np.nan if p is None or q is None else float(np.minimum(p, q).sum())
+
+    nthreads = threads or default_threads()
+    if nthreads <= 1:
+        for j in jobs:
+            run(j)
+    else:
+        with ThreadPoolExecutor(nthreads) as ex:
+            list(ex.map(run, jobs))
+    return alpha
+
+
+def expected_accept_len(alpha) -> np.ndarray:
+    """Closed-form mean accept length of each request from its accept rates:
+    the step emits position i (i = 0..gamma) when every draft before it was
+    accepted, so E[len] = sum_{i=0}^{gamma} prod_{j<i} alpha_j."""
+    a = np.asarray(alpha, np.float64)
+    surv = np.concatenate([np.ones((a.shape[0], 1)), np.cumprod(a, axis=1)], axis=1)
+    return surv.sum(axis=1)
+
+
 def _ranges(n: int, parts: int):
     parts = max(1, min(parts, n))
     step = (n + parts - 1) // parts

@@ -2,6 +2,7 @@
 // argument checks, workspace layout, launch configuration and the host-buffer
 // path. No device memory is allocated here; every buffer belongs to the caller.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -9,6 +10,8 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "../../include/dflash_verify.h"
 #include "dflash_internal.h"
@@ -27,23 +30,64 @@ int fail(int code, const char* fmt, ...) {
   return code;
 }
 
+// An NVTX range around an entry point's host work and launches, so that a
+// timeline profiler shows each call by name (a no-op without a profiler).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+
 int cuda_fail(cudaError_t e, const char* what) {
   return fail(DFLASH_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-int sm_count() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+// SMs the calling thread's current context may use: all of the device's
+// for a primary context, the partition's for a green context (from the
+// driver's resource query, reached through the runtime so the library does
+// not link the driver). Cached per context.
+typedef int (*CtxGetCurrentFn)(CUcontext*);
+typedef int (*CtxGetDevResourceFn)(CUcontext, CUdevResource*, CUdevResourceType);
+
+int available_sms(int dev) {
   static std::mutex mu;
-  static int cached[64] = {0};
+  static bool looked_up = false;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetDevResourceFn get_resource = nullptr;
+  static CUcontext ctx_cache[kMaxDevices * 4] = {};
+  static int sms_cache[kMaxDevices * 4] = {};
   std::lock_guard<std::mutex> lock(mu);
-  if (dev < 0 || dev >= 64) return 0;
-  if (cached[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    cached[dev] = n;
+  if (!looked_up) {
+    looked_up = true;
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12040, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetDevResource", &f, 12040, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_resource = reinterpret_cast<CtxGetDevResourceFn>(f);
   }
-  return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_resource || get_current(&ctx) != 0 || !ctx) return n;
+  for (int i = 0; i < kMaxDevices * 4 && ctx_cache[i]; ++i)
+    if (ctx_cache[i] == ctx) return sms_cache[i];
+  CUdevResource res;
+  memset(&res, 0, sizeof res);
+  if (get_resource(ctx, &res, CU_DEV_RESOURCE_TYPE_SM) == 0 && res.sm.smCount > 0 &&
+      (int)res.sm.smCount < n)
+    n = (int)res.sm.smCount;
+  for (int i = 0; i < kMaxDevices * 4; ++i)
+    if (!ctx_cache[i]) {
+      ctx_cache[i] = ctx;
+      sms_cache[i] = n;
+      break;
+    }
+  return n;
 }
 
 int esize_of(int dtype) { return dtype == DFLASH_BF16 ? 2 : (dtype == DFLASH_F32 ? 4 : 0); }
@@ -141,12 +185,19 @@ int run_fullvocab_draw(const Params& p, void* ws, void* stream, bool sampler = f
 }
 
 int run(Params& p, int total_slots, void* stream) {
-  const int sms = sm_count();
-  if (sms <= 0) return fail(DFLASH_ERR_CUDA, "no CUDA device");
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "no CUDA device");
+  if (dev < 0 || dev >= kMaxDevices) return fail(DFLASH_ERR_CUDA, "device %d beyond the supported %d", dev, kMaxDevices);
+  int per_sm = 0;
+  const int e_occ = sweep_occupancy(p.dtype, dev, &per_sm);
+  if (e_occ != 0) return cuda_fail((cudaError_t)e_occ, "sizing the verification kernel");
+  const int sms = available_sms(dev);
   const long long pieces = (long long)total_slots * p.geo.ppr;
-  long long grid = (long long)sms * kCtasPerSm;
-  if (grid > pieces) grid = pieces;
-  if (grid < 1) grid = 1;
+  const long long grid = persistent_grid(pieces, sms, per_sm < kCtasPerSm ? per_sm : kCtasPerSm);
+  if (grid < 1)
+    return fail(DFLASH_ERR_CUDA, "the verification kernel does not fit on this device's SMs (%d SMs, %d CTAs each)",
+                sms, per_sm);
   const int e = launch_sweep(p, (int)grid, stream);
   if (e != 0) return cuda_fail((cudaError_t)e, "launching the verification kernel");
   return DFLASH_OK;
@@ -213,6 +264,7 @@ int dflash_verify(const void* target_logits, const void* draft_logits, const int
                   int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
                   uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                   size_t workspace_bytes, uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_verify");
   int rc = check_shape(B, gamma, V, dtype);
   if (rc) return rc;
   if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
@@ -260,6 +312,7 @@ int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, in
                       int dtype, const float* temperature, int top_k, float top_p, uint64_t seed,
                       int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
                       uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_verify_det");
   int rc = check_shape(B, gamma, V, dtype);
   if (rc) return rc;
   if (!target_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len || !workspace)
@@ -301,6 +354,7 @@ int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, in
 int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
                          int dtype, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                          size_t workspace_bytes, uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_verify_greedy");
   int rc = check_shape(B, gamma, V, dtype);
   if (rc) return rc;
   if (!target_logits || !draft_tokens || !out_tokens || !out_accept_len || !workspace)
@@ -344,6 +398,7 @@ int dflash_verify_host(const void* target_logits, const void* draft_logits, cons
                        uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, uint32_t* out_status,
                        void* staging, size_t staging_bytes, void* workspace, size_t workspace_bytes,
                        void* stream) {
+  NvtxRange nvtx_range("dflash_verify_host");
   int rc = check_shape(B, gamma, V, dtype);
   if (rc) return rc;
   if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
@@ -502,6 +557,7 @@ static int rows_task(int task, const void* logits, int R, int V, int dtype, cons
 int dflash_filter(const void* logits, int R, int V, int dtype, const float* temperature, int top_k, float top_p,
                   int32_t* out_idx, float* out_prob, int32_t* out_count, void* workspace, size_t workspace_bytes,
                   uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_filter");
   if (!out_idx || !out_prob || !out_count) return fail(DFLASH_ERR_INVALID_ARG, "null output pointer");
   return rows_task(kTaskFilter, logits, R, V, dtype, temperature, top_k, top_p, 0, nullptr, out_idx, out_prob,
                    out_count, workspace, workspace_bytes, status, stream);
@@ -510,6 +566,7 @@ int dflash_filter(const void* logits, int R, int V, int dtype, const float* temp
 int dflash_sample(const void* logits, int R, int V, int dtype, const float* temperature, int top_k, float top_p,
                   uint64_t seed, int32_t* out_tokens, void* workspace, size_t workspace_bytes, uint32_t* status,
                   void* stream) {
+  NvtxRange nvtx_range("dflash_sample");
   if (!out_tokens) return fail(DFLASH_ERR_INVALID_ARG, "null output pointer");
   return rows_task(kTaskSample, logits, R, V, dtype, temperature, top_k, top_p, seed, out_tokens, nullptr, nullptr,
                    nullptr, workspace, workspace_bytes, status, stream);
@@ -557,6 +614,7 @@ static int candidates_pass(const void* logits, int R, int V_shard, int dtype, in
 int dflash_shard_candidates(const void* target_shard, const void* draft_shard, int B, int gamma, int V_shard,
                             int dtype, int vocab_offset, int k, uint32_t* record, void* workspace,
                             size_t workspace_bytes, uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_shard_candidates");
   int rc = check_shape(B, gamma, V_shard, dtype);
   if (rc) return rc;
   if (!target_shard || !draft_shard || !record || !workspace)
@@ -587,6 +645,7 @@ int dflash_shard_candidates(const void* target_shard, const void* draft_shard, i
 int dflash_verify_candidates(const uint32_t* records, int n_shards, int k, const int32_t* draft_tokens, int B,
                              int gamma, int V, const float* temperature, int top_k, float top_p, uint64_t seed,
                              int32_t* out_tokens, int32_t* out_accept_len, uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_verify_candidates");
   if (B < 1 || B > kMaxB) return fail(DFLASH_ERR_INVALID_ARG, "B=%d outside [1, %d]", B, kMaxB);
   if (gamma < 1 || gamma > kMaxGamma)
     return fail(DFLASH_ERR_INVALID_ARG, "gamma=%d outside [1, %d]", gamma, kMaxGamma);

@@ -77,6 +77,16 @@ __device__ __forceinline__ uint4 step_uniform_words(unsigned long long seed, uin
                        make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
 }
 
+// ---- programmatic dependent launch ------------------------------------------------
+// Waits until the kernel before this one in the stream has completed and its
+// memory is visible (a no-op when the launch did not allow an early start),
+// then lets the kernel after this one be scheduled. Nothing before the call
+// may read or write global memory.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- shared-memory barriers and bulk copies ----------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);

@@ -270,6 +270,7 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   __shared__ ff scratch[kFvThreads / 32];
   __shared__ int last_r, last_p;
   const int s = blockIdx.x, b = blockIdx.y;
+  grid_dependency_sync();
   const Req q = load_req(f, b);
   if (!q.live) return;
   load_table(f, th, tl);
@@ -349,6 +350,7 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   __shared__ ff slice_base;
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  grid_dependency_sync();
   const Req q = load_req(f, b);
   // every call leaves the workspace at zero (its regions move with the
   // shape): this launch is the last reader of the request's draw state
@@ -493,13 +495,22 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
 
 int launch_fullvocab_draw(const FvParams& f, void* stream) {
   if (f.B <= 0 || f.n_slices <= 0) return 0;
-  const cudaStream_t st = (cudaStream_t)stream;
-  const dim3 grid((unsigned)f.n_slices, (unsigned)f.B);
-  fv_sums_kernel<<<grid, kFvThreads, 0, st>>>(f);
-  const cudaError_t e = cudaGetLastError();
+  // both launches may start while the kernel before them ends (programmatic
+  // dependent launch); each waits for it before its first global access
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kFvThreads);
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3((unsigned)f.n_slices, (unsigned)f.B);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fv_sums_kernel, f);
   if (e != cudaSuccess) return (int)e;
-  fv_pick_kernel<<<f.B, kFvThreads, 0, st>>>(f);
-  return (int)cudaGetLastError();
+  cfg.gridDim = dim3((unsigned)f.B);
+  e = cudaLaunchKernelEx(&cfg, fv_pick_kernel, f);
+  return (int)e;
 }
 
 }  // namespace dflash

@@ -51,6 +51,20 @@ static_assert(kStages >= kConsumerWarps, "ring stages must cover every consumer 
 static_assert((2 * kStages) % kConsumerWarps == 0, "piece it - 2 kStages must be the consumer warp's own");
 static_assert(kKeyQueue >= kConsumerWarps, "key-queue slots must cover every consumer warp's piece");
 constexpr int kCtasPerSm = 1;
+constexpr int kMaxDevices = 64;
+
+// Grid of the persistent stream kernel. Its CTAs wait on each other (a row's
+// final polls tile keys that other CTAs' consumers write), so every CTA must
+// be resident at once: the grid is at most the CTAs the SMs available to the
+// calling context hold together (SMs x CTAs per SM at the kernel's shared
+// memory and thread counts), and never more than there are pieces. 0 when
+// no CTA fits at all.
+inline long long persistent_grid(long long pieces, int sms_available, int ctas_per_sm) {
+  if (sms_available < 1 || ctas_per_sm < 1) return 0;
+  long long g = (long long)sms_available * ctas_per_sm;
+  if (g > pieces) g = pieces;
+  return g < 1 ? 1 : g;
+}
 
 constexpr int kMaxTopK = 32;     // one kept token per lane of a warp
 constexpr int kListWords = kMaxTopK + 1;  // a row's filtered list, then its draft token's probability
@@ -251,6 +265,8 @@ void set_last_error(const char* msg);
 // launches (dflash_sweep.cu); return a cudaError_t value
 int launch_sweep(const Params& p, int grid, void* stream);
 int sweep_smem_bytes();
+// CTAs of the stream kernel (dtype 0 bf16, 1 fp32) one SM of device `dev` holds
+int sweep_occupancy(int dtype, int dev, int* ctas_per_sm);
 int launch_fullvocab_draw(const FvParams& f, void* stream);
 int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* out_accept,
                     float* out_draw, void* stream);

@@ -56,6 +56,7 @@
 #include <cfloat>
 #include <climits>
 #include <cstdint>
+#include <mutex>
 
 #include "dflash_device.cuh"
 #include "dflash_internal.h"
@@ -956,18 +957,32 @@ __device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, in
       if (v < nvec) wv[rr] = st4[v];
     }
     float m = -INFINITY;
+    if (DT == 0 && !argmax && 32 * (4 * blk + 3) + lane < nvec) {
+      // a whole block of bf16 logits: one packed maximum over its 16 words,
+      // converted to fp32 once (NaN propagates through every step)
+      __nv_bfloat162 acc = *reinterpret_cast<const __nv_bfloat162*>(&wv[0].x);
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int v = 32 * (4 * blk + rr) + lane;
-      if (v < nvec) {
-        const float vmax = vector_max<DT>(wv[rr]);
-        m = max_nan(m, vmax);
-        if (argmax) {
-          const uint32_t k = key_of(vmax);
-          if (k > best_key) {
-            best_key = k;
-            best_v = v;
-            best_w = wv[rr];
+      for (int rr = 0; rr < 4; ++rr) {
+        acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&wv[rr].x));
+        acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&wv[rr].y));
+        acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&wv[rr].z));
+        acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&wv[rr].w));
+      }
+      m = max_nan(__low2float(acc), __high2float(acc));
+    } else {
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const int v = 32 * (4 * blk + rr) + lane;
+        if (v < nvec) {
+          const float vmax = vector_max<DT>(wv[rr]);
+          m = max_nan(m, vmax);
+          if (argmax) {
+            const uint32_t k = key_of(vmax);
+            if (k > best_key) {
+              best_key = k;
+              best_v = v;
+              best_w = wv[rr];
+            }
           }
         }
       }
@@ -1460,6 +1475,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
       fence_barrier_init();
     }
   }
+  // Programmatic dependent launch: everything above touches only this CTA's
+  // shared memory, so it may overlap the end of the kernel before this one in
+  // the stream; every global load and store (the inputs may be that kernel's
+  // outputs, and the workspace its leftovers) comes after the wait. The next
+  // kernel may be scheduled at once: its CTAs only start on SMs this grid has
+  // left, and they wait in the same place.
+  grid_dependency_sync();
   build_request_order(p, S);  // contains __syncthreads
   __syncthreads();
   if (S.cancelled) {  // a cancelled workspace: report, and leave before any copy is issued
@@ -1492,19 +1514,58 @@ __global__ void uniforms_kernel(unsigned long long seed, int B, int npos, int st
 
 int sweep_smem_bytes() { return (int)sizeof(Smem); }
 
+namespace {
+// The kernel's shared-memory opt-in, set once per device (the attribute is a
+// property of the function on the current device).
+std::mutex g_attr_mu;
+bool g_attr_set[2][kMaxDevices] = {};
+
+template <int DT>
+cudaError_t prepare_sweep(int dev) {
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  if (g_attr_set[DT][dev]) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(sweep_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem));
+  if (e == cudaSuccess) g_attr_set[DT][dev] = true;
+  return e;
+}
+
+template <int DT>
+int launch_sweep_t(const Params& p, int grid, void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  if ((e = prepare_sweep<DT>(dev)) != cudaSuccess) return (int)e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaLaunchKernelEx(&cfg, sweep_kernel<DT>, p);
+}
+
+template <int DT>
+int occupancy_t(int dev, int* ctas_per_sm) {
+  cudaError_t e = prepare_sweep<DT>(dev);
+  if (e != cudaSuccess) return (int)e;
+  return (int)cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, sweep_kernel<DT>, kThreads,
+                                                            sizeof(Smem));
+}
+}  // namespace
+
 int launch_sweep(const Params& p, int grid, void* stream) {
-  const int smem = (int)sizeof(Smem);
-  cudaError_t e;
-  if (p.dtype == 0) {
-    e = cudaFuncSetAttribute(sweep_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return (int)e;
-    sweep_kernel<0><<<grid, kThreads, smem, (cudaStream_t)stream>>>(p);
-  } else {
-    e = cudaFuncSetAttribute(sweep_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return (int)e;
-    sweep_kernel<1><<<grid, kThreads, smem, (cudaStream_t)stream>>>(p);
-  }
-  return (int)cudaGetLastError();
+  return p.dtype == 0 ? launch_sweep_t<0>(p, grid, stream) : launch_sweep_t<1>(p, grid, stream);
+}
+
+int sweep_occupancy(int dtype, int dev, int* ctas_per_sm) {
+  if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  return dtype == 0 ? occupancy_t<0>(dev, ctas_per_sm) : occupancy_t<1>(dev, ctas_per_sm);
 }
 
 int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* ua, float* ud, void* stream) {

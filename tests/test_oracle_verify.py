@@ -247,10 +247,10 @@ def test_tiny_workload_mean_accept_length_matches_closed_form():
     inp = synth.make_workload("tiny_v1024", data_seed=0)
     B, gamma, V = inp.shape
     T, k, tp = float(inp.temperature[0]), inp.top_k, inp.top_p
-    p = [oracle.filter_row(inp.target[0, i], T, k, tp) for i in range(gamma + 1)]
-    q = [oracle.filter_row(inp.draft[0, i], T, k, tp) for i in range(gamma)]
-    alpha = np.array([np.minimum(p[i], q[i]).sum() for i in range(gamma)])
-    expected = np.concatenate([[1.0], np.cumprod(alpha)]).sum()
+    # the closed form the benchmark reports (oracle.accept_rates, expected_accept_len)
+    alpha = oracle.accept_rates(inp.target, inp.draft, inp.temperature, k, tp)
+    expected = float(oracle.expected_accept_len(alpha)[0])
+    assert 1.0 <= expected <= gamma + 1
     n = 20000
     rows = np.broadcast_to(inp.draft[0], (n, gamma, V)).reshape(n * gamma, V)
     d, _, _ = oracle.sample_rows(rows, np.full(n * gamma, T, np.float32), k, tp, 1234)
@@ -300,3 +300,25 @@ def test_split_margins_recombine():
         greedy = T == 0
         assert np.all(ma[greedy] > 1e300) and np.all(md[greedy] > 1e300)
         assert np.all(md[~greedy] < 1e300)  # every sampling request draws once
+
+
+def test_accept_rates_special_cases():
+    """alpha = sum min(p, q): 1 for a draft row equal to the target row, 0 when
+    the filtered supports are disjoint, NaN for greedy requests; the closed
+    form is gamma + 1 when every alpha is 1 and 1 when the first is 0."""
+    V, gamma = 64, 3
+    rng = np.random.default_rng(4)
+    X = (rng.standard_normal((3, gamma + 1, V)) * 2).astype(np.float32)
+    Y = X[:, :gamma].copy()
+    # request 1: each draft row's top tokens are far below the target's top-5 set
+    order = np.argsort(-X[1, :gamma], axis=-1)
+    for i in range(gamma):
+        Y[1, i] = -10.0
+        Y[1, i, order[i, 10:15]] = 5.0
+    T = np.array([1.0, 1.0, 0.0], np.float32)
+    a = oracle.accept_rates(X, Y, T, 5, 1.0)
+    assert np.allclose(a[0], 1.0, atol=1e-12)
+    assert np.allclose(a[1], 0.0, atol=1e-12)
+    assert np.all(np.isnan(a[2]))
+    e = oracle.expected_accept_len(np.array([[1.0, 1.0, 1.0], [0.0, 0.5, 0.5], [0.5, 0.5, 0.5]]))
+    assert np.allclose(e, [4.0, 1.0, 1.0 + 0.5 + 0.25 + 0.125])
