@@ -100,6 +100,7 @@ struct Smem {
   } u;
   alignas(16) uint32_t hist[256];              // a row final's tau histogram
   alignas(16) unsigned long long cand[kCandCap];  // also a warp's draw scratch
+  alignas(16) unsigned long long sorted[32];      // a row final's top 32 candidates, in order
   int32_t cand_tiles[kCandTileCap];
   int fin_slot;
   int fin_cmd;
@@ -259,26 +260,6 @@ __device__ __forceinline__ void draw_next_job(const Params& p, uint32_t& next) {
   if (fin_tid() == kFinDrawer) next = atomicAdd(p.job_cnt, 1u);  // read only when the job ends
 }
 
-// Group-wide maxima of two values at once. No barrier follows the read of
-// S.warp_red: its next writer is past a later group barrier.
-__device__ __forceinline__ void fin_max2_u32(Smem& S, uint32_t a, uint32_t b, uint32_t& ra, uint32_t& rb) {
-  const int gt = fin_tid(), lane = gt & 31, w = gt >> 5;
-  a = warp_max_u32(a);
-  b = warp_max_u32(b);
-  if (lane == 0) {
-    S.warp_red[w] = a;
-    S.warp_red[kFinWarps + w] = b;
-  }
-  fin_sync();
-  ra = 0u;
-  rb = 0u;
-#pragma unroll
-  for (int i = 0; i < kFinWarps; ++i) {
-    ra = max(ra, S.warp_red[i]);
-    rb = max(rb, S.warp_red[kFinWarps + i]);
-  }
-}
-
 // Finds, in S.hist, the digit holding the krem-th largest element (counts
 // from the top); sets S.digit and S.digit_above (elements in larger digits).
 // Run by the group's first warp.
@@ -423,6 +404,60 @@ __device__ __forceinline__ int warp_exclusive_count(int c, int lane, int& total)
 
 static_assert(sizeof(decltype(Smem::u)) >= sizeof(uint4) * 8 * kFin, "the gather's stage fits the union");
 
+// Bits (as a uint32) of the smallest logit value whose order key is at least
+// tau (key of -inf < tau <= key of +inf). A bf16 logit's key is its 16-bit
+// key k16 shifted up, with the low half all ones for a negative value and
+// zero otherwise (zeros share +0's key); so a negative k16 equal to tau's
+// upper half always passes, a non-negative one only when tau's lower half is
+// zero. The value of a 16-bit key is the inverse map; the key that -0 would
+// have maps to -0, which compares equal to +0 and above every negative.
+template <int DT>
+__device__ __forceinline__ uint32_t threshold_bits(uint32_t tau) {
+  if (DT == 0) {
+    const uint32_t t16 = tau >> 16;
+    const uint32_t k16 = t16 < 0x8000u ? t16 : t16 + ((tau & 0xffffu) ? 1u : 0u);
+    return (k16 & 0x8000u) ? (k16 & 0x7fffu) : (~k16 & 0xffffu);
+  }
+  return __float_as_uint(value_of_key(tau));
+}
+
+// Marks (bit e) of the logits of a 16-byte vector that are >= the threshold
+// value: packed bf16 compares, or fp32 compares. NaNs are never marked (a row
+// holding one is flagged bad).
+template <int DT>
+__device__ __forceinline__ uint32_t mark_at_least(const uint4& x, uint32_t thr) {
+  if (DT == 0) {
+    const __nv_bfloat162 t2 = __halves2bfloat162(__ushort_as_bfloat16((unsigned short)thr),
+                                                  __ushort_as_bfloat16((unsigned short)thr));
+    const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
+    uint32_t m = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t c = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&ws[q]), t2);
+      m |= ((c & 1u) | ((c >> 15) & 2u)) << (2 * q);
+    }
+    return m;
+  }
+  const float tf = __uint_as_float(thr);
+  return (__uint_as_float(x.x) >= tf ? 1u : 0u) | (__uint_as_float(x.y) >= tf ? 2u : 0u) |
+         (__uint_as_float(x.z) >= tf ? 4u : 0u) | (__uint_as_float(x.w) >= tf ? 8u : 0u);
+}
+
+// The same marks by order keys (any tau; NaNs compare by their keys).
+template <int DT>
+__device__ __forceinline__ uint32_t mark_keys_at_least(const uint4& x, uint32_t tau) {
+  const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
+  constexpr int per_vec = DT == 0 ? 8 : 4;
+  uint32_t m = 0u;
+#pragma unroll
+  for (int e = 0; e < per_vec; ++e) {
+    const uint32_t key = DT == 0 ? key_of(__uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16))
+                                 : key_of(__uint_as_float(ws[e]));
+    m |= (key >= tau ? 1u : 0u) << e;
+  }
+  return m;
+}
+
 // ---- row final ----------------------------------------------------------------------
 // Leaves the row's sorted top-k composites in the group's first warp (lane l:
 // rank l in `top_a`) and in the workspace.
@@ -484,36 +519,48 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
   }
   draw_next_job(p, next);
   const uint32_t emx = gt < n_edge ? (isnan(edge_x) ? 0xffffffffu : key_of(edge_x)) : 0u;
-  uint32_t tile_max, edge_max;
-  fin_max2_u32(S, mx, emx, tile_max, edge_max);
+  // the group's largest tile key and edge key (warp maxima in one
+  // instruction each), and this job's shared counters reset, behind one
+  // barrier; no barrier follows the read of S.warp_red, whose next writer is
+  // past a later group barrier
+  {
+    const uint32_t wm = __reduce_max_sync(0xffffffffu, mx);
+    const uint32_t we = __reduce_max_sync(0xffffffffu, emx);
+    if (lane == 0) {
+      S.warp_red[w] = wm;
+      S.warp_red[kFinWarps + w] = we;
+    }
+    S.hist[gt] = 0u;
+    S.hist[gt + kFin] = 0u;
+    if (gt == 0) {
+      S.n_cand_tiles = 0;
+      S.n_cand = 0;
+    }
+  }
+  fin_sync();
+  uint32_t tile_max = 0u, edge_max = 0u;
+#pragma unroll
+  for (int i = 0; i < kFinWarps; ++i) {
+    tile_max = max(tile_max, S.warp_red[i]);
+    edge_max = max(edge_max, S.warp_red[kFinWarps + i]);
+  }
   const bool bad = !key_is_finite(max(tile_max, edge_max));
 
-  // tau: a lower bound of the k-th largest tile maximum (0 keeps everything
-  // when tiles < k). Tile keys within 255 buckets of 2^16 key units below the
-  // largest are counted per bucket; the bucket where the count from the top
+  // tau: a lower bound of the k-th largest tile key (0 keeps everything when
+  // tiles < k). Each thread's largest key counts once: the k largest of those
+  // are k distinct tile keys, so the k-th largest of them is at most the
+  // row's k-th largest tile key, and that is at most its k-th largest logit.
+  // They are counted per bucket of 2^16 key units below the largest (one
+  // shared atomic per thread); the bucket where the count from the top
   // reaches k gives tau (exact for bf16 logits, whose keys have zero low 16
-  // bits). When the top k spread wider, an exact radix selection runs.
+  // bits). When they spread wider, an exact radix selection over the tile
+  // keys runs instead.
   uint32_t tau = 0u;
   if (k == 1) {
     tau = tile_max;
   } else if (n_tiles >= k) {
-    S.hist[gt] = 0u;
-    S.hist[gt + kFin] = 0u;
-    fin_sync();
-    // (the cached and uncached loops are separate: a branch inside one loop
-    // keeps the compiler from overlapping the iterations' loads)
-    if (cached) {
-#pragma unroll 4
-      for (int i = gt; i < n_tiles; i += kFin) {
-        const uint32_t bucket = (tile_max - S.u.key_cache[i]) >> 16;
-        if (bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
-      }
-    } else {
-      for (int i = gt; i < n_tiles; i += kFin) {
-        const uint32_t bucket = (tile_max - __ldcg(gkeys + i)) >> 16;
-        if (bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
-      }
-    }
+    const uint32_t bucket = (tile_max - mx) >> 16;
+    if (mx != 0u && bucket < 255u) atomicAdd(&S.hist[bucket], 1u);
     fin_sync();
     if (gt < 32) {
       // inclusive count over buckets 0..b, eight buckets per lane
@@ -555,11 +602,6 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     }
   }
 
-  if (gt == 0) {
-    S.n_cand_tiles = 0;
-    S.n_cand = 0;
-  }
-  fin_sync();
   // candidate tiles: each thread marks its tiles (every kFin-th) in a mask;
   // a warp reserves its slots with one atomic (shared atomics on one address
   // serialise) and places its lanes by a prefix of their counts
@@ -597,6 +639,12 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     // its code is fetched once and run eight times, where an unrolled one is
     // fetched line by line once per row final.
     uint4* stage = reinterpret_cast<uint4*>(&S.u);  // [8][kFin]
+    // key >= tau as a value comparison (one packed compare per two bf16
+    // logits): thr is the smallest value whose key is at least tau; a tau at
+    // or below the key of -inf, or above that of +inf, keeps the key
+    // comparison
+    const bool plain_thr = tau > kKeyNegInf && tau <= kKeyPosInf;
+    const uint32_t thr = threshold_bits<DT>(tau);
     for (int base = 0; base < n_vec_all; base += kFin * 8) {
       uint4 wv[8];
 #pragma unroll
@@ -618,15 +666,8 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
         if (f >= n_vec_all) break;
         if (candidate_vector(S, f) >= rb.nvec) continue;
         const uint4 x = stage[u * kFin + gt];
-        const uint32_t ws[4] = {x.x, x.y, x.z, x.w};
-        uint32_t m = 0u;
-#pragma unroll
-        for (int e = 0; e < per_vec; ++e) {
-          const uint32_t key = dtype == 0 ? key_of(__uint_as_float(((ws[e >> 1] >> ((e & 1) * 16)) & 0xffffu) << 16))
-                                          : key_of(__uint_as_float(ws[e]));
-          m |= (key >= tau ? 1u : 0u) << e;
-        }
-        cm |= (unsigned long long)m << (u * per_vec);
+        cm |= (unsigned long long)(plain_thr ? mark_at_least<DT>(x, thr) : mark_keys_at_least<DT>(x, tau))
+              << (u * per_vec);
       }
       if (cm) {  // few threads: one slot reservation, then the marked logits
         int pos = atomicAdd(&S.n_cand, __popcll(cm));
@@ -679,26 +720,25 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
     });
     fin_sync();
   }
-  // sort the (<= 64) candidates in the first warp; ranks < k are the row's top-k
+  // sort the (<= 64) candidates: the composites are distinct (each carries
+  // its logit's index), so a composite's rank is the number of larger ones;
+  // thread c ranks candidate c, and ranks < 32 (k <= 32) are kept in order
   const int n_c = min(S.n_cand, kCandCap);
-  if (w == 0) {
-    // by rank: the composites are distinct (each carries its logit's index),
-    // so a composite's rank is the number of larger ones
-    const unsigned long long a0 = lane < n_c ? S.cand[lane] : 0ull;
-    const unsigned long long b0 = lane + 32 < n_c ? S.cand[lane + 32] : 0ull;
-    int ra = 0, rb = 0;
+  if (gt < n_c) {
+    const unsigned long long c = S.cand[gt];
     const ulonglong2* c2 = reinterpret_cast<const ulonglong2*>(S.cand);
-#pragma unroll 1
-    for (int m = 0; m < n_c; m += 2) {
-      const ulonglong2 v = c2[m >> 1];
-      ra += (v.x > a0 ? 1 : 0) + (m + 1 < n_c && v.y > a0 ? 1 : 0);
-      rb += (v.x > b0 ? 1 : 0) + (m + 1 < n_c && v.y > b0 ? 1 : 0);
+    int r = 0;
+#pragma unroll 2
+    for (int m = 0; m < (n_c >> 1); ++m) {
+      const ulonglong2 v = c2[m];
+      r += (v.x > c ? 1 : 0) + (v.y > c ? 1 : 0);
     }
-    __syncwarp();
-    if (lane < n_c) S.cand[ra] = a0;
-    if (lane + 32 < n_c) S.cand[rb] = b0;
-    __syncwarp();
-    const unsigned long long a = lane < n_c ? S.cand[lane] : 0ull;
+    if (n_c & 1) r += S.cand[n_c - 1] > c ? 1 : 0;
+    if (r < 32) S.sorted[r] = c;
+  }
+  fin_sync();
+  if (w == 0) {
+    const unsigned long long a = lane < n_c ? S.sorted[lane] : 0ull;
     top_a = a;
     if (p.task == kTaskVerify) {
       // the row's filtered distribution (ranks < k, k <= 32), which the
@@ -1381,9 +1421,10 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
 // rows, every row of the rows tasks) in the order rows finish, then one job
 // per request (sampling requests, then greedy ones). A group draws its next
 // job while it works on the current one (once that one's inputs are ready),
-// so a job goes to whichever group frees up first. A row final waits only on the stream; a sampling request's
-// final may wait on its rows' finals, which were all drawn before it, so no
-// two groups can wait on each other in a cycle.
+// so a job goes to whichever group frees up first. A row final waits only on
+// the stream; a sampling request's final may wait on its rows' finals, which
+// were all drawn before it, so no two groups can wait on each other in a
+// cycle.
 template <int DT>
 __device__ bool finals_job(const Params& p, Smem& S, bool row_job, int j, int ord, uint32_t& next) {
   const int gt = fin_tid(), w = gt >> 5;
