@@ -146,11 +146,33 @@ int dflash_verify(const void* target_logits, const void* draft_logits,
                   int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
                   size_t workspace_bytes, uint32_t* status, void* stream);
 
+/* dflash_verify that also reports, for audits, the two probabilities each
+ * accept test compared: audit_pq [device] float [B, gamma, 2] receives, for
+ * every sampling request b and draft position i, p_i(d_i) (the filtered
+ * target probability of the draft token) and q_i(d_i) (the filtered draft
+ * probability; both 0 when the token is outside the kept set) as the test
+ * u < p/q used them, in fp32. Every position of a sampling request is
+ * written (the tests run at all positions at once); greedy requests' entries
+ * are left untouched. Otherwise identical to dflash_verify: same arguments,
+ * outputs, errors and results. The accept rule is standard speculative
+ * sampling as the draft/verify loop of "DFlash2 用投机解码给 Qwen 提速"
+ * (bml.asia) and step 3 of rytg.cn's "投机解码如何白嫖速度" apply it. */
+int dflash_verify_audit(const void* target_logits, const void* draft_logits,
+                        const int32_t* draft_tokens, int B, int gamma, int V, int dtype,
+                        const float* temperature, int top_k, float top_p, uint64_t seed,
+                        int32_t* out_tokens, int32_t* out_accept_len, float* audit_pq,
+                        void* workspace, size_t workspace_bytes, uint32_t* status,
+                        void* stream);
+
 /* Greedy verification of every request: a_i = argmax target_logits[b, i, :]
  * (lowest index on ties); n = length of the prefix with draft_tokens[b, i] ==
- * a_i; emits d_0..d_{n-1}, a_n and accept length n + 1. Draft logits are not
- * needed. Arguments as for dflash_verify (workspace sized with top_k = 1,
- * top_p = 1). */
+ * a_i; emits d_0..d_{n-1}, a_n and accept length n + 1. This is the greedy
+ * half of the lossless guarantee of "无损加速是真的吗？Qwen3.8-27B-DFlash2如何
+ * 保证输出与目标模型完全一致" (rytg.cn, the lossless definition: under greedy
+ * decoding the output is identical to the target's own), applied to the
+ * draft/verify loop of "DFlash2 用投机解码给 Qwen 提速" (bml.asia). Draft
+ * logits are not needed. Arguments as for dflash_verify (workspace sized with
+ * top_k = 1, top_p = 1). */
 int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B,
                          int gamma, int V, int dtype, int32_t* out_tokens,
                          int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
@@ -278,11 +300,16 @@ int dflash_uniforms(uint64_t seed, int B, int npos, int stream_id, float* out_ac
  * exits. Shapes whose workspace (dflash_workspace_bytes) exceeds it return
  * DFLASH_ERR_INVALID_ARG with a message naming the sizes. The first call on a
  * device looks the array up with that device current; make that first call
- * before any stream capture. Each call clears the array's counters on `stream`
- * before the kernel runs, and every call on a device shares the one array:
- * calls that may overlap on the GPU (other streams, other threads) race and
- * must be ordered by the caller. Nothing here allocates or frees memory.
- * Arguments and results as for dflash_verify. */
+ * before any stream capture. Each call clears the part of the array it uses
+ * on `stream` before the kernel runs (one memset of dflash_workspace_bytes()
+ * of its shape: about 3.6 MB at B = 32, block 8, V = 248320 bf16), and every
+ * call on a device shares the one array: calls that may overlap on the GPU
+ * (other streams, other threads) race and must be ordered by the caller.
+ * dflash_workspace_cancel cannot reach this array (its address is not
+ * handed out), so such a call cannot be cancelled: it ends when its work is
+ * done or its bounded waits (2 s each) give up. Nothing here allocates or
+ * frees memory. Arguments and results as for dflash_verify, including the
+ * code and message for an invalid or unsupported shape or filter. */
 size_t dflash_noalloc_scratch_bytes(void);
 int dflash_verify_noalloc(const void* target_logits, const void* draft_logits,
                           const int32_t* draft_tokens, int B, int gamma, int V, int dtype,

@@ -118,6 +118,17 @@ static void update_margin(double* margin, double a, double b) {
   if (gap < *margin) *margin = gap;
 }
 
+/* The absolute gap |a - b|: the margin of an inverse-CDF decision, whose two
+ * sides (u times the total weight, a cumulative weight) are sums of
+ * probabilities; an implementation's error on them is bounded in the same
+ * units (a multiple of the fp32 rounding unit times the mass summed), not
+ * relative to the cumulative weight, which can be tiny. */
+static void update_margin_abs(double* margin, double a, double b) {
+  if (!margin) return;
+  double gap = fabs(a - b);
+  if (gap < *margin) *margin = gap;
+}
+
 int32_t oracle_argmax_row(const void* row, int V, int dtype, uint32_t* status) {
   int32_t best = 0;
   double best_x = logit_at(row, dtype, 0);
@@ -262,8 +273,8 @@ static int32_t draw_ascending(const double* w, int V, float u, double* margin) {
     prev = cum;
     cum += w[j];
     if (target_f < (float)cum) {
-      update_margin(margin, target, cum);
-      if (prev > 0.0) update_margin(margin, target, prev);
+      update_margin_abs(margin, target, cum);
+      if (prev > 0.0) update_margin_abs(margin, target, prev);
       return j;
     }
   }

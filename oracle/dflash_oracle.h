@@ -75,8 +75,11 @@ int oracle_filter_row_sparse(const void* row, int V, int dtype, double temperatu
  * target: [B, gamma+1, V]; draft: [B, gamma, V]; draft_tokens: [B, gamma];
  * temperature: [B] (0 = greedy for that request).
  * out_tokens: [B, gamma+1] (-1 padded), out_accept_len: [B].
- * margin (optional, [B]): the smallest relative gap between the two sides of
- * any fp32 decision the request took (diagnostic for near-boundary rows).
+ * margin (optional, [B]): the smallest gap between the two sides of any fp32
+ * decision the request took (diagnostic for near-boundary rows): relative
+ * for the accept tests (|u - p/q| / (p/q)) and the top-p cuts
+ * (|mass before - top_p| / top_p), absolute for the inverse-CDF draw
+ * (|u * total - cumulative weight|, the weights being probabilities).
  * status (optional): OR of ORC_STATUS_* over the processed requests. */
 int oracle_verify(const void* target, const void* draft, const int32_t* draft_tokens, int B,
                   int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,

@@ -19,7 +19,7 @@ _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash_verify.so")
 SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_candidates.cu", "dflash_abi.cu", "dflash_noalloc.cu"]
-HEADERS = ["dflash_device.cuh", "dflash_internal.h", "dflash_rule.cuh"]
+HEADERS = ["dflash_device.cuh", "dflash_internal.h", "dflash_rule.cuh", "dflash_ff.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
@@ -97,6 +97,7 @@ EXPORTS = {
     "dflash_workspace_init": ("i", "pzp"),
     "dflash_workspace_cancel": ("i", "pzp"),
     "dflash_verify": ("i", "pppiiiipifQppp" "zpp"),
+    "dflash_verify_audit": ("i", "pppiiiipifQpppp" "zpp"),
     "dflash_verify_det": ("i", "ppiiiipifQpppzpp"),
     "dflash_verify_greedy": ("i", "ppiiiipppzpp"),
     "dflash_host_staging_bytes": ("z", "iiii"),
@@ -269,6 +270,37 @@ def verify(target, draft, draft_tokens, temperature, top_k: int, top_p: float, s
         None if status is None else _dev(status, "status", torch.int32), _stream_ptr(stream, dev))
     _check(rc)
     return out_tokens, out_accept_len
+
+
+def verify_audit(target, draft, draft_tokens, temperature, top_k: int, top_p: float, seed: int,
+                 status=None, workspace=None, stream=None):
+    """dflash_verify_audit on torch CUDA tensors. Returns (out_tokens,
+    out_accept_len, audit_pq): audit_pq [B, gamma, 2] holds p(d), q(d) of each
+    accept test (NaN where the call wrote nothing: greedy requests)."""
+    torch = _torch()
+    B, g1, V = target.shape
+    gamma = g1 - 1
+    if tuple(draft.shape) != (B, gamma, V) or draft.dtype != target.dtype:
+        raise ValueError("draft must be [B, gamma, V] with the target's dtype")
+    dt = _dtype_code(target)
+    dev = target.device
+    out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_accept_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    audit = torch.full((B, gamma, 2), float("nan"), dtype=torch.float32, device=dev)
+    _shape(draft_tokens, (B, gamma), "draft_tokens")
+    _shape(temperature, (B,), "temperature")
+    _status_ok(status)
+    _on(dev, draft=draft, draft_tokens=draft_tokens, temperature=temperature, status=status)
+    ws = _workspace_for(workspace_bytes(B, gamma, V, dt, top_k, top_p), dev, workspace)
+    rc = load().dflash_verify_audit(
+        _dev(target, "target"), _dev(draft, "draft"), _dev(draft_tokens, "draft_tokens", torch.int32),
+        B, gamma, V, dt, _dev(temperature, "temperature", torch.float32), int(top_k), float(top_p),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(out_accept_len, "out_accept_len", torch.int32), _dev(audit, "audit_pq", torch.float32),
+        ws.ptr, ws.nbytes, None if status is None else _dev(status, "status", torch.int32),
+        _stream_ptr(stream, dev))
+    _check(rc)
+    return out_tokens, out_accept_len, audit
 
 
 def verify_det(target, draft_tokens, temperature, top_k: int, top_p: float, seed: int,

@@ -208,6 +208,9 @@ Params base_params(int dtype, int V) {
   memset(&p, 0, sizeof p);
   p.dtype = dtype == DFLASH_BF16 ? 0 : 1;
   p.geo = make_geometry(V, esize_of(dtype));
+  const Exp2Table& e = exp2_table();
+  memcpy(p.exp2.hi, e.hi, sizeof e.hi);
+  memcpy(p.exp2.lo, e.lo, sizeof e.lo);
   return p;
 }
 
@@ -260,11 +263,14 @@ int dflash_workspace_cancel(void* workspace, size_t bytes, void* stream) {
   return DFLASH_OK;
 }
 
-int dflash_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
-                  int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
-                  uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
-                  size_t workspace_bytes, uint32_t* status, void* stream) {
-  NvtxRange nvtx_range("dflash_verify");
+}  // extern "C"
+
+namespace {
+// dflash_verify, and with audit_pq the accept tests' p(d), q(d) written out
+int verify_impl(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
+                int gamma, int V, int dtype, const float* temperature, int top_k, float top_p, uint64_t seed,
+                int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                uint32_t* status, float* audit_pq, void* stream) {
   int rc = check_shape(B, gamma, V, dtype);
   if (rc) return rc;
   if (!target_logits || !draft_logits || !draft_tokens || !temperature || !out_tokens || !out_accept_len ||
@@ -300,12 +306,36 @@ int dflash_verify(const void* target_logits, const void* draft_logits, const int
   p.fullvocab = fullvocab ? 1 : 0;
   p.out_tokens = out_tokens;
   p.out_len = out_accept_len;
+  p.audit_pq = audit_pq;
   p.status = status;
   bind_workspace(p, workspace, B * (2 * gamma + 1), B, fullvocab);
   // the slot count depends on the device-side temperatures; launch for the maximum
   rc = run(p, B * (2 * gamma + 1), stream);
   if (rc || !fullvocab) return rc;
   return run_fullvocab_draw(p, workspace, stream);
+}
+}  // namespace
+
+extern "C" {
+
+int dflash_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
+                  int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
+                  uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, void* workspace,
+                  size_t workspace_bytes, uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_verify");
+  return verify_impl(target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, top_k, top_p,
+                     seed, out_tokens, out_accept_len, workspace, workspace_bytes, status, nullptr, stream);
+}
+
+int dflash_verify_audit(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                        int B, int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,
+                        uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len, float* audit_pq,
+                        void* workspace, size_t workspace_bytes, uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_verify_audit");
+  if (!audit_pq) return fail(DFLASH_ERR_INVALID_ARG, "null audit_pq");
+  if (((uintptr_t)audit_pq) % 4u) return fail(DFLASH_ERR_INVALID_ARG, "audit_pq is not 4-byte aligned");
+  return verify_impl(target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, top_k, top_p,
+                     seed, out_tokens, out_accept_len, workspace, workspace_bytes, status, audit_pq, stream);
 }
 
 int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
@@ -682,6 +712,9 @@ int dflash_verify_candidates(const uint32_t* records, int n_shards, int k, const
   c.out_tokens = out_tokens;
   c.out_len = out_accept_len;
   c.status = status;
+  const Exp2Table& et = exp2_table();
+  memcpy(c.exp2.hi, et.hi, sizeof et.hi);
+  memcpy(c.exp2.lo, et.lo, sizeof et.lo);
   const int e = launch_verify_candidates(c, stream);
   if (e) return cuda_fail((cudaError_t)e, "launching the verification from shard candidates");
   return DFLASH_OK;

@@ -40,6 +40,7 @@ struct CandSmem {
   unsigned long long comp[kCandWarps][kMaxShardCand];
   unsigned long long sorted[kCandWarps][kMaxTopK];
   alignas(16) unsigned long long scratch[2 * kMaxTopK];
+  float exp_hi[kExpTable], exp_lo[kExpTable];  // 2^(j/64) for the filter's float-float exp
 };
 
 // candidate j of shard s for row `row` of the target (or draft) rows
@@ -87,6 +88,11 @@ __global__ void __launch_bounds__(kCandWarps * 32) verify_candidates_kernel(cons
   const float T = __ldg(c.temperature + b);
   int32_t* out = c.out_tokens + (size_t)b * (gamma + 1);
   const int32_t* d = c.draft_tokens + (size_t)b * gamma;
+  for (int j = threadIdx.x; j < kExpTable; j += blockDim.x) {
+    S.exp_hi[j] = c.exp2.hi[j];
+    S.exp_lo[j] = c.exp2.lo[j];
+  }
+  __syncthreads();
 
   if (!sampling_temperature(T)) {
     // greedy: the argmax of each target row is its largest candidate
@@ -158,7 +164,7 @@ __global__ void __launch_bounds__(kCandWarps * 32) verify_candidates_kernel(cons
     const unsigned long long a = lane < n_c ? S.sorted[w][lane] : 0ull;
     const bool valid = lane < k && lane < n_c;
     int32_t idx = valid ? composite_idx(a) : -1;
-    const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T, c.top_p, lane);
+    const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T, c.top_p, lane, S.exp_hi, S.exp_lo);
     const int32_t d_row = i < gamma ? __ldg(d + i) : -1;
     const uint32_t hit = __ballot_sync(0xffffffffu, idx >= 0 && idx == d_row);
     const float pd = hit ? __shfl_sync(0xffffffffu, pr, __ffs(hit) - 1) : 0.0f;

@@ -105,6 +105,13 @@ constexpr int kExpTable = 64;  // 2^(j/64), j < 64, as fp32 pairs
 
 enum FvMode : int { kFvNone = 0, kFvResidual = 1, kFvBonus = 2 };
 
+// 2^(j/64) = hi[j] + lo[j] (j < 64) for the float-float exp (computed on the
+// host in double precision)
+struct ExpTable {
+  float hi[kExpTable];
+  float lo[kExpTable];
+};
+
 // what the accept test left for the draw of request b
 struct FvDraw {
   int n;       // drafts accepted: the token drawn goes to position n
@@ -143,6 +150,7 @@ struct Params {
   float* out_prob;
   int32_t* out_count;
   float* out_rowmax;            // candidates task: each row's largest logit (NaN if it holds one)
+  float* audit_pq;              // verify, optional [B, gamma, 2]: p(d), q(d) each accept test used
   uint32_t* status;
   // workspace (zero-initialised once; counters reset by their last user)
   uint32_t* row_cnt;    // [n_slots]
@@ -158,6 +166,7 @@ struct Params {
   unsigned long long* res_list;
   FvDraw* fv_draw;      // [B]: full-vocabulary mode
   int n_slots;
+  ExpTable exp2;        // for the filter's float-float exp
 };
 
 // Second pass of the full-vocabulary draw (dflash_fullvocab.cu).
@@ -215,6 +224,7 @@ struct CandParams {
   int32_t* out_tokens;          // [B, gamma+1]
   int32_t* out_len;             // [B]
   uint32_t* status;
+  ExpTable exp2;                // for the filter's float-float exp
 };
 
 struct WorkspaceLayout {

@@ -80,9 +80,14 @@ int dflash_verify_noalloc(const void* target_logits, const void* draft_logits, c
                           void* stream) {
   const size_t need = dflash_workspace_bytes(B, gamma, V, dtype, top_k, top_p);
   if (need == 0) {
-    // invalid or unsupported shape / filter: let the main entry point say which
+    // Invalid or unsupported shape / filter: the main entry point says which,
+    // with the same code and message (DFLASH_ERR_UNSUPPORTED for a filter
+    // outside the supported set). It rejects such a call before it looks at
+    // its workspace, so a non-null stand-in is passed where the workspace
+    // goes: a null one would be reported as a null pointer first.
+    static unsigned char stand_in[16];
     return dflash_verify(target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, top_k,
-                         top_p, seed, out_tokens, out_accept_len, nullptr, 0, status, stream);
+                         top_p, seed, out_tokens, out_accept_len, stand_in, 0, status, stream);
   }
   char msg[256];
   if (need > kNoAllocScratchBytes) {
@@ -101,7 +106,7 @@ int dflash_verify_noalloc(const void* target_logits, const void* draft_logits, c
   // before every launch.
   cudaError_t e = cudaMemsetAsync(scratch, 0, need, (cudaStream_t)stream);
   if (e != cudaSuccess) {
-    snprintf(msg, sizeof msg, "dflash_verify_noalloc: clearing the scratch header: %s", cudaGetErrorString(e));
+    snprintf(msg, sizeof msg, "dflash_verify_noalloc: clearing the scratch: %s", cudaGetErrorString(e));
     return noalloc_fail(DFLASH_ERR_CUDA, msg);
   }
   return dflash_verify(target_logits, draft_logits, draft_tokens, B, gamma, V, dtype, temperature, top_k, top_p,

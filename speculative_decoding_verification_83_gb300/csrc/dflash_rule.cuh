@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "dflash_device.cuh"
+#include "dflash_ff.cuh"
 #include "dflash_internal.h"
 
 namespace dflash {
@@ -29,75 +30,59 @@ constexpr uint32_t kStatusBadToken = 1u, kStatusBadRow = 2u, kStatusTimeout = 4u
 __device__ __forceinline__ bool sampling_temperature(float t) { return t > 0.0f && t < INFINITY; }
 
 // ---- filtering and drawing ---------------------------------------------------------
-// Sorts in the finals place each element by its rank (independent loads from
-// a small shared scratch) rather than through a sorting network, which is
-// dozens of dependent shuffle steps; sums and prefix sums over a warp are
-// five shuffle steps each.
-
-// Total of the 32 values in sc (16-byte aligned), added in lane order, and in
-// `before` the part added before this lane's value. Every lane adds in the
-// same order, so all lanes get the same total.
-__device__ __forceinline__ float scratch_sums(const float* sc, int lane, float& before) {
-  const float4* s4 = reinterpret_cast<const float4*>(sc);
-  float total = 0.0f;
-  before = 0.0f;
-#pragma unroll 1
-  for (int q = 0; q < 8; ++q) {
-    const float4 v = s4[q];
-    const float e[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (4 * q + i == lane) before = total;
-      total += e[i];
-    }
-  }
-  return total;
-}
-
-// Warp-wide sum (butterfly: every lane gets the same total) and inclusive
-// prefix sum of a float. Short shuffle chains: five dependent steps each.
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_inclusive_scan(float v, int lane) {
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float n = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += n;
-  }
-  return v;
-}
+// Every decision here turns sums of probabilities into an integer (the top-p
+// cut, the accept test, the inverse CDF), and is taken in fp32 on the fp32
+// rounding of nearly exact quantities: the weights and prefix sums are
+// float-float (dflash_ff.cuh), so the only error a decision sees is the
+// final rounding of its operands. Sorts place each element by its rank
+// (independent loads from a small shared scratch) rather than through a
+// sorting network; sums and prefix sums over a warp are five shuffle steps.
 
 // Filters one row's sorted top-k (lane j holds rank j): temperature, softmax
 // over the survivors, top-p cut, renormalisation. Returns this lane's
 // probability (0 outside the kept set) and sets idx to -1 there.
+// The weight of rank j is exp((x_j - x_0) / T): the difference to the
+// largest logit is exact as a pair, its quotient by T a pair (the rounded
+// quotient and the exact remainder over T), and exp() float-float (th, tl:
+// Tang's table). The mass before rank j is its exclusive prefix over the
+// total, rounded to fp32 for the cut (kept while below top_p, so the kept
+// ranks are a prefix that always holds rank 0); a kept probability is its
+// weight over the kept total, rounded once to fp32.
 __device__ __forceinline__ float filter_lane(uint32_t key, int32_t& idx, int k_eff, float T, float top_p,
-                                             int lane) {
+                                             int lane, const float* th, const float* tl) {
   const bool in_k = lane < k_eff && idx >= 0;
-  const float z = value_of_key(key) / T;
-  const float z0 = __shfl_sync(0xffffffffu, z, 0);  // the largest
-  const float w = in_k ? expf(z - z0) : 0.0f;
+  const float x = value_of_key(key);
+  const float x0 = __shfl_sync(0xffffffffu, x, 0);  // the largest
+  const ff delta = two_sum(x, -x0);                 // x - x0, exactly
+  const float q_hi = __fdiv_rn(delta.hi, T);
+  const float rem = __fmaf_rn(-q_hi, T, delta.hi);  // delta.hi - q_hi T, exactly
+  const ff d = fast_two_sum(q_hi, __fdiv_rn(__fadd_rn(rem, delta.lo), T));
+  const ff w = in_k ? exp_ff(d, th, tl) : ff{0.0f, 0.0f};
+  const ff incl = warp_inclusive_scan_ff(w, lane);
   bool keep = in_k;
   if (top_p < 1.0f) {
-    const float W = warp_sum(w);
-    const float incl = warp_inclusive_scan(w / W, lane);
-    float before = __shfl_up_sync(0xffffffffu, incl, 1);  // mass of the higher ranks
-    if (lane == 0) before = 0.0f;
-    keep = keep && (before < top_p);
+    // every lane takes part in both shuffles (none may sit in a
+    // short-circuited operand: a lane skipping a full-mask shuffle leaves
+    // the others waiting for it)
+    const ff total = shfl_ff(incl, 31);
+    ff before = shfl_up_ff(incl, 1);  // mass of the higher ranks
+    if (lane == 0) before = ff{0.0f, 0.0f};
+    const float before_f = ff_round(ff_mul(before, ff_recip(total)));
+    keep = keep && before_f < top_p;
   }
-  const float wk = keep ? w : 0.0f;
-  const float Wk = warp_sum(wk);
+  const uint32_t kept = __ballot_sync(0xffffffffu, keep);
+  const ff Wk = shfl_ff(incl, kept ? 31 - __clz(kept) : 0);  // the kept total
   if (!keep) idx = -1;
-  return keep ? wk / Wk : 0.0f;
+  return keep ? ff_round(ff_mul(w, ff_recip(Wk))) : 0.0f;
 }
 
 // Inverse CDF in ascending token order: the smallest token whose cumulative
 // weight exceeds u * total; if rounding leaves none, the last token with
 // positive weight; tokens marked -1 have no weight. The lanes are put in
-// token order by rank (ties, only among the -1 marks, by lane); sk, sw: 32
-// words each of warp scratch, 16-byte aligned.
+// token order by rank (ties, only among the -1 marks, by lane); the
+// cumulative weights and the total are float-float prefix sums, and the
+// comparison is taken on the fp32 roundings of the cumulative weight and of
+// u * total. sk, sw: 32 words each of warp scratch, 16-byte aligned.
 __device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u, int lane, int32_t* sk,
                                                   float* sw) {
   const int32_t key = tok >= 0 ? tok : INT_MAX;
@@ -119,11 +104,9 @@ __device__ __forceinline__ int32_t draw_ascending(int32_t tok, float w, float u,
   __syncwarp();
   // lane l now stands for rank l
   const float wl = sw[lane];
-  float before;
-  const float total = scratch_sums(sw, lane, before);
-  const float cum = before + wl;
-  const float t = u * total;
-  const uint32_t hit = __ballot_sync(0xffffffffu, wl > 0.0f && t < cum);
+  const ff cum = warp_inclusive_scan_ff(ff{wl, 0.0f}, lane);
+  const float t = ff_round(ff_scale(u, shfl_ff(cum, 31)));
+  const uint32_t hit = __ballot_sync(0xffffffffu, wl > 0.0f && t < ff_round(cum));
   int chosen;
   if (hit) {
     chosen = __ffs(hit) - 1;
@@ -150,12 +133,13 @@ static_assert(2 * kMaxTopK == 64, "token_slot hashes into 64 slots");
 // draft token (i < gamma); wd: lane i's counter-based words for position i
 // (accept: x, draw: y). scratch: 64 words of warp scratch, 16-byte aligned.
 // Writes out[0..gamma] (the request's tokens), out_len[b] (its accept length)
-// and ORs its status bits into *status.
+// and ORs its status bits into *status; audit_pq (optional, [gamma][2])
+// receives each position's p(d) and q(d) as the accept test used them.
 __device__ __forceinline__ void sampling_rule(const int32_t (*idx)[33], const float (*prob)[33], int per_s,
                                               bool det, int gamma, int V, int32_t d_lane, uint4 wd,
                                               unsigned long long seed, int b, int lane,
                                               unsigned long long* scratch, int32_t* out, int32_t* out_len,
-                                              uint32_t* status) {
+                                              uint32_t* status, float* audit_pq = nullptr) {
   uint32_t st = 0;
   for (int r = lane; r < per_s; r += 32)
     if (idx[r][32]) st |= kStatusBadRow;
@@ -168,6 +152,10 @@ __device__ __forceinline__ void sampling_rule(const int32_t (*idx)[33], const fl
     const float q_d = det ? 1.0f : prob[2 * lane + 1][32];
     const float ratio = p_d / q_d;  // q = 0: +inf if p > 0, NaN if p == 0
     reject = !(uniform24(wd.x) < ratio);
+    if (audit_pq) {
+      audit_pq[2 * lane] = p_d;
+      audit_pq[2 * lane + 1] = q_d;
+    }
   }
   const uint32_t rej = __ballot_sync(0xffffffffu, reject);
   const int n = rej ? __ffs(rej) - 1 : gamma;  // drafts accepted

@@ -101,6 +101,7 @@ struct Smem {
   alignas(16) uint32_t hist[256];              // a row final's tau histogram
   alignas(16) unsigned long long cand[kCandCap];  // also a warp's draw scratch
   alignas(16) unsigned long long sorted[32];      // a row final's top 32 candidates, in order
+  float exp_hi[kExpTable], exp_lo[kExpTable];   // 2^(j/64) for the filter's float-float exp
   int32_t cand_tiles[kCandTileCap];
   int fin_slot;
   int fin_cmd;
@@ -745,7 +746,7 @@ __device__ bool row_final(const Params& p, Smem& S, int slot, const SlotInfo& si
       // request final reads
       const bool valid = lane < k && lane < n_c;
       int32_t idx = valid ? composite_idx(a) : -1;
-      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane);
+      const float pr = filter_lane(valid ? composite_key(a) : 0u, idx, k, T_row, p.top_p, lane, S.exp_hi, S.exp_lo);
       const uint32_t lo = __float_as_uint(pr) | ((bad && lane == 0) ? 0x80000000u : 0u);
       unsigned long long* list = p.res_list + (size_t)slot * kListWords;
       list[lane] = ((unsigned long long)(uint32_t)(idx + 2) << 32) | lo;
@@ -820,7 +821,7 @@ __device__ bool request_final(const Params& p, Smem& S, int ord, uint32_t& next)
   for (int i = gt; i < n_words; i += kFin) words[i] = 0ull;
   if (w == 0)
     sampling_rule(S.u.lists.idx, S.u.lists.prob, per_s, p.det != 0, gamma, V, d_lane, wd, p.seed, b, lane,
-                  S.cand, out, p.out_len, p.status);
+                  S.cand, out, p.out_len, p.status, p.audit_pq ? p.audit_pq + (size_t)b * gamma * 2 : nullptr);
   fin_sync();
   return true;
 }
@@ -837,7 +838,7 @@ __device__ void rows_final(const Params& p, Smem& S, int r, unsigned long long t
     int32_t idx = (lane < k_eff && lane < n_c) ? composite_idx(top_a) : -1;
     float pr;
     if (samp) {
-      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane);
+      pr = filter_lane(key, idx, k_eff, T, p.top_p, lane, S.exp_hi, S.exp_lo);
     } else {
       pr = lane == 0 ? 1.0f : 0.0f;
       if (lane != 0) idx = -1;
@@ -1391,6 +1392,10 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
         }
         const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
         stop = !(uniform24(wd.x) < p_d / q_d);  // q = 0: +inf if p > 0, NaN if p == 0
+        if (p.audit_pq) {
+          p.audit_pq[((size_t)b * gamma + i) * 2] = p_d;
+          p.audit_pq[((size_t)b * gamma + i) * 2 + 1] = q_d;
+        }
       }
     }
     const uint32_t ball = __ballot_sync(0xffffffffu, stop);
@@ -1478,6 +1483,10 @@ __device__ void finals(const Params& p, Smem& S) {
   const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * samp_slots(p) : p.B);
   const int ord0 = 0;  // every request has a final job (sampling first, then greedy)
   const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
+  if (gt < kExpTable) {
+    S.exp_hi[gt] = p.exp2.hi[gt];
+    S.exp_lo[gt] = p.exp2.lo[gt];
+  }
   if (gt == kFinDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);
   fin_sync();
   int j = S.fin_slot;

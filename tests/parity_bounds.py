@@ -1,0 +1,63 @@
+"""Bounds on how far a GPU decision can sit from the oracle's and still be
+taken the other way, from the fp32 arithmetic each side does (derived in the
+design notes, section "Parity bounds"). A GPU result that differs from the
+oracle's is accepted only when the oracle reports the decision's margin below
+its bound; everything else must match exactly.
+
+u = 2^-24 is the fp32 rounding unit.
+
+Top-k filter (dflash_rule.cuh): every weight, prefix sum and normaliser is
+float-float, the weights' exp() within about 1e-9 (2^-29.9) relative, so a
+kept probability is its exact value to 2^-29, rounded once to fp32
+(relative error <= u + 2^-29 < 1.05 u).
+- accept test u_i < p(d)/q(d): the GPU ratio is within 3.2u of the exact one,
+  the oracle's within u, and u_i is exact: a decision can differ only when
+  |u_i - p/q| <= 4.2u (p/q)                        -> ACCEPT_REL = 2^-21
+- top-p cut RN(mass before) < top_p: the mass before is within 2^-29 on the
+  GPU and exact on the oracle, each rounded to fp32; the test can differ
+  only if top_p lies between the two roundings: |before - top_p| <= u +
+  2^-29 <= 2^-22.9 top_p (top_p >= 1/2)             -> CUT_REL = 2^-21
+- inverse CDF RN(u * total) < RN(cumulative weight), in probability units:
+  the residual's weights max(0, p - q) come from fp32 p and q (error
+  <= 1.05u (p + q) each, plus u max(0, p - q) for the subtraction), the sums
+  are float-float, so each side is within 3.2u of the exact value, and the
+  two fp32 roundings add at most 2u:               -> DRAW_ABS = 2^-21
+Full-vocabulary filter: the draw is float-float over the whole row
+(dflash_fullvocab.cu), no fp32 list values in between: each side within
+2^-29 and two fp32 roundings (<= 2u)               -> FV_DRAW_ABS = 2^-22
+Its accept test uses the stream's fp32 normalisers (sums of ex2.approx
+weights), bounded in the design notes by FV_ACCEPT_REL.
+"""
+
+U = 2.0 ** -24
+ACCEPT_REL = 2.0 ** -21
+CUT_REL = 2.0 ** -21
+DRAW_ABS = 2.0 ** -21
+FV_DRAW_ABS = 2.0 ** -22
+FV_ACCEPT_REL = 2.0 ** -16
+
+# the sampling-mode bar: rows (tokens and accept length) equal on >= 99.99%
+ROW_BAR = 1e-4
+
+
+def excused_topk(m_acc, m_cut, m_draw):
+    """Whether a top-k request's oracle margins put one of its decisions
+    within the GPU's rounding (then a different result is not an error)."""
+    return m_acc < ACCEPT_REL or m_cut < CUT_REL or m_draw < DRAW_ABS
+
+
+def excused_fullvocab(m_acc, m_draw):
+    return m_acc < FV_ACCEPT_REL or m_draw < FV_DRAW_ABS
+
+
+def compare_rows(tok, ln, want_tok, want_len, excused, what=""):
+    """Rows (tokens, accept length) must match the oracle unless excused(b);
+    returns the number of differing rows."""
+    import numpy as np
+
+    same = np.all(tok == want_tok, axis=1) & (ln == want_len)
+    bad = np.nonzero(~same)[0]
+    for b in bad:
+        assert excused(b), (f"{what} request {b}: gpu {tok[b].tolist()} len {ln[b]} vs oracle "
+                            f"{want_tok[b].tolist()} len {want_len[b]}")
+    return len(bad)

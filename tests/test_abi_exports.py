@@ -76,3 +76,24 @@ def test_cancel_refuses_a_buffer_without_the_header(lib):
     assert lib.dflash_workspace_cancel(None, 1 << 20, None) == dv.ERR_INVALID_ARG
     assert lib.dflash_workspace_cancel(ctypes.c_void_p(256), 64, None) == dv.ERR_INVALID_ARG
     assert b"abort flag" in lib.dflash_last_error()
+
+
+@pytest.mark.parametrize("top_k,top_p", [(33, 0.95), (0, 0.9), (-1, 0.5)])
+def test_noalloc_reports_unsupported_filters_like_verify(lib, top_k, top_p):
+    """An unsupported filter gets DFLASH_ERR_UNSUPPORTED and the same message
+    from the workspace-free entry point as from dflash_verify (no launch, no
+    GPU needed: both reject the call on the host)."""
+    p = ctypes.c_void_p(1 << 20)
+    B, gamma, V = 4, 7, 50000
+    rc = lib.dflash_verify(p, p, p, B, gamma, V, 0, p, top_k, top_p, 0, p, p, p, 1 << 30, None, None)
+    want = lib.dflash_last_error()
+    assert rc == dv.ERR_UNSUPPORTED
+    rc2 = lib.dflash_verify_noalloc(p, p, p, B, gamma, V, 0, p, top_k, top_p, 0, p, p, None, None)
+    assert rc2 == dv.ERR_UNSUPPORTED
+    assert lib.dflash_last_error() == want
+
+
+def test_audit_entry_point_checks_its_output(lib):
+    p = ctypes.c_void_p(1 << 20)
+    rc = lib.dflash_verify_audit(p, p, p, 4, 7, 5000, 0, p, 20, 0.95, 0, p, p, None, p, 1 << 30, None, None)
+    assert rc == dv.ERR_INVALID_ARG and b"audit" in lib.dflash_last_error()

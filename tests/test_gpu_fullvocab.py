@@ -8,9 +8,9 @@ apart, so the draw is compared at fp32 resolution.
 Bars:
 - Greedy requests and status words are bit-exact.
 - A sampling request must match the oracle exactly (tokens and accept length)
-  unless the oracle's accept margin is below 1e-4, or its draw margin is below
-  2^-22 (the draw's cumulative weight sits within about two fp32 ulps of
-  u * total, where rounding can move the token).
+  unless the oracle's margins put a decision within the GPU's rounding
+  (parity_bounds: the accept test on the stream's fp32 normalisers, relative
+  FV_ACCEPT_REL; the float-float draw, absolute FV_DRAW_ABS = 2^-22).
 - Such near-boundary mismatches stay under 0.01% of requests.
 """
 import numpy as np
@@ -18,13 +18,12 @@ import pytest
 
 import oracle
 import synth
+from parity_bounds import FV_DRAW_ABS, ROW_BAR, compare_rows, excused_fullvocab
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
-ACCEPT_MARGIN = 1e-4
-DRAW_MARGIN = 2.0 ** -22
 
 
 @pytest.fixture(scope="module")
@@ -69,13 +68,8 @@ def _check(dv, X, Y, d, T, seed, **kw):
     assert st == want_st
     g = T == 0
     assert np.array_equal(tok[g], want_tok[g]) and np.array_equal(ln[g], want_len[g])
-    same = np.all(tok == want_tok, axis=1) & (ln == want_len)
-    bad = np.nonzero(~same)[0]
-    for b in bad:
-        assert m_acc[b] < ACCEPT_MARGIN or m_draw[b] < DRAW_MARGIN, (
-            f"request {b}: gpu {tok[b].tolist()} len {ln[b]} vs oracle {want_tok[b].tolist()} "
-            f"len {want_len[b]}, margins {m_acc[b]:.3g} / {m_draw[b]:.3g}")
-    return len(bad), len(ln)
+    n_bad = compare_rows(tok, ln, want_tok, want_len, lambda b: excused_fullvocab(m_acc[b], m_draw[b]))
+    return n_bad, len(ln)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -90,7 +84,7 @@ def test_fullvocab_small(dv, dtype, V, gamma):
             nb, nt = _check(dv, X, Y, d, T, seed)
             n_bad += nb
             total += nt
-    assert n_bad <= 1
+    assert n_bad <= ROW_BAR * total
 
 
 def test_fullvocab_identical_drafts_take_the_bonus(dv):
@@ -104,7 +98,7 @@ def test_fullvocab_identical_drafts_take_the_bonus(dv):
     want_tok, want_len, (m_acc, m_draw), _ = oracle.verify(X, Y, d, T, 0, 1.0, 99, split_margins=True)
     assert np.array_equal(want_len, ln)
     diff = np.nonzero(np.any(tok != want_tok, axis=1))[0]
-    assert all(m_draw[b] < DRAW_MARGIN for b in diff) and len(diff) <= 1
+    assert all(m_draw[b] < FV_DRAW_ABS for b in diff) and len(diff) <= ROW_BAR * len(ln)
 
 
 def test_fullvocab_temperatures_and_misaligned_rows(dv):
@@ -120,8 +114,8 @@ def test_fullvocab_temperatures_and_misaligned_rows(dv):
         fy = _t(np.concatenate([Y.reshape(-1)[:1], Y.reshape(-1)]))
         Xd, Yd = fx[1:].view(B, gamma + 1, V), fy[1:].view(B, gamma, V)
         assert Xd.data_ptr() % 16 != 0
-        n_bad, _ = _check(dv, X, Y, d, T, 5, Xd=Xd, Yd=Yd)
-        assert n_bad <= 1
+        n_bad, total = _check(dv, X, Y, d, T, 5, Xd=Xd, Yd=Yd)
+        assert n_bad <= ROW_BAR * total
 
 
 def test_fullvocab_status_bits(dv):
@@ -158,8 +152,8 @@ def test_fullvocab_workspace_shared_with_top_k_calls(dv):
               status=st, workspace=ws)
     again = _run(dv, X, Y, d, T, 8, ws=ws)
     assert np.array_equal(first[0], again[0]) and np.array_equal(first[1], again[1])
-    n_bad, _ = _check(dv, X, Y, d, T, 8, ws=ws)
-    assert n_bad <= 1
+    n_bad, total = _check(dv, X, Y, d, T, 8, ws=ws)
+    assert n_bad <= ROW_BAR * total
 
 
 def test_fullvocab_full_size_workload(dv):
@@ -168,7 +162,7 @@ def test_fullvocab_full_size_workload(dv):
     inp = synth.make_workload("b128_g15_fullvocab_f32", data_seed=0, seed=0)
     d = _draft_tokens(inp.draft, inp.temperature, 100)
     n_bad, total = _check(dv, inp.target, inp.draft, d, inp.temperature, inp.seed)
-    assert n_bad <= 1, n_bad
+    assert n_bad <= ROW_BAR * total, n_bad
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -190,5 +184,5 @@ def test_sampler_full_vocab_matches_oracle(dv, dtype):
             greedy = T <= 0
             assert np.array_equal(got[greedy], want[greedy])
             diff = np.nonzero(got != want)[0]
-            assert all(margin[r] < DRAW_MARGIN for r in diff), [(int(r), margin[r]) for r in diff[:5]]
-            assert len(diff) <= 1
+            assert all(margin[r] < FV_DRAW_ABS for r in diff), [(int(r), margin[r]) for r in diff[:5]]
+            assert len(diff) <= ROW_BAR * R

@@ -1,23 +1,24 @@
 """GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
 
 Bars: uniforms, greedy tokens and accept lengths, and status words are
-bit-exact. Filtered probabilities agree within 1e-5 absolute (fp32 kernel vs
-fp64 oracle). Sampled tokens and accept lengths agree on every request except
-ones whose oracle decision margin is below 1e-4 (a u vs p/q, top-p or
-inverse-CDF comparison that rounding can flip), and those stay under 0.01% of
-rows at the full sizes.
+bit-exact. Filtered probabilities agree within 1e-5 absolute (the sampling
+bar) and, as the filter is float-float, within one fp32 rounding of the
+oracle's fp64 value. Sampled tokens and accept lengths agree on every request
+except ones whose oracle margin puts a decision within the GPU's rounding
+(parity_bounds: 2^-21 relative for the accept tests and top-p cuts, 2^-21
+absolute for the draw), and differing rows stay under 0.01% of the rows.
 """
 import numpy as np
 import pytest
 
 import oracle
 import synth
+from parity_bounds import CUT_REL, DRAW_ABS, ROW_BAR, U, compare_rows, excused_fullvocab, excused_topk
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 PROB_TOL = 1e-5
-MARGIN = 1e-4
 
 
 @pytest.fixture(scope="module")
@@ -55,15 +56,12 @@ def _run_verify(dv, X, Y, d, T, top_k, top_p, seed):
     return tok.cpu().numpy(), ln.cpu().numpy(), int(st.item())
 
 
-def _compare_sampling(tok, ln, want_tok, want_len, margin):
-    """Rows must match unless the oracle marks a near-boundary decision."""
-    same = np.all(tok == want_tok, axis=1) & (ln == want_len)
-    bad = np.nonzero(~same)[0]
-    for b in bad:
-        assert margin[b] < MARGIN, (
-            f"request {b}: gpu {tok[b].tolist()} len {ln[b]} vs oracle {want_tok[b].tolist()} "
-            f"len {want_len[b]}, margin {margin[b]:.3g}")
-    return len(bad)
+def _compare_sampling(tok, ln, want_tok, want_len, margins):
+    """Rows must match unless the oracle's margins (accept, cut, draw) put a
+    decision within the GPU's rounding."""
+    m_acc, m_cut, m_draw = margins
+    return compare_rows(tok, ln, want_tok, want_len,
+                        lambda b: excused_topk(m_acc[b], m_cut[b], m_draw[b]))
 
 
 # ---------------------------------------------------------------- uniforms
@@ -146,16 +144,18 @@ def _check_filter_rows(dv, L, T, top_k, top_p):
         w_idx, w_prob = oracle.filter_row_sparse(L[r], float(T[r]), top_k, top_p)
         n = cnt[r]
         if n != len(w_idx):
-            # only a top-p cut that rounding can move may differ, by one token
+            # only a top-p cut within the GPU's rounding may differ, by one token
             full_idx, full_p = oracle.filter_row_sparse(L[r], float(T[r]), top_k, 1.0)
             m = min(n, len(w_idx))
             assert abs(n - len(w_idx)) == 1
-            assert abs(full_p[:m].sum() - top_p) < 1e-5
+            assert abs(full_p[:m].sum() - top_p) < CUT_REL * top_p
             boundary += 1
             continue
         assert np.array_equal(idx[r, :n], w_idx), f"row {r}"
         assert np.all(idx[r, n:] == -1)
         assert np.max(np.abs(prob[r, :n] - w_prob)) < PROB_TOL
+        # one fp32 rounding of the exact value, plus the float-float exp's 1e-9
+        assert np.all(np.abs(prob[r, :n] - w_prob) <= 1.05 * U * w_prob + 1e-30), f"row {r}"
         assert abs(prob[r, :n].sum() - 1.0) < 1e-5
     return boundary
 
@@ -169,7 +169,7 @@ def test_filter_matches_oracle(dv, dtype, top_k, top_p):
         L = synth.to_float(L)
     R = L.shape[0]
     T = np.array([0.6, 1.0, 1.7, 0.3, 1.0] * 4, np.float32)[:R]
-    assert _check_filter_rows(dv, L, T, top_k, top_p) <= 1
+    assert _check_filter_rows(dv, L, T, top_k, top_p) == 0
 
 
 def test_filter_full_vocab_rows(dv):
@@ -195,7 +195,9 @@ def test_sample_matches_oracle(dv, dtype):
         torch.cuda.synchronize()
         got = got.cpu().numpy()
         diff = np.nonzero(got != want)[0]
-        assert all(margin[r] < MARGIN for r in diff)
+        # the sampler's margin is the smaller of its cut (relative) and draw
+        # (absolute) margins; both are bounded by DRAW_ABS here
+        assert all(margin[r] < DRAW_ABS for r in diff)
         assert int(st.item()) == want_st
 
 
@@ -208,14 +210,14 @@ def test_verify_small_many_seeds(dv, V):
         inp.temperature[:] = np.array([1.0, 0.0, 0.6, 1.0, 1.5, 0.0, 0.8, 1.0, 2.0], np.float32)
         d = _draft_tokens(inp, seed=data_seed)
         for seed in (data_seed, 1000 + data_seed):
-            want_tok, want_len, margin, want_st = oracle.verify(
-                inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, seed)
+            want_tok, want_len, margins, want_st = oracle.verify(
+                inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, seed, cut_margin=True)
             tok, ln, st = _run_verify(dv, inp.target, inp.draft, d, inp.temperature, inp.top_k,
                                       inp.top_p, seed)
             assert st == want_st
-            n_bad += _compare_sampling(tok, ln, want_tok, want_len, margin)
+            n_bad += _compare_sampling(tok, ln, want_tok, want_len, margins)
             total += len(ln)
-    assert n_bad <= max(1, total // 1000)
+    assert n_bad <= ROW_BAR * total
 
 
 @pytest.mark.parametrize("gamma", [1, 2, 15, 32])
@@ -223,33 +225,78 @@ def test_verify_gamma_range(dv, gamma):
     inp = synth.make_workload("b8_v248320", data_seed=gamma, B=3, V=4099, gamma=gamma)
     inp.temperature[:] = np.array([1.0, 0.0, 0.7], np.float32)
     d = _draft_tokens(inp)
-    want_tok, want_len, margin, _ = oracle.verify(inp.target, inp.draft, d, inp.temperature,
-                                                  inp.top_k, inp.top_p, 3)
+    want_tok, want_len, margins, _ = oracle.verify(inp.target, inp.draft, d, inp.temperature,
+                                                   inp.top_k, inp.top_p, 3, cut_margin=True)
     tok, ln, _ = _run_verify(dv, inp.target, inp.draft, d, inp.temperature, inp.top_k,
                              inp.top_p, 3)
-    _compare_sampling(tok, ln, want_tok, want_len, margin)
+    assert _compare_sampling(tok, ln, want_tok, want_len, margins) <= ROW_BAR * len(ln)
 
 
-@pytest.mark.parametrize("name", ["b1_v248320", "b8_v248320", "b32_mixed_v248320", "b32_mixed_g3_v248320",
+@pytest.mark.parametrize("name", ["b8_v248320", "b32_mixed_v248320", "b32_mixed_g3_v248320",
                                   "b32_mixed_g15_v248320"])
 def test_verify_full_size_workloads(dv, name):
     """The full-size bf16 workloads, every request checked against the oracle."""
-    seeds = [0, 1, 2] if name == "b1_v248320" else [0]
+    inp = synth.make_workload(name, data_seed=0, seed=0)
+    d = _draft_tokens(inp, seed=100)
+    want_tok, want_len, margins, want_st = oracle.verify(
+        inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, inp.seed, cut_margin=True)
+    tok, ln, st = _run_verify(dv, inp.target, inp.draft, d, inp.temperature, inp.top_k,
+                              inp.top_p, inp.seed)
+    assert st == want_st == 0
+    n_bad = _compare_sampling(tok, ln, want_tok, want_len, margins)
+    # greedy requests of the mix are bit-exact
+    g = inp.temperature == 0
+    assert np.array_equal(tok[g], want_tok[g]) and np.array_equal(ln[g], want_len[g])
+    assert n_bad <= ROW_BAR * len(ln)
+
+
+def test_verify_single_request_seeds_0_to_99(dv):
+    """One request, block 8, V = 248320 bf16, T = 1, top-k 20, top-p 0.95:
+    data and Philox seeds 0..99, each step checked against the oracle (the
+    oracle calls run on the host threads side by side)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    n_bad = 0
+    threads = oracle.default_threads()
+    for s0 in range(0, 100, threads):
+        cases = []
+        for s in range(s0, min(100, s0 + threads)):
+            inp = synth.make_workload("b1_v248320", data_seed=s, seed=s)
+            cases.append((inp, _draft_tokens(inp, seed=100 + s)))
+        with ThreadPoolExecutor(threads) as ex:
+            wants = list(ex.map(lambda c: oracle.verify(c[0].target, c[0].draft, c[1], c[0].temperature,
+                                                        c[0].top_k, c[0].top_p, c[0].seed, threads=1,
+                                                        cut_margin=True), cases))
+        for (inp, d), (want_tok, want_len, margins, want_st) in zip(cases, wants):
+            tok, ln, st = _run_verify(dv, inp.target, inp.draft, d, inp.temperature, inp.top_k,
+                                      inp.top_p, inp.seed)
+            assert st == want_st == 0
+            n_bad += _compare_sampling(tok, ln, want_tok, want_len, margins)
+    assert n_bad <= ROW_BAR * 100
+
+
+def test_verify_10k_sampled_rows(dv):
+    """The sampling-mode bar on more than 10^4 sampled requests: 160 batches
+    of 64 requests (temperatures cycling 0.6 / 1 / 1.3, top-k 20, top-p 0.95,
+    draft noise sigma ~ U(0.3, 1.5)), V = 20011 bf16 (rows of several pieces
+    spread over many CTAs, starts off 16-byte boundaries), every request
+    checked against the oracle: a differing row must be excused by a margin
+    within the GPU's rounding, and differing rows stay under 0.01%."""
+    B, gamma, V = 64, 7, 20011
     n_bad = total = 0
-    for data_seed in seeds:
-        inp = synth.make_workload(name, data_seed=data_seed, seed=data_seed)
-        d = _draft_tokens(inp, seed=100 + data_seed)
-        want_tok, want_len, margin, want_st = oracle.verify(
-            inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, inp.seed)
+    for s in range(160):
+        inp = synth.make_workload("b32_mixed_v248320", data_seed=20_000 + s, seed=s, B=B, V=V)
+        inp.temperature[:] = synth.cycle_temperatures(B, (0.6, 1.0, 1.3))
+        d = _draft_tokens(inp, seed=500 + s)
+        want_tok, want_len, margins, want_st = oracle.verify(
+            inp.target, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, inp.seed, cut_margin=True)
         tok, ln, st = _run_verify(dv, inp.target, inp.draft, d, inp.temperature, inp.top_k,
                                   inp.top_p, inp.seed)
         assert st == want_st == 0
-        n_bad += _compare_sampling(tok, ln, want_tok, want_len, margin)
-        total += len(ln)
-        # greedy requests of the mix are bit-exact
-        g = inp.temperature == 0
-        assert np.array_equal(tok[g], want_tok[g]) and np.array_equal(ln[g], want_len[g])
-    assert n_bad == 0 or n_bad / total < 1e-4 or n_bad <= 1
+        n_bad += _compare_sampling(tok, ln, want_tok, want_len, margins)
+        total += B
+    assert total >= 10_000
+    assert n_bad <= ROW_BAR * total, f"{n_bad} of {total} rows differ"
 
 
 def test_verify_b8_all_greedy_matches_greedy_entry(dv):
@@ -272,8 +319,8 @@ def test_status_bits_and_bad_inputs(dv):
     d[1, 3] = -5
     X = inp.target.copy()
     X[1, 6, 17] = np.nan
-    want_tok, want_len, margin, want_st = oracle.verify(X, inp.draft, d, inp.temperature,
-                                                        inp.top_k, inp.top_p, 1)
+    want_tok, want_len, _, want_st = oracle.verify(X, inp.draft, d, inp.temperature,
+                                                   inp.top_k, inp.top_p, 1)
     tok, ln, st = _run_verify(dv, X, inp.draft, d, inp.temperature, inp.top_k, inp.top_p, 1)
     assert st == want_st == (oracle.STATUS_BAD_TOKEN | oracle.STATUS_BAD_ROW
                              | oracle.STATUS_BAD_TEMPERATURE)
@@ -293,9 +340,9 @@ def test_workspace_reuse_and_repeatability(dv):
                             torch.from_numpy(inp.temperature).to(DEV), 20, 0.95, 4, workspace=ws)
         outs.append((tok.cpu().numpy(), ln.cpu().numpy()))
     assert all(np.array_equal(o[0], outs[0][0]) and np.array_equal(o[1], outs[0][1]) for o in outs)
-    want_tok, want_len, margin, _ = oracle.verify(inp.target, inp.draft, d, inp.temperature, 20,
-                                                  0.95, 4)
-    _compare_sampling(outs[0][0], outs[0][1], want_tok, want_len, margin)
+    want_tok, want_len, margins, _ = oracle.verify(inp.target, inp.draft, d, inp.temperature, 20,
+                                                   0.95, 4, cut_margin=True)
+    assert _compare_sampling(outs[0][0], outs[0][1], want_tok, want_len, margins) == 0
 
 
 def test_verify_host_buffers(dv):
@@ -313,9 +360,9 @@ def test_verify_host_buffers(dv):
     ws = dv.Workspace(dv.workspace_bytes(B, gamma, V, 0, 20, 0.95), DEV)
     dv.verify_host(pin(inp.target), pin(inp.draft), pin(d), pin(inp.temperature), 20, 0.95, 8,
                    out_tok, out_len, out_st, staging, ws)
-    want_tok, want_len, margin, want_st = oracle.verify(inp.target, inp.draft, d, inp.temperature,
-                                                        20, 0.95, 8)
-    _compare_sampling(out_tok.numpy(), out_len.numpy(), want_tok, want_len, margin)
+    want_tok, want_len, margins, want_st = oracle.verify(inp.target, inp.draft, d, inp.temperature,
+                                                         20, 0.95, 8, cut_margin=True)
+    assert _compare_sampling(out_tok.numpy(), out_len.numpy(), want_tok, want_len, margins) == 0
     assert int(out_st.item()) == want_st
 
 
@@ -342,12 +389,13 @@ def test_workspace_left_zero_across_shapes(dv):
         tok, ln = dv.verify(_t(X), _t(Y), torch.from_numpy(d).to(DEV), torch.from_numpy(T).to(DEV), top_k,
                             top_p, 9, status=st, workspace=ws)
         torch.cuda.synchronize()
-        want_tok, want_len, (m_acc, m_draw), want_st = oracle.verify(X, Y, d, T, top_k, top_p, 9,
-                                                                      split_margins=True)
+        want_tok, want_len, (m_acc, m_cut, m_draw), want_st = oracle.verify(X, Y, d, T, top_k, top_p, 9,
+                                                                             cut_margin=True)
         assert int(st.item()) == want_st
-        same = np.all(tok.cpu().numpy() == want_tok, axis=1) & (ln.cpu().numpy() == want_len)
-        for b in np.nonzero(~same)[0]:
-            assert m_acc[b] < MARGIN or m_draw[b] < 2.0 ** -22, f"V={V} request {b}"
+        fv = top_k <= 0
+        compare_rows(tok.cpu().numpy(), ln.cpu().numpy(), want_tok, want_len,
+                     (lambda b: excused_fullvocab(m_acc[b], m_draw[b])) if fv
+                     else (lambda b: excused_topk(m_acc[b], m_cut[b], m_draw[b])), f"V={V}")
         assert int(torch.count_nonzero(ws.buf).item()) == 0, f"workspace not left at zero after V={V}"
 
 
@@ -375,10 +423,8 @@ def test_verify_narrow_and_wide_top_tiles(dv, dtype):
     d, _, _ = oracle.sample_rows(Y.reshape(B * gamma, V), synth.draft_sampling_temperatures(T, gamma),
                                  20, 0.95, 9)
     d = d.reshape(B, gamma)
-    n_bad = 0
     for seed in (1, 2, 3):
-        want_tok, want_len, margin, want_st = oracle.verify(X, Y, d, T, 20, 0.95, seed)
+        want_tok, want_len, margins, want_st = oracle.verify(X, Y, d, T, 20, 0.95, seed, cut_margin=True)
         tok, ln, st = _run_verify(dv, X, Y, d, T, 20, 0.95, seed)
         assert st == want_st
-        n_bad += _compare_sampling(tok, ln, want_tok, want_len, margin)
-    assert n_bad <= 1
+        assert _compare_sampling(tok, ln, want_tok, want_len, margins) == 0

@@ -74,3 +74,27 @@ def test_merged_margin_is_the_smaller_of_the_two(top_k, top_p):
     t3, l3, (a3, d3), _ = oracle.verify_det(X, d, T, top_k, top_p, 3, split_margins=True)
     t4, l4, (a4, c4, d4), _ = oracle.verify_det(X, d, T, top_k, top_p, 3, cut_margin=True)
     assert np.array_equal(t3, t4) and np.array_equal(a3, np.minimum(a4, c4)) and np.array_equal(d3, d4)
+
+
+@pytest.mark.parametrize("V", [4, 8, 16])
+def test_draw_margin_is_absolute_closed_form(V):
+    """The draw's margin is the absolute gap between u * total and the
+    cumulative weights on either side of the chosen token. With equal logits
+    and q = p every draft is accepted and the bonus token is drawn from the
+    uniform p_gamma: the total is 1, the cumulative weights are (j + 1) / V,
+    the token is j = floor(V u), and the margin is min(u - j / V, (j + 1) / V - u)
+    (the lower side only when j > 0), in probability units."""
+    B, gamma = 6, 2
+    X, Y = _rows(B, gamma, V)
+    d = np.zeros((B, gamma), np.int32)
+    T = np.ones(B, np.float32)
+    tok, ln, (m_acc, m_cut, m_draw), st = oracle.verify(X, Y, d, T, 0, 1.0, 21, cut_margin=True)
+    assert st == 0 and np.all(ln == gamma + 1)
+    for b in range(B):
+        u = oracle.uniforms(21, b, gamma)[1]
+        j = int(np.floor(V * u))
+        assert tok[b, gamma] == j
+        want = (j + 1) / V - u
+        if j > 0:
+            want = min(want, u - j / V)
+        assert m_draw[b] == pytest.approx(want, rel=0, abs=1e-15)

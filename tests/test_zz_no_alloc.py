@@ -35,37 +35,43 @@ def dv():
     return m
 
 
-def _case():
+def _case(dtype, top_k, top_p):
     inp = synth.make_workload("b32_mixed_v248320", data_seed=21, seed=3, B=12, V=50021)
+    if dtype == "f32":
+        inp.target, inp.draft = synth.to_float(inp.target), synth.to_float(inp.draft)
     B, gamma, V = inp.shape
     d, _, _ = oracle.sample_rows(inp.draft.reshape(B * gamma, V),
                                  synth.draft_sampling_temperatures(inp.temperature, gamma),
-                                 inp.top_k, inp.top_p, 5)
+                                 top_k, top_p, 5)
     return inp, d.reshape(B, gamma)
 
 
-def _noalloc(lib, X, Y, d, T, B, gamma, V, top_k, top_p, seed, out_tok, out_len, st):
+def _noalloc(lib, X, Y, d, T, B, gamma, V, dt, top_k, top_p, seed, out_tok, out_len, st):
     stream = torch.cuda.current_stream().cuda_stream
     return lib.dflash_verify_noalloc(X.data_ptr(), Y.data_ptr(), d.data_ptr(), B, gamma, V,
-                                     0, T.data_ptr(), top_k, top_p, seed, out_tok.data_ptr(),
+                                     dt, T.data_ptr(), top_k, top_p, seed, out_tok.data_ptr(),
                                      out_len.data_ptr(), st.data_ptr(), stream)
 
 
-def test_noalloc_matches_workspace_entry_point_twice(dv):
+# the top-k filter in bf16 and fp32, and the full-vocabulary softmax (which
+# also uses the draw's part of the scratch and a second pass of launches)
+@pytest.mark.parametrize("dtype,top_k,top_p", [("bf16", 20, 0.95), ("f32", 20, 0.95), ("bf16", 0, 1.0)])
+def test_noalloc_matches_workspace_entry_point_twice(dv, dtype, top_k, top_p):
     lib = dv.load()
-    inp, d_np = _case()
+    inp, d_np = _case(dtype, top_k, top_p)
     B, gamma, V = inp.shape
+    dt = dv.DFLASH_BF16 if dtype == "bf16" else dv.DFLASH_F32
     X, Y = synth.to_torch(inp.target, DEV), synth.to_torch(inp.draft, DEV)
     d = torch.from_numpy(d_np).to(DEV)
     T = torch.from_numpy(inp.temperature).to(DEV)
-    assert lib.dflash_workspace_bytes(B, gamma, V, 0, 20, 0.95) <= lib.dflash_noalloc_scratch_bytes()
+    assert 0 < lib.dflash_workspace_bytes(B, gamma, V, dt, top_k, top_p) <= lib.dflash_noalloc_scratch_bytes()
     for seed in (3, 4):            # two calls in a row on the shared scratch
         want_st = torch.zeros(1, dtype=torch.int32, device=DEV)
-        want_tok, want_len = dv.verify(X, Y, d, T, inp.top_k, inp.top_p, seed, status=want_st)
+        want_tok, want_len = dv.verify(X, Y, d, T, top_k, top_p, seed, status=want_st)
         tok = torch.full((B, gamma + 1), -7, dtype=torch.int32, device=DEV)
         ln = torch.full((B,), -7, dtype=torch.int32, device=DEV)
         st = torch.zeros(1, dtype=torch.int32, device=DEV)
-        rc = _noalloc(lib, X, Y, d, T, B, gamma, V, inp.top_k, inp.top_p, seed, tok, ln, st)
+        rc = _noalloc(lib, X, Y, d, T, B, gamma, V, dt, top_k, top_p, seed, tok, ln, st)
         assert rc == 0, lib.dflash_last_error()
         torch.cuda.synchronize()
         assert torch.equal(tok, want_tok) and torch.equal(ln, want_len)
