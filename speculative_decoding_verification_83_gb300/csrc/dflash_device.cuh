@@ -261,6 +261,11 @@ __device__ __forceinline__ uint32_t warp_max_u32(uint32_t v) {
   for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
 }
+__device__ __forceinline__ float warp_max_f32(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
 __device__ __forceinline__ unsigned long long shfl_xor_u64(unsigned long long v, int m) {
   uint32_t lo = __shfl_xor_sync(0xffffffffu, (uint32_t)v, m);
   uint32_t hi = __shfl_xor_sync(0xffffffffu, (uint32_t)(v >> 32), m);

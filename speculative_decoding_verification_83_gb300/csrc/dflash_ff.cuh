@@ -113,6 +113,20 @@ __device__ __forceinline__ ff exp_ff(ff a, const float* th, const float* tl) {
 }
 
 
+// (a_hi + a_lo) / T as a pair: the rounded quotient of a_hi, the exact
+// remainder of that division plus a_lo, divided by T (the low part's own
+// rounding is below 2^-48 of the quotient)
+__device__ __forceinline__ ff quot_ff(float a_hi, float a_lo, float T) {
+  const float q = __fdiv_rn(a_hi, T);
+  const float rem = __fmaf_rn(-q, T, a_hi);
+  return fast_two_sum(q, __fdiv_rn(__fadd_rn(rem, a_lo), T));
+}
+// exp((x - m) / T) for x <= m, as a pair (0 for x = -inf)
+__device__ __forceinline__ ff exp_diff_ff(float x, float m, float T, const float* th, const float* tl) {
+  const ff d = two_sum(x, -m);
+  return exp_ff(quot_ff(d.hi, d.lo, T), th, tl);
+}
+
 // warp-wide inclusive prefix sum of pairs over lanes (five shuffle steps)
 __device__ __forceinline__ ff warp_inclusive_scan_ff(ff a, int lane) {
 #pragma unroll

@@ -59,6 +59,7 @@
 #include <mutex>
 
 #include "dflash_device.cuh"
+#include "dflash_ff.cuh"
 #include "dflash_internal.h"
 #include "dflash_rule.cuh"
 
@@ -76,7 +77,10 @@ struct PieceDesc {
 };
 constexpr int kDescArgmax = 256;  // the consumers track this row's argmax in-stream
 constexpr int kDescStats = 512;   // the consumers reduce the piece to (max, sum of exp)
-constexpr float kLog2e = 1.4426950408889634f;
+// log2(e) = kLog2eHi + kLog2eLo (the nearest float and the rest)
+constexpr float kLog2eHi = 1.4426950216293335f;
+constexpr float kLog2eLo = 1.925963033500011e-08f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 struct Smem {
   alignas(128) unsigned char ring[kStages][kPieceBytes];
@@ -92,9 +96,10 @@ struct Smem {
       int32_t idx[kMaxRowsPerRequest][33];
       float prob[kMaxRowsPerRequest][33];
     } lists;
-    struct {  // full-vocabulary request final: per row max, sum of exp, bad flag
+    struct {  // full-vocabulary request final: per row max, sum of exp (a pair), bad flag
       float m[kMaxRowsPerRequest];
       float s[kMaxRowsPerRequest];
+      float s_lo[kMaxRowsPerRequest];
       int bad[kMaxRowsPerRequest];
     } fv;
   } u;
@@ -1058,78 +1063,61 @@ __device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, in
   }
 }
 
-// Online (max, sum of exp) of a running set: folds in a block whose largest
-// value is bm and rescales the sum when the maximum grows. An empty set is
-// (-inf, 0).
-__device__ __forceinline__ void stats_raise(float& m, float& s, float bm, float scale) {
-  if (bm > m) {
-    s = m == -INFINITY ? 0.0f : s * ex2_approx((m - bm) * scale);
-    m = bm;
-  }
-}
-// (m, s) of two sets combined
-__device__ __forceinline__ void stats_merge(float& m, float& s, float m2, float s2, float scale) {
-  if (m2 == -INFINITY) return;
-  stats_raise(m, s, m2, scale);
-  s += s2 * ex2_approx((m2 - m) * scale);
-}
-
-// Full-vocabulary rows: a piece's largest logit m and sum of 2^((x - m) *
-// scale) = exp((x - m) / T), written as one float2 per piece (sum NaN when
-// the piece holds a NaN). Precise enough for the accept test; the draw
-// recomputes its sums in float-float.
-// The request's temperature is fetched here, by the consumer warp, not by the
-// producer: a dependent load per piece on the single thread that issues the
-// bulk copies slows the whole stream.
+// Full-vocabulary rows: a piece's largest logit m and its sum of
+// exp((x - m) / T) = 2^((x - m) s), s = log2(e) / T, written as one float4
+// per piece (m, the sum as a float-float pair, NaN flag). The piece's
+// maximum comes first (one pass over the stage), so no sum is rescaled; the
+// weights (2^x on the special-function unit) of a lane's block are added
+// pairwise, the block sums are accumulated and the lanes merged in
+// float-float. The request's temperature is fetched here, by the consumer
+// warp, not by the producer: a dependent load per piece on the single
+// thread that issues the bulk copies slows the whole stream.
 template <int DT>
-__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, const float* temperature, float2* out,
+__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, const float* temperature, float4* out,
                                             int lane) {
-  const float scale = kLog2e / __ldg(temperature);  // log2(e) / T, as the request final computes it
-  float m = -INFINITY, s = 0.0f;
-  bool nan = false;
+  const float s = __fdiv_rn(kLog2eHi, __ldg(temperature));  // log2(e) / T, rounded
+  float m = -INFINITY;
+#pragma unroll 4
+  for (int r = 0; r < kRoundsPerPiece; ++r) {
+    const int v = 32 * r + lane;
+    if (v < nvec) m = max_nan(m, vector_max<DT>(st4[v]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+  ff acc = {0.0f, 0.0f};
+  if (m > -INFINITY && m < INFINITY) {  // the same in every lane
 #pragma unroll 2
-  for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
-    uint4 wv[4];
-    float bm = -INFINITY;
+    for (int blk = 0; blk < kTilesPerPiece / 4; ++blk) {
+      float bs[4];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int v = 32 * (4 * blk + rr) + lane;
-      if (v < nvec) {
-        wv[rr] = st4[v];
-        bm = max_nan(bm, vector_max<DT>(wv[rr]));
-      }
-    }
-    nan |= isnan(bm);
-    stats_raise(m, s, bm, scale);
-    if (m == -INFINITY) continue;  // nothing above -inf yet
-    // (x - m) first: exact or nearly so for the logits that carry the mass,
-    // and no overflow of m * scale at small temperatures
+      for (int rr = 0; rr < 4; ++rr) {
+        const int v = 32 * (4 * blk + rr) + lane;
+        bs[rr] = 0.0f;
+        if (v < nvec) {
+          const uint4 wv = st4[v];
+          const uint32_t ws[4] = {wv.x, wv.y, wv.z, wv.w};
+          float e[4];
 #pragma unroll
-    for (int rr = 0; rr < 4; ++rr) {
-      const int v = 32 * (4 * blk + rr) + lane;
-      if (v >= nvec) continue;
-      const uint32_t ws[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
-      if (DT == 0) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          s += ex2_approx((__uint_as_float(ws[e] << 16) - m) * scale);
-          s += ex2_approx((__uint_as_float(ws[e] & 0xffff0000u) - m) * scale);
+          for (int q = 0; q < 4; ++q) {
+            if (DT == 0)
+              e[q] = __fadd_rn(ex2_approx(__fmul_rn(__uint_as_float(ws[q] << 16) - m, s)),
+                               ex2_approx(__fmul_rn(__uint_as_float(ws[q] & 0xffff0000u) - m, s)));
+            else
+              e[q] = ex2_approx(__fmul_rn(__uint_as_float(ws[q]) - m, s));
+          }
+          bs[rr] = __fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3]));
         }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) s += ex2_approx((__uint_as_float(ws[e]) - m) * scale);
       }
+      acc = ff_add(acc, two_sum(__fadd_rn(bs[0], bs[1]), __fadd_rn(bs[2], bs[3])));
     }
   }
-  // combine the lanes
+  // the lanes share m: a float-float tree, lane 0's result
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
-    stats_merge(m, s, m2, s2, scale);
+    const ff b = shfl_down_ff(acc, o);
+    if (lane + o < 32) acc = ff_add(acc, b);
   }
-  nan = __any_sync(0xffffffffu, nan);
-  if (lane == 0) *out = make_float2(m, nan ? __int_as_float(0x7fffffff) : s);
+  if (lane == 0) *out = make_float4(m, acc.hi, acc.lo, isnan(m) ? 1.0f : 0.0f);
 }
 
 // Consumer warp: reduces whole pieces (this warp takes every 8th piece of the
@@ -1162,7 +1150,7 @@ __device__ void consumer(const Params& p, Smem& S, long long total) {
     const uint4* st4 = reinterpret_cast<const uint4*>(S.ring[stage]);
     if (dsc.head & kDescStats)
       piece_stats<DT>(st4, nvec, p.temperature + S.req_of_ord[dsc.ord],
-                      reinterpret_cast<float2*>(p.tile_keys + (size_t)dsc.slot * p.geo.tiles) + dsc.pp, lane);
+                      reinterpret_cast<float4*>(p.tile_keys + (size_t)dsc.slot * p.geo.tiles) + dsc.pp, lane);
     else
       piece_keys<DT>(p, st4, nvec, dsc.slot, dsc.pp, (dsc.head & kDescArgmax) != 0, dsc.head & (kDescArgmax - 1),
                      lane);
@@ -1328,39 +1316,53 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
   const bool det = p.det != 0;  // deterministic drafts: target rows only, q(d) = 1
   const int b = S.req_of_ord[ord];
   const int slot0 = ord * per_s;
-  const float scale = kLog2e / ld_nc_now(p.temperature + b);  // as the producer computed it
+  const float T_b = ld_nc_now(p.temperature + b);
   const int32_t d_lane = (w == 0 && lane < gamma) ? ld_nc_now(p.draft_tokens + (size_t)b * gamma + lane) : -1;
+  // each row's largest logit m and normaliser sum exp((x - m) / T), from its
+  // pieces' (m_p, sum_p) and the logits outside its aligned body: every
+  // piece's sum is rescaled by exp((m_p - m) / T) and added in float-float
   for (int r = w; r < per_s; r += kFinWarps) {
     const SlotInfo si = slot_info(p, S, slot0 + r);
     const RowBody rb = row_body(si.ptr, V, p.geo.esize);
-    const float2* st = reinterpret_cast<const float2*>(p.tile_keys + (size_t)(slot0 + r) * p.geo.tiles);
-    float m = -INFINITY, sum = 0.0f;
-    bool nan = false;
-    for (int pp = lane; pp < p.geo.ppr; pp += 32) {
-      const float2 v = __ldcg(st + pp);
-      nan |= isnan(v.y);
-      stats_merge(m, sum, v.x, v.y, scale);
-      // leave the region at zero: rows of later calls take tile keys there
-      const_cast<float2*>(st)[pp] = make_float2(0.0f, 0.0f);
-    }
+    float4* st = reinterpret_cast<float4*>(p.tile_keys + (size_t)(slot0 + r) * p.geo.tiles);
     const int n_edge = rb.head + (V - rb.tail_start);
+    bool nan = false;
+    float m = -INFINITY;
+    for (int pp = lane; pp < p.geo.ppr; pp += 32) {
+      const float4 v = __ldcg(st + pp);
+      nan |= v.w != 0.0f || isnan(v.x);
+      m = fmaxf(m, v.x);
+    }
     for (int e = lane; e < n_edge; e += 32) {
-      const int j = e < rb.head ? e : rb.tail_start + (e - rb.head);
-      const float x = load_logit(rb.row, j, DT);
+      const float x = load_logit(rb.row, e < rb.head ? e : rb.tail_start + (e - rb.head), DT);
       nan |= isnan(x);
-      if (!isnan(x)) stats_merge(m, sum, x, 1.0f, scale);
+      m = fmaxf(m, x);
+    }
+    m = warp_max_f32(m);
+    nan = __any_sync(0xffffffffu, nan);
+    ff sum = {0.0f, 0.0f};
+    if (!nan && m > -INFINITY && m < INFINITY) {
+      for (int pp = lane; pp < p.geo.ppr; pp += 32) {
+        const float4 v = __ldcg(st + pp);
+        if (v.x > -INFINITY) sum = ff_add(sum, ff_mul(ff{v.y, v.z}, exp_diff_ff(v.x, m, T_b, S.exp_hi, S.exp_lo)));
+      }
+      for (int e = lane; e < n_edge; e += 32) {
+        const float x = load_logit(rb.row, e < rb.head ? e : rb.tail_start + (e - rb.head), DT);
+        sum = ff_add(sum, exp_diff_ff(x, m, T_b, S.exp_hi, S.exp_lo));
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-      const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
-      stats_merge(m, sum, m2, s2, scale);
+      const ff o2 = shfl_down_ff(sum, o);
+      if (lane + o < 32) sum = ff_add(sum, o2);
     }
-    nan = __any_sync(0xffffffffu, nan);
+    // leave the region at zero: rows of later calls take tile keys there
+    for (int pp = lane; pp < p.geo.ppr; pp += 32) st[pp] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (lane == 0) {
       S.u.fv.m[r] = m;
-      S.u.fv.s[r] = sum;
-      S.u.fv.bad[r] = (nan || isnan(sum) || !(fabsf(m) < INFINITY)) ? 1 : 0;
+      S.u.fv.s[r] = sum.hi;
+      S.u.fv.s_lo[r] = sum.lo;
+      S.u.fv.bad[r] = (nan || !(fabsf(m) < INFINITY) || !(sum.hi > 0.0f)) ? 1 : 0;
     }
   }
   fin_sync();
@@ -1380,14 +1382,17 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
         stop = true;  // a bad row ends the loop at its position
       } else {
         // a token outside the vocabulary has p = q = 0; a deterministic draft has q = 1
+        // p(d) = exp((x_d - m) / T) / sum, in float-float, rounded once
         float p_d = 0.0f, q_d = det ? 1.0f : 0.0f;
         if (valid) {
           const SlotInfo sx = slot_info(p, S, slot0 + ti);
-          p_d = ex2_approx((load_logit(sx.ptr, di, DT) - S.u.fv.m[ti]) * scale) / S.u.fv.s[ti];
+          p_d = ff_round(ff_mul(exp_diff_ff(load_logit(sx.ptr, di, DT), S.u.fv.m[ti], T_b, S.exp_hi, S.exp_lo),
+                                ff_recip(ff{S.u.fv.s[ti], S.u.fv.s_lo[ti]})));
           if (!det) {
-            const SlotInfo sy = slot_info(p, S, slot0 + 2 * i + 1);
-            q_d = ex2_approx((load_logit(sy.ptr, di, DT) - S.u.fv.m[2 * i + 1]) * scale) /
-                  S.u.fv.s[2 * i + 1];
+            const int ty = 2 * i + 1;
+            const SlotInfo sy = slot_info(p, S, slot0 + ty);
+            q_d = ff_round(ff_mul(exp_diff_ff(load_logit(sy.ptr, di, DT), S.u.fv.m[ty], T_b, S.exp_hi, S.exp_lo),
+                                  ff_recip(ff{S.u.fv.s[ty], S.u.fv.s_lo[ty]})));
           }
         }
         const uint4 wd = step_uniform_words(p.seed, (uint32_t)b, (uint32_t)i, 0u);
@@ -1483,10 +1488,6 @@ __device__ void finals(const Params& p, Smem& S) {
   const int n_row_jobs = fv ? 0 : (verify ? S.n_samp * samp_slots(p) : p.B);
   const int ord0 = 0;  // every request has a final job (sampling first, then greedy)
   const int n_jobs = n_row_jobs + (verify ? p.B - ord0 : 0);
-  if (gt < kExpTable) {
-    S.exp_hi[gt] = p.exp2.hi[gt];
-    S.exp_lo[gt] = p.exp2.lo[gt];
-  }
   if (gt == kFinDrawer) S.fin_slot = (int)atomicAdd(p.job_cnt, 1u);
   fin_sync();
   int j = S.fin_slot;
@@ -1511,6 +1512,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
   Smem& S = *reinterpret_cast<Smem*>(smem_raw);
   const int tid = threadIdx.x, warp = tid >> 5;
 
+  // Tang's exp table (float-float exp of the filters and the full-vocabulary
+  // statistics), from the kernel parameters
+  if (tid < kExpTable) {
+    S.exp_hi[tid] = p.exp2.hi[tid];
+    S.exp_lo[tid] = p.exp2.lo[tid];
+  }
   // the mbarriers, one per thread of the warps that load no temperatures
   // (the consumer threads' loads of the request order are in flight meanwhile)
   static_assert(kThreads - kConsumers >= 2 * (kStages + kKeyQueue), "one thread per mbarrier");

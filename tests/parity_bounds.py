@@ -25,8 +25,19 @@ kept probability is its exact value to 2^-29, rounded once to fp32
 Full-vocabulary filter: the draw is float-float over the whole row
 (dflash_fullvocab.cu), no fp32 list values in between: each side within
 2^-29 and two fp32 roundings (<= 2u)               -> FV_DRAW_ABS = 2^-22
-Its accept test uses the stream's fp32 normalisers (sums of ex2.approx
-weights), bounded in the design notes by FV_ACCEPT_REL.
+Its accept test takes p(d) = exp((x_d - m)/T) / sum with a float-float
+numerator and the row normaliser sum from the stream: each weight there is
+2^x on the special-function unit (relative error below 2^-22.73, measured
+over every fp32 argument in [-126, 0]) of an exponent rounded on the way:
+x = (logit - m) s with s = RN(log2(e) / T) (1.22u), one product rounding (u)
+and, for fp32 logits, the difference (u); a relative error e in the
+exponent x <= 0 changes the weight by ln2 |x| e, and the weighted mean of
+|x| over the row is at most its entropy in bits, <= log2 V = 17.92 at
+V = 248320: <= 0.693 * 17.92 * 3.22u = 40u. Block sums are pairwise (<= 5u),
+everything above them float-float. So
+  sum:        <= 2.42u + 40u + 5u = 47.4u
+  p(d), q(d): <= 47.4u + u (rounded once)           -> FV_PROB_REL = 2^-18
+  the ratio (two of them, rounded) and the oracle's -> FV_ACCEPT_REL = 2^-17
 """
 
 U = 2.0 ** -24
@@ -34,7 +45,8 @@ ACCEPT_REL = 2.0 ** -21
 CUT_REL = 2.0 ** -21
 DRAW_ABS = 2.0 ** -21
 FV_DRAW_ABS = 2.0 ** -22
-FV_ACCEPT_REL = 2.0 ** -16
+FV_PROB_REL = 2.0 ** -18
+FV_ACCEPT_REL = 2.0 ** -17
 
 # the sampling-mode bar: rows (tokens and accept length) equal on >= 99.99%
 ROW_BAR = 1e-4
