@@ -47,9 +47,14 @@
  *    off); softmax over the survivors; top-p keeps the shortest prefix of
  *    that order whose mass reaches top_p (top_p >= 1: off) and renormalises.
  *    Supported: 1 <= top_k <= DFLASH_MAX_TOP_K with any top_p in (0, 1], or
- *    top-k off with top_p >= 1 (full-vocabulary softmax; dflash_verify and
- *    dflash_verify_host only). Other combinations return
+ *    top-k off with any top_p (the full-vocabulary softmax, with top_p < 1
+ *    cut by mass over the whole vocabulary, V <= 2^22; the verification entry
+ *    points and dflash_sample). Other combinations return
  *    DFLASH_ERR_UNSUPPORTED.
+ *    Over the full vocabulary with top_p < 1 the cut is taken on exact
+ *    fixed-point sums of the float-float weights, the decision "mass before
+ *    token j, over the row's mass, rounds (fp32) below top_p" in the order
+ *    logit descending, token index ascending.
  */
 #ifndef DFLASH_VERIFY_H
 #define DFLASH_VERIFY_H
@@ -137,9 +142,9 @@ int dflash_workspace_cancel(void* workspace, size_t bytes, void* stream);
  * Accept test at position i: u < p_i(d_i) / q_i(d_i) in fp32 (q = 0 with
  * p > 0 accepts; p = q = 0 rejects). The residual and bonus draws take the
  * smallest token index whose cumulative weight (ascending token order)
- * exceeds u * total; over the full vocabulary (top-k off, top_p >= 1) the
- * cumulative weights are carried in float-float and the comparison is taken
- * on their fp32 roundings. 1 <= gamma <= 32, 1 <= V < 2^31, 1 <= B <= 2048. */
+ * exceeds u * total; over the full vocabulary (top-k off) the cumulative
+ * weights are carried in float-float and the comparison is taken on their
+ * fp32 roundings (with top_p < 1 only the kept tokens weigh). 1 <= gamma <= 32, 1 <= V < 2^31, 1 <= B <= 2048. */
 int dflash_verify(const void* target_logits, const void* draft_logits,
                   const int32_t* draft_tokens, int B, int gamma, int V, int dtype,
                   const float* temperature, int top_k, float top_p, uint64_t seed,
@@ -193,8 +198,9 @@ int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
  * bits as for dflash_verify without draft_logits; workspace_bytes >=
  * dflash_workspace_bytes(...) of the same shape and filter. Filters as for
  * dflash_verify: top-k on (1 <= top_k <= DFLASH_MAX_TOP_K, top_k < V) with any
- * top_p, or the full-vocabulary softmax (top-k off, top_p = 1), where the
- * residual p without d is drawn over the whole vocabulary in float-float. */
+ * top_p, or top-k off with any top_p, where the residual p without d is
+ * drawn over the whole vocabulary (its kept set when top_p < 1) in
+ * float-float. */
 int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, int B, int gamma,
                       int V, int dtype, const float* temperature, int top_k, float top_p,
                       uint64_t seed, int32_t* out_tokens, int32_t* out_accept_len,
@@ -277,7 +283,9 @@ int dflash_filter(const void* logits, int R, int V, int dtype, const float* temp
 /* One token per row from its filtered distribution (the drafter's side of
  * the loop): temperature[r] == 0 takes the argmax; otherwise the inverse CDF
  * in ascending token order with the accept uniform of Philox counter
- * (r, 0, 1, 0). out_tokens [device] int32 [R]. */
+ * (r, 0, 1, 0). out_tokens [device] int32 [R]. Filters: top-k on as for
+ * dflash_verify, or top-k off with any top_p (drawn over the whole
+ * vocabulary, or its top-p set, in float-float). */
 int dflash_sample(const void* logits, int R, int V, int dtype, const float* temperature,
                   int top_k, float top_p, uint64_t seed, int32_t* out_tokens, void* workspace,
                   size_t workspace_bytes, uint32_t* status, void* stream);

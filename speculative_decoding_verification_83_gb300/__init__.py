@@ -18,7 +18,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash_verify.so")
-SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_candidates.cu", "dflash_abi.cu", "dflash_noalloc.cu"]
+SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_fvtp.cu", "dflash_candidates.cu", "dflash_abi.cu",
+           "dflash_noalloc.cu"]
 HEADERS = ["dflash_device.cuh", "dflash_internal.h", "dflash_rule.cuh", "dflash_ff.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]

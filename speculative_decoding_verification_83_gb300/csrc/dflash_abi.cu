@@ -93,15 +93,22 @@ int available_sms(int dev) {
 int esize_of(int dtype) { return dtype == DFLASH_BF16 ? 2 : (dtype == DFLASH_F32 ? 4 : 0); }
 
 // Filter mode of a call: 1 = top-k (1..32) with any top_p, 2 = full
-// vocabulary (top-k off, top_p >= 1), 0 = unsupported, -1 = invalid.
-constexpr int kModeTopK = 1, kModeFullVocab = 2;
+// vocabulary (top-k off, top_p >= 1), 3 = top-p over the full vocabulary
+// (top-k off, top_p < 1), 0 = unsupported, -1 = invalid.
+constexpr int kModeTopK = 1, kModeFullVocab = 2, kModeFullVocabTopP = 3;
+// The top-p cut over the full vocabulary sums fixed-point weights in 64 bits
+// with 62 - ceil(log2 V) fractional bits: the sums' error, as a fraction of
+// the row's mass, is below V^2 2^-62, which stays under 2^-18 up to 2^22 tokens.
+constexpr int kFvtpMaxV = 1 << 22;
 int filter_mode(int V, int top_k, float top_p) {
   if (!(top_p > 0.0f) || std::isnan(top_p)) return -1;
   const bool k_on = top_k > 0 && top_k < V;
   if (k_on && top_k <= DFLASH_MAX_TOP_K) return kModeTopK;
   if (!k_on && top_p >= 1.0f) return kModeFullVocab;
+  if (!k_on && V <= kFvtpMaxV) return kModeFullVocabTopP;
   return 0;
 }
+bool whole_vocab(int mode) { return mode == kModeFullVocab || mode == kModeFullVocabTopP; }
 
 // 2^(j/64), j < 64, split into fp32 pairs (hi = nearest float, lo = the rest)
 // for the full-vocabulary draw's exp; computed once in double precision.
@@ -135,13 +142,14 @@ int check_aligned(const void* p, int esize, const char* name) {
   return DFLASH_OK;
 }
 
-size_t verify_workspace(int B, int gamma, int V, int dtype, bool fullvocab = false) {
+size_t verify_workspace(int B, int gamma, int V, int dtype, int mode = kModeTopK) {
   const Geometry g = make_geometry(V, esize_of(dtype));
-  return make_layout(B * (2 * gamma + 1), B, g, fullvocab).total;
+  return make_layout(B * (2 * gamma + 1), B, g, whole_vocab(mode), mode == kModeFullVocabTopP).total;
 }
 
-void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, bool fullvocab = false) {
-  const WorkspaceLayout L = make_layout(n_slots, n_requests, p.geo, fullvocab);
+void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, int mode = kModeTopK) {
+  const bool fullvocab = whole_vocab(mode);
+  const WorkspaceLayout L = make_layout(n_slots, n_requests, p.geo, fullvocab, mode == kModeFullVocabTopP);
   unsigned char* base = static_cast<unsigned char*>(ws);
   p.row_cnt = reinterpret_cast<uint32_t*>(base + L.row_cnt);
   p.abort_flag = reinterpret_cast<uint32_t*>(base + L.abort_flag);
@@ -150,12 +158,63 @@ void bind_workspace(Params& p, void* ws, int n_slots, int n_requests, bool fullv
   p.tile_keys = reinterpret_cast<uint32_t*>(base + L.tile_keys);
   p.res_list = reinterpret_cast<unsigned long long*>(base + L.res_list);
   p.fv_draw = fullvocab ? reinterpret_cast<FvDraw*>(base + L.fv_draw) : nullptr;
+  p.fullvocab = fullvocab ? 1 : 0;
+  p.fvtp = mode == kModeFullVocabTopP ? 1 : 0;
+  p.fvtp_rows = p.fvtp ? reinterpret_cast<float4*>(base + L.tp_rows) : nullptr;
   p.n_slots = n_slots;
+}
+
+int ceil_log2(long long v) {
+  int c = 0;
+  while ((1ll << c) < v) ++c;
+  return c;
+}
+
+// top-p over the full vocabulary: the rows' cuts and the accept tests, between
+// the stream and the draw
+int run_fvtp(const Params& p, void* ws, void* stream, bool sampler) {
+  const WorkspaceLayout L = make_layout(p.n_slots, p.B, p.geo, true, true);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  FvtpParams t;
+  memset(&t, 0, sizeof t);
+  t.target = p.target;
+  t.draft = p.draft;
+  t.draft_tokens = p.draft_tokens;
+  t.temperature = p.temperature;
+  t.B = p.B;
+  t.gamma = p.gamma;
+  t.V = p.geo.V;
+  t.dtype = p.dtype;
+  t.det = p.det;
+  t.per_s = p.det ? p.gamma + 1 : 2 * p.gamma + 1;
+  t.n_slices = fv_slices(p.geo.V);
+  t.frac_bits = 62 - ceil_log2(p.geo.V);  // the row's mass, at most V, fits 63 bits
+  t.rounds = p.dtype == 0 ? 2 : 4;         // key bytes to find (bf16 keys: the upper two)
+  t.top_p = p.top_p;
+  t.seed = p.seed;
+  t.sampler = sampler ? 1 : 0;
+  t.row_base = p.row_base;
+  t.out_tokens = p.out_tokens;
+  t.out_len = p.out_len;
+  t.status = p.status;
+  t.audit_pq = p.audit_pq;
+  t.rows = reinterpret_cast<float4*>(base + L.tp_rows);
+  t.cut = reinterpret_cast<FvtpCut*>(base + L.tp_cut);
+  t.hist_m = reinterpret_cast<unsigned long long*>(base + L.tp_hist_m);
+  t.hist_c = reinterpret_cast<uint32_t*>(base + L.tp_hist_c);
+  t.kcount = reinterpret_cast<uint32_t*>(base + L.tp_kcount);
+  t.draw = reinterpret_cast<FvDraw*>(base + L.fv_draw);
+  t.draw_cut = reinterpret_cast<FvtpDrawCut*>(base + L.tp_draw);
+  t.abort_flag = p.abort_flag;
+  t.exp2 = p.exp2;
+  const int e = launch_fvtp_cut(t, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "launching the top-p cut over the full vocabulary");
+  return DFLASH_OK;
 }
 
 // the full-vocabulary draw's second pass over the rows the accept test left
 int run_fullvocab_draw(const Params& p, void* ws, void* stream, bool sampler = false) {
-  const WorkspaceLayout L = make_layout(p.n_slots, p.B, p.geo, true);
+  const WorkspaceLayout L = make_layout(p.n_slots, p.B, p.geo, true, p.fvtp != 0);
   unsigned char* base = static_cast<unsigned char*>(ws);
   FvParams f;
   memset(&f, 0, sizeof f);
@@ -176,6 +235,7 @@ int run_fullvocab_draw(const Params& p, void* ws, void* stream, bool sampler = f
   f.abort_flag = p.abort_flag;
   f.sampler = sampler ? 1 : 0;
   f.row_base = p.row_base;
+  f.cut = p.fvtp ? reinterpret_cast<FvtpDrawCut*>(base + L.tp_draw) : nullptr;
   const Exp2Table& t = exp2_table();
   memcpy(f.exp_hi, t.hi, sizeof t.hi);
   memcpy(f.exp_lo, t.lo, sizeof t.lo);
@@ -203,6 +263,15 @@ int run(Params& p, int total_slots, void* stream) {
   return DFLASH_OK;
 }
 
+// the stream, then (top-p over the full vocabulary) the cut and accept
+// kernels, then (either full-vocabulary mode) the draw
+int run_step(Params& p, int total_slots, void* ws, void* stream, bool sampler = false) {
+  int rc = run(p, total_slots, stream);
+  if (rc || !p.fullvocab) return rc;
+  if (p.fvtp && (rc = run_fvtp(p, ws, stream, sampler))) return rc;
+  return run_fullvocab_draw(p, ws, stream, sampler);
+}
+
 Params base_params(int dtype, int V) {
   Params p;
   memset(&p, 0, sizeof p);
@@ -228,15 +297,15 @@ size_t dflash_workspace_bytes(int B, int gamma, int V, int dtype, int top_k, flo
   if (B < 1 || B > kMaxB || gamma < 1 || gamma > kMaxGamma || V < 1 || !esize_of(dtype)) return 0;
   const int mode = filter_mode(V, top_k, top_p);
   if (mode <= 0 && !(top_k == 1 && top_p >= 1.0f)) return 0;
-  return verify_workspace(B, gamma, V, dtype, mode == kModeFullVocab);
+  return verify_workspace(B, gamma, V, dtype, mode > 0 ? mode : kModeTopK);
 }
 
 size_t dflash_rows_workspace_bytes(int R, int V, int dtype, int top_k, float top_p) {
   if (R < 1 || V < 1 || !esize_of(dtype)) return 0;
   const int mode = filter_mode(V, top_k, top_p);
-  if (mode == kModeFullVocab) {  // the sampler over the full vocabulary: rows of kMaxB at a time
+  if (whole_vocab(mode)) {  // the sampler over the full vocabulary: rows of kMaxB at a time
     const int chunk = R < kMaxB ? R : kMaxB;
-    return verify_workspace(chunk, 0, V, dtype, true);
+    return verify_workspace(chunk, 0, V, dtype, mode);
   }
   if (mode != kModeTopK) return 0;
   const int chunk = R < kMaxCounterSlots ? R : kMaxCounterSlots;
@@ -280,15 +349,14 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
   if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
   if (mode == 0)
     return fail(DFLASH_ERR_UNSUPPORTED,
-                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d and top_k < V, or top-k "
-                "off with top_p = 1)",
-                top_k, (double)top_p, DFLASH_MAX_TOP_K);
-  const bool fullvocab = mode == kModeFullVocab;
+                "top_k=%d with top_p=%g is not supported (need 1 <= top_k <= %d and top_k < V, or top-k off; "
+                "top-k off with top_p < 1 needs V <= %d)",
+                top_k, (double)top_p, DFLASH_MAX_TOP_K, kFvtpMaxV);
   const int es = esize_of(dtype);
   if ((rc = check_aligned(target_logits, es, "target_logits")) ||
       (rc = check_aligned(draft_logits, es, "draft_logits")))
     return rc;
-  const size_t need = verify_workspace(B, gamma, V, dtype, fullvocab);
+  const size_t need = verify_workspace(B, gamma, V, dtype, mode);
   if (workspace_bytes < need)
     return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, need);
@@ -303,16 +371,13 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
   p.top_p = top_p >= 1.0f ? 1.0f : top_p;
   p.seed = seed;
   p.task = kTaskVerify;
-  p.fullvocab = fullvocab ? 1 : 0;
   p.out_tokens = out_tokens;
   p.out_len = out_accept_len;
   p.audit_pq = audit_pq;
   p.status = status;
-  bind_workspace(p, workspace, B * (2 * gamma + 1), B, fullvocab);
+  bind_workspace(p, workspace, B * (2 * gamma + 1), B, mode);
   // the slot count depends on the device-side temperatures; launch for the maximum
-  rc = run(p, B * (2 * gamma + 1), stream);
-  if (rc || !fullvocab) return rc;
-  return run_fullvocab_draw(p, workspace, stream);
+  return run_step(p, B * (2 * gamma + 1), workspace, stream);
 }
 }  // namespace
 
@@ -352,11 +417,10 @@ int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, in
   if (mode == 0)
     return fail(DFLASH_ERR_UNSUPPORTED,
                 "top_k=%d with top_p=%g is not supported for deterministic drafts (need 1 <= top_k <= %d "
-                "and top_k < V, or top-k off with top_p = 1)",
+                "and top_k < V, or top-k off)",
                 top_k, (double)top_p, DFLASH_MAX_TOP_K);
-  const bool fullvocab = mode == kModeFullVocab;
   if ((rc = check_aligned(target_logits, esize_of(dtype), "target_logits"))) return rc;
-  const size_t need = verify_workspace(B, gamma, V, dtype, fullvocab);
+  const size_t need = verify_workspace(B, gamma, V, dtype, mode);
   if (workspace_bytes < need)
     return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
                 workspace_bytes, need);
@@ -371,14 +435,11 @@ int dflash_verify_det(const void* target_logits, const int32_t* draft_tokens, in
   p.seed = seed;
   p.task = kTaskVerify;
   p.det = 1;
-  p.fullvocab = fullvocab ? 1 : 0;
   p.out_tokens = out_tokens;
   p.out_len = out_accept_len;
   p.status = status;
-  bind_workspace(p, workspace, B * (gamma + 1), B, fullvocab);
-  rc = run(p, B * (gamma + 1), stream);
-  if (rc || !fullvocab) return rc;
-  return run_fullvocab_draw(p, workspace, stream);  // reads target rows only: no residual mode here
+  bind_workspace(p, workspace, B * (gamma + 1), B, mode);
+  return run_step(p, B * (gamma + 1), workspace, stream);  // reads target rows only: no residual mode here
 }
 
 int dflash_verify_greedy(const void* target_logits, const int32_t* draft_tokens, int B, int gamma, int V,
@@ -503,8 +564,9 @@ int dflash_verify_host(const void* target_logits, const void* draft_logits, cons
 // vocabulary verification with no draft positions: each row is a request
 // whose only row is its bonus row, drawn from the whole softmax (T = 0: the
 // argmax), with the sampler's uniforms. Rows go kMaxB at a time.
-static int sample_fullvocab(const void* logits, int R, int V, int dtype, const float* temperature, uint64_t seed,
-                            int32_t* out_tokens, void* workspace, uint32_t* status, void* stream) {
+static int sample_fullvocab(const void* logits, int R, int V, int dtype, const float* temperature, float top_p,
+                            uint64_t seed, int32_t* out_tokens, void* workspace, uint32_t* status, void* stream) {
+  const int mode = top_p >= 1.0f ? kModeFullVocab : kModeFullVocabTopP;
   const size_t row_bytes = (size_t)V * esize_of(dtype);
   for (int r0 = 0; r0 < R; r0 += kMaxB) {
     const int n = R - r0 < kMaxB ? R - r0 : kMaxB;
@@ -516,18 +578,15 @@ static int sample_fullvocab(const void* logits, int R, int V, int dtype, const f
     p.B = n;
     p.gamma = 0;
     p.top_k = 0;
-    p.top_p = 1.0f;
+    p.top_p = top_p >= 1.0f ? 1.0f : top_p;
     p.seed = seed;
     p.task = kTaskVerify;
-    p.fullvocab = 1;
     p.row_base = r0;
     p.out_tokens = out_tokens + r0;
     p.out_len = nullptr;
     p.status = status;
-    bind_workspace(p, workspace, n, n, true);
-    int rc = run(p, n, stream);
-    if (rc) return rc;
-    rc = run_fullvocab_draw(p, workspace, stream, true);
+    bind_workspace(p, workspace, n, n, mode);
+    const int rc = run_step(p, n, workspace, stream, true);
     if (rc) return rc;
   }
   return DFLASH_OK;
@@ -541,10 +600,10 @@ static int rows_task(int task, const void* logits, int R, int V, int dtype, cons
   if (!logits || !temperature || !workspace) return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
   const int mode = filter_mode(V, top_k, top_p);
   if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
-  if (mode != kModeTopK && !(mode == kModeFullVocab && task == kTaskSample))
+  if (mode != kModeTopK && !(whole_vocab(mode) && task == kTaskSample))
     return fail(DFLASH_ERR_UNSUPPORTED,
                 "top_k=%d with top_p=%g is not supported here (need 1 <= top_k <= %d and top_k < V; the "
-                "sampler also takes top-k off with top_p = 1)",
+                "sampler also takes top-k off)",
                 top_k, (double)top_p, DFLASH_MAX_TOP_K);
   int rc = check_aligned(logits, esize_of(dtype), "logits");
   if (rc) return rc;
@@ -552,8 +611,8 @@ static int rows_task(int task, const void* logits, int R, int V, int dtype, cons
   if (workspace_bytes < need)
     return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed", workspace_bytes,
                 need);
-  if (mode == kModeFullVocab) return sample_fullvocab(logits, R, V, dtype, temperature, seed, out_tokens,
-                                                      workspace, status, stream);
+  if (whole_vocab(mode))
+    return sample_fullvocab(logits, R, V, dtype, temperature, top_p, seed, out_tokens, workspace, status, stream);
   Params p = base_params(dtype, V);
   p.temperature = temperature;
   p.gamma = 1;  // unused by the rows tasks (a row is its own slot); any valid value

@@ -64,7 +64,18 @@ struct Req {
   ff zmx, zmy;             // row maxima / T
   float sx0, sy0;          // the stream's fp32 normalisers (residual: which side of p = q)
   int excl;                // token with no weight in this draw (-1: none)
+  bool cut;                // top-p over the full vocabulary: only the kept sets weigh
+  uint32_t kx, ky;         // ... the key of each row's last kept token
+  int jx, jy;              // ... and the last kept index among that key's tokens
 };
+
+// whether token j (logit x) is in a row's kept set: every key above kappa,
+// and key kappa's tokens up to index j_cut
+__device__ __forceinline__ bool in_kept(bool cut, uint32_t kappa, int j_cut, float x, int j) {
+  if (!cut) return true;
+  const uint32_t k = key_of(x);
+  return k > kappa || (k == kappa && j <= j_cut);
+}
 
 __device__ __forceinline__ Req load_req(const FvParams& f, int b) {
   Req q;
@@ -89,6 +100,17 @@ __device__ __forceinline__ Req load_req(const FvParams& f, int b) {
   q.sx0 = d.sx0;
   q.sy0 = d.sy0;
   q.excl = d.mode == kFvBonus ? d.excl : -1;
+  q.cut = f.cut != nullptr;
+  if (q.cut) {
+    const FvtpDrawCut c = f.cut[b];
+    q.kx = c.kappa_x;
+    q.ky = c.kappa_y;
+    q.jx = c.jcut_x;
+    q.jy = c.jcut_y;
+  } else {
+    q.kx = q.ky = 0u;
+    q.jx = q.jy = 0;
+  }
   return q;
 }
 
@@ -182,7 +204,8 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   const int s = blockIdx.x, b = blockIdx.y;
   grid_dependency_sync();
   const Req q = load_req(f, b);
-  if (!q.live) return;
+  // one decision for the block: the abort flag can be raised while it runs
+  if (!__syncthreads_and(q.live)) return;
   load_table(f, th, tl);
   if (threadIdx.x == 0) {
     last_r = -1;
@@ -203,8 +226,9 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   if (q.residual) {
 #pragma unroll
     for (int k = 0; k < kFvPerThread; ++k) {
-      const ff wx = weight(xs[k], q.inv_t, q.zmx, th, tl);
-      const ff wy = weight(ys[k], q.inv_t, q.zmy, th, tl);
+      const int j = j0 + k * kFvThreads;
+      const ff wx = in_kept(q.cut, q.kx, q.jx, xs[k], j) ? weight(xs[k], q.inv_t, q.zmx, th, tl) : ff{0.0f, 0.0f};
+      const ff wy = in_kept(q.cut, q.ky, q.jy, ys[k], j) ? weight(ys[k], q.inv_t, q.zmy, th, tl) : ff{0.0f, 0.0f};
       acc_add(sx, wx);
       acc_add(sy, wy);
       if (__fmul_rn(wx.hi, q.sy0) > __fmul_rn(wy.hi, q.sx0)) {
@@ -217,8 +241,9 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   } else {
 #pragma unroll
     for (int k = 0; k < kFvPerThread; ++k) {
-      ff wx = weight(xs[k], q.inv_t, q.zmx, th, tl);
-      if (j0 + k * kFvThreads == q.excl) wx = {0.0f, 0.0f};  // p without the deterministic draft
+      const int j = j0 + k * kFvThreads;
+      ff wx = in_kept(q.cut, q.kx, q.jx, xs[k], j) ? weight(xs[k], q.inv_t, q.zmx, th, tl) : ff{0.0f, 0.0f};
+      if (j == q.excl) wx = {0.0f, 0.0f};  // p without the deterministic draft
       acc_add(sx, wx);
       if (wx.hi > 0.0f) lp = j0 + k * kFvThreads;
     }
@@ -240,12 +265,13 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
 // ---- launch 2: the draw -----------------------------------------------------------------
 // p_j and r_j = max(0, p_j - q_j) of a token with target logit x and draft
 // logit y (r = 0 for a bonus draw), normalised exactly
-__device__ __forceinline__ void token_weights(const Req& q, const Norm& nm, float x, float y, const float* th,
+__device__ __forceinline__ void token_weights(const Req& q, const Norm& nm, float x, float y, int j, const float* th,
                                               const float* tl, ff& p, ff& r) {
-  p = ff_mul(weight(x, q.inv_t, q.zmx, th, tl), nm.inv_sx);
+  p = in_kept(q.cut, q.kx, q.jx, x, j) ? ff_mul(weight(x, q.inv_t, q.zmx, th, tl), nm.inv_sx) : ff{0.0f, 0.0f};
   r = {0.0f, 0.0f};
   if (q.residual) {
-    const ff qq = ff_mul(weight(y, q.inv_t, q.zmy, th, tl), nm.inv_sy);
+    const ff qq =
+        in_kept(q.cut, q.ky, q.jy, y, j) ? ff_mul(weight(y, q.inv_t, q.zmy, th, tl), nm.inv_sy) : ff{0.0f, 0.0f};
     const ff d = ff_add(p, ff_neg(qq));
     if (d.hi > 0.0f) r = d;
   }
@@ -265,8 +291,11 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
   // every call leaves the workspace at zero (its regions move with the
   // shape): this launch is the last reader of the request's draw state
   FvDraw* draw_w = const_cast<FvDraw*>(f.draw) + b;
-  if (!q.live) {
-    if (tid == 0 && *reinterpret_cast<const volatile uint32_t*>(f.abort_flag) == 0u) *draw_w = FvDraw{};
+  if (!__syncthreads_and(q.live)) {  // one decision for the block, as in fv_sums
+    if (tid == 0 && *reinterpret_cast<const volatile uint32_t*>(f.abort_flag) == 0u) {
+      *draw_w = FvDraw{};
+      if (f.cut) f.cut[b] = FvtpDrawCut{};
+    }
     return;
   }
   load_table(f, th, tl);
@@ -343,7 +372,10 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
     f.part[c0 + c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     f.pos[c0 + c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
   }
-  if (tid == 0) *draw_w = FvDraw{};
+  if (tid == 0) {
+    *draw_w = FvDraw{};
+    if (f.cut) f.cut[b] = FvtpDrawCut{};
+  }
   if (s < 0) {  // rounding left no token above u * total: the last with weight
     if (tid == 0) *out = last_any >= 0 ? last_any : 0;
     for (int c = tid; c < f.n_slices; c += kFvThreads) f.last[c0 + c] = make_int2(0, 0);
@@ -364,7 +396,7 @@ __global__ void __launch_bounds__(kFvThreads) fv_pick_kernel(const FvParams f) {
 #pragma unroll
   for (int k = 0; k < kFvPerThread; ++k) {
     ff p, r;
-    token_weights(q, nm, xs[k], ys[k], th, tl, p, r);
+    token_weights(q, nm, xs[k], ys[k], jb + k, th, tl, p, r);
     if (jb + k == q.excl) p = {0.0f, 0.0f};
     wk[k] = resid ? r : p;
     mine = ff_add(mine, wk[k]);

@@ -165,8 +165,33 @@ struct Params {
   // written word is zero, so the request final polls the words themselves.
   unsigned long long* res_list;
   FvDraw* fv_draw;      // [B]: full-vocabulary mode
+  int fvtp;             // full-vocabulary top-p (top-k off, top_p < 1): the stream leaves the rows' statistics
+  float4* fvtp_rows;    // [B * rows per request]: (max, normaliser pair, bad flag) of each sampling row
   int n_slots;
   ExpTable exp2;        // for the filter's float-float exp
+};
+
+// ---- full-vocabulary top-p (top-k off, 0 < top_p < 1) --------------------------------
+// The kept set of a row is the shortest prefix of its (logit desc, index asc)
+// order whose mass reaches top_p: every token whose order key is above kappa,
+// and the tokens whose key is kappa up to index j_cut. The masses are sums of
+// float-float weights exp((x - m) / T) rounded to fixed point (frac_bits
+// fractional bits), so every sum is exact and the same wherever it is taken.
+struct FvtpCut {
+  uint32_t prefix;               // key bits found so far (radix rounds from the top)
+  uint32_t mask;                 // which bits of prefix are found
+  unsigned long long above;      // mass of the keys above the current prefix group
+  unsigned long long total;      // mass of the row
+  unsigned long long kept;       // mass of the kept set (after the last round)
+  uint32_t count;                // tokens in the prefix group (the key kappa's, at the end)
+  uint32_t keep;                 // of those, how many are kept (first in index order)
+  int32_t j_cut;                 // last kept index among key kappa's tokens (V: all of them)
+  int32_t state;                 // 0 = not a sampling row or bad, 1 = live
+};
+// what the draw needs of the kept sets of the two rows it reads
+struct FvtpDrawCut {
+  uint32_t kappa_x, kappa_y;
+  int32_t jcut_x, jcut_y;
 };
 
 // Second pass of the full-vocabulary draw (dflash_fullvocab.cu).
@@ -183,9 +208,37 @@ struct FvParams {
   float4* part;                 // [B, n_slices]: slice sums of the two rows' exp weights
   float4* pos;                  // [B, n_slices]: the same sums over the tokens with p > q
   int2* last;                   // [B, n_slices]: last token with p > q / with p > 0
+  FvtpDrawCut* cut;             // top-p over the full vocabulary: the kept sets ([B]); null otherwise
   const uint32_t* abort_flag;
   float exp_hi[kExpTable];      // 2^(j/64) = exp_hi[j] + exp_lo[j]
   float exp_lo[kExpTable];
+};
+
+// Kernels between the stream and the draw under top-p over the full
+// vocabulary (dflash_fvtp.cu): the cut of every sampling row, then the accept
+// tests, which leave the draw descriptors for the second pass.
+struct FvtpParams {
+  const unsigned char* target;  // [B, gamma+1, V]
+  const unsigned char* draft;   // [B, gamma, V] (unused with deterministic drafts)
+  const int32_t* draft_tokens;  // [B, gamma]
+  const float* temperature;     // [B]
+  int B, gamma, V, dtype, det, per_s, n_slices, frac_bits, round, rounds;
+  float top_p;
+  unsigned long long seed;
+  int sampler, row_base;        // the sampler's uniforms (as for FvParams)
+  int32_t* out_tokens;          // [B, gamma+1]
+  int32_t* out_len;             // [B] (may be null: the sampler)
+  uint32_t* status;
+  float* audit_pq;              // optional [B, gamma, 2]
+  float4* rows;                 // [B * per_s] from the stream
+  FvtpCut* cut;                 // [B * per_s]
+  unsigned long long* hist_m;   // [B * per_s, 256]
+  uint32_t* hist_c;             // [B * per_s, 256]
+  uint32_t* kcount;             // [B * per_s, n_slices]
+  FvDraw* draw;                 // [B]
+  FvtpDrawCut* draw_cut;        // [B]
+  const uint32_t* abort_flag;
+  ExpTable exp2;
 };
 
 // ---- vocabulary-shard candidates ----------------------------------------------------
@@ -229,7 +282,8 @@ struct CandParams {
 
 struct WorkspaceLayout {
   size_t row_cnt, abort_flag, row_best, tile_keys, res_list;
-  size_t fv_draw, fv_part, fv_pos, fv_last, total;
+  size_t fv_draw, fv_part, fv_pos, fv_last;
+  size_t tp_rows, tp_cut, tp_hist_m, tp_hist_c, tp_kcount, tp_draw, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -251,7 +305,8 @@ inline Geometry make_geometry(int V, int esize) {
 // ready for the next call of any shape. The per-row data follows the header.
 constexpr int kMaxCounterSlots = kMaxB * kMaxRowsPerRequest;  // also the rows-task chunk
 
-inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g, bool fullvocab = false) {
+inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& g, bool fullvocab = false,
+                                   bool fvtp = false) {
   WorkspaceLayout L;
   size_t off = 0;
   L.row_cnt = off;    off = align_up(off + sizeof(uint32_t) * (size_t)kMaxCounterSlots, 256);
@@ -265,6 +320,16 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.fv_part = off;    off = align_up(off + 16 * fv_cells, 256);
   L.fv_pos = off;     off = align_up(off + 16 * fv_cells, 256);
   L.fv_last = off;    off = align_up(off + 8 * fv_cells, 256);
+  // top-p over the full vocabulary: per row (n_slots of them) its statistics,
+  // cut state, 256-bin mass and count histograms and per-slice counts; per
+  // request the draw's kept sets
+  const size_t tp_rows = fvtp ? (size_t)n_slots : 0, tp_req = fvtp ? (size_t)n_requests : 0;
+  L.tp_rows = off;    off = align_up(off + 16 * tp_rows, 256);
+  L.tp_cut = off;     off = align_up(off + sizeof(FvtpCut) * tp_rows, 256);
+  L.tp_hist_m = off;  off = align_up(off + 8 * 256 * tp_rows, 256);
+  L.tp_hist_c = off;  off = align_up(off + 4 * 256 * tp_rows, 256);
+  L.tp_kcount = off;  off = align_up(off + 4 * tp_rows * (size_t)fv_slices(g.V), 256);
+  L.tp_draw = off;    off = align_up(off + sizeof(FvtpDrawCut) * tp_req, 256);
   L.total = off;
   return L;
 }
@@ -278,6 +343,8 @@ int sweep_smem_bytes();
 // CTAs of the stream kernel (dtype 0 bf16, 1 fp32) one SM of device `dev` holds
 int sweep_occupancy(int dtype, int dev, int* ctas_per_sm);
 int launch_fullvocab_draw(const FvParams& f, void* stream);
+struct FvtpParams;
+int launch_fvtp_cut(const FvtpParams& t, void* stream);  // dflash_fvtp.cu
 int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* out_accept,
                     float* out_draw, void* stream);
 int launch_verify_candidates(const CandParams& c, void* stream);  // dflash_candidates.cu

@@ -77,10 +77,7 @@ struct PieceDesc {
 };
 constexpr int kDescArgmax = 256;  // the consumers track this row's argmax in-stream
 constexpr int kDescStats = 512;   // the consumers reduce the piece to (max, sum of exp)
-// log2(e) = kLog2eHi + kLog2eLo (the nearest float and the rest)
-constexpr float kLog2eHi = 1.4426950216293335f;
-constexpr float kLog2eLo = 1.925963033500011e-08f;
-constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2eHi = 1.4426950216293335f;  // log2(e), the nearest float
 
 struct Smem {
   alignas(128) unsigned char ring[kStages][kPieceBytes];
@@ -1359,13 +1356,18 @@ __device__ void fullvocab_request_final(const Params& p, Smem& S, int ord) {
     // leave the region at zero: rows of later calls take tile keys there
     for (int pp = lane; pp < p.geo.ppr; pp += 32) st[pp] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     if (lane == 0) {
+      const int bad = (nan || !(fabsf(m) < INFINITY) || !(sum.hi > 0.0f)) ? 1 : 0;
       S.u.fv.m[r] = m;
       S.u.fv.s[r] = sum.hi;
       S.u.fv.s_lo[r] = sum.lo;
-      S.u.fv.bad[r] = (nan || !(fabsf(m) < INFINITY) || !(sum.hi > 0.0f)) ? 1 : 0;
+      S.u.fv.bad[r] = bad;
+      // top-p over the full vocabulary: the rows' cuts come first (other
+      // kernels), and with them the accept tests
+      if (p.fvtp) p.fvtp_rows[(size_t)b * per_s + r] = make_float4(m, sum.hi, sum.lo, bad ? 1.0f : 0.0f);
     }
   }
   fin_sync();
+  if (p.fvtp) return;
   if (w == 0) {
     int32_t* out = p.out_tokens + (size_t)b * (gamma + 1);
     uint32_t st = 0;

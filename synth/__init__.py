@@ -113,6 +113,9 @@ WORKLOADS = {
                                  temperature=(0.0, 0.6, 1.0), top_k=20, top_p=0.95),
     "b32_mixed_g15_v248320": dict(B=32, gamma=15, V=248320, dtype=BF16, sigma_d=(0.3, 1.5),
                                   temperature=(0.0, 0.6, 1.0), top_k=20, top_p=0.95),
+    # the concurrency-32 mix with top-k off: top-p 0.95 over the full vocabulary
+    "b32_mixed_topp_v248320": dict(B=32, gamma=7, V=248320, dtype=BF16, sigma_d=(0.3, 1.5),
+                                   temperature=(0.0, 0.6, 1.0), top_k=0, top_p=0.95),
     # block 16, fp32, top-k off and top-p 1: full-vocabulary softmax and residual
     "b128_g15_fullvocab_f32": dict(B=128, gamma=15, V=248320, dtype=F32, sigma_d=0.5,
                                    temperature=1.0, top_k=0, top_p=1.0),

@@ -38,7 +38,23 @@ everything above them float-float. So
   sum:        <= 2.42u + 40u + 5u = 47.4u
   p(d), q(d): <= 47.4u + u (rounded once)           -> FV_PROB_REL = 2^-18
   the ratio (two of them, rounded) and the oracle's -> FV_ACCEPT_REL = 2^-17
+Top-p over the full vocabulary (top-k off, top_p < 1; dflash_fvtp.cu): each
+weight exp((x - m)/T) is float-float (2^-29.9 relative) and is rounded to
+fixed point with f = 62 - ceil(log2 V) fractional bits (two roundings of half
+a unit), so a sum of n <= V weights is exact up to n 2^-f <= V^2 2^-62
+in units of the row's largest weight, 1, which every row's mass exceeds:
+eps_V = V^2 2^-62 (2^-26 at V = 248320) as a fraction of the mass.
+- the cut RN32(mass before / mass) < top_p: the GPU's fraction is within
+  eps_V + 2^-29.9 of the exact one; the two decisions differ only when the
+  two fp32 roundings straddle top_p, so the exact fraction is within
+  eps_V + 2^-29.9 + u top_p of top_p        -> fvtp_cut_rel(V, top_p)
+- p(d) = RN32(w(d) / kept mass): within u + eps_V + 2^-29.9 relative
+  (1.31u at V = 248320)                       -> fvtp_prob_rel(V)
+- the accept ratio: two such values and one fp32 division, the oracle's
+  exact: 3.7u at V = 248320, under ACCEPT_REL = 8u
+- the draw is the full-vocabulary one over the kept set: FV_DRAW_ABS.
 """
+import math
 
 U = 2.0 ** -24
 ACCEPT_REL = 2.0 ** -21
@@ -60,6 +76,26 @@ def excused_topk(m_acc, m_cut, m_draw):
 
 def excused_fullvocab(m_acc, m_draw):
     return m_acc < FV_ACCEPT_REL or m_draw < FV_DRAW_ABS
+
+
+def fvtp_eps(V):
+    """Bound on the fixed-point mass sums' error, as a fraction of the mass."""
+    frac = 62 - math.ceil(math.log2(V)) if V > 1 else 62
+    return V * 2.0 ** -frac + 2.0 ** -29.9
+
+
+def fvtp_cut_rel(V, top_p):
+    """The oracle's cut margin (relative to top_p) below which a top-p cut over
+    the full vocabulary may be taken the other way."""
+    return (fvtp_eps(V) + U * top_p) / top_p * 1.01
+
+
+def fvtp_prob_rel(V):
+    return (U + fvtp_eps(V)) * 1.01
+
+
+def excused_fvtp(V, top_p, m_acc, m_cut, m_draw):
+    return m_acc < ACCEPT_REL or m_cut < fvtp_cut_rel(V, top_p) or m_draw < FV_DRAW_ABS
 
 
 def compare_rows(tok, ln, want_tok, want_len, excused, what=""):

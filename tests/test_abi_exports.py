@@ -38,6 +38,13 @@ def test_workspace_sizes(lib):
     assert lib.dflash_workspace_bytes(0, 7, 248320, 0, 20, 0.95) == 0
     assert lib.dflash_workspace_bytes(32, 7, 248320, 7, 20, 0.95) == 0
     assert lib.dflash_workspace_bytes(32, 7, 248320, 0, 64, 0.95) == 0   # top_k > 32
+    # top-p over the full vocabulary keeps per-row cuts and histograms on top
+    # of the full-vocabulary regions
+    fv = lib.dflash_workspace_bytes(32, 7, 248320, 0, 0, 1.0)
+    tp = lib.dflash_workspace_bytes(32, 7, 248320, 0, 0, 0.9)
+    assert 0 < fv < tp and tp % 256 == 0
+    assert lib.dflash_workspace_bytes(32, 7, 248320, 0, -1, 0.5) == tp
+    assert lib.dflash_rows_workspace_bytes(224, 248320, 0, 0, 0.9) > 0   # the sampler
     assert lib.dflash_rows_workspace_bytes(224, 248320, 0, 20, 0.95) > 0
     assert lib.dflash_host_staging_bytes(32, 7, 248320, 0) >= 32 * 15 * 248320 * 2
 
@@ -59,7 +66,9 @@ def test_argument_checks_happen_on_the_host(lib):
     assert _verify(lib, top_p=0.0) == dv.ERR_INVALID_ARG
     assert _verify(lib, top_p=float("nan")) == dv.ERR_INVALID_ARG
     assert _verify(lib, top_k=33) == dv.ERR_UNSUPPORTED
-    assert _verify(lib, top_k=0, top_p=0.9) == dv.ERR_UNSUPPORTED      # full-vocab top-p
+    assert _verify(lib, top_k=40, top_p=0.9) == dv.ERR_UNSUPPORTED
+    # top-p over the full vocabulary: up to 2^22 tokens (the fixed-point sums)
+    assert _verify(lib, V=(1 << 22) + 1, top_k=0, top_p=0.9) == dv.ERR_UNSUPPORTED
     assert _verify(lib, dtype=1, ptr=(1 << 20) + 2) == dv.ERR_INVALID_ARG  # fp32 misaligned
     n = ctypes.c_void_p(0)
     assert lib.dflash_verify(n, n, n, 2, 3, 100, 0, n, 20, 0.95, 0, n, n, n, 0, None,
@@ -78,7 +87,7 @@ def test_cancel_refuses_a_buffer_without_the_header(lib):
     assert b"abort flag" in lib.dflash_last_error()
 
 
-@pytest.mark.parametrize("top_k,top_p", [(33, 0.95), (0, 0.9), (-1, 0.5)])
+@pytest.mark.parametrize("top_k,top_p", [(33, 0.95), (64, 0.5), (40, 1.0)])
 def test_noalloc_reports_unsupported_filters_like_verify(lib, top_k, top_p):
     """An unsupported filter gets DFLASH_ERR_UNSUPPORTED and the same message
     from the workspace-free entry point as from dflash_verify (no launch, no

@@ -158,15 +158,15 @@ def test_det_status_bits_and_rejected_filters(dv):
     assert np.all((tok >= -1) & (tok < 3001)) and np.all((ln >= 1) & (ln <= 8))
     for b in (0, 2, 3):
         assert np.array_equal(tok[b], want_tok[b]) and ln[b] == want_len[b]
-    # top-p over the whole vocabulary (top-k off, top_p < 1) and top-k
-    # beyond 32 are refused by the entry point itself, before any launch
+    # top-k beyond 32, with or without top-p, is refused by the entry point
+    # itself, before any launch
     ws = dv.Workspace(dv.workspace_bytes(4, 7, 3001, dv.DFLASH_F32, 0, 1.0), DEV)
     Xd, dd = _t(X), torch.from_numpy(d).to(DEV)
     Td = torch.ones(4, dtype=torch.float32, device=DEV)
     out_t = torch.full((4, 8), -7, dtype=torch.int32, device=DEV)
     out_l = torch.zeros(4, dtype=torch.int32, device=DEV)
     lib = dv.load()
-    for k, tp in ((0, 0.9), (64, 0.95)):
+    for k, tp in ((40, 0.9), (64, 0.95)):
         rc = lib.dflash_verify_det(Xd.data_ptr(), dd.data_ptr(), 4, 7, 3001, dv.DFLASH_F32, Td.data_ptr(),
                                    k, tp, 1, out_t.data_ptr(), out_l.data_ptr(), ws.ptr, ws.nbytes, None,
                                    torch.cuda.current_stream().cuda_stream)

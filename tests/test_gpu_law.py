@@ -76,6 +76,8 @@ CASES = [
     (8, 3, 0.7, 5, 1.0, 1.0, "f32"),     # top-k
     (7, 3, 1.0, 4, 0.9, 2.0, "bf16"),    # top-k and top-p
     (8, 2, 1.3, 7, 0.8, 1.2, "f32"),     # top-p with a top-k that drops one token
+    (8, 3, 1.0, 0, 0.85, 1.0, "f32"),    # top-p over the full vocabulary (top-k off)
+    (7, 3, 0.9, 0, 0.7, 1.5, "bf16"),
 ]
 
 
