@@ -163,23 +163,33 @@ def algorithmic_bytes(inp, accept_len=None, det=False) -> int:
     """Logit bytes one step must read: every target row, and the draft rows of
     requests that sample (greedy requests never read their draft rows, nor
     does the verification of deterministic drafts). Over the full vocabulary
-    (top-k off, top-p 1) the residual or bonus draw reads its rows once more:
-    two rows after a rejection, one for a bonus token (from the step's accept
-    lengths)."""
+    (top-k off) the residual or bonus draw reads its rows once more: two rows
+    after a rejection, one for a bonus token (from the step's accept lengths).
+    With top-p < 1 the passes that find each row's cut read the sampling rows
+    again; they are counted as the path's overhead, not as algorithmic bytes
+    (a cut that could be found inside the statistics pass would not need
+    them)."""
     B, gamma, V = inp.shape
     es = 2 if inp.target.dtype == np.uint16 else 4
     samp = inp.temperature > 0
     rows = B * (gamma + 1) + (0 if det else int(np.sum(samp)) * gamma)
-    if inp.top_k <= 0 and inp.top_p >= 1.0 and accept_len is not None:
+    if inp.top_k <= 0 and accept_len is not None:
         lens = np.asarray(accept_len)[samp]
         rows += int(np.sum(np.where(lens <= gamma, 2, 1)))
     return rows * V * es
 
 
-def launches_per_step(top_k: int, top_p: float) -> int:
+def launches_per_step(top_k: int, top_p: float, bf16: bool = True) -> int:
     """Kernel launches of one verification call: the stream kernel, plus the
-    full-vocabulary draw's two launches when top-k is off and top-p is 1."""
-    return 3 if top_k <= 0 and top_p >= 1.0 else 1
+    full-vocabulary draw's two launches when top-k is off; with top-p < 1
+    also the cut's radix rounds (a histogram and a select launch for each key
+    byte: two bytes of a bf16 key, four of fp32), its two tie launches and the
+    accept launch."""
+    if top_k > 0:
+        return 1
+    if top_p >= 1.0:
+        return 3
+    return 3 + 2 * (2 if bf16 else 4) + 3
 
 
 def cpu_baseline(inp, d, workload, threads=None, det=False, min_s=10.0, max_batches=200):
@@ -514,7 +524,7 @@ def run_gpu(args):
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": args.steps * launches_per_step(top_k, top_p),
+        "gpu_launches": args.steps * launches_per_step(top_k, top_p, bf16),
         "clocks": clk,
         "accept_len": accept,
     }

@@ -119,6 +119,9 @@ WORKLOADS = {
     # block 16, fp32, top-k off and top-p 1: full-vocabulary softmax and residual
     "b128_g15_fullvocab_f32": dict(B=128, gamma=15, V=248320, dtype=F32, sigma_d=0.5,
                                    temperature=1.0, top_k=0, top_p=1.0),
+    # the same with top-p 0.95 over the full vocabulary
+    "b128_g15_topp_f32": dict(B=128, gamma=15, V=248320, dtype=F32, sigma_d=0.5,
+                              temperature=1.0, top_k=0, top_p=0.95),
 }
 
 

@@ -27,6 +27,16 @@ def test_full_vocabulary_draw_reads():
     assert bench.algorithmic_bytes(inp, lens) == base + (2 + 1 + 2 + 1) * V * 4
 
 
+def test_top_p_over_the_vocabulary_counts_the_draw_not_the_cut():
+    inp = synth.make_workload("b32_mixed_topp_v248320", B=6, V=700)
+    B, gamma, V = inp.shape
+    samp = inp.temperature > 0                      # 0 / 0.6 / 1.0: four of six sample
+    lens = np.array([1, 2, gamma + 1, 3, 8, gamma + 1])
+    base = (B * (gamma + 1) + int(samp.sum()) * gamma) * V * 2
+    extra = sum((2 if n <= gamma else 1) for n in lens[samp])
+    assert bench.algorithmic_bytes(inp, lens) == base + extra * V * 2
+
+
 def test_profile_lookup_names():
     assert bench.profile_summary("b32_mixed_v248320") == bench.PROFILE_SUMMARY
     assert bench.profile_summary("b32_mixed_v248320", det=True).endswith("verify_sweep_b32_mixed_v248320_det.md")
@@ -36,3 +46,7 @@ def test_profile_lookup_names():
 def test_launches_per_step():
     assert bench.launches_per_step(20, 0.95) == 1
     assert bench.launches_per_step(0, 1.0) == 3
+    # top-p over the full vocabulary: stream, 2 radix rounds (bf16) or 4
+    # (fp32) of two launches, the two tie launches, accept, the draw's two
+    assert bench.launches_per_step(0, 0.95) == 10
+    assert bench.launches_per_step(0, 0.95, bf16=False) == 14
