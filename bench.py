@@ -182,14 +182,14 @@ def algorithmic_bytes(inp, accept_len=None, det=False) -> int:
 def launches_per_step(top_k: int, top_p: float, bf16: bool = True) -> int:
     """Kernel launches of one verification call: the stream kernel, plus the
     full-vocabulary draw's two launches when top-k is off; with top-p < 1
-    also the cut's radix rounds (a histogram and a select launch for each key
-    byte: two bytes of a bf16 key, four of fp32), its two tie launches and the
-    accept launch."""
+    also the cut's rounds (a histogram and a select launch for the first
+    round and for each refinement round: up to four for fp32 keys, two for
+    bf16), its two tie launches and the accept launch."""
     if top_k > 0:
         return 1
     if top_p >= 1.0:
         return 3
-    return 3 + 2 * (2 if bf16 else 4) + 3
+    return 3 + 2 * (3 if bf16 else 5) + 3
 
 
 def cpu_baseline(inp, d, workload, threads=None, det=False, min_s=10.0, max_batches=200):

@@ -189,7 +189,6 @@ int run_fvtp(const Params& p, void* ws, void* stream, bool sampler) {
   t.per_s = p.det ? p.gamma + 1 : 2 * p.gamma + 1;
   t.n_slices = fv_slices(p.geo.V);
   t.frac_bits = 62 - ceil_log2(p.geo.V);  // the row's mass, at most V, fits 63 bits
-  t.rounds = p.dtype == 0 ? 2 : 4;         // key bytes to find (bf16 keys: the upper two)
   t.top_p = p.top_p;
   t.seed = p.seed;
   t.sampler = sampler ? 1 : 0;
@@ -201,7 +200,6 @@ int run_fvtp(const Params& p, void* ws, void* stream, bool sampler) {
   t.rows = reinterpret_cast<float4*>(base + L.tp_rows);
   t.cut = reinterpret_cast<FvtpCut*>(base + L.tp_cut);
   t.hist_m = reinterpret_cast<unsigned long long*>(base + L.tp_hist_m);
-  t.hist_c = reinterpret_cast<uint32_t*>(base + L.tp_hist_c);
   t.kcount = reinterpret_cast<uint32_t*>(base + L.tp_kcount);
   t.draw = reinterpret_cast<FvDraw*>(base + L.fv_draw);
   t.draw_cut = reinterpret_cast<FvtpDrawCut*>(base + L.tp_draw);

@@ -178,15 +178,18 @@ struct Params {
 // float-float weights exp((x - m) / T) rounded to fixed point (frac_bits
 // fractional bits), so every sum is exact and the same wherever it is taken.
 struct FvtpCut {
-  uint32_t prefix;               // key bits found so far (radix rounds from the top)
-  uint32_t mask;                 // which bits of prefix are found
-  unsigned long long above;      // mass of the keys above the current prefix group
+  uint32_t kmin, kmax;           // the first round's crossing bin: its keys (refinement units)
+  uint32_t prefix;               // bits of (key - kmin) found by the refinement rounds
+                                 // (refinement units: the key, or for bf16 its upper half)
+  uint32_t kappa;                // the last kept token's key (state 2)
+  int32_t nref;                  // refinement rounds the crossing bin needs (bytes of its key span)
+  unsigned long long above;      // mass of the keys above the current group
   unsigned long long total;      // mass of the row
-  unsigned long long kept;       // mass of the kept set (after the last round)
-  uint32_t count;                // tokens in the prefix group (the key kappa's, at the end)
-  uint32_t keep;                 // of those, how many are kept (first in index order)
+  unsigned long long kept;       // mass of the kept set (state 2)
+  uint32_t count;                // tokens in the current group (key kappa's, state 2)
+  uint32_t keep;                 // of key kappa's tokens, how many are kept (first in index order)
   int32_t j_cut;                 // last kept index among key kappa's tokens (V: all of them)
-  int32_t state;                 // 0 = not a sampling row or bad, 1 = live
+  int32_t state;                 // 0 = no cut (not a sampling row, or bad), 1 = searching, 2 = found
 };
 // what the draw needs of the kept sets of the two rows it reads
 struct FvtpDrawCut {
@@ -222,7 +225,7 @@ struct FvtpParams {
   const unsigned char* draft;   // [B, gamma, V] (unused with deterministic drafts)
   const int32_t* draft_tokens;  // [B, gamma]
   const float* temperature;     // [B]
-  int B, gamma, V, dtype, det, per_s, n_slices, frac_bits, round, rounds;
+  int B, gamma, V, dtype, det, per_s, n_slices, frac_bits, round;
   float top_p;
   unsigned long long seed;
   int sampler, row_base;        // the sampler's uniforms (as for FvParams)
@@ -232,8 +235,7 @@ struct FvtpParams {
   float* audit_pq;              // optional [B, gamma, 2]
   float4* rows;                 // [B * per_s] from the stream
   FvtpCut* cut;                 // [B * per_s]
-  unsigned long long* hist_m;   // [B * per_s, 256]
-  uint32_t* hist_c;             // [B * per_s, 256]
+  unsigned long long* hist_m;   // [B * per_s, 256] masses of the current round's bins
   uint32_t* kcount;             // [B * per_s, n_slices]
   FvDraw* draw;                 // [B]
   FvtpDrawCut* draw_cut;        // [B]
@@ -283,7 +285,7 @@ struct CandParams {
 struct WorkspaceLayout {
   size_t row_cnt, abort_flag, row_best, tile_keys, res_list;
   size_t fv_draw, fv_part, fv_pos, fv_last;
-  size_t tp_rows, tp_cut, tp_hist_m, tp_hist_c, tp_kcount, tp_draw, total;
+  size_t tp_rows, tp_cut, tp_hist_m, tp_kcount, tp_draw, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -327,7 +329,6 @@ inline WorkspaceLayout make_layout(int n_slots, int n_requests, const Geometry& 
   L.tp_rows = off;    off = align_up(off + 16 * tp_rows, 256);
   L.tp_cut = off;     off = align_up(off + sizeof(FvtpCut) * tp_rows, 256);
   L.tp_hist_m = off;  off = align_up(off + 8 * 256 * tp_rows, 256);
-  L.tp_hist_c = off;  off = align_up(off + 4 * 256 * tp_rows, 256);
   L.tp_kcount = off;  off = align_up(off + 4 * tp_rows * (size_t)fv_slices(g.V), 256);
   L.tp_draw = off;    off = align_up(off + sizeof(FvtpDrawCut) * tp_req, 256);
   L.total = off;

@@ -46,7 +46,8 @@ def test_profile_lookup_names():
 def test_launches_per_step():
     assert bench.launches_per_step(20, 0.95) == 1
     assert bench.launches_per_step(0, 1.0) == 3
-    # top-p over the full vocabulary: stream, 2 radix rounds (bf16) or 4
-    # (fp32) of two launches, the two tie launches, accept, the draw's two
-    assert bench.launches_per_step(0, 0.95) == 10
-    assert bench.launches_per_step(0, 0.95, bf16=False) == 14
+    # top-p over the full vocabulary: stream, the rounds' two launches each
+    # (the first and up to two refinements for bf16 keys, four for fp32),
+    # the two tie launches, accept, the draw's two
+    assert bench.launches_per_step(0, 0.95) == 12
+    assert bench.launches_per_step(0, 0.95, bf16=False) == 16

@@ -302,3 +302,21 @@ def test_fvtp_workspace_left_zero_across_modes(dv):
                                   top_p, 4, workspace=ws)
         torch.cuda.synchronize()
         assert int(torch.count_nonzero(ws.buf).item()) == 0, f"workspace not left at zero after det {V}"
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_fvtp_rows_of_one_value(dv, dtype):
+    """Every logit of a row equal: each row is one key group of V tokens, the
+    kept set the first ceil(top_p V) or so by index. V = 2 x 65528 puts as
+    many equal bf16 logits in one counting block as it may hold."""
+    B, gamma, V = 2, 2, 2 * 65528
+    X = np.full((B, gamma + 1, V), 0.75, np.float32)
+    X[1] = -3.0
+    Y = np.full((B, gamma, V), 0.25, np.float32)
+    if dtype == "bf16":
+        X, Y = synth.f32_to_bf16_bits(X), synth.f32_to_bf16_bits(Y)
+    T = np.ones(B, np.float32)
+    for top_p, seed in ((0.3, 1), (0.9, 2)):
+        d = _drafts(Y, T, top_p, 3)
+        n_bad, total = _check(dv, X, Y, d, T, top_p, seed)
+        assert n_bad == 0
