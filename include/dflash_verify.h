@@ -325,6 +325,41 @@ int dflash_verify_noalloc(const void* target_logits, const void* draft_logits,
                           int32_t* out_tokens, int32_t* out_accept_len, uint32_t* status,
                           void* stream);
 
+/* ---- the LM head on the tensor cores -------------------------------------------------
+ * The draft/verify loop ("DFlash2 用投机解码给 Qwen 提速", bml.asia, the
+ * listing of the loop) runs the target over the block and verifies from its
+ * logits: logits = h W^T, with h the positions' last hidden states and W the
+ * vocabulary projection.
+ *
+ * dflash_lmhead_logits: logits [M, V] = h [M, K] W^T for h [M, K] and W [V, K],
+ * all bf16 row-major [device], fp32 accumulation on the tensor cores, each
+ * logit rounded to the nearest bf16 (ties to even). 1 <= M <= 512; V a
+ * positive multiple of 8; K a positive multiple of 64; h, W and logits
+ * 16-byte aligned (caller-owned; logits is overwritten). status may be NULL
+ * (a bounded wait that gave up ORs DFLASH_STATUS_TIMEOUT into it). */
+int dflash_lmhead_logits(const void* h, const void* w, int M, int V, int K, void* logits, uint32_t* status,
+                         void* stream);
+
+/* dflash_lmhead_verify: the LM head and dflash_verify in one, without the
+ * verification's pass over the logits. h holds the B (gamma + 1) target rows
+ * ([B, gamma + 1, K]) and then the B gamma draft rows ([B, gamma, K]), bf16;
+ * logits [B (2 gamma + 1), V] bf16 receives the target logits and then the
+ * draft logits (the verification's target_logits and draft_logits). The
+ * GEMM's epilogue writes the statistics the verification would have taken
+ * from them (each 256-logit tile's maximum for the top-k rows, the argmax of
+ * the greedy rows) into the workspace; the verification then runs only its
+ * row and request finals. Outputs, uniforms, status bits and workspace rules
+ * are those of dflash_verify on the same logits (the outputs equal
+ * dflash_lmhead_logits followed by dflash_verify bit for bit). Shape limits
+ * as for dflash_lmhead_logits with M = B (2 gamma + 1) <= 512; the top-k
+ * filter only (1 <= top_k <= DFLASH_MAX_TOP_K, top_k < V, any top_p; others
+ * return DFLASH_ERR_UNSUPPORTED). workspace_bytes >= dflash_workspace_bytes(B,
+ * gamma, V, DFLASH_BF16, top_k, top_p). */
+int dflash_lmhead_verify(const void* h, const void* w, int B, int gamma, int V, int K,
+                         const int32_t* draft_tokens, const float* temperature, int top_k, float top_p,
+                         uint64_t seed, void* logits, int32_t* out_tokens, int32_t* out_accept_len,
+                         void* workspace, size_t workspace_bytes, uint32_t* status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

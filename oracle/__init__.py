@@ -379,3 +379,23 @@ def sample_rows(logits, temperature, top_k, top_p, seed, threads=None, lib=None)
     for s in statuses:
         status |= s
     return out, margin, status
+
+
+# ---- the LM head ---------------------------------------------------------------------------
+def _bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def lmhead_logits(h_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """logits[m, n] = sum_k h[m, k] w[n, k] (the target's vocabulary projection
+    of the positions' last hidden states, the logits the draft/verify loop of
+    "DFlash2 用投机解码给 Qwen 提速" verifies from), from bf16 bit patterns
+    (uint16 [M, K] and [V, K]). Every product of two bf16 values is exact in
+    fp64, and the sum is accurate to about 2^-53 relative to sum |h_k w_k|
+    (numpy's matmul as the summing step)."""
+    return _bf16_to_f64(h_bits) @ _bf16_to_f64(w_bits).T
+
+
+def lmhead_abs(h_bits: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """sum_k |h[m, k] w[n, k]|: the scale of each logit's rounding error."""
+    return np.abs(_bf16_to_f64(h_bits)) @ np.abs(_bf16_to_f64(w_bits)).T

@@ -18,7 +18,8 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(_ROOT, "include")
 _BUILD = os.path.join(_HERE, "_build")
 LIB_PATH = os.path.join(_BUILD, "libdflash_verify.so")
-SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_fvtp.cu", "dflash_candidates.cu", "dflash_abi.cu",
+SOURCES = ["dflash_sweep.cu", "dflash_fullvocab.cu", "dflash_fvtp.cu", "dflash_candidates.cu", "dflash_lmhead.cu",
+           "dflash_abi.cu",
            "dflash_noalloc.cu"]
 HEADERS = ["dflash_device.cuh", "dflash_internal.h", "dflash_rule.cuh", "dflash_ff.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -112,6 +113,8 @@ EXPORTS = {
     "dflash_verify_candidates": ("i", "piipiiipifQpppp"),
     "dflash_noalloc_scratch_bytes": ("z", ""),
     "dflash_verify_noalloc": ("i", "pppiiiipifQpppp"),
+    "dflash_lmhead_logits": ("i", "ppiiippp"),
+    "dflash_lmhead_verify": ("i", "ppiiiippifQppppzpp"),
 }
 _CT = {"i": ctypes.c_int, "p": ctypes.c_void_p, "z": ctypes.c_size_t, "f": ctypes.c_float,
        "Q": ctypes.c_uint64, "s": ctypes.c_char_p, "": None}
@@ -302,6 +305,61 @@ def verify_audit(target, draft, draft_tokens, temperature, top_k: int, top_p: fl
         _stream_ptr(stream, dev))
     _check(rc)
     return out_tokens, out_accept_len, audit
+
+
+def lmhead_logits(h, w, out=None, status=None, stream=None):
+    """dflash_lmhead_logits: logits [M, V] = h [M, K] @ w [V, K]^T in bf16 on
+    the tensor cores (fp32 accumulation). Returns the logits tensor."""
+    torch = _torch()
+    if h.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise ValueError("h and w must be bfloat16")
+    M, K = h.shape
+    V, K2 = w.shape
+    if K2 != K:
+        raise ValueError("h and w must share the hidden size")
+    dev = h.device
+    if out is None:
+        out = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+    _shape(out, (M, V), "out")
+    _status_ok(status)
+    _on(dev, w=w, out=out, status=status)
+    rc = load().dflash_lmhead_logits(_dev(h, "h"), _dev(w, "w"), M, V, K, _dev(out, "out"),
+                                     None if status is None else _dev(status, "status", torch.int32),
+                                     _stream_ptr(stream, dev))
+    _check(rc)
+    return out
+
+
+def lmhead_verify(h, w, B: int, gamma: int, draft_tokens, temperature, top_k: int, top_p: float, seed: int,
+                  logits=None, status=None, workspace=None, stream=None):
+    """dflash_lmhead_verify: the LM head over h [B (gamma + 1) + B gamma, K]
+    (target rows, then draft rows) with the verification's tile statistics in
+    its epilogue, then the verification's finals. Returns (out_tokens,
+    out_accept_len, logits)."""
+    torch = _torch()
+    M, K = h.shape
+    V = w.shape[0]
+    if M != B * (2 * gamma + 1):
+        raise ValueError("h must hold B (gamma + 1) target rows and B gamma draft rows")
+    dev = h.device
+    if logits is None:
+        logits = torch.empty((M, V), dtype=torch.bfloat16, device=dev)
+    out_tokens = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    _shape(draft_tokens, (B, gamma), "draft_tokens")
+    _shape(temperature, (B,), "temperature")
+    _shape(logits, (M, V), "logits")
+    _status_ok(status)
+    _on(dev, w=w, draft_tokens=draft_tokens, temperature=temperature, logits=logits, status=status)
+    ws = _workspace_for(workspace_bytes(B, gamma, V, DFLASH_BF16, top_k, top_p), dev, workspace)
+    rc = load().dflash_lmhead_verify(
+        _dev(h, "h"), _dev(w, "w"), B, gamma, V, K, _dev(draft_tokens, "draft_tokens", torch.int32),
+        _dev(temperature, "temperature", torch.float32), int(top_k), float(top_p),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _dev(logits, "logits"), _dev(out_tokens, "out_tokens", torch.int32),
+        _dev(out_len, "out_accept_len", torch.int32), ws.ptr, ws.nbytes,
+        None if status is None else _dev(status, "status", torch.int32), _stream_ptr(stream, dev))
+    _check(rc)
+    return out_tokens, out_len, logits
 
 
 def verify_det(target, draft_tokens, temperature, top_k: int, top_p: float, seed: int,

@@ -377,9 +377,110 @@ int verify_impl(const void* target_logits, const void* draft_logits, const int32
   // the slot count depends on the device-side temperatures; launch for the maximum
   return run_step(p, B * (2 * gamma + 1), workspace, stream);
 }
+
+// ---- the LM head on the tensor cores ---------------------------------------------------
+int check_lmhead(const void* h, const void* w, int M, int V, int K, const void* logits) {
+  if (!h || !w || !logits) return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  if (M < 1 || M > kLmMaxRows) return fail(DFLASH_ERR_INVALID_ARG, "M=%d outside [1, %d]", M, kLmMaxRows);
+  if (V < 8 || V % 8) return fail(DFLASH_ERR_INVALID_ARG, "V=%d must be a positive multiple of 8", V);
+  if (K < 64 || K % 64) return fail(DFLASH_ERR_INVALID_ARG, "K=%d must be a positive multiple of 64", K);
+  if (((uintptr_t)h | (uintptr_t)w | (uintptr_t)logits) % 16u)
+    return fail(DFLASH_ERR_INVALID_ARG, "h, W and logits must be 16-byte aligned");
+  return DFLASH_OK;
+}
+int lmhead_grid(int V, int* grid) {
+  int dev = 0;
+  cudaError_t ce = cudaGetDevice(&dev);
+  if (ce != cudaSuccess) return cuda_fail(ce, "no CUDA device");
+  const int tiles = (V + 127) / 128, sms = available_sms(dev);
+  *grid = tiles < sms ? tiles : sms;
+  return DFLASH_OK;
+}
 }  // namespace
 
 extern "C" {
+
+int dflash_lmhead_logits(const void* h, const void* w, int M, int V, int K, void* logits, uint32_t* status,
+                         void* stream) {
+  NvtxRange nvtx_range("dflash_lmhead_logits");
+  int rc = check_lmhead(h, w, M, V, K, logits);
+  int grid = 0;
+  if (rc || (rc = lmhead_grid(V, &grid))) return rc;
+  LmParams lp;
+  memset(&lp, 0, sizeof lp);
+  lp.M = M;
+  lp.Mt = M;
+  lp.V = V;
+  lp.K = K;
+  lp.logits = static_cast<uint16_t*>(logits);
+  lp.status = status;
+  const int e = launch_lmhead(lp, h, w, false, grid, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "launching the LM head");
+  return DFLASH_OK;
+}
+
+int dflash_lmhead_verify(const void* h, const void* w, int B, int gamma, int V, int K, const int32_t* draft_tokens,
+                         const float* temperature, int top_k, float top_p, uint64_t seed, void* logits,
+                         int32_t* out_tokens, int32_t* out_accept_len, void* workspace, size_t workspace_bytes,
+                         uint32_t* status, void* stream) {
+  NvtxRange nvtx_range("dflash_lmhead_verify");
+  int rc = check_shape(B, gamma, V, DFLASH_BF16);
+  if (rc) return rc;
+  const long long M = (long long)B * (2 * gamma + 1);
+  if (M > kLmMaxRows)
+    return fail(DFLASH_ERR_INVALID_ARG, "B=%d gamma=%d gives %lld rows, more than the LM head's %d", B, gamma, M,
+                kLmMaxRows);
+  if ((rc = check_lmhead(h, w, (int)M, V, K, logits))) return rc;
+  if (!draft_tokens || !temperature || !out_tokens || !out_accept_len || !workspace)
+    return fail(DFLASH_ERR_INVALID_ARG, "null pointer argument");
+  const int mode = filter_mode(V, top_k, top_p);
+  if (mode < 0) return fail(DFLASH_ERR_INVALID_ARG, "top_p=%g must be in (0, 1]", (double)top_p);
+  if (mode != kModeTopK)
+    return fail(DFLASH_ERR_UNSUPPORTED,
+                "top_k=%d with top_p=%g is not supported in the LM head's epilogue (need 1 <= top_k <= %d and "
+                "top_k < V)",
+                top_k, (double)top_p, DFLASH_MAX_TOP_K);
+  const size_t need = verify_workspace(B, gamma, V, DFLASH_BF16, mode);
+  if (workspace_bytes < need)
+    return fail(DFLASH_ERR_INVALID_ARG, "workspace of %zu bytes is smaller than the %zu needed",
+                workspace_bytes, need);
+  int grid = 0;
+  if ((rc = lmhead_grid(V, &grid))) return rc;
+  const int Mt = B * (gamma + 1);
+  Params p = base_params(DFLASH_BF16, V);
+  p.target = static_cast<const unsigned char*>(logits);
+  p.draft = static_cast<const unsigned char*>(logits) + (size_t)Mt * V * 2;
+  p.draft_tokens = draft_tokens;
+  p.temperature = temperature;
+  p.B = B;
+  p.gamma = gamma;
+  p.top_k = top_k;
+  p.top_p = top_p >= 1.0f ? 1.0f : top_p;
+  p.seed = seed;
+  p.task = kTaskVerify;
+  p.out_tokens = out_tokens;
+  p.out_len = out_accept_len;
+  p.status = status;
+  p.keys_ready = 1;
+  bind_workspace(p, workspace, B * (2 * gamma + 1), B, mode);
+  LmParams lp;
+  memset(&lp, 0, sizeof lp);
+  lp.M = (int)M;
+  lp.Mt = Mt;
+  lp.V = V;
+  lp.K = K;
+  lp.logits = static_cast<uint16_t*>(logits);
+  lp.B = B;
+  lp.gamma = gamma;
+  lp.tiles = p.geo.tiles;
+  lp.temperature = temperature;
+  lp.tile_keys = p.tile_keys;
+  lp.row_best = p.row_best;
+  lp.status = status;
+  const int e = launch_lmhead(lp, h, w, true, grid, stream);
+  if (e != 0) return cuda_fail((cudaError_t)e, "launching the LM head");
+  return run(p, B * (2 * gamma + 1), stream);
+}
 
 int dflash_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens, int B,
                   int gamma, int V, int dtype, const float* temperature, int top_k, float top_p,

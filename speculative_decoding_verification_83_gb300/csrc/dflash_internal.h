@@ -140,6 +140,8 @@ struct Params {
   int task;
   int fullvocab;                // top-k off and top-p 1: softmax over the whole vocabulary
   int det;                      // verify: deterministic drafts (q = point mass at the draft; no draft rows)
+  int keys_ready;               // verify: the tile keys and greedy argmaxes were written by the LM head's
+                                // epilogue (before this launch); stream nothing, run the finals
   int row_base;                 // rows tasks: index of this launch's first row
   int vocab_offset;             // candidates task: token id of the shard's first logit
   Geometry geo;
@@ -346,6 +348,25 @@ int sweep_occupancy(int dtype, int dev, int* ctas_per_sm);
 int launch_fullvocab_draw(const FvParams& f, void* stream);
 struct FvtpParams;
 int launch_fvtp_cut(const FvtpParams& t, void* stream);  // dflash_fvtp.cu
+
+// ---- the LM head on the tensor cores (dflash_lmhead.cu) -----------------------------
+// logits [M, V] = h [M, K] W^T (W [V, K]), bf16 in and out, fp32 accumulation;
+// M <= kLmMaxRows (four 128-row token tiles), K a multiple of 64. Fused: the
+// rows are a verification's target rows (Mt = B (gamma + 1)) then its draft
+// rows (B gamma), and the epilogue also writes the top-k rows' tile keys and
+// the greedy rows' argmax composites into the verification's workspace.
+constexpr int kLmMaxRows = 512;
+struct LmParams {
+  int M, Mt, V, K;
+  uint16_t* logits;               // [M, V] bf16 bits
+  int B, gamma, tiles;            // fused: the verification's shape and tiles per row
+  const float* temperature;       // fused: [B]
+  uint32_t* tile_keys;            // fused: [slots, tiles]
+  unsigned long long* row_best;   // fused: [slots]
+  uint32_t* status;
+};
+int launch_lmhead(const LmParams& p, const void* h, const void* w, bool fused, int grid, void* stream);
+int lmhead_smem_bytes();
 int launch_uniforms(unsigned long long seed, int B, int npos, int stream_id, float* out_accept,
                     float* out_draw, void* stream);
 int launch_verify_candidates(const CandParams& c, void* stream);  // dflash_candidates.cu

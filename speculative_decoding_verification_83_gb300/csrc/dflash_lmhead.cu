@@ -1,0 +1,438 @@
+// dflash_lmhead.cu -- the target's LM head on the 5th-generation tensor cores,
+// with the verification's per-tile statistics in its epilogue.
+//
+// The draft/verify loop of "DFlash2 用投机解码给 Qwen 提速" (bml.asia) runs the
+// target over the prompt plus the block's drafts and reads the logits of
+// every position: logits = h W^T, h the positions' last hidden states [M, K]
+// and W the vocabulary projection [V, K] (bf16). The verification step then
+// reads those logits again. Here the GEMM's epilogue also produces what the
+// stream kernel would have computed from them (dflash_sweep.cu): each
+// 256-logit tile's maximum as an order key for the top-k rows, and the running
+// argmax of the greedy rows. The verification that follows streams nothing
+// and runs only its finals (Params::keys_ready), which gather the few
+// candidate tiles from the stored logits.
+//
+// Kernel layout (one CTA per SM, persistent over 128-column vocabulary tiles):
+//  * warp 0: TMA producer. Per 64-element step of K it loads the W tile
+//    [128 x 64] and the h tiles [128 x 64] of every 128-row token tile into a
+//    two-stage ring (cp.async.bulk.tensor, 128-byte swizzle, mbarrier
+//    complete_tx);
+//  * warp 1: allocates the tensor memory and issues the MMAs from one thread:
+//    tcgen05.mma.cta_group::1.kind::f16, M = 128 tokens, N = 128 vocabulary
+//    rows, K = 16 per instruction, bf16 in, fp32 accumulated in tensor memory
+//    (one 128-column accumulator per token tile, at most four: M <= 512);
+//    tcgen05.commit frees a stage when its MMAs have read it, and signals the
+//    epilogue after a tile's last step;
+//  * warps 2-5: epilogue. Each thread owns one token row of a 32-lane quarter
+//    of the accumulators (tcgen05.ld.32x32b), rounds the 128 fp32 sums to
+//    bf16 (round to nearest even), stores them, and in the fused mode folds
+//    them into the row's tile keys (red.max) or argmax (red.max of the
+//    (key, index) composite).
+// Every wait is bounded; a CTA that gives up raises DFLASH_STATUS_TIMEOUT,
+// waits (bounded) for its loads in flight and frees its tensor memory.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "dflash_device.cuh"
+#include "dflash_internal.h"
+#include "dflash_rule.cuh"
+
+namespace dflash {
+namespace {
+
+constexpr int kLmThreads = 192;
+constexpr int kBN = 128;                          // vocabulary rows per tile
+constexpr int kBK = 64;                           // hidden elements per stage (one 128-byte swizzle row)
+constexpr int kMaxMT = kLmMaxRows / 128;          // token tiles
+constexpr int kLmStages = 2;
+constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 64 bf16 tile, 16 KB
+constexpr int kEpiWarp0 = 2;
+
+struct LmSmem {
+  unsigned char a[kLmStages][kMaxMT][kTileBytes];  // h tiles (1024-byte aligned: the swizzle atom)
+  unsigned char b[kLmStages][kTileBytes];          // W tiles
+  uint64_t full[kLmStages], empty[kLmStages];
+  uint64_t acc_full, acc_empty;
+  uint32_t tmem_base;
+  int failed;
+  int slot_base[kMaxB];  // per request: its first slot (sampling requests), or -(1 + first slot) (greedy)
+  int n_samp;
+};
+constexpr size_t kLmSmemBytes = sizeof(LmSmem) + 1024;  // + room to align the base to 1024 bytes
+
+// ---- PTX wrappers: tensor memory, MMA, TMA --------------------------------------------
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, one instruction (M = 128, N = 128, K = 16)
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrive on the mbarrier once the MMAs issued so far have completed
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+               : "memory");
+}
+// 32 consecutive fp32 columns of this thread's lane
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// a [128 x 64] bf16 box of a 2-D tensor map at (k, row) into shared memory
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int k, int row, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile written by TMA
+// with the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes
+// apart (stride byte offset), descriptor version 1, swizzle mode 2. The
+// leading byte offset is unused in this layout (one MMA's K extent, 32
+// bytes, lies inside a swizzle row). Moving along K inside the 128-byte row
+// adds the byte offset to the start address.
+__device__ __forceinline__ uint64_t sw128_desc(const void* tile) {
+  const uint32_t a = smem_addr(tile);
+  uint64_t d = (uint64_t)((a & 0x3ffffu) >> 4);
+  d |= (uint64_t)1u << 16;            // leading byte offset (unused)
+  d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset
+  d |= (uint64_t)1u << 46;            // descriptor version
+  d |= (uint64_t)2u << 61;            // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, unsigned long long t0) {
+  while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+__device__ __forceinline__ uint16_t bf16_rn(float f) {  // round to nearest even (finite and inf; NaN stays NaN)
+  const uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
+  return (uint16_t)((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
+}
+
+// ---- the kernel ----------------------------------------------------------------------------
+template <bool kFused>
+__global__ void __launch_bounds__(kLmThreads, 1)
+    lmhead_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_h,
+                  const LmParams p) {
+  extern __shared__ unsigned char lm_raw[];
+  LmSmem& S = *reinterpret_cast<LmSmem*>((reinterpret_cast<uintptr_t>(lm_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = (p.M + 127) / 128;
+  const int n_tiles = (p.V + kBN - 1) / kBN;
+  const int nk = p.K / kBK;
+  const uint32_t ncols = mt <= 1 ? 128u : (mt <= 2 ? 256u : 512u);
+
+  if (tid == 0) {
+    for (int s = 0; s < kLmStages; ++s) {
+      mbar_init(&S.full[s], 1);
+      mbar_init(&S.empty[s], 1);
+    }
+    mbar_init(&S.acc_full, 1);
+    mbar_init(&S.acc_empty, 128);
+    S.failed = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&S.tmem_base, ncols);
+  if (kFused) {
+    // slots of the verification (sampling requests first, in request order,
+    // 2 gamma + 1 slots each; then greedy requests, gamma + 1 each): each
+    // thread counts the sampling requests of its run of requests, a block
+    // scan gives every run its ordinals
+    const int chunk = (p.B + kLmThreads - 1) / kLmThreads;
+    const int lo = min(p.B, tid * chunk), hi = min(p.B, lo + chunk);
+    int mine = 0;
+    for (int b = lo; b < hi; ++b) mine += sampling_temperature(__ldg(p.temperature + b)) ? 1 : 0;
+    int incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    __shared__ int warp_tot[kLmThreads / 32];
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    int before = incl - mine, ns = 0;
+    for (int w = 0; w < kLmThreads / 32; ++w) {
+      if (w < warp) before += warp_tot[w];
+      ns += warp_tot[w];
+    }
+    int os = before, og = lo - before;
+    for (int b = lo; b < hi; ++b) {
+      if (sampling_temperature(__ldg(p.temperature + b)))
+        S.slot_base[b] = (os++) * (2 * p.gamma + 1);
+      else
+        S.slot_base[b] = -1 - (ns * (2 * p.gamma + 1) + (og++) * (p.gamma + 1));
+    }
+    if (tid == 0) S.n_samp = ns;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = S.tmem_base;
+
+  if (warp == 0) {
+    // ---- TMA producer
+    if (lane == 0) {
+      const unsigned long long t0 = global_timer_ns();
+      long long it = 0;
+      for (int nt = blockIdx.x; nt < n_tiles && !S.failed; nt += gridDim.x)
+        for (int ks = 0; ks < nk; ++ks, ++it) {
+          const int s = (int)(it % kLmStages);
+          const uint32_t ph = (uint32_t)((it / kLmStages) & 1);
+          if (it >= kLmStages && !lm_wait(&S.empty[s], ph ^ 1u, t0)) {
+            S.failed = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&S.full[s], (uint32_t)(mt + 1) * kTileBytes);
+          tma_load_2d(S.b[s], &map_w, ks * kBK, nt * kBN, &S.full[s]);
+          for (int j = 0; j < mt; ++j) tma_load_2d(S.a[s][j], &map_h, ks * kBK, j * 128, &S.full[s]);
+        }
+      // loads still in flight land before the CTA leaves (bounded)
+      const unsigned long long t1 = global_timer_ns();
+      for (long long q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
+        (void)lm_wait(&S.full[q % kLmStages], (uint32_t)((q / kLmStages) & 1), t1);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      const unsigned long long t0 = global_timer_ns();
+      long long it = 0;
+      int lt = 0;
+      for (int nt = blockIdx.x; nt < n_tiles && !S.failed; nt += gridDim.x, ++lt) {
+        if (lt > 0 && !lm_wait(&S.acc_empty, (uint32_t)((lt - 1) & 1), t0)) {
+          S.failed = 1;
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int ks = 0; ks < nk; ++ks, ++it) {
+          const int s = (int)(it % kLmStages);
+          if (!lm_wait(&S.full[s], (uint32_t)((it / kLmStages) & 1), t0)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t bd = sw128_desc(S.b[s]);
+          for (int j = 0; j < mt; ++j) {
+            const uint64_t ad = sw128_desc(S.a[s][j]);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
+              mma_bf16(tmem + (uint32_t)(j * kBN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&S.empty[s]);
+        }
+        if (!ok) {
+          S.failed = 1;
+          break;
+        }
+        mma_commit(&S.acc_full);
+      }
+    }
+  } else {
+    // ---- epilogue: warps 2-5, lane quarter q of the accumulators
+    const int q = warp & 3;
+    const unsigned long long t0 = global_timer_ns();
+    int lt = 0;
+    for (int nt = blockIdx.x; nt < n_tiles; nt += gridDim.x, ++lt) {
+      const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1), t0);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) S.failed = 1;
+        break;
+      }
+      tc_fence_after();
+      const int n0 = nt * kBN;
+      for (int j = 0; j < mt; ++j) {
+        const int m = j * 128 + q * 32 + lane;
+        const bool row_ok = m < p.M;
+        // the row's place in the verification (fused): its slot and what the
+        // stream would have done with it
+        int slot = -1;
+        bool greedy = false;
+        if (kFused && row_ok) {
+          const int g1 = p.gamma + 1;
+          if (m < p.Mt) {
+            const int b = m / g1, i = m - b * g1;
+            const int base = S.slot_base[b];
+            if (base >= 0) {
+              slot = base + 2 * i;
+            } else {
+              slot = -1 - base + i;
+              greedy = true;
+            }
+          } else {
+            const int b = (m - p.Mt) / p.gamma, i = (m - p.Mt) - b * p.gamma;
+            const int base = S.slot_base[b];
+            if (base >= 0) slot = base + 2 * i + 1;  // a greedy request reads no draft rows
+          }
+        }
+        uint16_t* out = p.logits + (size_t)m * p.V + n0;
+        uint32_t best_key = 0u;
+        int best_col = 0;
+        uint32_t chunk_key = 0u;
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kBN + c * 32), r);
+          uint16_t h[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) h[e] = bf16_rn(__uint_as_float(r[e]));
+          if (row_ok) {
+            const int col0 = n0 + c * 32;
+            if (col0 + 32 <= p.V) {
+              uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                o4[v] = make_uint4(h[8 * v] | ((uint32_t)h[8 * v + 1] << 16), h[8 * v + 2] | ((uint32_t)h[8 * v + 3] << 16),
+                                   h[8 * v + 4] | ((uint32_t)h[8 * v + 5] << 16),
+                                   h[8 * v + 6] | ((uint32_t)h[8 * v + 7] << 16));
+            } else {
+              for (int e = 0; e < 32 && col0 + e < p.V; ++e) out[c * 32 + e] = h[e];
+            }
+          }
+          if (kFused && slot >= 0) {
+            const int col0 = n0 + c * 32;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              if (col0 + e >= p.V) break;
+              const uint32_t k = key_of(__uint_as_float((uint32_t)h[e] << 16));
+              if (k > best_key) {
+                best_key = k;
+                best_col = col0 + e;
+              }
+              chunk_key = max(chunk_key, k);
+            }
+            if ((c & 1) == 1 && !greedy) {
+              // a 64-logit chunk done: it belongs to tile 4 blk + g, blk its
+              // 1024-logit block, g its place in a 256-logit row of that block
+              const int ch0 = n0 + (c - 1) * 32;
+              if (ch0 < p.V && chunk_key) {
+                const int tile = (ch0 >> 10) * 4 + ((ch0 & 255) >> 6);
+                atomicMax(p.tile_keys + (size_t)slot * p.tiles + tile, chunk_key);
+              }
+              chunk_key = 0u;
+            }
+          }
+        }
+        if (kFused && greedy && best_key) red_max_gpu(p.row_best + slot, composite(best_key, best_col));
+      }
+      tc_fence_before();
+      mbar_arrive(&S.acc_empty);
+    }
+  }
+
+  if (kFused && blockIdx.x == 0 && warp >= kEpiWarp0) {
+    // Tiles with no logit (past the row's end, inside its last 16 KB piece):
+    // the stream writes the key of -inf for them, and the finals wait for
+    // every key of a row to be non-zero.
+    const int first = ((p.V + 1023) >> 10) * 4;  // whole 1024-logit blocks past the end
+    const int partial_blk = p.V >> 10, rem = p.V & 1023;
+    const int n_topk_slots = S.n_samp * (2 * p.gamma + 1);
+    for (int slot = tid - kEpiWarp0 * 32; slot < n_topk_slots; slot += 128) {
+      uint32_t* keys = p.tile_keys + (size_t)slot * p.tiles;
+      for (int t = first; t < p.tiles; ++t) keys[t] = kKeyNegInf;
+      if (rem)  // tiles of the last block whose four 64-logit chunks all lie past the end
+        for (int g = 0; g < 4; ++g)
+          if (g * 64 >= rem) keys[partial_blk * 4 + g] = kKeyNegInf;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+  if (tid == 0 && S.failed && p.status) atomicOr(p.status, kStatusTimeout);
+}
+
+// ---- host: tensor maps ------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+// a [rows, K] bf16 row-major matrix read in [128 x 64] boxes, 128-byte swizzle
+bool make_map(CUtensorMap* map, const void* base, long long rows, int K) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2u};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int lmhead_smem_bytes() { return (int)kLmSmemBytes; }
+
+int launch_lmhead(const LmParams& p, const void* h, const void* w, bool fused, int grid, void* stream) {
+  CUtensorMap mw, mh;
+  if (!make_map(&mw, w, p.V, p.K) || !make_map(&mh, h, p.M, p.K)) return (int)cudaErrorInvalidValue;
+  static bool ready[kMaxDevices][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev < 0 || dev >= kMaxDevices) return (int)cudaErrorInvalidDevice;
+  if (!ready[dev][fused ? 1 : 0]) {
+    e = fused ? cudaFuncSetAttribute(lmhead_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kLmSmemBytes)
+              : cudaFuncSetAttribute(lmhead_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kLmSmemBytes);
+    if (e != cudaSuccess) return (int)e;
+    ready[dev][fused ? 1 : 0] = true;
+  }
+  if (fused)
+    lmhead_kernel<true><<<grid, kLmThreads, kLmSmemBytes, (cudaStream_t)stream>>>(mw, mh, p);
+  else
+    lmhead_kernel<false><<<grid, kLmThreads, kLmSmemBytes, (cudaStream_t)stream>>>(mw, mh, p);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace dflash

@@ -1217,6 +1217,7 @@ __device__ void publisher(const Params& p, Smem& S, long long total) {
 // Waits (bounded) until `n` consecutive rows from `slot0` have all their
 // pieces counted, then returns their counters to zero. Run by one warp.
 __device__ __forceinline__ bool wait_rows(const Params& p, int slot0, int n) {
+  if (p.keys_ready) return true;  // written by the kernel before this one; nothing was counted
   const int lane = threadIdx.x & 31;
   const volatile uint32_t* abort_flag = p.abort_flag;
   const uint32_t need = (uint32_t)p.geo.ppr;
@@ -1547,7 +1548,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) sweep_kernel(const Param
     if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
     return;
   }
-  const long long total = (long long)active_slots(p, S) * p.geo.ppr;
+  // with keys from the LM head's epilogue nothing is streamed: only the finals run
+  const long long total = p.keys_ready ? 0 : (long long)active_slots(p, S) * p.geo.ppr;
 
   if (warp < kConsumerWarps)
     consumer<DT>(p, S, total);
