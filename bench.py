@@ -270,6 +270,9 @@ def run_reference(args):
         return 0
     import oracle
 
+    if args.workload == LMHEAD_WORKLOAD:
+        return run_reference_lmhead(args)
+
     inp = synth.make_workload(args.workload, data_seed=0, seed=0)
     B, gamma, V = inp.shape
     det = args.drafts == "det"
@@ -535,17 +538,242 @@ def run_gpu(args):
     return 0
 
 
+# ---------------------------------------------------------------- LM head + verification
+LMHEAD_WORKLOAD = "lmhead_b32_mixed_v248320_k5120"
+LMHEAD_K = 5120
+
+
+def lmhead_flops(M: int, V: int, K: int) -> int:
+    """Dense flops of one LM-head product logits [M, V] = h [M, K] W^T."""
+    return 2 * M * V * K
+
+
+def run_lmhead(args):
+    """The verification fused into the LM head's epilogue (dflash_lmhead_verify)
+    at B = 32, block 8, hidden size 5120, V = 248320, against the same step
+    unfused (dflash_lmhead_logits, then dflash_verify). W is a random
+    bf16 matrix (no trained weights exist here); h and the draft tokens are
+    drawn per input set. The roofline is the tensor cores': the product's
+    dense flops over the step time against the measured bf16 peak."""
+    import torch
+
+    import speculative_decoding_verification_83_gb300 as dv
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as tdist
+
+        tdist.init_process_group("nccl", device_id=torch.device(f"cuda:{local_rank}"))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device(f"cuda:{local_rank}")
+    dv.build()
+    lib = dv.load()
+    B, gamma, V, K = 32, 7, 248320, LMHEAD_K
+    M, Mt = B * (2 * gamma + 1), B * (gamma + 1)
+    top_k, top_p = 20, 0.95
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    w = (torch.randn((V, K), generator=g, device=dev) * (2.0 / K ** 0.5)).to(torch.bfloat16)
+    T = torch.tensor([(0.0, 0.6, 1.0)[b % 3] for b in range(B)], dtype=torch.float32, device=dev)
+    sets = []
+    samp_ws = dv.Workspace(dv.rows_workspace_bytes(B * gamma, V, dv.DFLASH_BF16, top_k, top_p), dev)
+    for s in range(2):
+        h = torch.randn((M, K), generator=g, device=dev).to(torch.bfloat16)
+        logits = dv.lmhead_logits(h, w)
+        # drafts: the library's sampler on the draft rows (argmax for greedy requests)
+        d = dv.sample_rows(logits[Mt:], T.repeat_interleave(gamma), top_k, top_p, 7 + s,
+                           workspace=samp_ws).view(B, gamma).contiguous()
+        sets.append((h, d, logits))
+    torch.cuda.synchronize()
+    ws = dv.Workspace(dv.workspace_bytes(B, gamma, V, dv.DFLASH_BF16, top_k, top_p), dev)
+    out_tok = torch.empty((B, gamma + 1), dtype=torch.int32, device=dev)
+    out_len = torch.empty((B,), dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    row_bytes = V * 2
+
+    def fused(i):
+        h, d, logits = sets[i % 2]
+        rc = lib.dflash_lmhead_verify(h.data_ptr(), w.data_ptr(), B, gamma, V, K, d.data_ptr(), T.data_ptr(),
+                                      top_k, top_p, i + 1, logits.data_ptr(), out_tok.data_ptr(),
+                                      out_len.data_ptr(), ws.ptr, ws.nbytes, status.data_ptr(), sp)
+        if rc:
+            raise RuntimeError(lib.dflash_last_error().decode())
+
+    def unfused(i):
+        h, d, logits = sets[i % 2]
+        rc = lib.dflash_lmhead_logits(h.data_ptr(), w.data_ptr(), M, V, K, logits.data_ptr(), status.data_ptr(), sp)
+        rc = rc or lib.dflash_verify(logits.data_ptr(), logits.data_ptr() + Mt * row_bytes, d.data_ptr(), B, gamma,
+                                     V, dv.DFLASH_BF16, T.data_ptr(), top_k, top_p, i + 1, out_tok.data_ptr(),
+                                     out_len.data_ptr(), ws.ptr, ws.nbytes, status.data_ptr(), sp)
+        if rc:
+            raise RuntimeError(lib.dflash_last_error().decode())
+
+    def timed(fn, steps):
+        for i in range(max(3, args.warmup)):
+            fn(i)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(int(2e6))
+        a.record(stream)
+        for i in range(steps):
+            fn(i)
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    clocks = ClockSampler(local_rank)
+    time.sleep(0.3)
+    region_ms = timed(fused, args.steps)
+    clk = clocks.stop()
+    unfused_ms = timed(unfused, args.steps) / args.steps
+    if int(status.item()) != 0:
+        raise RuntimeError(f"status word {int(status.item())}")
+    # the same outputs both ways, on the last input set
+    fused(0)
+    t_f, l_f = out_tok.clone(), out_len.clone()
+    unfused(0)
+    torch.cuda.synchronize()
+    same = bool(torch.equal(t_f, out_tok) and torch.equal(l_f, out_len))
+
+    # end to end through the binding: h from pinned host memory, the tokens back
+    h_host = sets[0][0].cpu().pin_memory()
+    d_host = sets[0][1].cpu().pin_memory()
+    h_dev, d_dev = torch.empty_like(sets[0][0]), torch.empty_like(sets[0][1])
+    tok_host = torch.empty((B, gamma + 1), dtype=torch.int32).pin_memory()
+    len_host = torch.empty((B,), dtype=torch.int32).pin_memory()
+
+    def e2e_step(i):
+        h_dev.copy_(h_host, non_blocking=True)
+        d_dev.copy_(d_host, non_blocking=True)
+        t_, l_, _ = dv.lmhead_verify(h_dev, w, B, gamma, d_dev, T, top_k, top_p, i, logits=sets[0][2],
+                                     workspace=ws, stream=stream)
+        tok_host.copy_(t_, non_blocking=True)
+        len_host.copy_(l_, non_blocking=True)
+        stream.synchronize()
+
+    for i in range(2):
+        e2e_step(i)
+    n_e2e = max(3, min(20, args.steps))
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i)
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    job = combine_over_ranks(region_ms, e2e_s, args.steps, B * gamma, dev)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return 0
+    step_s = job["ms_per_step"] / 1e3
+    flops = lmhead_flops(M, V, K)
+    peaks, peak_kind = measured_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops", 1700.0)))
+    cpu = None
+    if world == 1:
+        # the oracle's product on 1/64 of the vocabulary (scaled), and its
+        # verification of one batch of the GPU's logits
+        import oracle
+
+        h0 = sets[0][0].view(torch.int16).cpu().numpy().view(np.uint16)
+        w0 = w[: V // 64].view(torch.int16).cpu().numpy().view(np.uint16)
+        L = sets[0][2].view(torch.int16).cpu().numpy().view(np.uint16)
+        d0, T0 = sets[0][1].cpu().numpy(), T.cpu().numpy()
+        c0 = time.perf_counter()
+        oracle.lmhead_logits(h0, w0)
+        t_gemm = (time.perf_counter() - c0) * 64
+        c0 = time.perf_counter()
+        oracle.verify(L[:Mt].reshape(B, gamma + 1, V), L[Mt:].reshape(B, gamma, V), d0, T0, top_k, top_p, 1)
+        t_ver = time.perf_counter() - c0
+        cpu = {"value": B * gamma / (t_gemm + t_ver), "unit": UNIT, "cores": oracle.default_threads(),
+               "kind": "oracle",
+               "sample": f"the fp64 product on {V // 64} of {V} vocabulary rows (x64) and the verification of "
+                         f"one batch: {t_gemm:.1f} s + {t_ver:.1f} s"}
+    line = {
+        "metric": "verified draft-positions/sec of the LM head with the verification in its epilogue "
+                  "(B=32, block 8, K=5120, V=248320)",
+        "value": job["value"], "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": job["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (random-init W and h)",
+        "config": {"workload": LMHEAD_WORKLOAD, "B": B, "gamma": gamma, "V": V, "K": K, "M": M,
+                   "top_k": top_k, "top_p": top_p, "temperatures": "cycling 0 (greedy) / 0.6 / 1",
+                   "l2": f"W ({V * K * 2 / 1e9:.2f} GB) is read once per step, larger than L2",
+                   "per_rank_batch": B},
+        "roofline": {"bound": "tensor", "achieved": flops / step_s / 1e12, "peak": peak, "unit": "TFLOP/s",
+                     "frac": flops / step_s / 1e12 / peak, "traffic": None,
+                     "peak_source": f"{peak_kind} bf16_tflops_sustained (cuBLAS, a seconds-long loop)",
+                     "flops_per_step": flops, "w_bytes_per_step": V * K * 2,
+                     "w_read_gbs": V * K * 2 / step_s / 1e9},
+        "unfused_ms_per_step": unfused_ms,
+        "fused_equals_unfused": same,
+        "cpu_baseline": cpu,
+        "e2e": {"value": job["e2e_value"], "unit": UNIT, "h2d_bytes_per_step": M * K * 2 + B * gamma * 4,
+                "d2h_bytes_per_step": B * (gamma + 1) * 4 + B * 4, "ms_per_step": job["e2e_s"] * 1e3},
+        "gpu_launches": args.steps * 2,
+        "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_reference_lmhead(args):
+    """The oracle on the fused LM-head workload: its fp64 product on 1/64 of
+    the vocabulary (scaled to all of it) plus its verification of one
+    headline batch, per step."""
+    import oracle
+
+    B, gamma, V, K = 32, 7, 248320, LMHEAD_K
+    M = B * (2 * gamma + 1)
+    rng = np.random.default_rng(0)
+    h = synth.f32_to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32))
+    w = synth.f32_to_bf16_bits((rng.standard_normal((V // 64, K)) * (2.0 / K ** 0.5)).astype(np.float32))
+    inp = synth.make_workload(WORKLOAD, data_seed=0, seed=0)
+    d, _, _ = oracle.sample_rows(inp.draft.reshape(B * gamma, V),
+                                 synth.draft_sampling_temperatures(inp.temperature, gamma), 20, 0.95, 7)
+    d = d.reshape(B, gamma)
+    times = []
+    for i in range(max(1, args.warmup) + max(1, args.steps)):
+        c0 = time.perf_counter()
+        oracle.lmhead_logits(h, w)
+        t_gemm = (time.perf_counter() - c0) * 64
+        c0 = time.perf_counter()
+        oracle.verify(inp.target, inp.draft, d, inp.temperature, 20, 0.95, i)
+        times.append(t_gemm + time.perf_counter() - c0)
+    step_s = float(np.mean(times[max(1, args.warmup):]))
+    value = B * gamma / step_s
+    print(json.dumps({
+        "impl": "reference", "metric": "verified draft-positions/sec of the LM head with the verification in its "
+                                       "epilogue (B=32, block 8, K=5120, V=248320)",
+        "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (random-init W and h)",
+        "config": {"workload": LMHEAD_WORKLOAD, "B": B, "gamma": gamma, "V": V, "K": K},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.default_threads(), "kind": "oracle",
+                         "sample": f"per step: the fp64 product on {V // 64} of {V} vocabulary rows (x64) and "
+                                   "the verification of one B=32 batch"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS) + [LMHEAD_WORKLOAD])
     ap.add_argument("--drafts", default="sampled", choices=["sampled", "det"])
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == LMHEAD_WORKLOAD:
+        return run_lmhead(args)
     return run_gpu(args)
 
 

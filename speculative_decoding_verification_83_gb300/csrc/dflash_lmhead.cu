@@ -13,9 +13,9 @@
 // candidate tiles from the stored logits.
 //
 // Kernel layout (one CTA per SM, persistent over 128-column vocabulary tiles):
-//  * warp 0: TMA producer. Per 64-element step of K it loads the W tile
-//    [128 x 64] and the h tiles [128 x 64] of every 128-row token tile into a
-//    two-stage ring (cp.async.bulk.tensor, 128-byte swizzle, mbarrier
+//  * warp 0: TMA producer. Per 32-element step of K it loads the W tile
+//    [128 x 32] and the h tiles [128 x 32] of every 128-row token tile into a
+//    five-stage ring (cp.async.bulk.tensor, 64-byte swizzle, mbarrier
 //    complete_tx);
 //  * warp 1: allocates the tensor memory and issues the MMAs from one thread:
 //    tcgen05.mma.cta_group::1.kind::f16, M = 128 tokens, N = 128 vocabulary
@@ -23,15 +23,16 @@
 //    (one 128-column accumulator per token tile, at most four: M <= 512);
 //    tcgen05.commit frees a stage when its MMAs have read it, and signals the
 //    epilogue after a tile's last step;
-//  * warps 2-5: epilogue. Each thread owns one token row of a 32-lane quarter
-//    of the accumulators (tcgen05.ld.32x32b), rounds the 128 fp32 sums to
-//    bf16 (round to nearest even), stores them, and in the fused mode folds
-//    them into the row's tile keys (red.max) or argmax (red.max of the
-//    (key, index) composite).
+//  * warps 2-9: epilogue. Each thread owns one token row of a 32-lane quarter
+//    of the accumulators and 64 of a tile's 128 columns (tcgen05.ld.32x32b),
+//    rounds the fp32 sums to bf16 (round to nearest even), stores them, and
+//    in the fused mode folds them into the row's tile keys (red.max) or
+//    argmax (red.max of the (key, index) composite).
 // Every wait is bounded; a CTA that gives up raises DFLASH_STATUS_TIMEOUT,
 // waits (bounded) for its loads in flight and frees its tensor memory.
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
@@ -46,16 +47,17 @@
 namespace dflash {
 namespace {
 
-constexpr int kLmThreads = 192;
+constexpr int kLmThreads = 320;
 constexpr int kBN = 128;                          // vocabulary rows per tile
-constexpr int kBK = 64;                           // hidden elements per stage (one 128-byte swizzle row)
+constexpr int kBK = 32;                           // hidden elements per stage (one 64-byte swizzle row)
 constexpr int kMaxMT = kLmMaxRows / 128;          // token tiles
-constexpr int kLmStages = 2;
-constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 64 bf16 tile, 16 KB
-constexpr int kEpiWarp0 = 2;
+constexpr int kLmStages = 5;
+constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 32 bf16 tile, 8 KB
+constexpr int kEpiWarp0 = 2;                      // warps 2-9: the epilogue
+constexpr int kEpiThreads = kLmThreads - 32 * kEpiWarp0;
 
 struct LmSmem {
-  unsigned char a[kLmStages][kMaxMT][kTileBytes];  // h tiles (1024-byte aligned: the swizzle atom)
+  unsigned char a[kLmStages][kMaxMT][kTileBytes];  // h tiles (on 1024-byte boundaries: whole swizzle atoms)
   unsigned char b[kLmStages][kTileBytes];          // W tiles
   uint64_t full[kLmStages], empty[kLmStages];
   uint64_t acc_full, acc_empty;
@@ -65,6 +67,7 @@ struct LmSmem {
   int n_samp;
 };
 constexpr size_t kLmSmemBytes = sizeof(LmSmem) + 1024;  // + room to align the base to 1024 bytes
+static_assert(kLmSmemBytes <= 232448, "one CTA's shared memory (227 KB)");
 
 // ---- PTX wrappers: tensor memory, MMA, TMA --------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -93,7 +96,7 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
                : "memory");
 }
-// 32 consecutive fp32 columns of this thread's lane
+// 32 consecutive fp32 columns of this thread's lane (completes at tmem_wait_ld)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
@@ -103,9 +106,9 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
         "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
-// a [128 x 64] bf16 box of a 2-D tensor map at (k, row) into shared memory
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// a [128 x 32] bf16 box of a 2-D tensor map at (k, row) into shared memory
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int k, int row, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
@@ -115,18 +118,18 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
-// with the 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes
-// apart (stride byte offset), descriptor version 1, swizzle mode 2. The
-// leading byte offset is unused in this layout (one MMA's K extent, 32
-// bytes, lies inside a swizzle row). Moving along K inside the 128-byte row
+// with the 64-byte swizzle: rows of 64 bytes (32 bf16 of K), 8-row groups
+// 512 bytes apart (stride byte offset), descriptor version 1, swizzle mode 4.
+// The leading byte offset is unused in this layout (one MMA's K extent, 32
+// bytes, lies inside a swizzle row). Moving along K inside the 64-byte row
 // adds the byte offset to the start address.
-__device__ __forceinline__ uint64_t sw128_desc(const void* tile) {
+__device__ __forceinline__ uint64_t sw64_desc(const void* tile) {
   const uint32_t a = smem_addr(tile);
   uint64_t d = (uint64_t)((a & 0x3ffffu) >> 4);
-  d |= (uint64_t)1u << 16;            // leading byte offset (unused)
-  d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset
-  d |= (uint64_t)1u << 46;            // descriptor version
-  d |= (uint64_t)2u << 61;            // 128-byte swizzle
+  d |= (uint64_t)1u << 16;           // leading byte offset (unused)
+  d |= (uint64_t)(512u >> 4) << 32;  // stride byte offset
+  d |= (uint64_t)1u << 46;           // descriptor version
+  d |= (uint64_t)4u << 61;           // 64-byte swizzle
   return d;
 }
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
@@ -137,12 +140,6 @@ __device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, unsigned
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   return true;
-}
-
-__device__ __forceinline__ uint16_t bf16_rn(float f) {  // round to nearest even (finite and inf; NaN stays NaN)
-  const uint32_t u = __float_as_uint(f);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x40u);
-  return (uint16_t)((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);
 }
 
 // ---- the kernel ----------------------------------------------------------------------------
@@ -164,7 +161,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       mbar_init(&S.empty[s], 1);
     }
     mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, 128);
+    mbar_init(&S.acc_empty, kEpiThreads);
     S.failed = 0;
     fence_barrier_init();
   }
@@ -248,9 +245,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t bd = sw128_desc(S.b[s]);
+          const uint64_t bd = sw64_desc(S.b[s]);
           for (int j = 0; j < mt; ++j) {
-            const uint64_t ad = sw128_desc(S.a[s][j]);
+            const uint64_t ad = sw64_desc(S.a[s][j]);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
               mma_bf16(tmem + (uint32_t)(j * kBN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
@@ -265,8 +262,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       }
     }
   } else {
-    // ---- epilogue: warps 2-5, lane quarter q of the accumulators
-    const int q = warp & 3;
+    // ---- epilogue: warps 2-9. Warp w reads lane quarter w % 4 of the
+    // accumulators (the lanes a warp may access) and half (w - 2) / 4 of each
+    // tile's 128 columns: one 64-logit chunk per row, which is one part of
+    // one of the stream's 256-logit tiles
+    const int q = warp & 3, hf = (warp - kEpiWarp0) >> 2;
     const unsigned long long t0 = global_timer_ns();
     int lt = 0;
     for (int nt = blockIdx.x; nt < n_tiles; nt += gridDim.x, ++lt) {
@@ -276,15 +276,42 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tc_fence_after();
-      const int n0 = nt * kBN;
+      const int c0 = nt * kBN + hf * 64;  // this thread's first column
       for (int j = 0; j < mt; ++j) {
+        uint32_t ra[32], rb[32];
+        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kBN + hf * 64);
+        tmem_ld32(ta, ra);
+        tmem_ld32(ta + 32u, rb);
+        tmem_wait_ld();
         const int m = j * 128 + q * 32 + lane;
         const bool row_ok = m < p.M;
-        // the row's place in the verification (fused): its slot and what the
-        // stream would have done with it
-        int slot = -1;
-        bool greedy = false;
-        if (kFused && row_ok) {
+        // bf16 pairs, round to nearest even: word i holds columns 2i, 2i + 1
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const __nv_bfloat162 x = __float22bfloat162_rn(make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])));
+          const __nv_bfloat162 y = __float22bfloat162_rn(make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])));
+          pk[i] = *reinterpret_cast<const uint32_t*>(&x);
+          pk[16 + i] = *reinterpret_cast<const uint32_t*>(&y);
+        }
+        const bool whole = c0 + 64 <= p.V;
+        if (row_ok && c0 < p.V) {
+          uint16_t* out = p.logits + (size_t)m * p.V + c0;
+          if (whole) {
+            uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (c0 + e < p.V) out[e] = (uint16_t)(pk[e >> 1] >> ((e & 1) * 16));
+          }
+        }
+        if (kFused && row_ok && c0 < p.V) {
+          // the row's place in the verification: its slot and what the stream
+          // would have done with it
+          int slot = -1;
+          bool greedy = false;
           const int g1 = p.gamma + 1;
           if (m < p.Mt) {
             const int b = m / g1, i = m - b * g1;
@@ -300,56 +327,39 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const int base = S.slot_base[b];
             if (base >= 0) slot = base + 2 * i + 1;  // a greedy request reads no draft rows
           }
-        }
-        uint16_t* out = p.logits + (size_t)m * p.V + n0;
-        uint32_t best_key = 0u;
-        int best_col = 0;
-        uint32_t chunk_key = 0u;
+          if (slot >= 0 && !greedy) {
+            // the chunk's maximum (packed, NaN propagating as in the stream),
+            // into tile 4 blk + g: blk its 1024-logit block, g its place in a
+            // 256-logit row of that block
+            uint32_t key;
+            if (whole) {
+              __nv_bfloat162 acc = *reinterpret_cast<const __nv_bfloat162*>(&pk[0]);
 #pragma unroll
-        for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kBN + c * 32), r);
-          uint16_t h[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) h[e] = bf16_rn(__uint_as_float(r[e]));
-          if (row_ok) {
-            const int col0 = n0 + c * 32;
-            if (col0 + 32 <= p.V) {
-              uint4* o4 = reinterpret_cast<uint4*>(out + c * 32);
-#pragma unroll
-              for (int v = 0; v < 4; ++v)
-                o4[v] = make_uint4(h[8 * v] | ((uint32_t)h[8 * v + 1] << 16), h[8 * v + 2] | ((uint32_t)h[8 * v + 3] << 16),
-                                   h[8 * v + 4] | ((uint32_t)h[8 * v + 5] << 16),
-                                   h[8 * v + 6] | ((uint32_t)h[8 * v + 7] << 16));
+              for (int i = 1; i < 32; ++i) acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&pk[i]));
+              key = key_of(max_nan(__low2float(acc), __high2float(acc)));
             } else {
-              for (int e = 0; e < 32 && col0 + e < p.V; ++e) out[c * 32 + e] = h[e];
-            }
-          }
-          if (kFused && slot >= 0) {
-            const int col0 = n0 + c * 32;
+              float mx = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if (col0 + e >= p.V) break;
-              const uint32_t k = key_of(__uint_as_float((uint32_t)h[e] << 16));
-              if (k > best_key) {
-                best_key = k;
-                best_col = col0 + e;
-              }
-              chunk_key = max(chunk_key, k);
+              for (int e = 0; e < 64; ++e)
+                if (c0 + e < p.V) mx = max_nan(mx, __uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16));
+              key = key_of(mx);
             }
-            if ((c & 1) == 1 && !greedy) {
-              // a 64-logit chunk done: it belongs to tile 4 blk + g, blk its
-              // 1024-logit block, g its place in a 256-logit row of that block
-              const int ch0 = n0 + (c - 1) * 32;
-              if (ch0 < p.V && chunk_key) {
-                const int tile = (ch0 >> 10) * 4 + ((ch0 & 255) >> 6);
-                atomicMax(p.tile_keys + (size_t)slot * p.tiles + tile, chunk_key);
+            atomicMax(p.tile_keys + (size_t)slot * p.tiles + (c0 >> 10) * 4 + ((c0 & 255) >> 6), key);
+          } else if (greedy) {
+            // the lowest column holding the largest key
+            uint32_t best = 0u;
+            int col = 0;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+              const uint32_t k = c0 + e < p.V ? key_of(__uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16)) : 0u;
+              if (k > best) {
+                best = k;
+                col = c0 + e;
               }
-              chunk_key = 0u;
             }
+            if (best) red_max_gpu(p.row_best + slot, composite(best, col));
           }
         }
-        if (kFused && greedy && best_key) red_max_gpu(p.row_best + slot, composite(best_key, best_col));
       }
       tc_fence_before();
       mbar_arrive(&S.acc_empty);
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int first = ((p.V + 1023) >> 10) * 4;  // whole 1024-logit blocks past the end
     const int partial_blk = p.V >> 10, rem = p.V & 1023;
     const int n_topk_slots = S.n_samp * (2 * p.gamma + 1);
-    for (int slot = tid - kEpiWarp0 * 32; slot < n_topk_slots; slot += 128) {
+    for (int slot = tid - kEpiWarp0 * 32; slot < n_topk_slots; slot += kEpiThreads) {
       uint32_t* keys = p.tile_keys + (size_t)slot * p.tiles;
       for (int t = first; t < p.tiles; ++t) keys[t] = kKeyNegInf;
       if (rem)  // tiles of the last block whose four 64-logit chunks all lie past the end
@@ -395,16 +405,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
-// a [rows, K] bf16 row-major matrix read in [128 x 64] boxes, 128-byte swizzle
+// a [rows, K] bf16 row-major matrix read in [128 x 32] boxes, 64-byte swizzle
 bool make_map(CUtensorMap* map, const void* base, long long rows, int K) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2u};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};  // 64 bytes of K: the 64-byte swizzle
   const cuuint32_t estr[2] = {1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
