@@ -354,23 +354,35 @@ __device__ __forceinline__ void b16_count(const unsigned char* row, int j0, int 
   const bool vec = ((reinterpret_cast<uintptr_t>(row) + 2 * (uintptr_t)j0) & 15u) == 0u;
   int j = j0 + (int)threadIdx.x * 8;
   if (vec) {
-    for (; j + 8 <= j1; j += kB16Threads * 8) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(r16 + j));
-      add(v.x & 0xffffu);
-      add(v.x >> 16);
-      add(v.y & 0xffffu);
-      add(v.y >> 16);
-      add(v.z & 0xffffu);
-      add(v.z >> 16);
-      add(v.w & 0xffffu);
-      add(v.w >> 16);
+    // a block takes at most 65 528 tokens: at most 8 vectors a thread, all
+    // loaded before any is counted (one memory latency, not eight)
+    constexpr int kMaxVec = (65528 + kB16Threads * 8 - 1) / (kB16Threads * 8);
+    uint4 v[kMaxVec];
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r) {
+      const int jr = j + r * kB16Threads * 8;
+      v[r] = jr + 8 <= j1 ? __ldg(reinterpret_cast<const uint4*>(r16 + jr)) : make_uint4(0u, 0u, 0u, 0u);
     }
+#pragma unroll
+    for (int r = 0; r < kMaxVec; ++r) {
+      if (j + r * kB16Threads * 8 + 8 > j1) continue;
+      add(v[r].x & 0xffffu);
+      add(v[r].x >> 16);
+      add(v[r].y & 0xffffu);
+      add(v[r].y >> 16);
+      add(v[r].z & 0xffffu);
+      add(v[r].z >> 16);
+      add(v[r].w & 0xffffu);
+      add(v[r].w >> 16);
+    }
+    while (j + 8 <= j1) j += kB16Threads * 8;  // to the first vector not counted
   }
   for (; j < j1; j += kB16Threads * 8)  // the ragged end, or an unaligned row
     for (int i = 0; i < 8 && j + i < j1; ++i) add(__ldg(r16 + j + i));
 }
 
-// weigh each key seen: bin(k16) receives count x weight
+// weigh each key seen: bin(k16, x) receives count x weight (bin < 0: the
+// key does not take part)
 template <class Bin>
 __device__ __forceinline__ void b16_weigh(const uint32_t* cnt, const RowRef& rr, int frac, const float* th,
                                           const float* tl, unsigned long long* hm, Bin bin) {
@@ -383,8 +395,10 @@ __device__ __forceinline__ void b16_weigh(const uint32_t* cnt, const RowRef& rr,
       if (!n) continue;
       const uint32_t k16 = 2u * (uint32_t)w + (uint32_t)half;
       const float x = value_of_key(full_key(k16, 0));
+      const int b = bin(k16, x);
+      if (b < 0) continue;
       const unsigned long long wk = to_fixed(tp_weight(x, rr, th, tl), frac);
-      if (wk) atomicAdd(&hm[bin(k16, x)], (unsigned long long)n * wk);
+      if (wk) atomicAdd(&hm[b], (unsigned long long)n * wk);
     }
   }
 }
@@ -428,12 +442,14 @@ __global__ void __launch_bounds__(kB16Threads) fvtp_histr_b16_kernel(const FvtpP
   int j0, j1;
   b16_range(t.V, blockIdx.y, gridDim.y, &j0, &j1);
   __syncthreads();
-  b16_count(rr.ptr, j0, j1, cnt, [&](uint32_t k16) {
+  auto in_group = [&](uint32_t k16) {
     return k16 >= c.kmin && k16 <= c.kmax && ((unsigned long long)(k16 - c.kmin) >> (shift + 8)) == known;
-  });
+  };
+  b16_count(rr.ptr, j0, j1, cnt, in_group);
   __syncthreads();
-  b16_weigh(cnt, rr, t.frac_bits, th, tl, hm,
-            [&](uint32_t k16, float) { return (int)(((k16 - c.kmin) >> shift) & 255u); });
+  b16_weigh(cnt, rr, t.frac_bits, th, tl, hm, [&](uint32_t k16, float) {
+    return in_group(k16) ? (int)(((k16 - c.kmin) >> shift) & 255u) : -1;
+  });
   __syncthreads();
   if (tid < 256 && hm[tid]) atomicAdd(t.hist_m + (size_t)rho * 256 + tid, hm[tid]);
 }

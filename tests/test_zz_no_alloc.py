@@ -53,9 +53,11 @@ def _noalloc(lib, X, Y, d, T, B, gamma, V, dt, top_k, top_p, seed, out_tok, out_
                                      out_len.data_ptr(), st.data_ptr(), stream)
 
 
-# the top-k filter in bf16 and fp32, and the full-vocabulary softmax (which
-# also uses the draw's part of the scratch and a second pass of launches)
-@pytest.mark.parametrize("dtype,top_k,top_p", [("bf16", 20, 0.95), ("f32", 20, 0.95), ("bf16", 0, 1.0)])
+# the top-k filter in bf16 and fp32, the full-vocabulary softmax (which also
+# uses the draw's part of the scratch and a second pass of launches), and
+# top-p over the full vocabulary (its cut's rounds and histograms too)
+@pytest.mark.parametrize("dtype,top_k,top_p", [("bf16", 20, 0.95), ("f32", 20, 0.95), ("bf16", 0, 1.0),
+                                               ("bf16", 0, 0.9)])
 def test_noalloc_matches_workspace_entry_point_twice(dv, dtype, top_k, top_p):
     lib = dv.load()
     inp, d_np = _case(dtype, top_k, top_p)
