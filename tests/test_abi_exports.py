@@ -106,3 +106,27 @@ def test_audit_entry_point_checks_its_output(lib):
     p = ctypes.c_void_p(1 << 20)
     rc = lib.dflash_verify_audit(p, p, p, 4, 7, 5000, 0, p, 20, 0.95, 0, p, p, None, p, 1 << 30, None, None)
     assert rc == dv.ERR_INVALID_ARG and b"audit" in lib.dflash_last_error()
+
+
+def test_lmhead_argument_checks_happen_on_the_host(lib):
+    """The LM head's shape, alignment and filter checks return before any CUDA
+    call (fake non-null pointers, no GPU needed)."""
+    p, q = ctypes.c_void_p(1 << 20), ctypes.c_void_p((1 << 20) + 8)
+    assert lib.dflash_lmhead_logits(p, p, 513, 4096, 64, p, None, None) == dv.ERR_INVALID_ARG   # M > 512
+    assert lib.dflash_lmhead_logits(p, p, 16, 4100, 64, p, None, None) == dv.ERR_INVALID_ARG   # V % 8
+    assert lib.dflash_lmhead_logits(p, p, 16, 4096, 96, p, None, None) == dv.ERR_INVALID_ARG   # K % 64
+    assert lib.dflash_lmhead_logits(q, p, 16, 4096, 64, p, None, None) == dv.ERR_INVALID_ARG   # 16-byte alignment
+    assert b"aligned" in lib.dflash_last_error()
+    n = ctypes.c_void_p(0)
+    assert lib.dflash_lmhead_logits(n, p, 16, 4096, 64, p, None, None) == dv.ERR_INVALID_ARG
+
+    def fused(B, gamma, top_k, top_p, V=4096, K=64):
+        return lib.dflash_lmhead_verify(p, p, B, gamma, V, K, p, p, top_k, top_p, 0, p, p, p, p, 1 << 30, None,
+                                        None)
+
+    assert fused(32, 8, 20, 0.95) == dv.ERR_INVALID_ARG      # 32 x 17 = 544 rows > 512
+    assert b"rows" in lib.dflash_last_error()
+    assert fused(4, 3, 0, 1.0) == dv.ERR_UNSUPPORTED         # the full-vocabulary filter
+    assert fused(4, 3, 0, 0.9) == dv.ERR_UNSUPPORTED         # top-p over the full vocabulary
+    assert fused(4, 3, 40, 0.9) == dv.ERR_UNSUPPORTED
+    assert fused(4, 3, 20, 0.0) == dv.ERR_INVALID_ARG
