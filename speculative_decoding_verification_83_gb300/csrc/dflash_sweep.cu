@@ -1062,15 +1062,14 @@ __device__ __forceinline__ void piece_keys(const Params& p, const uint4* st4, in
 
 // Full-vocabulary rows: a piece's largest logit m and its sum of
 // exp((x - m) / T) = 2^((x - m) s), s = log2(e) / T, written as one float4
-// per piece (m, the sum as a float-float pair, NaN flag). The piece's
-// maximum comes first (one pass over the stage), so no sum is rescaled; the
-// weights (2^x on the special-function unit) of a lane's block are added
-// pairwise, the block sums are accumulated and the lanes merged in
-// float-float. The request's temperature is fetched here, by the consumer
-// warp, not by the producer: a dependent load per piece on the single
-// thread that issues the bulk copies slows the whole stream.
+// per piece (m, the sum as a float-float pair, NaN flag).
+//
+// bf16 rows (two passes over the stage): the piece's maximum comes first,
+// so no sum is rescaled; the weights (2^x on the special-function unit) of
+// a lane's block are added pairwise, the block sums are accumulated and the
+// lanes merged in float-float.
 template <int DT>
-__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, const float* temperature, float4* out,
+__device__ __forceinline__ void piece_stats_two_pass(const uint4* st4, int nvec, const float* temperature, float4* out,
                                             int lane) {
   const float s = __fdiv_rn(kLog2eHi, __ldg(temperature));  // log2(e) / T, rounded
   float m = -INFINITY;
@@ -1115,6 +1114,91 @@ __device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, const fl
     if (lane + o < 32) acc = ff_add(acc, b);
   }
   if (lane == 0) *out = make_float4(m, acc.hi, acc.lo, isnan(m) ? 1.0f : 0.0f);
+}
+
+// fp32 rows (one pass over the stage, which their stream needs: a second
+// pass over 4 bytes a logit costs more issue slots than the stream has to
+// spare): per block of 4 rounds each lane takes its 16 logits' maximum b and
+// their weights 2^((x - b) s) (the special-function unit's 2^x), added
+// pairwise; once the piece's maximum is known each block sum is scaled once
+// by 2^((b - m) s) and the products are accumulated and the lanes merged in
+// float-float. Every weight then carries two 2^x roundings instead of one,
+// and its exponent the same roundings as (x - m) s, split in two parts of one
+// sign.
+template <int DT>
+__device__ __forceinline__ void piece_stats_one_pass(const uint4* st4, int nvec, const float* temperature, float4* out,
+                                            int lane) {
+  const float s = __fdiv_rn(kLog2eHi, __ldg(temperature));  // log2(e) / T, rounded
+  constexpr int kBlocks = kTilesPerPiece / 4;
+  float bmax[kBlocks], bsum[kBlocks];
+  float m = -INFINITY;
+#pragma unroll
+  for (int blk = 0; blk < kBlocks; ++blk) {
+    uint4 wv[4];
+    float b = -INFINITY;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int v = 32 * (4 * blk + rr) + lane;
+      const uint32_t pad = DT == 0 ? 0xff80ff80u : 0xff800000u;  // -inf past the piece: weight 0
+      wv[rr] = v < nvec ? st4[v] : make_uint4(pad, pad, pad, pad);
+      b = max_nan(b, vector_max<DT>(wv[rr]));
+    }
+    float bs = 0.0f;
+    if (b > -INFINITY && b < INFINITY) {
+      float r4[4];
+#pragma unroll
+      for (int rr = 0; rr < 4; ++rr) {
+        const uint32_t ws[4] = {wv[rr].x, wv[rr].y, wv[rr].z, wv[rr].w};
+        float e[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (DT == 0)
+            e[q] = __fadd_rn(ex2_approx(__fmul_rn(__uint_as_float(ws[q] << 16) - b, s)),
+                             ex2_approx(__fmul_rn(__uint_as_float(ws[q] & 0xffff0000u) - b, s)));
+          else
+            e[q] = ex2_approx(__fmul_rn(__uint_as_float(ws[q]) - b, s));
+        }
+        r4[rr] = __fadd_rn(__fadd_rn(e[0], e[1]), __fadd_rn(e[2], e[3]));
+      }
+      bs = __fadd_rn(__fadd_rn(r4[0], r4[1]), __fadd_rn(r4[2], r4[3]));
+    }
+    bmax[blk] = b;
+    bsum[blk] = bs;
+    m = max_nan(m, b);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = max_nan(m, __shfl_xor_sync(0xffffffffu, m, o));
+  ff acc = {0.0f, 0.0f};
+  if (m > -INFINITY && m < INFINITY) {  // the same in every lane
+#pragma unroll
+    for (int blk = 0; blk < kBlocks; ++blk)
+      if (bsum[blk] > 0.0f) {
+        const float sc = ex2_approx(__fmul_rn(bmax[blk] - m, s));
+        const float prod = __fmul_rn(bsum[blk], sc);
+        acc = ff_add(acc, ff{prod, __fmaf_rn(bsum[blk], sc, -prod)});
+      }
+  }
+  // the lanes share m: a float-float tree, lane 0's result
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const ff b = shfl_down_ff(acc, o);
+    if (lane + o < 32) acc = ff_add(acc, b);
+  }
+  if (lane == 0) *out = make_float4(m, acc.hi, acc.lo, isnan(m) ? 1.0f : 0.0f);
+}
+
+// Both forms keep the per-weight error within the accept test's derived
+// bound. The request's temperature is fetched here, by the consumer warp,
+// not by the producer: a dependent load per piece on the single thread that
+// issues the bulk copies slows the whole stream. (The one-pass form takes 34
+// more registers, which the bf16 instantiation, the headline's, is spared.)
+template <int DT>
+__device__ __forceinline__ void piece_stats(const uint4* st4, int nvec, const float* temperature, float4* out,
+                                            int lane) {
+  if constexpr (DT == 0)
+    piece_stats_two_pass<DT>(st4, nvec, temperature, out, lane);
+  else
+    piece_stats_one_pass<DT>(st4, nvec, temperature, out, lane);
 }
 
 // Consumer warp: reduces whole pieces (this warp takes every 8th piece of the

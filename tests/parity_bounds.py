@@ -27,16 +27,19 @@ Full-vocabulary filter: the draw is float-float over the whole row
 2^-29 and two fp32 roundings (<= 2u)               -> FV_DRAW_ABS = 2^-22
 Its accept test takes p(d) = exp((x_d - m)/T) / sum with a float-float
 numerator and the row normaliser sum from the stream: each weight there is
-2^x on the special-function unit (relative error below 2^-22.73, measured
-over every fp32 argument in [-126, 0]) of an exponent rounded on the way:
-x = (logit - m) s with s = RN(log2(e) / T) (1.22u), one product rounding (u)
-and, for fp32 logits, the difference (u); a relative error e in the
-exponent x <= 0 changes the weight by ln2 |x| e, and the weighted mean of
-|x| over the row is at most its entropy in bits, <= log2 V = 17.92 at
-V = 248320: <= 0.693 * 17.92 * 3.22u = 40u. Block sums are pairwise (<= 5u),
+2^a 2^c on the special-function unit (relative error below 2^-22.73 = 0.6u
+each, measured over every fp32 argument in [-126, 0]; a = (logit - b) s for
+b the maximum of the lane's block, c = (b - m) s once per block, then one
+product rounding, u) of exponents rounded on the way: s = RN(log2(e) / T)
+(1.22u), a product rounding (u) and, for fp32 logits, the difference (u)
+in each part; a and c are <= 0, so their errors add to at most 3.22u of
+|x|, x = (logit - m) s. A relative error e in the exponent x <= 0 changes
+the weight by ln2 |x| e, and the weighted mean of |x| over the row is at
+most its entropy in bits, <= log2 V = 17.92 at V = 248320:
+<= 0.693 * 17.92 * 3.22u = 40u. Block sums are pairwise (<= 5u),
 everything above them float-float. So
-  sum:        <= 2.42u + 40u + 5u = 47.4u
-  p(d), q(d): <= 47.4u + u (rounded once)           -> FV_PROB_REL = 2^-18
+  sum:        <= 1.2u + u + 1.22u + 40u + 5u = 48.4u
+  p(d), q(d): <= 48.4u + u (rounded once)           -> FV_PROB_REL = 2^-18
   the ratio (two of them, rounded) and the oracle's -> FV_ACCEPT_REL = 2^-17
 Top-p over the full vocabulary (top-k off, top_p < 1; dflash_fvtp.cu): each
 weight exp((x - m)/T) is float-float (2^-29.9 relative) and is rounded to
