@@ -197,6 +197,7 @@ __device__ __forceinline__ ff warp_exclusive_ff(ff v, ff& inclusive) {
 // comes from the stream's fp32 normalisers (w_x S_y0 > w_y S_x0); a token
 // they place wrongly has |p - q| below about 1e-6 p and carries under 1e-11 of
 // the mass.
+template <int DT, bool kCut>
 __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
   __shared__ float th[kExpTable], tl[kExpTable];
   __shared__ ff scratch[kFvThreads / 32];
@@ -220,15 +221,15 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
 #pragma unroll
   for (int k = 0; k < kFvPerThread; ++k) {
     const int j = j0 + k * kFvThreads;
-    xs[k] = j < jn ? fv_load(q.x, j, f.dtype) : -INFINITY;
-    ys[k] = (q.residual && j < jn) ? fv_load(q.y, j, f.dtype) : -INFINITY;
+    xs[k] = j < jn ? fv_load(q.x, j, DT) : -INFINITY;
+    ys[k] = (q.residual && j < jn) ? fv_load(q.y, j, DT) : -INFINITY;
   }
   if (q.residual) {
 #pragma unroll
     for (int k = 0; k < kFvPerThread; ++k) {
       const int j = j0 + k * kFvThreads;
-      const ff wx = in_kept(q.cut, q.kx, q.jx, xs[k], j) ? weight(xs[k], q.inv_t, q.zmx, th, tl) : ff{0.0f, 0.0f};
-      const ff wy = in_kept(q.cut, q.ky, q.jy, ys[k], j) ? weight(ys[k], q.inv_t, q.zmy, th, tl) : ff{0.0f, 0.0f};
+      const ff wx = in_kept(kCut, q.kx, q.jx, xs[k], j) ? weight(xs[k], q.inv_t, q.zmx, th, tl) : ff{0.0f, 0.0f};
+      const ff wy = in_kept(kCut, q.ky, q.jy, ys[k], j) ? weight(ys[k], q.inv_t, q.zmy, th, tl) : ff{0.0f, 0.0f};
       acc_add(sx, wx);
       acc_add(sy, wy);
       if (__fmul_rn(wx.hi, q.sy0) > __fmul_rn(wy.hi, q.sx0)) {
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kFvThreads) fv_sums_kernel(const FvParams f) {
 #pragma unroll
     for (int k = 0; k < kFvPerThread; ++k) {
       const int j = j0 + k * kFvThreads;
-      ff wx = in_kept(q.cut, q.kx, q.jx, xs[k], j) ? weight(xs[k], q.inv_t, q.zmx, th, tl) : ff{0.0f, 0.0f};
+      ff wx = in_kept(kCut, q.kx, q.jx, xs[k], j) ? weight(xs[k], q.inv_t, q.zmx, th, tl) : ff{0.0f, 0.0f};
       if (j == q.excl) wx = {0.0f, 0.0f};  // p without the deterministic draft
       acc_add(sx, wx);
       if (wx.hi > 0.0f) lp = j0 + k * kFvThreads;
@@ -448,7 +449,11 @@ int launch_fullvocab_draw(const FvParams& f, void* stream) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   cfg.gridDim = dim3((unsigned)f.n_slices, (unsigned)f.B);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, fv_sums_kernel, f);
+  // the storage type and whether a top-p cut masks the weights are the
+  // launch's: one instantiation each, no per-logit test of either
+  void (*sums)(const FvParams) = f.dtype == 0 ? (f.cut ? fv_sums_kernel<0, true> : fv_sums_kernel<0, false>)
+                                              : (f.cut ? fv_sums_kernel<1, true> : fv_sums_kernel<1, false>);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sums, f);
   if (e != cudaSuccess) return (int)e;
   cfg.gridDim = dim3((unsigned)f.B);
   e = cudaLaunchKernelEx(&cfg, fv_pick_kernel, f);
