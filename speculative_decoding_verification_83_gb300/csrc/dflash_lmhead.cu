@@ -12,11 +12,13 @@
 // and runs only its finals (Params::keys_ready), which gather the few
 // candidate tiles from the stored logits.
 //
-// Kernel layout (one CTA per SM, persistent over 128-column vocabulary tiles):
-//  * warp 0: TMA producer. Per 32-element step of K it loads the W tile
-//    [128 x 32] and the h tiles [128 x 32] of every 128-row token tile into a
+// Kernel layout (one CTA per SM, clusters of two CTAs persistent over pairs
+// of 128-column vocabulary tiles):
+//  * warp 0: TMA producer. Per 32-element step of K it loads its W tile
+//    [128 x 32] and half of the h tiles [128 x 32] of the 128-row token
+//    tiles, the latter multicast into both CTAs of the cluster, into a
 //    five-stage ring (cp.async.bulk.tensor, 64-byte swizzle, mbarrier
-//    complete_tx);
+//    complete_tx; a stage is reloaded once both CTAs' MMAs have read it);
 //  * warp 1: allocates the tensor memory and issues the MMAs from one thread:
 //    tcgen05.mma.cta_group::1.kind::f16, M = 128 tokens, N = 128 vocabulary
 //    rows, K = 16 per instruction, bf16 in, fp32 accumulated in tensor memory
@@ -108,6 +110,34 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// this CTA's rank in its cluster, and a barrier over the cluster's threads
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// a [128 x 32] bf16 box into the same shared-memory offset of every CTA of
+// the cluster in mask, completing bytes on each one's barrier at bar's offset
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int k, int row, uint64_t* bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(smem_addr(bar)), "h"(mask)
+      : "memory");
+}
+// arrive on the barrier at bar's offset in every CTA of mask once this CTA's
+// MMAs issued so far have completed
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
+}
 // a [128 x 32] bf16 box of a 2-D tensor map at (k, row) into shared memory
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int k, int row, uint64_t* bar) {
   asm volatile(
@@ -152,13 +182,17 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int mt = (p.M + 127) / 128;
   const int n_tiles = (p.V + kBN - 1) / kBN;
+  // clusters of two CTAs take pairs of vocabulary tiles (this CTA the one of
+  // its rank) and share the h tiles: each loads half of them into both
+  const int rank = (int)cluster_rank();
+  const int n_pairs = (n_tiles + 1) / 2, pair0 = blockIdx.x / 2, n_clusters = gridDim.x / 2;
   const int nk = p.K / kBK;
   const uint32_t ncols = mt <= 1 ? 128u : (mt <= 2 ? 256u : 512u);
 
   if (tid == 0) {
     for (int s = 0; s < kLmStages; ++s) {
       mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 1);
+      mbar_init(&S.empty[s], 2);  // a stage is free once both CTAs' MMAs have read it
     }
     mbar_init(&S.acc_full, 1);
     mbar_init(&S.acc_empty, kEpiThreads);
@@ -200,6 +234,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any load reaches them
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
@@ -208,7 +243,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (lane == 0) {
       const unsigned long long t0 = global_timer_ns();
       long long it = 0;
-      for (int nt = blockIdx.x; nt < n_tiles && !S.failed; nt += gridDim.x)
+      for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters) {
+        const int nt = 2 * np + rank;  // past the last tile for one CTA of an odd pair: W is zero-filled
         for (int ks = 0; ks < nk; ++ks, ++it) {
           const int s = (int)(it % kLmStages);
           const uint32_t ph = (uint32_t)((it / kLmStages) & 1);
@@ -218,8 +254,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           }
           mbar_arrive_expect_tx(&S.full[s], (uint32_t)(mt + 1) * kTileBytes);
           tma_load_2d(S.b[s], &map_w, ks * kBK, nt * kBN, &S.full[s]);
-          for (int j = 0; j < mt; ++j) tma_load_2d(S.a[s][j], &map_h, ks * kBK, j * 128, &S.full[s]);
+          for (int j = rank; j < mt; j += 2) tma_load_2d_mc(S.a[s][j], &map_h, ks * kBK, j * 128, &S.full[s], 3);
         }
+      }
       // loads still in flight land before the CTA leaves (bounded)
       const unsigned long long t1 = global_timer_ns();
       for (long long q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
@@ -231,7 +268,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       const unsigned long long t0 = global_timer_ns();
       long long it = 0;
       int lt = 0;
-      for (int nt = blockIdx.x; nt < n_tiles && !S.failed; nt += gridDim.x, ++lt) {
+      for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters, ++lt) {
         if (lt > 0 && !lm_wait(&S.acc_empty, (uint32_t)((lt - 1) & 1), t0)) {
           S.failed = 1;
           break;
@@ -252,7 +289,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
               mma_bf16(tmem + (uint32_t)(j * kBN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
           }
-          mma_commit(&S.empty[s]);
+          mma_commit_mc(&S.empty[s], 3);  // frees the stage in both CTAs' rings
         }
         if (!ok) {
           S.failed = 1;
@@ -269,7 +306,8 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     const int q = warp & 3, hf = (warp - kEpiWarp0) >> 2;
     const unsigned long long t0 = global_timer_ns();
     int lt = 0;
-    for (int nt = blockIdx.x; nt < n_tiles; nt += gridDim.x, ++lt) {
+    for (int np = pair0; np < n_pairs; np += n_clusters, ++lt) {
+      const int nt = 2 * np + rank;
       const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1), t0);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) S.failed = 1;
@@ -384,6 +422,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no load or arrival of the peer's still reaches this CTA
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
@@ -438,11 +477,21 @@ int launch_lmhead(const LmParams& p, const void* h, const void* w, bool fused, i
     if (e != cudaSuccess) return (int)e;
     ready[dev][fused ? 1 : 0] = true;
   }
-  if (fused)
-    lmhead_kernel<true><<<grid, kLmThreads, kLmSmemBytes, (cudaStream_t)stream>>>(mw, mh, p);
-  else
-    lmhead_kernel<false><<<grid, kLmThreads, kLmSmemBytes, (cudaStream_t)stream>>>(mw, mh, p);
-  return (int)cudaGetLastError();
+  // clusters of two CTAs (an even grid: two SMs a cluster)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(grid < 2 ? 2 : grid & ~1));
+  cfg.blockDim = dim3(kLmThreads);
+  cfg.dynamicSmemBytes = kLmSmemBytes;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)(fused ? cudaLaunchKernelEx(&cfg, lmhead_kernel<true>, mw, mh, p)
+                     : cudaLaunchKernelEx(&cfg, lmhead_kernel<false>, mw, mh, p));
 }
 
 }  // namespace dflash
