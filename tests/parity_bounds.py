@@ -1,6 +1,6 @@
 """Bounds on how far a GPU decision can sit from the oracle's and still be
-taken the other way, from the fp32 arithmetic each side does (derived in the
-design notes, section "Parity bounds"). A GPU result that differs from the
+taken the other way, from the fp32 arithmetic each side does (derived
+below, decision by decision). A GPU result that differs from the
 oracle's is accepted only when the oracle reports the decision's margin below
 its bound; everything else must match exactly.
 
