@@ -32,12 +32,13 @@ def dv():
     return m
 
 
-@pytest.mark.parametrize("mode", ["top_k", "full_vocab", "det", "greedy", "sample_rows", "shard"])
+@pytest.mark.parametrize("mode", ["top_k", "full_vocab", "top_p_vocab", "det", "greedy", "sample_rows", "shard",
+                                  "lmhead"])
 def test_cancelled_call_reports_timeout_and_the_workspace_recovers(dv, mode):
-    B, gamma, V = 6, 7, 20011
+    B, gamma, V = 6, 7, 20011 if mode != "lmhead" else 20008  # the LM head wants V % 8 == 0
     X, Y, _ = synth.make_logits(B, gamma, V, "bf16", data_seed=17, sigma_d=0.5)
     T = np.array([1.0, 0.0, 0.6, 1.0, 1.5, 0.0], np.float32)
-    top_k, top_p = (0, 1.0) if mode == "full_vocab" else (20, 0.95)
+    top_k, top_p = {"full_vocab": (0, 1.0), "top_p_vocab": (0, 0.9)}.get(mode, (20, 0.95))
     d, _, _ = oracle.sample_rows(Y.reshape(B * gamma, V), synth.draft_sampling_temperatures(T, gamma), top_k,
                                  top_p, 4)
     Xd, Yd = synth.to_torch(X, DEV), synth.to_torch(Y, DEV)
@@ -49,9 +50,15 @@ def test_cancelled_call_reports_timeout_and_the_workspace_recovers(dv, mode):
     else:
         ws = dv.Workspace(dv.workspace_bytes(B, gamma, V, dv.DFLASH_BF16, top_k, top_p), DEV)
 
+    if mode == "lmhead":
+        rng = np.random.default_rng(3)
+        h = synth.to_torch(synth.f32_to_bf16_bits(rng.standard_normal((B * (2 * gamma + 1), 64)).astype(np.float32)),
+                           DEV)
+        w = synth.to_torch(synth.f32_to_bf16_bits((rng.standard_normal((V, 64)) * 0.25).astype(np.float32)), DEV)
+
     def call():
         st = torch.zeros(1, dtype=torch.int32, device=DEV)
-        if mode in ("top_k", "full_vocab"):
+        if mode in ("top_k", "full_vocab", "top_p_vocab"):
             out = dv.verify(Xd, Yd, dd, Td, top_k, top_p, 9, status=st, workspace=ws)
         elif mode == "det":
             out = dv.verify_det(Xd, dd, Td, top_k, top_p, 9, status=st, workspace=ws)
@@ -60,8 +67,10 @@ def test_cancelled_call_reports_timeout_and_the_workspace_recovers(dv, mode):
         elif mode == "sample_rows":
             out = (dv.sample_rows(Yd.view(B * gamma, V), Td.repeat_interleave(gamma), 20, 0.95, 3, status=st,
                                   workspace=ws),)
-        else:
+        elif mode == "shard":
             out = (dv.shard_candidates(Xd, Yd, 0, 20, status=st, workspace=ws),)
+        else:  # the LM head runs whatever the flag; its finals-only verification reports the cancel
+            out = dv.lmhead_verify(h, w, B, gamma, dd, Td, top_k, top_p, 9, status=st, workspace=ws)[:2]
         torch.cuda.synchronize()
         return [o.cpu().numpy() for o in out], int(st.item())
 
