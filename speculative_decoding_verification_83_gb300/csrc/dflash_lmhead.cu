@@ -12,24 +12,29 @@
 // and runs only its finals (Params::keys_ready), which gather the few
 // candidate tiles from the stored logits.
 //
-// Kernel layout (one CTA per SM, clusters of two CTAs persistent over pairs
-// of 128-column vocabulary tiles):
-//  * warp 0: TMA producer. Per 32-element step of K it loads its W tile
-//    [128 x 32] and half of the h tiles [128 x 32] of the 128-row token
-//    tiles, the latter multicast into both CTAs of the cluster, into a
-//    five-stage ring (cp.async.bulk.tensor, 64-byte swizzle, mbarrier
-//    complete_tx; a stage is reloaded once both CTAs' MMAs have read it);
-//  * warp 1: allocates the tensor memory and issues the MMAs from one thread:
-//    tcgen05.mma.cta_group::1.kind::f16, M = 128 tokens, N = 128 vocabulary
-//    rows, K = 16 per instruction, bf16 in, fp32 accumulated in tensor memory
-//    (one 128-column accumulator per token tile, at most four: M <= 512);
-//    tcgen05.commit frees a stage when its MMAs have read it, and signals the
-//    epilogue after a tile's last step;
+// Kernel layout: clusters of two CTAs (one per SM) work as one pair of the
+// tensor cores (cta_group::2), persistent over 256-column vocabulary tiles.
+// One pair MMA computes D [256 tokens, 256 vocabulary columns] (K = 16):
+// each CTA holds the A rows of its 128 tokens and the B rows of its 128
+// vocabulary columns, and its tensor memory receives D's rows of its tokens
+// over all 256 columns. The tokens come in up to two groups of 256 (M <= 512).
+//  * warp 0: TMA producer. Per 32-element step of K each CTA loads its W tile
+//    [128 x 32] and its h tile [128 x 32] of each token group into a
+//    nine-stage ring (cp.async.bulk.tensor, 64-byte swizzle); the bytes of
+//    both CTAs complete on the first CTA's barrier, and a stage is reloaded
+//    once the pair's MMAs have read it;
+//  * warp 1: allocates the pair's tensor memory; in the first CTA, one thread
+//    issues the MMAs (tcgen05.mma.cta_group::2.kind::f16, bf16 in, fp32
+//    accumulated in tensor memory, one 256-column accumulator per token
+//    group) and the commits that free a stage in both CTAs and signal both
+//    epilogues after a tile's last step;
 //  * warps 2-9: epilogue. Each thread owns one token row of a 32-lane quarter
-//    of the accumulators and 64 of a tile's 128 columns (tcgen05.ld.32x32b),
-//    rounds the fp32 sums to bf16 (round to nearest even), stores them, and
-//    in the fused mode folds them into the row's tile keys (red.max) or
-//    argmax (red.max of the (key, index) composite).
+//    of its CTA's accumulators and 128 of a tile's 256 columns
+//    (tcgen05.ld.32x32b), rounds the fp32 sums to bf16 (round to nearest
+//    even), stores them, and in the fused mode folds them into the row's
+//    tile keys (red.max) or argmax (red.max of the (key, index) composite).
+//    The two CTAs' epilogues both report to the first CTA before its MMAs
+//    overwrite the accumulators.
 // Every wait is bounded; a CTA that gives up raises DFLASH_STATUS_TIMEOUT,
 // waits (bounded) for its loads in flight and frees its tensor memory.
 
@@ -50,53 +55,66 @@ namespace dflash {
 namespace {
 
 constexpr int kLmThreads = 320;
-constexpr int kBN = 128;                          // vocabulary rows per tile
+constexpr int kBN = 128;                          // vocabulary rows per CTA (B rows of its half)
+constexpr int kPairN = 2 * kBN;                   // vocabulary columns per pair: N of one MMA
+constexpr int kGroupM = 256;                      // tokens per group: M of one MMA, 128 per CTA
 constexpr int kBK = 32;                           // hidden elements per stage (one 64-byte swizzle row)
-constexpr int kMaxMT = kLmMaxRows / 128;          // token tiles
-constexpr int kLmStages = 5;
+constexpr int kMaxG = kLmMaxRows / kGroupM;       // token groups
+constexpr int kLmMaxB = kLmMaxRows / 3;           // requests of a fused call (2 gamma + 1 >= 3 rows each)
+constexpr int kLmStages = 9;
 constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 32 bf16 tile, 8 KB
 constexpr int kEpiWarp0 = 2;                      // warps 2-9: the epilogue
 constexpr int kEpiThreads = kLmThreads - 32 * kEpiWarp0;
+constexpr int kEpiBarrier = 1;                    // named barrier of the epilogue warps
+static_assert(kMaxG * kGroupM == kLmMaxRows, "token groups cover the rows");
 
 struct LmSmem {
-  unsigned char a[kLmStages][kMaxMT][kTileBytes];  // h tiles (on 1024-byte boundaries: whole swizzle atoms)
-  unsigned char b[kLmStages][kTileBytes];          // W tiles
+  unsigned char b[kLmStages][kTileBytes];          // W tiles (on 1024-byte boundaries: whole swizzle atoms)
+  unsigned char a[kLmStages][kMaxG][kTileBytes];   // h tiles of this CTA's tokens
   uint64_t full[kLmStages], empty[kLmStages];
   uint64_t acc_full, acc_empty;
   uint32_t tmem_base;
   int failed;
-  int slot_base[kMaxB];  // per request: its first slot (sampling requests), or -(1 + first slot) (greedy)
+  int slot_base[kLmMaxB];  // per request: its first slot (sampling requests), or -(1 + first slot) (greedy)
   int n_samp;
 };
 constexpr size_t kLmSmemBytes = sizeof(LmSmem) + 1024;  // + room to align the base to 1024 bytes
 static_assert(kLmSmemBytes <= 232448, "one CTA's shared memory (227 KB)");
 
-// ---- PTX wrappers: tensor memory, MMA, TMA --------------------------------------------
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
+// ---- PTX wrappers: tensor memory, MMA, TMA, cluster barriers ---------------------------
+// Every tcgen05 instruction of the kernel that names a CTA group names the
+// pair (cta_group::2): allocation and release are made by one warp of each
+// CTA together, the MMAs and their commits by one thread of the first CTA.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
                "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, one instruction (M = 128, N = 128, K = 16)
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+// D[tmem of both CTAs] (+)= A[smem desc, both CTAs] * B[smem desc, both CTAs]^T:
+// one pair instruction, M = 256 (128 rows per CTA), N = 256 (128 B rows per CTA), K = 16
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// arrive on the mbarrier once the MMAs issued so far have completed
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-               : "memory");
+// arrive on the barrier at bar's offset in every CTA of mask once the pair
+// MMAs issued so far have completed
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_addr(bar)),
+      "h"(mask)
+      : "memory");
 }
 // 32 consecutive fp32 columns of this thread's lane (completes at tmem_wait_ld)
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
@@ -119,32 +137,50 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// a [128 x 32] bf16 box into the same shared-memory offset of every CTA of
-// the cluster in mask, completing bytes on each one's barrier at bar's offset
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int k, int row, uint64_t* bar,
-                                               uint16_t mask) {
+// the cluster-window address of the same shared-memory object in the first CTA
+__device__ __forceinline__ uint32_t first_cta_addr(const void* p) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_addr(p)));
+  return r;
+}
+// a [128 x 32] bf16 box of a 2-D tensor map at (k, row) into this CTA's shared
+// memory, its bytes completing on a barrier of either CTA of the pair
+__device__ __forceinline__ void tma_load_pair(void* dst, const CUtensorMap* map, int k, int row,
+                                              uint32_t bar_cluster) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(smem_addr(bar)), "h"(mask)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(bar_cluster)
       : "memory");
 }
-// arrive on the barrier at bar's offset in every CTA of mask once this CTA's
-// MMAs issued so far have completed
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_addr(bar)),
-      "h"(mask)
-      : "memory");
+// arrive on a barrier of another CTA of the cluster
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
-// a [128 x 32] bf16 box of a 2-D tensor map at (k, row) into shared memory
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int k, int row, uint64_t* bar) {
+// a wait that also orders what the other CTA of the pair did before it arrived
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-          "r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(k), "r"(row), "r"(smem_addr(bar))
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
       : "memory");
+  return ok != 0u;
+}
+// the epilogue warps' own barrier: the AND of every epilogue thread's flag
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kEpiBarrier), "n"(kEpiThreads)
+      : "memory");
+  return r != 0u;
+}
+__device__ __forceinline__ void epi_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
@@ -152,7 +188,8 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
 // 512 bytes apart (stride byte offset), descriptor version 1, swizzle mode 4.
 // The leading byte offset is unused in this layout (one MMA's K extent, 32
 // bytes, lies inside a swizzle row). Moving along K inside the 64-byte row
-// adds the byte offset to the start address.
+// adds the byte offset to the start address. In a pair MMA the same offset
+// addresses each CTA's own tile.
 __device__ __forceinline__ uint64_t sw64_desc(const void* tile) {
   const uint32_t a = smem_addr(tile);
   uint64_t d = (uint64_t)((a & 0x3ffffu) >> 4);
@@ -163,11 +200,17 @@ __device__ __forceinline__ uint64_t sw64_desc(const void* tile) {
   return d;
 }
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = 128, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kBN >> 3) << 17) | ((128u >> 4) << 24);
+// K-major, N = 256, M = 256 (the pair's rows).
+constexpr uint32_t kIdesc =
+    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(kGroupM >> 4) << 24);
 
 __device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, unsigned long long t0) {
   while (!mbar_try_wait(bar, parity))
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+__device__ __forceinline__ bool lm_wait_cluster(uint64_t* bar, uint32_t parity, unsigned long long t0) {
+  while (!mbar_try_wait_cluster(bar, parity))
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }
@@ -180,26 +223,26 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   extern __shared__ unsigned char lm_raw[];
   LmSmem& S = *reinterpret_cast<LmSmem*>((reinterpret_cast<uintptr_t>(lm_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int mt = (p.M + 127) / 128;
-  const int n_tiles = (p.V + kBN - 1) / kBN;
-  // clusters of two CTAs take pairs of vocabulary tiles (this CTA the one of
-  // its rank) and share the h tiles: each loads half of them into both
+  const int groups = (p.M + kGroupM - 1) / kGroupM;
+  // each cluster is one pair of the tensor cores over 256-column vocabulary
+  // tiles: this CTA holds the W rows of its half of the tile and the h rows
+  // of its half of each token group
   const int rank = (int)cluster_rank();
-  const int n_pairs = (n_tiles + 1) / 2, pair0 = blockIdx.x / 2, n_clusters = gridDim.x / 2;
+  const int n_pairs = (p.V + kPairN - 1) / kPairN, pair0 = blockIdx.x / 2, n_clusters = gridDim.x / 2;
   const int nk = p.K / kBK;
-  const uint32_t ncols = mt <= 1 ? 128u : (mt <= 2 ? 256u : 512u);
+  const uint32_t ncols = groups <= 1 ? 256u : 512u;
 
   if (tid == 0) {
     for (int s = 0; s < kLmStages; ++s) {
-      mbar_init(&S.full[s], 1);
-      mbar_init(&S.empty[s], 2);  // a stage is free once both CTAs' MMAs have read it
+      mbar_init(&S.full[s], 1);   // the first CTA's producer; both CTAs' bytes
+      mbar_init(&S.empty[s], 1);  // the pair's commit
     }
     mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, kEpiThreads);
+    mbar_init(&S.acc_empty, 2);   // one arrival from each CTA's epilogue
     S.failed = 0;
     fence_barrier_init();
   }
-  if (warp == 1) tmem_alloc(&S.tmem_base, ncols);
+  if (warp == 1) tmem_alloc_pair(&S.tmem_base, ncols);
   if (kFused) {
     // slots of the verification (sampling requests first, in request order,
     // 2 gamma + 1 slots each; then greedy requests, gamma + 1 each): each
@@ -234,17 +277,16 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before any load reaches them
+  cluster_sync();  // both CTAs' barriers are initialised before any load or arrival reaches them
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
 
   if (warp == 0) {
-    // ---- TMA producer
+    // ---- TMA producer (both CTAs)
     if (lane == 0) {
       const unsigned long long t0 = global_timer_ns();
       long long it = 0;
       for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters) {
-        const int nt = 2 * np + rank;  // past the last tile for one CTA of an odd pair: W is zero-filled
         for (int ks = 0; ks < nk; ++ks, ++it) {
           const int s = (int)(it % kLmStages);
           const uint32_t ph = (uint32_t)((it / kLmStages) & 1);
@@ -252,24 +294,28 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             S.failed = 1;
             break;
           }
-          mbar_arrive_expect_tx(&S.full[s], (uint32_t)(mt + 1) * kTileBytes);
-          tma_load_2d(S.b[s], &map_w, ks * kBK, nt * kBN, &S.full[s]);
-          for (int j = rank; j < mt; j += 2) tma_load_2d_mc(S.a[s][j], &map_h, ks * kBK, j * 128, &S.full[s], 3);
+          if (rank == 0) mbar_arrive_expect_tx(&S.full[s], 2u * (uint32_t)(groups + 1) * kTileBytes);
+          const uint32_t bar = first_cta_addr(&S.full[s]);
+          // rows past the end of W or h (a last half tile, a last token group) are zero-filled
+          tma_load_pair(S.b[s], &map_w, ks * kBK, np * kPairN + rank * kBN, bar);
+          for (int j = 0; j < groups; ++j)
+            tma_load_pair(S.a[s][j], &map_h, ks * kBK, j * kGroupM + rank * 128, bar);
         }
       }
-      // loads still in flight land before the CTA leaves (bounded)
+      // every load issued has landed once the MMAs that read it have
+      // completed and freed its stage (bounded)
       const unsigned long long t1 = global_timer_ns();
       for (long long q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
-        (void)lm_wait(&S.full[q % kLmStages], (uint32_t)((q / kLmStages) & 1), t1);
+        (void)lm_wait(&S.empty[q % kLmStages], (uint32_t)((q / kLmStages) & 1), t1);
     }
   } else if (warp == 1) {
-    // ---- MMA issuer
-    if (lane == 0) {
+    // ---- MMA issuer (the first CTA, for the pair)
+    if (lane == 0 && rank == 0) {
       const unsigned long long t0 = global_timer_ns();
       long long it = 0;
       int lt = 0;
       for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters, ++lt) {
-        if (lt > 0 && !lm_wait(&S.acc_empty, (uint32_t)((lt - 1) & 1), t0)) {
+        if (lt > 0 && !lm_wait_cluster(&S.acc_empty, (uint32_t)((lt - 1) & 1), t0)) {
           S.failed = 1;
           break;
         }
@@ -283,73 +329,46 @@ __global__ void __launch_bounds__(kLmThreads, 1)
           }
           tc_fence_after();
           const uint64_t bd = sw64_desc(S.b[s]);
-          for (int j = 0; j < mt; ++j) {
+          for (int j = 0; j < groups; ++j) {
             const uint64_t ad = sw64_desc(S.a[s][j]);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
-              mma_bf16(tmem + (uint32_t)(j * kBN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+              mma_pair(tmem + (uint32_t)(j * kPairN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
           }
-          mma_commit_mc(&S.empty[s], 3);  // frees the stage in both CTAs' rings
+          mma_commit_pair(&S.empty[s], 3);  // frees the stage in both CTAs' rings
         }
         if (!ok) {
           S.failed = 1;
           break;
         }
-        mma_commit(&S.acc_full);
+        mma_commit_pair(&S.acc_full, 3);  // both CTAs' accumulators are complete
       }
     }
   } else {
-    // ---- epilogue: warps 2-9. Warp w reads lane quarter w % 4 of the
+    // ---- epilogue: warps 2-9. Warp w reads lane quarter w % 4 of this CTA's
     // accumulators (the lanes a warp may access) and half (w - 2) / 4 of each
-    // tile's 128 columns: one 64-logit chunk per row, which is one part of
-    // one of the stream's 256-logit tiles
+    // tile's 256 columns: two 64-logit chunks per row, each one part of one
+    // of the stream's 256-logit tiles
     const int q = warp & 3, hf = (warp - kEpiWarp0) >> 2;
     const unsigned long long t0 = global_timer_ns();
     int lt = 0;
     for (int np = pair0; np < n_pairs; np += n_clusters, ++lt) {
-      const int nt = 2 * np + rank;
       const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1), t0);
-      if (!__all_sync(0xffffffffu, ok)) {
-        if (lane == 0) S.failed = 1;
+      if (!epi_all(ok)) {
+        if (tid == kEpiWarp0 * 32) S.failed = 1;
         break;
       }
       tc_fence_after();
-      const int c0 = nt * kBN + hf * 64;  // this thread's first column
-      for (int j = 0; j < mt; ++j) {
-        uint32_t ra[32], rb[32];
-        const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kBN + hf * 64);
-        tmem_ld32(ta, ra);
-        tmem_ld32(ta + 32u, rb);
-        tmem_wait_ld();
-        const int m = j * 128 + q * 32 + lane;
+      for (int j = 0; j < groups; ++j) {
+        const int m0 = j * kGroupM + rank * 128 + q * 32;
+        if (m0 >= p.M) continue;  // the warp's rows are past the last token
+        const int m = m0 + lane;
         const bool row_ok = m < p.M;
-        // bf16 pairs, round to nearest even: word i holds columns 2i, 2i + 1
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const __nv_bfloat162 x = __float22bfloat162_rn(make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])));
-          const __nv_bfloat162 y = __float22bfloat162_rn(make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])));
-          pk[i] = *reinterpret_cast<const uint32_t*>(&x);
-          pk[16 + i] = *reinterpret_cast<const uint32_t*>(&y);
-        }
-        const bool whole = c0 + 64 <= p.V;
-        if (row_ok && c0 < p.V) {
-          uint16_t* out = p.logits + (size_t)m * p.V + c0;
-          if (whole) {
-            uint4* o4 = reinterpret_cast<uint4*>(out);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 64; ++e)
-              if (c0 + e < p.V) out[e] = (uint16_t)(pk[e >> 1] >> ((e & 1) * 16));
-          }
-        }
-        if (kFused && row_ok && c0 < p.V) {
-          // the row's place in the verification: its slot and what the stream
-          // would have done with it
-          int slot = -1;
-          bool greedy = false;
+        // the row's place in the verification: its slot and what the stream
+        // would have done with it
+        int slot = -1;
+        bool greedy = false;
+        if (kFused && row_ok) {
           const int g1 = p.gamma + 1;
           if (m < p.Mt) {
             const int b = m / g1, i = m - b * g1;
@@ -365,42 +384,84 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             const int base = S.slot_base[b];
             if (base >= 0) slot = base + 2 * i + 1;  // a greedy request reads no draft rows
           }
-          if (slot >= 0 && !greedy) {
-            // the chunk's maximum (packed, NaN propagating as in the stream),
-            // into tile 4 blk + g: blk its 1024-logit block, g its place in a
-            // 256-logit row of that block
-            uint32_t key;
-            if (whole) {
-              __nv_bfloat162 acc = *reinterpret_cast<const __nv_bfloat162*>(&pk[0]);
+        }
+        for (int c = 0; c < 2; ++c) {
+          uint32_t ra[32], rb[32];
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kPairN + hf * 128 + c * 64);
+          tmem_ld32(ta, ra);
+          tmem_ld32(ta + 32u, rb);
+          tmem_wait_ld();
+          const int c0 = np * kPairN + hf * 128 + c * 64;  // this thread's first column
+          // bf16 pairs, round to nearest even: word i holds columns 2i, 2i + 1
+          uint32_t pk[32];
 #pragma unroll
-              for (int i = 1; i < 32; ++i) acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&pk[i]));
-              key = key_of(max_nan(__low2float(acc), __high2float(acc)));
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 x =
+                __float22bfloat162_rn(make_float2(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])));
+            const __nv_bfloat162 y =
+                __float22bfloat162_rn(make_float2(__uint_as_float(rb[2 * i]), __uint_as_float(rb[2 * i + 1])));
+            pk[i] = *reinterpret_cast<const uint32_t*>(&x);
+            pk[16 + i] = *reinterpret_cast<const uint32_t*>(&y);
+          }
+          const bool whole = c0 + 64 <= p.V;
+          if (row_ok && c0 < p.V) {
+            uint16_t* out = p.logits + (size_t)m * p.V + c0;
+            if (whole) {
+              uint4* o4 = reinterpret_cast<uint4*>(out);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             } else {
-              float mx = -INFINITY;
 #pragma unroll
               for (int e = 0; e < 64; ++e)
-                if (c0 + e < p.V) mx = max_nan(mx, __uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16));
-              key = key_of(mx);
+                if (c0 + e < p.V) out[e] = (uint16_t)(pk[e >> 1] >> ((e & 1) * 16));
             }
-            atomicMax(p.tile_keys + (size_t)slot * p.tiles + (c0 >> 10) * 4 + ((c0 & 255) >> 6), key);
-          } else if (greedy) {
-            // the lowest column holding the largest key
-            uint32_t best = 0u;
-            int col = 0;
+          }
+          if (kFused && row_ok && c0 < p.V) {
+            if (slot >= 0 && !greedy) {
+              // the chunk's maximum (packed, NaN propagating as in the stream),
+              // into tile 4 blk + g: blk its 1024-logit block, g its place in a
+              // 256-logit row of that block
+              uint32_t key;
+              if (whole) {
+                __nv_bfloat162 acc = *reinterpret_cast<const __nv_bfloat162*>(&pk[0]);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-              const uint32_t k = c0 + e < p.V ? key_of(__uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16)) : 0u;
-              if (k > best) {
-                best = k;
-                col = c0 + e;
+                for (int i = 1; i < 32; ++i) acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&pk[i]));
+                key = key_of(max_nan(__low2float(acc), __high2float(acc)));
+              } else {
+                float mx = -INFINITY;
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                  if (c0 + e < p.V) mx = max_nan(mx, __uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16));
+                key = key_of(mx);
               }
+              atomicMax(p.tile_keys + (size_t)slot * p.tiles + (c0 >> 10) * 4 + ((c0 & 255) >> 6), key);
+            } else if (greedy) {
+              // the lowest column holding the largest key
+              uint32_t best = 0u;
+              int col = 0;
+#pragma unroll
+              for (int e = 0; e < 64; ++e) {
+                const uint32_t k = c0 + e < p.V ? key_of(__uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16)) : 0u;
+                if (k > best) {
+                  best = k;
+                  col = c0 + e;
+                }
+              }
+              if (best) red_max_gpu(p.row_best + slot, composite(best, col));
             }
-            if (best) red_max_gpu(p.row_best + slot, composite(best, col));
           }
         }
       }
+      // this CTA's accumulators are read: one arrival per CTA on the first
+      // CTA's barrier before its next MMAs overwrite them
       tc_fence_before();
-      mbar_arrive(&S.acc_empty);
+      epi_sync();
+      if (tid == kEpiWarp0 * 32) {
+        if (rank == 0)
+          mbar_arrive(&S.acc_empty);
+        else
+          mbar_arrive_cluster(first_cta_addr(&S.acc_empty));
+      }
     }
   }
 
@@ -422,10 +483,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no load or arrival of the peer's still reaches this CTA
+  cluster_sync();  // no load, commit or arrival of the pair still reaches either CTA
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, ncols);
+    tmem_dealloc_pair(tmem, ncols);
   }
   if (tid == 0 && S.failed && p.status) atomicOr(p.status, kStatusTimeout);
 }
