@@ -18,9 +18,9 @@
 // each CTA holds the A rows of its 128 tokens and the B rows of its 128
 // vocabulary columns, and its tensor memory receives D's rows of its tokens
 // over all 256 columns. The tokens come in up to two groups of 256 (M <= 512).
-//  * warp 0: TMA producer. Per 32-element step of K each CTA loads its W tile
-//    [128 x 32] and its h tile [128 x 32] of each token group into a
-//    nine-stage ring (cp.async.bulk.tensor, 64-byte swizzle); the bytes of
+//  * warp 0: TMA producer. Per 64-element step of K each CTA loads its W tile
+//    [128 x 64] and its h tile [128 x 64] of each token group into a
+//    four-stage ring (cp.async.bulk.tensor, 128-byte swizzle); the bytes of
 //    both CTAs complete on the first CTA's barrier, and a stage is reloaded
 //    once the pair's MMAs have read it;
 //  * warp 1: allocates the pair's tensor memory; in the first CTA, one thread
@@ -58,11 +58,11 @@ constexpr int kLmThreads = 320;
 constexpr int kBN = 128;                          // vocabulary rows per CTA (B rows of its half)
 constexpr int kPairN = 2 * kBN;                   // vocabulary columns per pair: N of one MMA
 constexpr int kGroupM = 256;                      // tokens per group: M of one MMA, 128 per CTA
-constexpr int kBK = 32;                           // hidden elements per stage (one 64-byte swizzle row)
+constexpr int kBK = 64;                           // hidden elements per stage (one 128-byte swizzle row)
 constexpr int kMaxG = kLmMaxRows / kGroupM;       // token groups
 constexpr int kLmMaxB = kLmMaxRows / 3;           // requests of a fused call (2 gamma + 1 >= 3 rows each)
-constexpr int kLmStages = 9;
-constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 32 bf16 tile, 8 KB
+constexpr int kLmStages = 4;
+constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 64 bf16 tile, 16 KB
 constexpr int kEpiWarp0 = 2;                      // warps 2-9: the epilogue
 constexpr int kEpiThreads = kLmThreads - 32 * kEpiWarp0;
 constexpr int kEpiBarrier = 1;                    // named barrier of the epilogue warps
@@ -143,7 +143,7 @@ __device__ __forceinline__ uint32_t first_cta_addr(const void* p) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_addr(p)));
   return r;
 }
-// a [128 x 32] bf16 box of a 2-D tensor map at (k, row) into this CTA's shared
+// a [128 x 64] bf16 box of a 2-D tensor map at (k, row) into this CTA's shared
 // memory, its bytes completing on a barrier of either CTA of the pair
 __device__ __forceinline__ void tma_load_pair(void* dst, const CUtensorMap* map, int k, int row,
                                               uint32_t bar_cluster) {
@@ -184,19 +184,19 @@ __device__ __forceinline__ void epi_sync() {
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
-// with the 64-byte swizzle: rows of 64 bytes (32 bf16 of K), 8-row groups
-// 512 bytes apart (stride byte offset), descriptor version 1, swizzle mode 4.
+// with the 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row groups
+// 1024 bytes apart (stride byte offset), descriptor version 1, swizzle mode 2.
 // The leading byte offset is unused in this layout (one MMA's K extent, 32
-// bytes, lies inside a swizzle row). Moving along K inside the 64-byte row
+// bytes, lies inside a swizzle row). Moving along K inside the 128-byte row
 // adds the byte offset to the start address. In a pair MMA the same offset
 // addresses each CTA's own tile.
-__device__ __forceinline__ uint64_t sw64_desc(const void* tile) {
+__device__ __forceinline__ uint64_t sw128_desc(const void* tile) {
   const uint32_t a = smem_addr(tile);
   uint64_t d = (uint64_t)((a & 0x3ffffu) >> 4);
-  d |= (uint64_t)1u << 16;           // leading byte offset (unused)
-  d |= (uint64_t)(512u >> 4) << 32;  // stride byte offset
-  d |= (uint64_t)1u << 46;           // descriptor version
-  d |= (uint64_t)4u << 61;           // 64-byte swizzle
+  d |= (uint64_t)1u << 16;            // leading byte offset (unused)
+  d |= (uint64_t)(1024u >> 4) << 32;  // stride byte offset
+  d |= (uint64_t)1u << 46;            // descriptor version
+  d |= (uint64_t)2u << 61;            // 128-byte swizzle
   return d;
 }
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
@@ -328,9 +328,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t bd = sw64_desc(S.b[s]);
+          const uint64_t bd = sw128_desc(S.b[s]);
           for (int j = 0; j < groups; ++j) {
-            const uint64_t ad = sw64_desc(S.a[s][j]);
+            const uint64_t ad = sw128_desc(S.a[s][j]);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
               mma_pair(tmem + (uint32_t)(j * kPairN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
@@ -505,16 +505,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   });
   return fn;
 }
-// a [rows, K] bf16 row-major matrix read in [128 x 32] boxes, 64-byte swizzle
+// a [rows, K] bf16 row-major matrix read in [128 x 64] boxes, 128-byte swizzle
 bool make_map(CUtensorMap* map, const void* base, long long rows, int K) {
   PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)K * 2u};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};  // 64 bytes of K: the 64-byte swizzle
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, 128u};  // 128 bytes of K: the 128-byte swizzle
   const cuuint32_t estr[2] = {1u, 1u};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
