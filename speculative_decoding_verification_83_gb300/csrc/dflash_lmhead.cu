@@ -31,8 +31,9 @@
 //  * warps 2-9: epilogue. Each thread owns one token row of a 32-lane quarter
 //    of its CTA's accumulators and 128 of a tile's 256 columns
 //    (tcgen05.ld.32x32b), rounds the fp32 sums to bf16 (round to nearest
-//    even), stores them, and in the fused mode folds them into the row's
-//    tile keys (red.max) or argmax (red.max of the (key, index) composite).
+//    even), in the fused mode folds them into the row's tile keys (red.max)
+//    or argmax (red.max of the (key, index) composite), and stores them,
+//    whole 128-byte row segments per store after a transpose in registers.
 //    The two CTAs' epilogues both report to the first CTA before its MMAs
 //    overwrite the accumulators.
 // Every wait is bounded; a CTA that gives up raises DFLASH_STATUS_TIMEOUT,
@@ -203,6 +204,31 @@ __device__ __forceinline__ uint64_t sw128_desc(const void* tile) {
 // K-major, N = 256, M = 256 (the pair's rows).
 constexpr uint32_t kIdesc =
     (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kPairN >> 3) << 17) | ((uint32_t)(kGroupM >> 4) << 24);
+
+// Inside each group of 8 lanes, lane t holds the eight 16-byte pieces of row
+// t (piece p in words 4p..4p+3); afterwards it holds piece t of the group's
+// row i in words 4i..4i+3. Three butterfly stages (lane masks 4, 2, 1) each
+// swap the four pieces whose index differs from the lane's in that bit.
+__device__ __forceinline__ void transpose_pieces8(uint32_t (&pk)[32], int lane) {
+#pragma unroll
+  for (int b = 2; b >= 0; --b) {
+    const int m = 1 << b;
+    const bool hi = (lane & m) != 0;
+#pragma unroll
+    for (int s0 = 0; s0 < 8; ++s0) {
+      if (s0 & m) continue;
+      const int s1 = s0 | m;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, hi ? pk[4 * s0 + w] : pk[4 * s1 + w], m);
+        if (hi)
+          pk[4 * s0 + w] = recv;
+        else
+          pk[4 * s1 + w] = recv;
+      }
+    }
+  }
+}
 
 __device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, unsigned long long t0) {
   while (!mbar_try_wait(bar, parity))
@@ -404,39 +430,37 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             pk[16 + i] = *reinterpret_cast<const uint32_t*>(&y);
           }
           const bool whole = c0 + 64 <= p.V;
-          if (row_ok && c0 < p.V) {
-            uint16_t* out = p.logits + (size_t)m * p.V + c0;
+          if (kFused && row_ok && c0 < p.V && slot >= 0) {
+            // the chunk's maximum (packed, NaN propagating as in the stream)
+            float mx = -INFINITY;
             if (whole) {
-              uint4* o4 = reinterpret_cast<uint4*>(out);
+              __nv_bfloat162 acc = *reinterpret_cast<const __nv_bfloat162*>(&pk[0]);
 #pragma unroll
-              for (int v = 0; v < 8; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              for (int i = 1; i < 32; ++i) acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&pk[i]));
+              mx = max_nan(__low2float(acc), __high2float(acc));
             } else {
 #pragma unroll
               for (int e = 0; e < 64; ++e)
-                if (c0 + e < p.V) out[e] = (uint16_t)(pk[e >> 1] >> ((e & 1) * 16));
+                if (c0 + e < p.V) mx = max_nan(mx, __uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16));
             }
-          }
-          if (kFused && row_ok && c0 < p.V) {
-            if (slot >= 0 && !greedy) {
-              // the chunk's maximum (packed, NaN propagating as in the stream),
-              // into tile 4 blk + g: blk its 1024-logit block, g its place in a
-              // 256-logit row of that block
-              uint32_t key;
-              if (whole) {
-                __nv_bfloat162 acc = *reinterpret_cast<const __nv_bfloat162*>(&pk[0]);
+            if (!greedy) {
+              // into tile 4 blk + g: blk its 1024-logit block, g its place in
+              // a 256-logit row of that block
+              atomicMax(p.tile_keys + (size_t)slot * p.tiles + (c0 >> 10) * 4 + ((c0 & 255) >> 6), key_of(mx));
+            } else if (whole && !isnan(mx)) {
+              // the lowest column holding the maximum (-0 equal to +0, as in
+              // the key order; no NaN in the chunk)
+              const __nv_bfloat162 m2 = __float2bfloat162_rn(mx);  // exact: mx is a bf16 value
+              int col = 0;
 #pragma unroll
-                for (int i = 1; i < 32; ++i) acc = __hmax2_nan(acc, *reinterpret_cast<const __nv_bfloat162*>(&pk[i]));
-                key = key_of(max_nan(__low2float(acc), __high2float(acc)));
-              } else {
-                float mx = -INFINITY;
-#pragma unroll
-                for (int e = 0; e < 64; ++e)
-                  if (c0 + e < p.V) mx = max_nan(mx, __uint_as_float((pk[e >> 1] >> ((e & 1) * 16)) << 16));
-                key = key_of(mx);
+              for (int i = 31; i >= 0; --i) {
+                const uint32_t eq = __heq2_mask(*reinterpret_cast<const __nv_bfloat162*>(&pk[i]), m2);
+                col = (eq & 0xffffu) ? 2 * i : (eq ? 2 * i + 1 : col);
               }
-              atomicMax(p.tile_keys + (size_t)slot * p.tiles + (c0 >> 10) * 4 + ((c0 & 255) >> 6), key);
-            } else if (greedy) {
-              // the lowest column holding the largest key
+              red_max_gpu(p.row_best + slot, composite(key_of(mx), c0 + col));
+            } else {
+              // a NaN in the chunk, or its last columns past the end: the key
+              // order decides, element by element
               uint32_t best = 0u;
               int col = 0;
 #pragma unroll
@@ -449,6 +473,22 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               }
               if (best) red_max_gpu(p.row_best + slot, composite(best, col));
             }
+          }
+          if (whole) {
+            // whole 128-byte rows per store: after the transpose the lanes of
+            // each 8-lane group write the eight pieces of one of its rows
+            transpose_pieces8(pk, lane);
+            const int r0 = m0 + (lane & ~7), t8 = lane & 7;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (r0 + i < p.M)
+                *reinterpret_cast<uint4*>(p.logits + (size_t)(r0 + i) * p.V + c0 + 8 * t8) =
+                    make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          } else if (row_ok && c0 < p.V) {
+            uint16_t* out = p.logits + (size_t)m * p.V + c0;
+#pragma unroll
+            for (int e = 0; e < 64; ++e)
+              if (c0 + e < p.V) out[e] = (uint16_t)(pk[e >> 1] >> ((e & 1) * 16));
           }
         }
       }

@@ -64,10 +64,13 @@ def test_lmhead_logits_match_the_oracle(dv, M, V, K):
     _check_logits(got, h, w)
 
 
-def _fused_vs_unfused(dv, B, gamma, V, K, T, top_k, top_p, seed, data_seed):
+def _fused_vs_unfused(dv, B, gamma, V, K, T, top_k, top_p, seed, data_seed, edit_h=None):
     rng = np.random.default_rng(data_seed)
     M, Mt = B * (2 * gamma + 1), B * (gamma + 1)
-    h = synth.to_torch(_bits(rng, (M, K), 1.0), DEV)
+    hb = _bits(rng, (M, K), 1.0)
+    if edit_h is not None:
+        edit_h(hb)
+    h = synth.to_torch(hb, DEV)
     g = torch.Generator(device=DEV)
     g.manual_seed(data_seed)
     w = (torch.randn((V, K), generator=g, device=DEV) * (2.0 / K ** 0.5)).to(torch.bfloat16)
@@ -86,6 +89,8 @@ def _fused_vs_unfused(dv, B, gamma, V, K, T, top_k, top_p, seed, data_seed):
     assert torch.equal(logits_f.view(torch.int16), logits_u.view(torch.int16))
     assert torch.equal(tok_f, tok_u) and torch.equal(len_f, len_u)
     assert int(st_f.item()) == int(st_u.item())
+    if edit_h is not None:
+        assert int(st_f.item()) & dv.STATUS_BAD_ROW
     return tok_f.cpu().numpy(), len_f.cpu().numpy(), logits_u, d.cpu().numpy()
 
 
@@ -111,3 +116,22 @@ def test_fused_equals_unfused_full_shape(dv):
     B, gamma, V, K = 32, 7, 248320, 5120
     T = np.array([(0.0, 0.6, 1.0)[b % 3] for b in range(B)], np.float32)
     _fused_vs_unfused(dv, B, gamma, V, K, T, 20, 0.95, 1, 7)
+
+
+def test_fused_equals_unfused_zero_and_nan_rows(dv):
+    """Hidden states that are zero (every logit of the row ties at 0: the
+    argmax is column 0) or hold a NaN (the whole row is NaN: BAD_ROW, and the
+    key order still decides the argmax), on target rows of greedy and of
+    sampling requests."""
+    B, gamma, V, K = 4, 3, 20000, 128
+    T = np.array([0.0, 1.0, 0.0, 0.7], np.float32)
+    g1 = gamma + 1
+
+    def edit(hb):
+        hb[0 * g1 + 1] = 0  # greedy request 0, position 1: zeros
+        hb[2 * g1 + 0, 5] = 0x7FC0  # greedy request 2, position 0: a NaN
+        hb[1 * g1 + 2, 0] = 0x7FC0  # sampling request 1, position 2: a NaN
+        hb[3 * g1 + 0] = 0  # sampling request 3, position 0: zeros
+
+    for seed in (0, 3):
+        _fused_vs_unfused(dv, B, gamma, V, K, T, 20, 0.95, seed, 77, edit_h=edit)
