@@ -306,6 +306,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   cluster_sync();  // both CTAs' barriers are initialised before any load or arrival reaches them
   tc_fence_after();
   const uint32_t tmem = S.tmem_base;
+  // the verification launched after this kernel may be scheduled as SMs free
+  // up; it waits for this grid's completion before reading what it wrote
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     // ---- TMA producer (both CTAs)

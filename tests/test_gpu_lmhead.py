@@ -95,9 +95,9 @@ def _fused_vs_unfused(dv, B, gamma, V, K, T, top_k, top_p, seed, data_seed, edit
 
 
 @pytest.mark.parametrize("B,gamma,V,K", [(4, 3, 20000, 256), (2, 7, 8192, 64), (6, 2, 33000, 128),
-                                         (1, 1, 1032, 64)])
+                                         (1, 1, 1032, 64), (34, 7, 4104, 128)])
 def test_fused_equals_unfused_small(dv, B, gamma, V, K):
-    T = np.array([1.0, 0.0, 0.7, 1.3, 0.0, 2.0], np.float32)[:B]
+    T = np.resize(np.array([1.0, 0.0, 0.7, 1.3, 0.0, 2.0], np.float32), B)  # cycled over the requests
     for seed in (0, 5):
         tok, ln, logits, d = _fused_vs_unfused(dv, B, gamma, V, K, T, 20, 0.95, seed, B * 100 + V)
         # and the verification of those logits against the oracle
