@@ -230,12 +230,20 @@ __device__ __forceinline__ void transpose_pieces8(uint32_t (&pk)[32], int lane) 
   }
 }
 
-__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity, unsigned long long t0) {
+// Bounded waits: each gives up kWaitLimitNs after it began (a long GEMM
+// makes progress between its waits); lm_wait_from counts from t0, so that
+// several waits share one limit.
+__device__ __forceinline__ bool lm_wait_from(uint64_t* bar, uint32_t parity, unsigned long long t0) {
   while (!mbar_try_wait(bar, parity))
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }
-__device__ __forceinline__ bool lm_wait_cluster(uint64_t* bar, uint32_t parity, unsigned long long t0) {
+__device__ __forceinline__ bool lm_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_try_wait(bar, parity) || lm_wait_from(bar, parity, global_timer_ns());
+}
+__device__ __forceinline__ bool lm_wait_cluster(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
   while (!mbar_try_wait_cluster(bar, parity))
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   return true;
@@ -313,13 +321,12 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   if (warp == 0) {
     // ---- TMA producer (both CTAs)
     if (lane == 0) {
-      const unsigned long long t0 = global_timer_ns();
       long long it = 0;
       for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters) {
         for (int ks = 0; ks < nk; ++ks, ++it) {
           const int s = (int)(it % kLmStages);
           const uint32_t ph = (uint32_t)((it / kLmStages) & 1);
-          if (it >= kLmStages && !lm_wait(&S.empty[s], ph ^ 1u, t0)) {
+          if (it >= kLmStages && !lm_wait(&S.empty[s], ph ^ 1u)) {
             S.failed = 1;
             break;
           }
@@ -335,16 +342,15 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       // completed and freed its stage (bounded)
       const unsigned long long t1 = global_timer_ns();
       for (long long q = it > kLmStages ? it - kLmStages : 0; q < it; ++q)
-        (void)lm_wait(&S.empty[q % kLmStages], (uint32_t)((q / kLmStages) & 1), t1);
+        (void)lm_wait_from(&S.empty[q % kLmStages], (uint32_t)((q / kLmStages) & 1), t1);
     }
   } else if (warp == 1) {
     // ---- MMA issuer (the first CTA, for the pair)
     if (lane == 0 && rank == 0) {
-      const unsigned long long t0 = global_timer_ns();
       long long it = 0;
       int lt = 0;
       for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters, ++lt) {
-        if (lt > 0 && !lm_wait_cluster(&S.acc_empty, (uint32_t)((lt - 1) & 1), t0)) {
+        if (lt > 0 && !lm_wait_cluster(&S.acc_empty, (uint32_t)((lt - 1) & 1))) {
           S.failed = 1;
           break;
         }
@@ -352,7 +358,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         bool ok = true;
         for (int ks = 0; ks < nk; ++ks, ++it) {
           const int s = (int)(it % kLmStages);
-          if (!lm_wait(&S.full[s], (uint32_t)((it / kLmStages) & 1), t0)) {
+          if (!lm_wait(&S.full[s], (uint32_t)((it / kLmStages) & 1))) {
             ok = false;
             break;
           }
@@ -379,10 +385,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // tile's 256 columns: two 64-logit chunks per row, each one part of one
     // of the stream's 256-logit tiles
     const int q = warp & 3, hf = (warp - kEpiWarp0) >> 2;
-    const unsigned long long t0 = global_timer_ns();
     int lt = 0;
     for (int np = pair0; np < n_pairs; np += n_clusters, ++lt) {
-      const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1), t0);
+      const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1));
       if (!epi_all(ok)) {
         if (tid == kEpiWarp0 * 32) S.failed = 1;
         break;
