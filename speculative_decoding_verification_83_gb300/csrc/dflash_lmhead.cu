@@ -28,8 +28,8 @@
 //    accumulated in tensor memory, one 256-column accumulator per token
 //    group) and the commits that free a stage in both CTAs and signal both
 //    epilogues after a tile's last step;
-//  * warps 2-9: epilogue. Each thread owns one token row of a 32-lane quarter
-//    of its CTA's accumulators and 128 of a tile's 256 columns
+//  * warps 2-13: epilogue. Each thread owns one token row of a 32-lane quarter
+//    of its CTA's accumulators and every third 64-column chunk of its groups
 //    (tcgen05.ld.32x32b), rounds the fp32 sums to bf16 (round to nearest
 //    even), in the fused mode folds them into the row's tile keys (red.max)
 //    or argmax (red.max of the (key, index) composite), and stores them,
@@ -55,7 +55,6 @@
 namespace dflash {
 namespace {
 
-constexpr int kLmThreads = 320;
 constexpr int kBN = 128;                          // vocabulary rows per CTA (B rows of its half)
 constexpr int kPairN = 2 * kBN;                   // vocabulary columns per pair: N of one MMA
 constexpr int kGroupM = 256;                      // tokens per group: M of one MMA, 128 per CTA
@@ -64,8 +63,12 @@ constexpr int kMaxG = kLmMaxRows / kGroupM;       // token groups
 constexpr int kLmMaxB = kLmMaxRows / 3;           // requests of a fused call (2 gamma + 1 >= 3 rows each)
 constexpr int kLmStages = 4;
 constexpr uint32_t kTileBytes = 128u * kBK * 2u;  // a 128 x 64 bf16 tile, 16 KB
-constexpr int kEpiWarp0 = 2;                      // warps 2-9: the epilogue
-constexpr int kEpiThreads = kLmThreads - 32 * kEpiWarp0;
+constexpr int kEpiWarp0 = 2;                      // warps 2-13: the epilogue
+constexpr int kEpiWarps = 12;                     // three per lane quarter of the accumulators
+constexpr int kEpiSlots = kEpiWarps / 4;
+constexpr int kLmThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kEpiThreads = 32 * kEpiWarps;
+static_assert(kEpiWarps % 4 == 0, "whole lane quarters");
 constexpr int kEpiBarrier = 1;                    // named barrier of the epilogue warps
 static_assert(kMaxG * kGroupM == kLmMaxRows, "token groups cover the rows");
 
@@ -380,11 +383,11 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       }
     }
   } else {
-    // ---- epilogue: warps 2-9. Warp w reads lane quarter w % 4 of this CTA's
-    // accumulators (the lanes a warp may access) and half (w - 2) / 4 of each
-    // tile's 256 columns: two 64-logit chunks per row, each one part of one
-    // of the stream's 256-logit tiles
-    const int q = warp & 3, hf = (warp - kEpiWarp0) >> 2;
+    // ---- epilogue: warps 2-13. Warp w reads lane quarter w % 4 of this CTA's
+    // accumulators (the lanes a warp may access) and every third of the
+    // quarter's 64-column chunks from (w - 2) / 4 on: each chunk one part of
+    // one of the stream's 256-logit tiles
+    const int q = warp & 3, es = (warp - kEpiWarp0) >> 2;
     int lt = 0;
     for (int np = pair0; np < n_pairs; np += n_clusters, ++lt) {
       const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1));
@@ -393,7 +396,10 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         break;
       }
       tc_fence_after();
-      for (int j = 0; j < groups; ++j) {
+      // the quarter's 64-column chunks (four per token group), dealt to its
+      // kEpiSlots warps in turn
+      for (int ci = es; ci < 4 * groups; ci += kEpiSlots) {
+        const int j = ci >> 2, cc = ci & 3;
         const int m0 = j * kGroupM + rank * 128 + q * 32;
         if (m0 >= p.M) continue;  // the warp's rows are past the last token
         const int m = m0 + lane;
@@ -419,13 +425,13 @@ __global__ void __launch_bounds__(kLmThreads, 1)
             if (base >= 0) slot = base + 2 * i + 1;  // a greedy request reads no draft rows
           }
         }
-        for (int c = 0; c < 2; ++c) {
+        {
           uint32_t ra[32], rb[32];
-          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kPairN + hf * 128 + c * 64);
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kPairN + cc * 64);
           tmem_ld32(ta, ra);
           tmem_ld32(ta + 32u, rb);
           tmem_wait_ld();
-          const int c0 = np * kPairN + hf * 128 + c * 64;  // this thread's first column
+          const int c0 = np * kPairN + cc * 64;  // this thread's first column
           // bf16 pairs, round to nearest even: word i holds columns 2i, 2i + 1
           uint32_t pk[32];
 #pragma unroll
