@@ -25,8 +25,10 @@
 //    once the pair's MMAs have read it;
 //  * warp 1: allocates the pair's tensor memory; in the first CTA, one thread
 //    issues the MMAs (tcgen05.mma.cta_group::2.kind::f16, bf16 in, fp32
-//    accumulated in tensor memory, one 256-column accumulator per token
-//    group) and the commits that free a stage in both CTAs and signal both
+//    accumulated in tensor memory in two 256-column slots: with one token
+//    group the slots alternate between tiles, with two each group has its
+//    own, and the next tile's group 0 starts as soon as its slot is read)
+//    and the commits that free a stage in both CTAs and signal both
 //    epilogues after a tile's last step;
 //  * warps 2-13: epilogue. Each thread owns one token row of a 32-lane quarter
 //    of its CTA's accumulators and every third 64-column chunk of its groups
@@ -34,8 +36,8 @@
 //    even), in the fused mode folds them into the row's tile keys (red.max)
 //    or argmax (red.max of the (key, index) composite), and stores them,
 //    whole 128-byte row segments per store after a transpose in registers.
-//    The two CTAs' epilogues both report to the first CTA before its MMAs
-//    overwrite the accumulators.
+//    Every epilogue warp of both CTAs reports to the first CTA when it is
+//    done with a slot, before its MMAs overwrite the slot.
 // Every wait is bounded; a CTA that gives up raises DFLASH_STATUS_TIMEOUT,
 // waits (bounded) for its loads in flight and frees its tensor memory.
 
@@ -76,7 +78,7 @@ struct LmSmem {
   unsigned char b[kLmStages][kTileBytes];          // W tiles (on 1024-byte boundaries: whole swizzle atoms)
   unsigned char a[kLmStages][kMaxG][kTileBytes];   // h tiles of this CTA's tokens
   uint64_t full[kLmStages], empty[kLmStages];
-  uint64_t acc_full, acc_empty;
+  uint64_t acc_full[2], acc_empty[2];  // per 256-column accumulator slot of the tensor memory
   uint32_t tmem_base;
   int failed;
   int slot_base[kLmMaxB];  // per request: its first slot (sampling requests), or -(1 + first slot) (greedy)
@@ -183,9 +185,6 @@ __device__ __forceinline__ bool epi_all(bool v) {
       : "memory");
   return r != 0u;
 }
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiThreads) : "memory");
-}
 
 // Shared-memory matrix descriptor of a K-major operand tile written by TMA
 // with the 128-byte swizzle: rows of 128 bytes (64 bf16 of K), 8-row groups
@@ -267,15 +266,21 @@ __global__ void __launch_bounds__(kLmThreads, 1)
   const int rank = (int)cluster_rank();
   const int n_pairs = (p.V + kPairN - 1) / kPairN, pair0 = blockIdx.x / 2, n_clusters = gridDim.x / 2;
   const int nk = p.K / kBK;
-  const uint32_t ncols = groups <= 1 ? 256u : 512u;
+  // Tensor memory: two 256-column accumulator slots. With one token group
+  // they alternate between vocabulary tiles, so the epilogue of one tile runs
+  // while the MMAs of the next fill the other slot; with two groups each
+  // group has its slot, released as soon as the epilogue has read it.
+  const uint32_t ncols = 512u;
 
   if (tid == 0) {
     for (int s = 0; s < kLmStages; ++s) {
       mbar_init(&S.full[s], 1);   // the first CTA's producer; both CTAs' bytes
       mbar_init(&S.empty[s], 1);  // the pair's commit
     }
-    mbar_init(&S.acc_full, 1);
-    mbar_init(&S.acc_empty, 2);   // one arrival from each CTA's epilogue
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&S.acc_full[a], 1);
+      mbar_init(&S.acc_empty[a], 2 * kEpiWarps);  // every epilogue warp of both CTAs
+    }
     S.failed = 0;
     fence_barrier_init();
   }
@@ -352,35 +357,66 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     if (lane == 0 && rank == 0) {
       long long it = 0;
       int lt = 0;
-      for (int np = pair0; np < n_pairs && !S.failed; np += n_clusters, ++lt) {
-        if (lt > 0 && !lm_wait_cluster(&S.acc_empty, (uint32_t)((lt - 1) & 1))) {
-          S.failed = 1;
-          break;
-        }
+      // this step's MMAs of group j into accumulator slot `slot`
+      auto mma_step = [&](int s, int j, int slot, int ks) {
+        const uint64_t bd = sw128_desc(S.b[s]), ad = sw128_desc(S.a[s][j]);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
+          mma_pair(tmem + (uint32_t)(slot * kPairN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+      };
+      auto stage_full = [&](long long i) {
+        const bool ok = lm_wait(&S.full[i % kLmStages], (uint32_t)((i / kLmStages) & 1));
         tc_fence_after();
-        bool ok = true;
-        for (int ks = 0; ks < nk; ++ks, ++it) {
-          const int s = (int)(it % kLmStages);
-          if (!lm_wait(&S.full[s], (uint32_t)((it / kLmStages) & 1))) {
+        return ok;
+      };
+      bool ok = true;
+      for (int np = pair0; np < n_pairs && ok; np += n_clusters, ++lt) {
+        if (groups == 1) {
+          // one group: the slots alternate; slot lt % 2 was last read by the
+          // epilogue of tile lt - 2
+          const int slot = lt & 1, use = lt >> 1;
+          if (use > 0 && !lm_wait_cluster(&S.acc_empty[slot], (uint32_t)((use - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bd = sw128_desc(S.b[s]);
-          for (int j = 0; j < groups; ++j) {
-            const uint64_t ad = sw128_desc(S.a[s][j]);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)  // 16 elements = 32 bytes = 2 descriptor units
-              mma_pair(tmem + (uint32_t)(j * kPairN), ad + 2u * kk, bd + 2u * kk, kIdesc, (ks | kk) != 0 ? 1u : 0u);
+          for (int ks = 0; ks < nk && ok; ++ks, ++it) {
+            if (!(ok = stage_full(it))) break;
+            mma_step((int)(it % kLmStages), 0, slot, ks);
+            mma_commit_pair(&S.empty[it % kLmStages], 3);  // frees the stage in both CTAs' rings
           }
-          mma_commit_pair(&S.empty[s], 3);  // frees the stage in both CTAs' rings
+          if (ok) mma_commit_pair(&S.acc_full[slot], 3);  // both CTAs' accumulators are complete
+        } else {
+          // two groups, slot j for group j: the first ring's worth of steps
+          // goes to group 0 as soon as its slot is read, then group 1 catches
+          // up on the same stages once its slot is read too
+          if (lt > 0 && !lm_wait_cluster(&S.acc_empty[0], (uint32_t)((lt - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int head = nk < kLmStages ? nk : kLmStages;
+          for (int ks = 0; ks < head && ok; ++ks)
+            if ((ok = stage_full(it + ks))) mma_step((int)((it + ks) % kLmStages), 0, 0, ks);
+          if (ok && lt > 0 && !lm_wait_cluster(&S.acc_empty[1], (uint32_t)((lt - 1) & 1))) ok = false;
+          if (!ok) break;
+          tc_fence_after();
+          for (int ks = 0; ks < head; ++ks) {
+            mma_step((int)((it + ks) % kLmStages), 1, 1, ks);
+            mma_commit_pair(&S.empty[(it + ks) % kLmStages], 3);
+          }
+          it += head;
+          for (int ks = head; ks < nk && ok; ++ks, ++it) {
+            if (!(ok = stage_full(it))) break;
+            const int s = (int)(it % kLmStages);
+            mma_step(s, 0, 0, ks);
+            mma_step(s, 1, 1, ks);
+            mma_commit_pair(&S.empty[s], 3);
+          }
+          if (ok) mma_commit_pair(&S.acc_full[0], 3);  // both groups, both CTAs
         }
-        if (!ok) {
-          S.failed = 1;
-          break;
-        }
-        mma_commit_pair(&S.acc_full, 3);  // both CTAs' accumulators are complete
       }
+      if (!ok) S.failed = 1;
     }
   } else {
     // ---- epilogue: warps 2-13. Warp w reads lane quarter w % 4 of this CTA's
@@ -389,8 +425,22 @@ __global__ void __launch_bounds__(kLmThreads, 1)
     // one of the stream's 256-logit tiles
     const int q = warp & 3, es = (warp - kEpiWarp0) >> 2;
     int lt = 0;
+    // one arrival per warp and slot use on the first CTA's barrier, before
+    // its MMAs overwrite the slot
+    auto release = [&](int slot) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0)
+          mbar_arrive(&S.acc_empty[slot]);
+        else
+          mbar_arrive_cluster(first_cta_addr(&S.acc_empty[slot]));
+      }
+    };
     for (int np = pair0; np < n_pairs; np += n_clusters, ++lt) {
-      const bool ok = lm_wait(&S.acc_full, (uint32_t)(lt & 1));
+      const int slot1 = lt & 1;  // one group: this tile's slot
+      const bool ok = groups == 1 ? lm_wait(&S.acc_full[slot1], (uint32_t)((lt >> 1) & 1))
+                                  : lm_wait(&S.acc_full[0], (uint32_t)(lt & 1));
       if (!epi_all(ok)) {
         if (tid == kEpiWarp0 * 32) S.failed = 1;
         break;
@@ -400,8 +450,15 @@ __global__ void __launch_bounds__(kLmThreads, 1)
       // kEpiSlots warps in turn
       for (int ci = es; ci < 4 * groups; ci += kEpiSlots) {
         const int j = ci >> 2, cc = ci & 3;
+        const int acc = groups == 1 ? slot1 : j;  // the accumulator slot
         const int m0 = j * kGroupM + rank * 128 + q * 32;
-        if (m0 >= p.M) continue;  // the warp's rows are past the last token
+        // with two groups, group 0's slot is released after the warp's last
+        // chunk of it (every warp has one: es < 4)
+        const bool last_of_group0 = groups == 2 && ci < 4 && ci + kEpiSlots >= 4;
+        if (m0 >= p.M) {  // the warp's rows are past the last token
+          if (last_of_group0) release(0);
+          continue;
+        }
         const int m = m0 + lane;
         const bool row_ok = m < p.M;
         // the row's place in the verification: its slot and what the stream
@@ -427,7 +484,7 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         }
         {
           uint32_t ra[32], rb[32];
-          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(j * kPairN + cc * 64);
+          const uint32_t ta = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * kPairN + cc * 64);
           tmem_ld32(ta, ra);
           tmem_ld32(ta + 32u, rb);
           tmem_wait_ld();
@@ -505,17 +562,9 @@ __global__ void __launch_bounds__(kLmThreads, 1)
               if (c0 + e < p.V) out[e] = (uint16_t)(pk[e >> 1] >> ((e & 1) * 16));
           }
         }
+        if (last_of_group0) release(0);
       }
-      // this CTA's accumulators are read: one arrival per CTA on the first
-      // CTA's barrier before its next MMAs overwrite them
-      tc_fence_before();
-      epi_sync();
-      if (tid == kEpiWarp0 * 32) {
-        if (rank == 0)
-          mbar_arrive(&S.acc_empty);
-        else
-          mbar_arrive_cluster(first_cta_addr(&S.acc_empty));
-      }
+      release(groups == 1 ? slot1 : 1);  // the warp is done with this tile's (last) slot
     }
   }
 
