@@ -50,7 +50,10 @@ def _check_logits(got_bits, h_bits, w_bits):
 
 
 @pytest.mark.parametrize("M,V,K", [(128, 128, 64), (1, 8, 64), (37, 1032, 128), (200, 1000, 256),
-                                   (512, 4104, 512), (480, 2056, 1024), (256, 40000, 128)])
+                                   (512, 4104, 512), (480, 2056, 1024), (256, 40000, 128),
+                                   # the full vocabulary: about 13 tiles per SM pair, each accumulator
+                                   # slot reused many times, with one token group and with two
+                                   (200, 248320, 64), (480, 248320, 64)])
 def test_lmhead_logits_match_the_oracle(dv, M, V, K):
     rng = np.random.default_rng(M * 7 + V + K)
     h = _bits(rng, (M, K), 1.0)
