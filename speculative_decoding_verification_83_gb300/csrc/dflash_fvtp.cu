@@ -293,13 +293,18 @@ __global__ void __launch_bounds__(kTpThreads) fvtp_hist0_kernel(const FvtpParams
 // Refinement round i (1 <= i <= nref) takes bits [8 (nref - i), 8 (nref - i) + 8)
 // of the offset ok - kmin (ok: the key in refinement units); the tokens in
 // the bin are exactly those with kmin <= ok <= kmax, and of them the ones
-// whose higher offset bits match the bits found so far take part.
+// whose higher offset bits match the bits found so far take part. Few tokens
+// do: a thread marks its 16 tokens that take part, a warp with any gathers
+// them into a queue (a scan of its lanes' counts) and weighs them with every
+// lane busy (weighing them where they lie would run the float-float weight
+// in many warps for one or two lanes).
 __global__ void __launch_bounds__(kTpThreads) fvtp_histr_kernel(const FvtpParams t) {
   __shared__ __align__(16) float xs_s[kFvSlice];
   __shared__ unsigned long long hm[256];
   __shared__ float th[kExpTable], tl[kExpTable];
+  __shared__ float queue[kTpWarps][32 * kTpPer];
   grid_dependency_sync();
-  const int rho = blockIdx.x, tid = threadIdx.x;
+  const int rho = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
   const RowRef rr = row_ref(t, rho);
   if (!block_live(rr)) return;
   const FvtpCut c = t.cut[rho];
@@ -308,18 +313,40 @@ __global__ void __launch_bounds__(kTpThreads) fvtp_histr_kernel(const FvtpParams
   const unsigned long long known = (unsigned long long)c.prefix >> (shift + 8);
   load_exp_table(t, th, tl);
   hm[tid] = 0ull;
+  float* q = queue[tid >> 5];
   for (int s = blockIdx.y; s < t.n_slices; s += gridDim.y) {
     const int n = stage_slice(rr.ptr, s, t.V, t.dtype, xs_s);
     __syncthreads();
-    for (int l = tid; l < n; l += kTpThreads) {
-      const float x = xs_s[l];
-      const uint32_t ok = okey_of(key_of(x), t.dtype);
-      if (ok < c.kmin || ok > c.kmax) continue;
-      const unsigned long long off = ok - c.kmin;
-      if ((off >> (shift + 8)) != known) continue;
-      atomicAdd(&hm[(off >> shift) & 255u], to_fixed(tp_weight(x, rr, th, tl), t.frac_bits));
+    uint32_t mine = 0u;  // bit e: token tid + e kTpThreads of the slice takes part
+#pragma unroll
+    for (int e = 0; e < kTpPer; ++e) {
+      const int l = tid + e * kTpThreads;
+      const uint32_t ok = okey_of(key_of(xs_s[l]), t.dtype);
+      const bool in = l < n && ok >= c.kmin && ok <= c.kmax &&
+                      ((unsigned long long)(ok - c.kmin) >> (shift + 8)) == known;
+      mine |= (in ? 1u : 0u) << e;
     }
-    __syncthreads();
+    if (__any_sync(0xffffffffu, mine != 0u)) {
+      // the warp's queue: each lane's tokens after those of the lanes below
+      const int cnt = __popc(mine);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int nq = __shfl_sync(0xffffffffu, incl, 31);
+      int pos = incl - cnt;
+      for (uint32_t m = mine; m; m &= m - 1u) q[pos++] = xs_s[tid + (__ffs(m) - 1) * kTpThreads];
+      __syncwarp();
+      for (int i = lane; i < nq; i += 32) {
+        const float v = q[i];
+        const uint32_t ok = okey_of(key_of(v), t.dtype);
+        atomicAdd(&hm[((ok - c.kmin) >> shift) & 255u], to_fixed(tp_weight(v, rr, th, tl), t.frac_bits));
+      }
+      __syncwarp();  // the queue is refilled for the next slice
+    }
+    __syncthreads();  // before the next slice overwrites the stage
   }
   if (hm[tid]) atomicAdd(t.hist_m + (size_t)rho * 256 + tid, hm[tid]);
 }
