@@ -370,14 +370,11 @@ __device__ __forceinline__ void b16_range(int V, int g, int G, int* j0, int* j1)
   *j1 = (int)(b < V ? b : V);
 }
 
-// count the range's tokens whose 16-bit key passes keep(k16) into cnt
-template <class Keep>
-__device__ __forceinline__ void b16_count(const unsigned char* row, int j0, int j1, uint32_t* cnt, Keep keep) {
+// hand each of the range's tokens to count(k16), its 16-bit key
+template <class Count>
+__device__ __forceinline__ void b16_count(const unsigned char* row, int j0, int j1, Count count) {
   const unsigned short* r16 = reinterpret_cast<const unsigned short*>(row);
-  auto add = [&](uint32_t bits) {
-    const uint32_t k16 = okey_of(key_of(__uint_as_float(bits << 16)), 0);
-    if (keep(k16)) atomicAdd(&cnt[k16 >> 1], (k16 & 1u) ? 0x10000u : 1u);
-  };
+  auto add = [&](uint32_t bits) { count(okey_of(key_of(__uint_as_float(bits << 16)), 0)); };
   const bool vec = ((reinterpret_cast<uintptr_t>(row) + 2 * (uintptr_t)j0) & 15u) == 0u;
   int j = j0 + (int)threadIdx.x * 8;
   if (vec) {
@@ -444,13 +441,17 @@ __global__ void __launch_bounds__(kB16Threads) fvtp_hist0_b16_kernel(const FvtpP
   int j0, j1;
   b16_range(t.V, blockIdx.y, gridDim.y, &j0, &j1);
   __syncthreads();
-  b16_count(rr.ptr, j0, j1, cnt, [](uint32_t) { return true; });
+  b16_count(rr.ptr, j0, j1, [&](uint32_t k16) { atomicAdd(&cnt[k16 >> 1], (k16 & 1u) ? 0x10000u : 1u); });
   __syncthreads();
   b16_weigh(cnt, rr, t.frac_bits, th, tl, hm, [&](uint32_t, float x) { return bin0_of(x, rr); });
   __syncthreads();
   if (tid < 256 && hm[tid]) atomicAdd(t.hist_m + (size_t)rho * 256 + tid, hm[tid]);
 }
 
+// A refinement round on bf16 rows. In the round that takes the last byte of
+// the offset (shift 0) the tokens that take part have at most 256 keys,
+// kmin + 256 known + d: the block counts them per digit d in 256 words, and
+// neither clears nor scans the 65 536 counts.
 __global__ void __launch_bounds__(kB16Threads) fvtp_histr_b16_kernel(const FvtpParams t) {
   extern __shared__ __align__(16) uint32_t cnt[];
   __shared__ unsigned long long hm[256];
@@ -463,20 +464,35 @@ __global__ void __launch_bounds__(kB16Threads) fvtp_histr_b16_kernel(const FvtpP
   if (c.state != 1 || c.nref < t.round) return;  // the same for every thread of the block
   const int shift = 8 * (c.nref - t.round);
   const unsigned long long known = (unsigned long long)c.prefix >> (shift + 8);
+  const bool last_byte = shift == 0;
   load_exp_table(t, th, tl);
   if (tid < 256) hm[tid] = 0ull;
-  for (int w = tid; w < kB16Words; w += kB16Threads) cnt[w] = 0u;
+  for (int w = tid; w < (last_byte ? 256 : kB16Words); w += kB16Threads) cnt[w] = 0u;
   int j0, j1;
   b16_range(t.V, blockIdx.y, gridDim.y, &j0, &j1);
   __syncthreads();
   auto in_group = [&](uint32_t k16) {
     return k16 >= c.kmin && k16 <= c.kmax && ((unsigned long long)(k16 - c.kmin) >> (shift + 8)) == known;
   };
-  b16_count(rr.ptr, j0, j1, cnt, in_group);
-  __syncthreads();
-  b16_weigh(cnt, rr, t.frac_bits, th, tl, hm, [&](uint32_t k16, float) {
-    return in_group(k16) ? (int)(((k16 - c.kmin) >> shift) & 255u) : -1;
-  });
+  if (last_byte) {
+    b16_count(rr.ptr, j0, j1, [&](uint32_t k16) {
+      if (in_group(k16)) atomicAdd(&cnt[(k16 - c.kmin) & 255u], 1u);
+    });
+    __syncthreads();
+    if (tid < 256 && cnt[tid]) {  // digit tid: one key, all its tokens weigh the same
+      const uint32_t k16 = c.kmin + (uint32_t)((known << 8) | (unsigned)tid);
+      hm[tid] = (unsigned long long)cnt[tid] *
+                to_fixed(tp_weight(value_of_key(full_key(k16, 0)), rr, th, tl), t.frac_bits);
+    }
+  } else {
+    b16_count(rr.ptr, j0, j1, [&](uint32_t k16) {
+      if (in_group(k16)) atomicAdd(&cnt[k16 >> 1], (k16 & 1u) ? 0x10000u : 1u);
+    });
+    __syncthreads();
+    b16_weigh(cnt, rr, t.frac_bits, th, tl, hm, [&](uint32_t k16, float) {
+      return in_group(k16) ? (int)(((k16 - c.kmin) >> shift) & 255u) : -1;
+    });
+  }
   __syncthreads();
   if (tid < 256 && hm[tid]) atomicAdd(t.hist_m + (size_t)rho * 256 + tid, hm[tid]);
 }
