@@ -23,6 +23,12 @@ N > 1 runs under torch.distributed.run: every rank verifies its own batch (the
 step shards by request, no data exchange), timing is the max over ranks.
 ``--impl reference`` times the CPU oracle (fp64, host threads) on samples of
 the same workload.
+
+``--calls N`` makes no measurement: it runs N verification calls on one batch
+of the workload (drafts = each draft row's argmax; ``--batch B`` for fewer
+requests; ``--gpu-logits`` draws N(0, 2) target and target + N(0, 0.5) draft
+logits on the GPU instead of the host) and exits, a short program for a
+profiler's launch list or capture.
 """
 from __future__ import annotations
 
@@ -775,6 +781,42 @@ def run_reference_lmhead(args):
     return 0
 
 
+def run_calls(args):
+    """--calls N: N verification calls on one batch of the workload and nothing
+    else (no timing, no oracle), for a profiler."""
+    import torch
+
+    import speculative_decoding_verification_83_gb300 as dv
+
+    dv.build()
+    dv.load()
+    w = synth.WORKLOADS[args.workload]
+    B = args.batch or w["B"]
+    t = w["temperature"]
+    temps = synth.cycle_temperatures(B, t) if isinstance(t, tuple) else np.full(B, t, np.float32)
+    if args.gpu_logits:
+        gamma, V = w["gamma"], w["V"]
+        g = torch.Generator(device="cuda")
+        g.manual_seed(0)
+        X = torch.randn((B, gamma + 1, V), generator=g, device="cuda") * 2.0
+        Y = (X[:, :gamma] + 0.5 * torch.randn((B, gamma, V), generator=g, device="cuda")).contiguous()
+        d = Y.argmax(-1).to(torch.int32).contiguous()
+        if w["dtype"] == synth.BF16:
+            X, Y = X.to(torch.bfloat16), Y.to(torch.bfloat16)
+    else:
+        inp = synth.make_workload(args.workload, data_seed=0, seed=0, B=B)
+        X, Y = synth.to_torch(inp.target, "cuda"), synth.to_torch(inp.draft, "cuda")
+        d = torch.from_numpy(np.argmax(synth.to_float(inp.draft), -1).astype(np.int32)).cuda()
+    T = torch.from_numpy(np.asarray(temps, np.float32)).cuda()
+    ln = None
+    for i in range(args.calls):
+        _, ln = dv.verify(X, Y, d, T, w["top_k"], w["top_p"], i)
+    torch.cuda.synchronize()
+    print(json.dumps({"workload": args.workload, "B": B, "calls": args.calls,
+                      "accept_len": ln.cpu().numpy()[:8].tolist() if ln is not None else []}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -783,7 +825,14 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.WORKLOADS) + [LMHEAD_WORKLOAD])
     ap.add_argument("--drafts", default="sampled", choices=["sampled", "det"])
+    ap.add_argument("--calls", type=int, default=0, help="run this many calls for a profiler and exit")
+    ap.add_argument("--batch", type=int, default=0, help="with --calls: requests per call (default: the workload's)")
+    ap.add_argument("--gpu-logits", action="store_true", help="with --calls: draw the logits on the GPU")
     args = ap.parse_args()
+    if args.calls > 0:
+        if args.workload == LMHEAD_WORKLOAD:
+            ap.error("--calls runs a verification workload")
+        return run_calls(args)
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == LMHEAD_WORKLOAD:
