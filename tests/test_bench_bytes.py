@@ -51,3 +51,14 @@ def test_launches_per_step():
     # the two tie launches, accept, the draw's two
     assert bench.launches_per_step(0, 0.95) == 12
     assert bench.launches_per_step(0, 0.95, bf16=False) == 16
+
+
+def test_profiler_calls_mode_takes_verification_workloads_only():
+    """bench.py --calls runs verification calls; the LM head's workload is
+    refused on the command line, before anything touches a GPU."""
+    import subprocess
+    import sys
+
+    r = subprocess.run([sys.executable, bench.__file__, "--workload", bench.LMHEAD_WORKLOAD, "--calls", "1"],
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "--calls runs a verification workload" in r.stderr
